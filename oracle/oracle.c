@@ -1,0 +1,400 @@
+/*
+ * oracle.c -- plain float64 CPU oracle for the Matryoshka contrastive losses.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file; only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline /
+ * "--impl reference" leg use it.  It shares no code, header or constant with the
+ * CUDA library.
+ *
+ * What it computes (written out from the definitions, no blocking or fusion):
+ *   Inputs are bf16 bit patterns, widened exactly to double.  For every prefix p of
+ *   the Matryoshka ladder (UForm README, "Matryoshka" paragraph: the leading 64,
+ *   128, 256, 512 and 1024 dimensions must each work as an embedding; blog post
+ *   "Scaling-Up Contrastive Learning over NVLink Multicast", section "One Set or
+ *   Two": five grids, not one) the vectors a_i[:p], b_j[:p] are compared by cosine
+ *   (each prefix normalised on its own), scaled, and fed to
+ *     CLIP   symmetric InfoNCE: L = 1/2 [ mean_i CE(row i) + mean_j CE(column j) ],
+ *            logits s = scale * cos, positives on the diagonal (blog, "One Set or
+ *            Two": CLIP turns each row of cosines into a softmax over the batch);
+ *     SIGLIP pairwise sigmoid: L = -(1/N) sum_i sum_j log sigmoid(z_ij (t cos + b)),
+ *            z = +1 on the diagonal, -1 elsewhere (blog, "One Set or Two", the
+ *            SigLIP equation);
+ *     ROWS   row-direction InfoNCE: L = mean_{i<Nq} CE(row i) over all Nk keys,
+ *            the positive of query i being key i.
+ *   Gradients are taken by the chain rule, prefix by prefix, and summed with the
+ *   caller's per-prefix weights:
+ *     G_ij = dL/dcos_ij,  dcos_ij/da_i = (bhat_j - cos_ij * ahat_i) / |a_i|,
+ *     dcos_ij/db_j = (ahat_i - cos_ij * bhat_j) / |b_j|.
+ *   A zero-norm prefix uses 1/max(|x|, 1e-30) as its inverse norm (the pages are
+ *   silent; this is the reading the library documents as well).
+ *
+ * Build: gcc -O2 -fopenmp -shared -fPIC oracle.c -o liboracle.so -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_CLIP = 0, ORC_SIGLIP = 1, ORC_ROWS = 2 };
+
+static double widen(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static double softplus(double y) { /* log(1 + e^y), evaluated without overflow */
+  return (y > 0 ? y : 0.0) + log1p(exp(-fabs(y)));
+}
+
+static double sigmoid(double y) {
+  if (y >= 0) return 1.0 / (1.0 + exp(-y));
+  double e = exp(y);
+  return e / (1.0 + e);
+}
+
+static double inv_norm(const double* x, int p) {
+  double ss = 0;
+  for (int d = 0; d < p; ++d) ss += x[d] * x[d];
+  double n = sqrt(ss);
+  return 1.0 / (n > 1e-30 ? n : 1e-30);
+}
+
+static double* widen_matrix(const uint16_t* X, int64_t rows, int D) {
+  double* W = (double*)malloc((size_t)rows * D * sizeof(double));
+  if (!W) return NULL;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < rows; ++i)
+    for (int d = 0; d < D; ++d) W[i * D + d] = widen(X[i * D + d]);
+  return W;
+}
+
+static int check_args(int kind, int64_t Na, int64_t Nb, int D, const int* prefixes, int n) {
+  if (Na <= 0 || Nb <= 0 || D <= 0 || n <= 0 || !prefixes) return -1;
+  for (int k = 0; k < n; ++k) {
+    if (prefixes[k] <= 0 || prefixes[k] > D) return -1;
+    if (k && prefixes[k] <= prefixes[k - 1]) return -1;
+  }
+  if ((kind == ORC_CLIP || kind == ORC_SIGLIP) && Na != Nb) return -1;
+  if (kind == ORC_ROWS && Nb < Na) return -1;
+  if (kind < 0 || kind > 2) return -1;
+  return 0;
+}
+
+/*
+ * Full forward and backward over the whole Na x Nb grid, on float64 inputs.
+ *   loss[k]            unweighted loss of prefix k
+ *   dA (Na x D), dB (Nb x D)   gradients of sum_k weights[k] * L_k (NULL to skip;
+ *                      weights NULL means all ones); columns >= the last prefix are 0
+ *   row_terms[k][i]    per-row term: CLIP/ROWS: LSE_j(s_ij) - s_ii (every row of A is
+ *                      a query in ROWS); SIGLIP: sum_j softplus(-z_ij x_ij)
+ *   col_terms[k][j]    CLIP: LSE_i(s_ij) - s_jj; SIGLIP: sum_i softplus(-z_ij x_ij);
+ *                      ROWS: 0
+ * Returns 0, or -1 on bad arguments, -2 when out of memory.
+ */
+int orc_fwd_bwd_f64(int kind, const double* A, const double* B, int64_t Na, int64_t Nb, int D,
+                    const int* prefixes, int n, double scale, double bias, const double* weights,
+                    double* loss, double* dA, double* dB, double* row_terms, double* col_terms) {
+  if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
+  double* C = (double*)malloc((size_t)Na * Nb * sizeof(double));  /* cosines */
+  double* G = (double*)malloc((size_t)Na * Nb * sizeof(double));  /* dL/dcos */
+  double* ra = (double*)malloc((size_t)Na * sizeof(double));
+  double* rb = (double*)malloc((size_t)Nb * sizeof(double));
+  double* lse_r = (double*)malloc((size_t)Na * sizeof(double));
+  double* lse_c = (double*)malloc((size_t)Nb * sizeof(double));
+  if (!C || !G || !ra || !rb || !lse_r || !lse_c) {
+    free(C); free(G); free(ra); free(rb); free(lse_r); free(lse_c);
+    return -2;
+  }
+  if (dA) memset(dA, 0, (size_t)Na * D * sizeof(double));
+  if (dB) memset(dB, 0, (size_t)Nb * D * sizeof(double));
+
+  for (int k = 0; k < n; ++k) {
+    const int p = prefixes[k];
+    const double w = weights ? weights[k] : 1.0;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < Na; ++i) ra[i] = inv_norm(A + i * D, p);
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < Nb; ++j) rb[j] = inv_norm(B + j * D, p);
+
+    /* cosine of every pair, on the first p dimensions */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t i = 0; i < Na; ++i)
+      for (int64_t j = 0; j < Nb; ++j) {
+        double dot = 0;
+        for (int d = 0; d < p; ++d) dot += A[i * D + d] * B[j * D + d];
+        C[i * Nb + j] = dot * ra[i] * rb[j];
+      }
+
+    double L = 0;
+    if (kind == ORC_CLIP || kind == ORC_ROWS) {
+      const double tau = scale;
+      /* row log-sum-exp of the logits s = tau * cos, shifted by the row maximum */
+#pragma omp parallel for schedule(static)
+      for (int64_t i = 0; i < Na; ++i) {
+        double m = -INFINITY, s = 0;
+        for (int64_t j = 0; j < Nb; ++j) m = fmax(m, tau * C[i * Nb + j]);
+        for (int64_t j = 0; j < Nb; ++j) s += exp(tau * C[i * Nb + j] - m);
+        lse_r[i] = m + log(s);
+      }
+      if (kind == ORC_CLIP) {
+#pragma omp parallel for schedule(static)
+        for (int64_t j = 0; j < Nb; ++j) {
+          double m = -INFINITY, s = 0;
+          for (int64_t i = 0; i < Na; ++i) m = fmax(m, tau * C[i * Nb + j]);
+          for (int64_t i = 0; i < Na; ++i) s += exp(tau * C[i * Nb + j] - m);
+          lse_c[j] = m + log(s);
+        }
+        const double N = (double)Na;
+        double Lr = 0, Lc = 0;
+        for (int64_t i = 0; i < Na; ++i) {
+          double t = lse_r[i] - tau * C[i * Nb + i];
+          Lr += t;
+          if (row_terms) row_terms[(int64_t)k * Na + i] = t;
+        }
+        for (int64_t j = 0; j < Nb; ++j) {
+          double t = lse_c[j] - tau * C[j * Nb + j];
+          Lc += t;
+          if (col_terms) col_terms[(int64_t)k * Nb + j] = t;
+        }
+        L = 0.5 * (Lr / N + Lc / N);
+        /* dL/ds_ij = (softmax_row + softmax_col - 2 [i==j]) / (2N); dL/dcos = tau * that */
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < Na; ++i)
+          for (int64_t j = 0; j < Nb; ++j) {
+            double s = tau * C[i * Nb + j];
+            double g = exp(s - lse_r[i]) + exp(s - lse_c[j]) - (i == j ? 2.0 : 0.0);
+            G[i * Nb + j] = tau * g / (2.0 * N);
+          }
+      } else {
+        const double Nq = (double)Na;
+        for (int64_t i = 0; i < Na; ++i) {
+          double t = lse_r[i] - tau * C[i * Nb + i];
+          L += t;
+          if (row_terms) row_terms[(int64_t)k * Na + i] = t;
+        }
+        if (col_terms)
+          for (int64_t j = 0; j < Nb; ++j) col_terms[(int64_t)k * Nb + j] = 0.0;
+        L /= Nq;
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < Na; ++i)
+          for (int64_t j = 0; j < Nb; ++j) {
+            double s = tau * C[i * Nb + j];
+            double g = exp(s - lse_r[i]) - (i == j ? 1.0 : 0.0);
+            G[i * Nb + j] = tau * g / Nq;
+          }
+      }
+    } else { /* SIGLIP */
+      const double t = scale, b = bias, N = (double)Na;
+      if (row_terms)
+        for (int64_t i = 0; i < Na; ++i) row_terms[(int64_t)k * Na + i] = 0.0;
+      if (col_terms)
+        for (int64_t j = 0; j < Nb; ++j) col_terms[(int64_t)k * Nb + j] = 0.0;
+      for (int64_t i = 0; i < Na; ++i)
+        for (int64_t j = 0; j < Nb; ++j) {
+          double x = t * C[i * Nb + j] + b;
+          double z = (i == j) ? 1.0 : -1.0;
+          double l = softplus(-z * x); /* -log sigmoid(z x) */
+          L += l;
+          if (row_terms) row_terms[(int64_t)k * Na + i] += l;
+          if (col_terms) col_terms[(int64_t)k * Nb + j] += l;
+          /* d/dx softplus(-z x) = -z sigmoid(-z x) = sigmoid(x) - [z == +1] */
+          G[i * Nb + j] = t * (sigmoid(x) - (i == j ? 1.0 : 0.0)) / N;
+        }
+      L /= N;
+    }
+    loss[k] = L;
+
+    /* chain rule through the cosine: dA_i += w sum_j G_ij (bhat_j - cos_ij ahat_i) / |a_i| */
+    if (dA) {
+#pragma omp parallel for schedule(dynamic, 4)
+      for (int64_t i = 0; i < Na; ++i) {
+        double* out = dA + i * D;
+        for (int64_t j = 0; j < Nb; ++j) {
+          const double g = w * G[i * Nb + j], c = C[i * Nb + j];
+          if (g == 0.0) continue;
+          for (int d = 0; d < p; ++d)
+            out[d] += g * (B[j * D + d] * rb[j] - c * A[i * D + d] * ra[i]) * ra[i];
+        }
+      }
+    }
+    if (dB) {
+#pragma omp parallel for schedule(dynamic, 4)
+      for (int64_t j = 0; j < Nb; ++j) {
+        double* out = dB + j * D;
+        for (int64_t i = 0; i < Na; ++i) {
+          const double g = w * G[i * Nb + j], c = C[i * Nb + j];
+          if (g == 0.0) continue;
+          for (int d = 0; d < p; ++d)
+            out[d] += g * (A[i * D + d] * ra[i] - c * B[j * D + d] * rb[j]) * rb[j];
+        }
+      }
+    }
+  }
+  free(C); free(G); free(ra); free(rb); free(lse_r); free(lse_c);
+  return 0;
+}
+
+/* The same on bf16 inputs (the form every test and the library consume): widen, then compute. */
+int orc_fwd_bwd(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
+                const int* prefixes, int n, double scale, double bias, const double* weights,
+                double* loss, double* dA, double* dB, double* row_terms, double* col_terms) {
+  if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
+  double* A = widen_matrix(A16, Na, D);
+  double* B = widen_matrix(B16, Nb, D);
+  int rc = (A && B) ? orc_fwd_bwd_f64(kind, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, loss,
+                                      dA, dB, row_terms, col_terms)
+                    : -2;
+  free(A);
+  free(B);
+  return rc;
+}
+
+/*
+ * Row statistics for selected rows of X against every row of Y, one row at a time
+ * (for batches too large for the full grid).  The positive of row i of X is row i
+ * of Y.  For each selected row and prefix k:
+ *   CLIP/ROWS:  lse[r][k] = log sum_j exp(scale * cos_ij)   (max-shifted)
+ *               pos[r][k] = scale * cos_ii  (0 if i >= Ny)
+ *   SIGLIP:     lse[r][k] = sum_j softplus(-z_ij (scale * cos_ij + bias)),  pos = 0
+ * So the CLIP/ROWS row term is lse - pos and the SIGLIP row term is lse.
+ */
+int orc_row_stats(int kind, const uint16_t* X16, const uint16_t* Y16, int64_t Nx, int64_t Ny, int D,
+                  const int* prefixes, int n, double scale, double bias, const int64_t* rows,
+                  int64_t nrows, double* lse, double* pos) {
+  if (Nx <= 0 || Ny <= 0 || D <= 0 || n <= 0 || !prefixes || nrows < 0) return -1;
+  for (int k = 0; k < n; ++k)
+    if (prefixes[k] <= 0 || prefixes[k] > D || (k && prefixes[k] <= prefixes[k - 1])) return -1;
+  for (int64_t r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= Nx) return -1;
+  double* Y = widen_matrix(Y16, Ny, D);
+  double* ryk = (double*)malloc((size_t)n * Ny * sizeof(double)); /* inverse norms of Y per prefix */
+  if (!Y || !ryk) { free(Y); free(ryk); return -2; }
+  for (int k = 0; k < n; ++k) {
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < Ny; ++j) ryk[(int64_t)k * Ny + j] = inv_norm(Y + j * D, prefixes[k]);
+  }
+  int err = 0;
+#pragma omp parallel
+  {
+    double* x = (double*)malloc((size_t)D * sizeof(double));
+    double* cs = (double*)malloc((size_t)Ny * sizeof(double));
+    if (!x || !cs) {
+#pragma omp atomic write
+      err = -2;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows[r];
+        for (int d = 0; d < D; ++d) x[d] = widen(X16[i * D + d]);
+        for (int k = 0; k < n; ++k) {
+          const int p = prefixes[k];
+          const double rx = inv_norm(x, p);
+          for (int64_t j = 0; j < Ny; ++j) {
+            const double* y = Y + j * D;
+            double dot = 0;
+            for (int d = 0; d < p; ++d) dot += x[d] * y[d];
+            cs[j] = dot * rx * ryk[(int64_t)k * Ny + j];
+          }
+          if (kind == ORC_SIGLIP) {
+            double s = 0;
+            for (int64_t j = 0; j < Ny; ++j) {
+              double xx = scale * cs[j] + bias;
+              s += softplus(j == i ? -xx : xx);
+            }
+            lse[r * n + k] = s;
+            pos[r * n + k] = 0;
+          } else {
+            double m = -INFINITY, s = 0;
+            for (int64_t j = 0; j < Ny; ++j) m = fmax(m, scale * cs[j]);
+            for (int64_t j = 0; j < Ny; ++j) s += exp(scale * cs[j] - m);
+            lse[r * n + k] = m + log(s);
+            pos[r * n + k] = (i < Ny) ? scale * cs[i] : 0.0;
+          }
+        }
+      }
+    }
+    free(x);
+    free(cs);
+  }
+  free(Y);
+  free(ryk);
+  return err;
+}
+
+/*
+ * Gradient rows for selected rows of X (X is A when x_is_a, else B) against all
+ * rows of Y, given the log-normalisers the loss needs:
+ *   lse_x[k][Nx]  log-normaliser of X's own rows   (CLIP, and ROWS with X = queries)
+ *   lse_y[k][Ny]  log-normaliser of Y's rows       (CLIP, and ROWS with X = keys)
+ * (SIGLIP needs neither; arrays not needed may be NULL.)  out[r][D] receives the
+ * gradient of sum_k weights[k] * L_k with respect to X's row rows[r].
+ * Na and Nb are the batch sizes of A and B (for the loss normalisers).
+ */
+int orc_grad_rows(int kind, int x_is_a, const uint16_t* X16, const uint16_t* Y16, int64_t Nx, int64_t Ny,
+                  int D, const int* prefixes, int n, double scale, double bias, const double* weights,
+                  const double* lse_x, const double* lse_y, const int64_t* rows, int64_t nrows,
+                  double* out) {
+  if (Nx <= 0 || Ny <= 0 || D <= 0 || n <= 0 || !prefixes || nrows < 0) return -1;
+  for (int64_t r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= Nx) return -1;
+  const int64_t Na = x_is_a ? Nx : Ny, Nb = x_is_a ? Ny : Nx;
+  if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
+  double* Y = widen_matrix(Y16, Ny, D);
+  double* ryk = (double*)malloc((size_t)n * Ny * sizeof(double)); /* inverse norms of Y per prefix */
+  if (!Y || !ryk) { free(Y); free(ryk); return -2; }
+  for (int k = 0; k < n; ++k) {
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < Ny; ++j) ryk[(int64_t)k * Ny + j] = inv_norm(Y + j * D, prefixes[k]);
+  }
+  int err = 0;
+#pragma omp parallel
+  {
+    double* x = (double*)malloc((size_t)D * sizeof(double));
+    if (!x) {
+#pragma omp atomic write
+      err = -2;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows[r];
+        double* o = out + r * D;
+        for (int d = 0; d < D; ++d) { x[d] = widen(X16[i * D + d]); o[d] = 0; }
+        for (int k = 0; k < n; ++k) {
+          const int p = prefixes[k];
+          const double w = weights ? weights[k] : 1.0;
+          const double rx = inv_norm(x, p);
+          const double* ry = ryk + (int64_t)k * Ny;
+          for (int64_t j = 0; j < Ny; ++j) {
+            const double* y = Y + j * D;
+            double dot = 0;
+            for (int d = 0; d < p; ++d) dot += x[d] * y[d];
+            const double c = dot * rx * ry[j];
+            const int diag = (j == i);
+            double g; /* dL/dcos for the pair (x_i, y_j) */
+            if (kind == ORC_CLIP) {
+              const double s = scale * c;
+              g = scale * (exp(s - lse_x[(int64_t)k * Nx + i]) + exp(s - lse_y[(int64_t)k * Ny + j]) -
+                           (diag ? 2.0 : 0.0)) / (2.0 * (double)Na);
+            } else if (kind == ORC_ROWS) {
+              const double s = scale * c;
+              /* the query of the pair is row i of X when X holds the queries, else row j of Y */
+              const double lq = x_is_a ? lse_x[(int64_t)k * Nx + i] : lse_y[(int64_t)k * Ny + j];
+              g = scale * (exp(s - lq) - (diag ? 1.0 : 0.0)) / (double)Na;
+            } else {
+              const double xx = scale * c + bias;
+              g = scale * (sigmoid(xx) - (diag ? 1.0 : 0.0)) / (double)Na;
+            }
+            g *= w;
+            for (int d = 0; d < p; ++d) o[d] += g * (y[d] * ry[j] - c * x[d] * rx) * rx;
+          }
+        }
+      }
+    }
+    free(x);
+  }
+  free(Y);
+  free(ryk);
+  return err;
+}

@@ -1,0 +1,153 @@
+"""ctypes wrapper around ``oracle.c`` (test infrastructure; see package docstring)."""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import hashlib
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+KINDS = {"clip": 0, "siglip": 1, "rows": 2}
+
+_lib = None
+
+
+def _so_path() -> str:
+    with open(_SRC, "rb") as f:
+        h = hashlib.sha1(f.read()).hexdigest()[:12]
+    return os.path.join(_BUILD, f"liboracle_{os.uname().machine}_{h}.so")
+
+
+def build() -> str:
+    """Compile oracle.c (if needed) and return the shared-object path."""
+    so = _so_path()
+    if not os.path.exists(so):
+        os.makedirs(_BUILD, exist_ok=True)
+        tmp = so + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, so)
+    return so
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    lib.orc_fwd_bwd.argtypes = [ctypes.c_int, P, P, i64, i64, ctypes.c_int, P, ctypes.c_int,
+                                ctypes.c_double, ctypes.c_double, P, P, P, P, P, P]
+    lib.orc_fwd_bwd_f64.argtypes = lib.orc_fwd_bwd.argtypes
+    lib.orc_row_stats.argtypes = [ctypes.c_int, P, P, i64, i64, ctypes.c_int, P, ctypes.c_int,
+                                  ctypes.c_double, ctypes.c_double, P, i64, P, P]
+    lib.orc_grad_rows.argtypes = [ctypes.c_int, ctypes.c_int, P, P, i64, i64, ctypes.c_int, P,
+                                  ctypes.c_int, ctypes.c_double, ctypes.c_double, P, P, P, P,
+                                  i64, P]
+    for f in (lib.orc_fwd_bwd, lib.orc_fwd_bwd_f64, lib.orc_row_stats, lib.orc_grad_rows):
+        f.restype = ctypes.c_int
+    return lib
+
+
+@contextlib.contextmanager
+def use_library(path):
+    """Temporarily route every call to another build of oracle.c (planted-mistake tests)."""
+    global _lib
+    saved = _load()
+    _lib = _bind(path)
+    try:
+        yield
+    finally:
+        _lib = saved
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _bind(build())
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _bits(x):
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint16:
+        raise TypeError("embeddings must be bf16 bit patterns (uint16)")
+    return x
+
+
+def _prefix_array(prefixes):
+    return np.ascontiguousarray(np.asarray(prefixes, dtype=np.int32))
+
+
+def fwd_bwd(kind, A, B, prefixes, scale, bias=0.0, weights=None, grads=True):
+    """Full float64 forward and backward.
+
+    A and B are bf16 bit patterns (uint16), or float64 arrays (used by the
+    finite-difference pins, which need continuous inputs).
+    Returns dict(loss=[n], dA=(Na,D), dB=(Nb,D), row_terms=(n,Na), col_terms=(n,Nb)).
+    """
+    A, B = np.ascontiguousarray(A), np.ascontiguousarray(B)
+    if A.dtype == np.float64 and B.dtype == np.float64:
+        fn = _load().orc_fwd_bwd_f64
+    else:
+        A, B = _bits(A), _bits(B)
+        fn = _load().orc_fwd_bwd
+    Na, D = A.shape
+    Nb = B.shape[0]
+    pre = _prefix_array(prefixes)
+    n = pre.size
+    w = None if weights is None else np.ascontiguousarray(np.asarray(weights, np.float64))
+    loss = np.zeros(n)
+    dA = np.zeros((Na, D)) if grads else None
+    dB = np.zeros((Nb, D)) if grads else None
+    rt = np.zeros((n, Na))
+    ct = np.zeros((n, Nb))
+    rc = fn(KINDS[kind], _ptr(A), _ptr(B), Na, Nb, D, _ptr(pre), n, float(scale), float(bias), _ptr(w),
+            _ptr(loss), _ptr(dA), _ptr(dB), _ptr(rt), _ptr(ct))
+    if rc:
+        raise ValueError(f"oracle fwd_bwd failed ({rc})")
+    return dict(loss=loss, dA=dA, dB=dB, row_terms=rt, col_terms=ct)
+
+
+def row_stats(kind, X, Y, prefixes, scale, bias, rows):
+    """Per selected row of X against all of Y: (lse[r, k], pos[r, k]); see oracle.c."""
+    X, Y = _bits(X), _bits(Y)
+    pre = _prefix_array(prefixes)
+    rows = np.ascontiguousarray(np.asarray(rows, np.int64))
+    lse = np.zeros((rows.size, pre.size))
+    pos = np.zeros((rows.size, pre.size))
+    rc = _load().orc_row_stats(KINDS[kind], _ptr(X), _ptr(Y), X.shape[0], Y.shape[0], X.shape[1],
+                               _ptr(pre), pre.size, float(scale), float(bias), _ptr(rows), rows.size,
+                               _ptr(lse), _ptr(pos))
+    if rc:
+        raise ValueError(f"oracle row_stats failed ({rc})")
+    return lse, pos
+
+
+def row_terms_sampled(kind, X, Y, prefixes, scale, bias, rows):
+    """Per-row loss terms (shape (n, len(rows))), computed one row at a time."""
+    lse, pos = row_stats(kind, X, Y, prefixes, scale, bias, rows)
+    return (lse - pos).T if kind != "siglip" else lse.T
+
+
+def grad_rows(kind, x_is_a, X, Y, prefixes, scale, bias, rows, lse_x=None, lse_y=None, weights=None):
+    """Gradient rows of sum_k w_k L_k for selected rows of X; see oracle.c."""
+    X, Y = _bits(X), _bits(Y)
+    pre = _prefix_array(prefixes)
+    rows = np.ascontiguousarray(np.asarray(rows, np.int64))
+    w = None if weights is None else np.ascontiguousarray(np.asarray(weights, np.float64))
+    lx = None if lse_x is None else np.ascontiguousarray(np.asarray(lse_x, np.float64))
+    ly = None if lse_y is None else np.ascontiguousarray(np.asarray(lse_y, np.float64))
+    out = np.zeros((rows.size, X.shape[1]))
+    rc = _load().orc_grad_rows(KINDS[kind], int(bool(x_is_a)), _ptr(X), _ptr(Y), X.shape[0], Y.shape[0],
+                               X.shape[1], _ptr(pre), pre.size, float(scale), float(bias), _ptr(w),
+                               _ptr(lx), _ptr(ly), _ptr(rows), rows.size, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle grad_rows failed ({rc})")
+    return out

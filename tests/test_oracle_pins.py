@@ -1,0 +1,340 @@
+"""Pins for the float64 oracle: checks against things other than the oracle itself.
+
+Each pin ties the oracle to something the pages or mathematics fix:
+  * closed forms (identical embeddings give InfoNCE = ln N and SigLIP = N ln 2 with
+    zero gradients; one-hot orthogonal rows give ln(1 + (N-1) e^-tau));
+  * library routines: torch's cross_entropy / logsigmoid for each prefix's loss and
+    torch autograd for the gradients (an independent derivation of the chain rule);
+  * brute-force central finite differences on tiny float64 inputs;
+  * invariants: A<->B swap symmetry, ROWS(A,B) + ROWS(B,A) = 2 CLIP(A,B), per-row
+    scale invariance and its Euler identity, permutation equivariance.
+A dropped term, a wrong sign or index, or a transposed operand in the oracle fails at
+least one of these (see the planted-mistake tests at the end).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from contrastive_embedding_loss_gb300 import synth
+
+
+def _bits(x):
+    return synth.round_to_bf16_bits(np.asarray(x, np.float64))
+
+
+def _wide(bits):
+    return synth.bf16_bits_to_float(bits).astype(np.float64)
+
+
+def torch_reference(kind, A, B, prefixes, scale, bias, weights):
+    """Per-prefix losses and gradients from torch library routines + autograd (float64)."""
+    At = torch.tensor(A, dtype=torch.float64, requires_grad=True)
+    Bt = torch.tensor(B, dtype=torch.float64, requires_grad=True)
+    Na, Nb = At.shape[0], Bt.shape[0]
+    losses, total = [], 0.0
+    for p, w in zip(prefixes, weights):
+        a = F.normalize(At[:, :p], dim=1, eps=1e-30)
+        b = F.normalize(Bt[:, :p], dim=1, eps=1e-30)
+        cos = a @ b.T
+        if kind == "clip":
+            s = scale * cos
+            t = torch.arange(Na)
+            L = 0.5 * (F.cross_entropy(s, t) + F.cross_entropy(s.T, t))
+        elif kind == "rows":
+            L = F.cross_entropy(scale * cos, torch.arange(Na))
+        else:
+            x = scale * cos + bias
+            z = 2.0 * torch.eye(Na, Nb, dtype=torch.float64) - 1.0
+            L = -F.logsigmoid(z * x).sum() / Na
+        losses.append(L.item())
+        total = total + w * L
+    total.backward()
+    return np.array(losses), At.grad.numpy(), Bt.grad.numpy()
+
+
+CASES = [
+    ("clip", 12, 12, 192, (64, 128, 192), 1 / 0.07, 0.0),
+    ("siglip", 10, 10, 128, (32, 64, 128), 10.0, -10.0),
+    ("rows", 6, 15, 128, (64, 128), 1 / 0.05, 0.0),
+    ("clip", 9, 9, 128, (128,), 3.0, 0.0),
+]
+
+
+@pytest.mark.parametrize("kind,Na,Nb,D,prefixes,scale,bias", CASES)
+def test_matches_torch_library_and_autograd(kind, Na, Nb, D, prefixes, scale, bias):
+    rng = np.random.default_rng(7)
+    a = rng.standard_normal((Na, D))
+    b = np.concatenate([a, rng.standard_normal((Nb - Na, D))])[:Nb] + 0.8 * rng.standard_normal((Nb, D))
+    A, B = _bits(a), _bits(b)
+    weights = rng.uniform(0.5, 2.0, len(prefixes))
+    got = oracle.fwd_bwd(kind, A, B, prefixes, scale, bias, weights)
+    L, gA, gB = torch_reference(kind, _wide(A), _wide(B), prefixes, scale, bias, weights)
+    np.testing.assert_allclose(got["loss"], L, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(got["dA"], gA, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(got["dB"], gB, rtol=1e-10, atol=1e-13)
+    if kind == "rows":
+        assert np.all(got["col_terms"] == 0)
+    np.testing.assert_allclose(got["row_terms"].mean(axis=1) if kind == "rows" else got["loss"],
+                               got["loss"], rtol=1e-13)
+
+
+@pytest.mark.parametrize("kind", ["clip", "siglip", "rows"])
+def test_finite_differences(kind):
+    rng = np.random.default_rng(11)
+    Na, Nb, D = 4, (6 if kind == "rows" else 4), 12
+    prefixes = (4, 8, 12)
+    A = rng.standard_normal((Na, D))
+    B = rng.standard_normal((Nb, D))
+    B[:Na] += A
+    scale, bias = (2.5, -1.5) if kind == "siglip" else (3.0, 0.0)
+    w = np.array([1.0, 0.5, 2.0])
+    got = oracle.fwd_bwd(kind, A, B, prefixes, scale, bias, w)
+
+    def f(A_, B_):
+        return float(np.dot(w, oracle.fwd_bwd(kind, A_, B_, prefixes, scale, bias, w, grads=False)["loss"]))
+
+    h = 1e-6
+    for X, g in ((A, got["dA"]), (B, got["dB"])):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            x0 = X[idx]
+            X[idx] = x0 + h
+            fp = f(A, B)
+            X[idx] = x0 - h
+            fm = f(A, B)
+            X[idx] = x0
+            num[idx] = (fp - fm) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def test_identical_embeddings_closed_forms():
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(128)
+    N = 8
+    A = _bits(np.tile(v, (N, 1)))
+    pre = (64, 128)
+    clip = oracle.fwd_bwd("clip", A, A, pre, 1 / 0.07)
+    np.testing.assert_allclose(clip["loss"], math.log(N), rtol=1e-13)
+    assert np.abs(clip["dA"]).max() < 1e-12 and np.abs(clip["dB"]).max() < 1e-12
+    sig = oracle.fwd_bwd("siglip", A, A, pre, 10.0, -10.0)
+    np.testing.assert_allclose(sig["loss"], N * math.log(2.0), rtol=1e-13)
+    assert np.abs(sig["dA"]).max() < 1e-12 and np.abs(sig["dB"]).max() < 1e-12
+    K = _bits(np.tile(v, (9, 1)))
+    rows = oracle.fwd_bwd("rows", A[:4], K, pre, 1 / 0.05)
+    np.testing.assert_allclose(rows["loss"], math.log(9), rtol=1e-13)
+    assert np.abs(rows["dA"]).max() < 1e-12 and np.abs(rows["dB"]).max() < 1e-12
+
+
+def test_one_hot_orthogonal_closed_forms():
+    N, D = 8, 128
+    E = np.zeros((N, D))
+    E[np.arange(N), np.arange(N) * 5] = 1.0
+    A = _bits(E)
+    tau = 1 / 0.07
+    clip = oracle.fwd_bwd("clip", A, A, (64, 128), tau)
+    # the oracle forms LSE - s_ii around s = tau, so allow a few ulp(tau) of absolute error
+    np.testing.assert_allclose(clip["loss"], math.log1p((N - 1) * math.exp(-tau)), rtol=0, atol=1e-14)
+    t, b = 10.0, -10.0
+    sig = oracle.fwd_bwd("siglip", A, A, (64, 128), t, b)
+    sp = lambda y: math.log1p(math.exp(y))  # noqa: E731
+    np.testing.assert_allclose(sig["loss"], sp(-(t + b)) + (N - 1) * sp(b), rtol=1e-12)
+    np.testing.assert_allclose(sig["loss"], math.log(2) + (N - 1) * 4.5398899216870535e-05, rtol=1e-9)
+
+
+def _random_pair(N, D, seed, noise=1.0):
+    return synth.paired(N, D, noise, seed)
+
+
+def test_swap_symmetry():
+    A, B = _random_pair(10, 128, 5)
+    pre = (64, 128)
+    for kind, s, b in (("clip", 1 / 0.07, 0.0), ("siglip", 10.0, -10.0)):
+        r1 = oracle.fwd_bwd(kind, A, B, pre, s, b)
+        r2 = oracle.fwd_bwd(kind, B, A, pre, s, b)
+        np.testing.assert_allclose(r1["loss"], r2["loss"], rtol=1e-9, atol=1e-15)
+        np.testing.assert_allclose(r1["dA"], r2["dB"], rtol=1e-10, atol=1e-14)
+        np.testing.assert_allclose(r1["dB"], r2["dA"], rtol=1e-10, atol=1e-14)
+
+
+def test_rows_identity():
+    A, B = _random_pair(11, 128, 6)
+    pre = (64, 128)
+    tau = 1 / 0.07
+    c = oracle.fwd_bwd("clip", A, B, pre, tau)
+    r1 = oracle.fwd_bwd("rows", A, B, pre, tau)
+    r2 = oracle.fwd_bwd("rows", B, A, pre, tau)
+    np.testing.assert_allclose(r1["loss"] + r2["loss"], 2 * c["loss"], rtol=1e-9, atol=1e-15)
+    np.testing.assert_allclose(r1["dA"] + r2["dB"], 2 * c["dA"], rtol=1e-9, atol=1e-14)
+
+
+@pytest.mark.parametrize("kind", ["clip", "siglip", "rows"])
+def test_scale_invariance_and_euler(kind):
+    A, B = _random_pair(7, 128, 9)
+    if kind == "rows":
+        B = np.concatenate([B, _random_pair(5, 128, 10)[0]])
+    pre = (64, 128)
+    s, b = (10.0, -10.0) if kind == "siglip" else (1 / 0.07, 0.0)
+    r = oracle.fwd_bwd(kind, A, B, pre, s, b)
+    for X, G in ((A, r["dA"]), (B, r["dB"])):
+        x = _wide(X)
+        euler = np.abs((x * G).sum(axis=1))
+        assert np.all(euler <= 1e-12 * (np.linalg.norm(x, axis=1) * np.linalg.norm(G, axis=1) + 1e-300))
+    # scaling a row by 2 (exact in bf16) leaves the loss unchanged and halves its gradient
+    A2 = _bits(2.0 * _wide(A))
+    r2 = oracle.fwd_bwd(kind, A2, B, pre, s, b)
+    np.testing.assert_allclose(r2["loss"], r["loss"], rtol=1e-9, atol=1e-15)
+    np.testing.assert_allclose(r2["dA"], 0.5 * r["dA"], rtol=1e-9, atol=1e-15)
+
+
+def test_permutation_equivariance():
+    A, B = _random_pair(9, 128, 12)
+    perm = np.random.default_rng(0).permutation(9)
+    for kind, s, b in (("clip", 1 / 0.07, 0.0), ("siglip", 10.0, -10.0), ("rows", 1 / 0.05, 0.0)):
+        r = oracle.fwd_bwd(kind, A, B, (64, 128), s, b)
+        rp = oracle.fwd_bwd(kind, A[perm], B[perm], (64, 128), s, b)
+        np.testing.assert_allclose(rp["loss"], r["loss"], rtol=1e-9, atol=1e-15)
+        np.testing.assert_allclose(rp["dA"], r["dA"][perm], rtol=1e-10, atol=1e-15)
+        np.testing.assert_allclose(rp["dB"], r["dB"][perm], rtol=1e-10, atol=1e-15)
+
+
+def test_full_prefix_equals_unprefixed_cross_entropy():
+    A, B = _random_pair(16, 256, 13)
+    tau = 1 / 0.07
+    r = oracle.fwd_bwd("clip", A, B, (64, 256), tau)
+    a = F.normalize(torch.tensor(_wide(A)), dim=1)
+    b = F.normalize(torch.tensor(_wide(B)), dim=1)
+    s = tau * a @ b.T
+    t = torch.arange(16)
+    ce = 0.5 * (F.cross_entropy(s, t) + F.cross_entropy(s.T, t))
+    np.testing.assert_allclose(r["loss"][-1], ce.item(), rtol=1e-12)
+
+
+@pytest.mark.parametrize("kind", ["clip", "siglip", "rows"])
+def test_sampled_row_functions_match_full(kind):
+    Na, Nb = 12, (20 if kind == "rows" else 12)
+    A, _ = _random_pair(Na, 128, 21)
+    B, _ = _random_pair(Nb, 128, 22)
+    B[:Na] = _bits(_wide(A) + 0.5 * _wide(B[:Na]))
+    pre = (64, 128)
+    s, b = (10.0, -10.0) if kind == "siglip" else (1 / 0.07, 0.0)
+    w = np.array([0.7, 1.3])
+    full = oracle.fwd_bwd(kind, A, B, pre, s, b, w)
+    rows_a = np.array([0, 5, 11])
+    rt = oracle.row_terms_sampled(kind, A, B, pre, s, b, rows_a)
+    np.testing.assert_allclose(rt, full["row_terms"][:, rows_a], rtol=1e-12, atol=1e-14)
+    lse_a, _ = oracle.row_stats(kind, A, B, pre, s, b, np.arange(Na))
+    lse_b, _ = oracle.row_stats(kind, B, A, pre, s, b, np.arange(Nb))
+    if kind == "clip":
+        ct = oracle.row_terms_sampled(kind, B, A, pre, s, b, rows_a)
+        np.testing.assert_allclose(ct, full["col_terms"][:, rows_a], rtol=1e-12, atol=1e-14)
+    gA = oracle.grad_rows(kind, True, A, B, pre, s, b, rows_a, lse_a.T, lse_b.T, w)
+    np.testing.assert_allclose(gA, full["dA"][rows_a], rtol=1e-10, atol=1e-15)
+    rows_b = np.array([1, 7, Nb - 1])
+    gB = oracle.grad_rows(kind, False, B, A, pre, s, b, rows_b, lse_b.T, lse_a.T, w)
+    np.testing.assert_allclose(gB, full["dB"][rows_b], rtol=1e-10, atol=1e-15)
+
+
+def test_zero_norm_prefix_reading():
+    """A row whose prefix is all zero scores cosine 0 there (inverse norm floored at 1e30)."""
+    A, B = _random_pair(6, 128, 30)
+    a = _wide(A)
+    a[2, :64] = 0.0
+    A = _bits_safe(a)
+    r = oracle.fwd_bwd("clip", A, B, (64, 128), 1 / 0.07)
+    assert np.all(np.isfinite(r["loss"])) and np.all(np.isfinite(r["dA"]))
+    assert abs(r["row_terms"][0, 2] - math.log(6)) < 1e-12  # all six logits are 0
+
+
+def _bits_safe(x):
+    out = np.zeros(x.shape, np.uint16)
+    nz = x != 0
+    out[nz] = synth.round_to_bf16_bits(x[nz])
+    return out
+
+
+# ---- the input generator ----------------------------------------------------------
+
+def test_bf16_rounding_matches_float32_bit_rounding():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(100000).astype(np.float32)  # exactly representable inputs
+    u = x.view(np.uint32).astype(np.uint64)
+    ref = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)  # f32 -> bf16 RNE on the bits
+    assert np.array_equal(synth.round_to_bf16_bits(x.astype(np.float64)), ref)
+    # exact ties go to the even neighbour
+    lo = synth.bf16_bits_to_float(np.array([0x3F80, 0x3F81], np.uint16)).astype(np.float64)
+    assert synth.round_to_bf16_bits(np.array([(lo[0] + lo[1]) / 2]))[0] == 0x3F80
+    lo = synth.bf16_bits_to_float(np.array([0x3F81, 0x3F82], np.uint16)).astype(np.float64)
+    assert synth.round_to_bf16_bits(np.array([(lo[0] + lo[1]) / 2]))[0] == 0x3F82
+
+
+def test_generators_are_seeded_and_chunk_invariant():
+    A1, B1 = synth.paired(20000, 64, 1.0, 4)
+    A2, B2 = synth.paired(20000, 64, 1.0, 4)
+    assert np.array_equal(A1, A2) and np.array_equal(B1, B2)
+    A3, _ = synth.paired(100, 64, 1.0, 4)
+    assert np.array_equal(A3, A1[:100])
+    Q, K = synth.queries_keys(50, 300, 64, 0.8, 4)
+    assert Q.shape == (50, 64) and K.shape == (300, 64)
+    c = np.corrcoef(_wide(Q[:, :]).ravel(), _wide(K[:50]).ravel())[0, 1]
+    assert 0.7 < c < 0.85  # 1/sqrt(1 + 0.8^2) = 0.78
+    Ah, Bh = synth.paired_hard(1000, 64, 1.0, 0.1, 0.05, 3)
+    a = _wide(Ah)
+    an = a / np.linalg.norm(a, axis=1, keepdims=True)
+    near = (an @ an.T > 0.99).sum(axis=1) - 1
+    assert 90 <= (near > 0).sum() <= 200  # ~100 duplicated rows, plus their sources
+
+
+# ---- planted mistakes: each plausible error in the oracle must break some pin ----
+# The test copies oracle.c, plants one mistake by text substitution, compiles the copy
+# into a temporary library and checks that the pins above reject it.
+
+MUTATIONS = {
+    "dropped_projection_term": (
+        "out[d] += g * (B[j * D + d] * rb[j] - c * A[i * D + d] * ra[i]) * ra[i];",
+        "out[d] += g * (B[j * D + d] * rb[j]) * ra[i];"),
+    "siglip_label_sign": ("double z = (i == j) ? 1.0 : -1.0;", "double z = (i == j) ? -1.0 : 1.0;"),
+    "column_lse_transposed": (
+        "for (int64_t i = 0; i < Na; ++i) s += exp(tau * C[i * Nb + j] - m);",
+        "for (int64_t i = 0; i < Na; ++i) s += exp(tau * C[j * Nb + i] - m);"),
+    "prefix_off_by_one": ("for (int d = 0; d < p; ++d) dot += A[i * D + d] * B[j * D + d];",
+                          "for (int d = 0; d < p - 1; ++d) dot += A[i * D + d] * B[j * D + d];"),
+    "clip_normaliser": ("L = 0.5 * (Lr / N + Lc / N);", "L = (Lr / N + Lc / N);"),
+    "dB_wrong_norm": ("out[d] += g * (A[i * D + d] * ra[i] - c * B[j * D + d] * rb[j]) * rb[j];",
+                      "out[d] += g * (A[i * D + d] * ra[i] - c * B[j * D + d] * rb[j]) * ra[i];"),
+}
+
+
+def _pins_pass():
+    """Run the cheap pins; return False as soon as one fails."""
+    checks = [
+        lambda: test_matches_torch_library_and_autograd(*CASES[0]),
+        lambda: test_matches_torch_library_and_autograd(*CASES[1]),
+        test_identical_embeddings_closed_forms,
+        test_one_hot_orthogonal_closed_forms,
+    ]
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            return False
+    return True
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistakes_are_caught(name, tmp_path):
+    import subprocess
+
+    old, new = MUTATIONS[name]
+    src = open(oracle.ref._SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path = tmp_path / "oracle_mut.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / "liboracle_mut.so"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", str(path), "-o", str(so), "-lm"])
+    with oracle.ref.use_library(str(so)):
+        assert not _pins_pass(), f"planted mistake {name} was not caught"
+    assert _pins_pass()
