@@ -1,0 +1,143 @@
+"""Thin Python binding of ``include/uf_contrastive.h`` (argument marshalling only).
+
+The functions named like the C entry points take plain integers (device pointers,
+sizes, a stream handle) and return the C status.  ``contrastive_fwd_bwd`` is the
+torch-facing convenience: it allocates the outputs and the workspace with torch (device
+memory only) and makes one C call on the current stream.  Every step of the loss runs in
+the library's CUDA kernels; there is no fallback: if the library is missing, or a call
+fails, this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+KINDS = {"clip": 0, "siglip": 1, "rows": 2}
+STATUS_NAMES = {0: "ok", 1: "invalid-argument", 2: "unsupported", 3: "workspace-too-small", 4: "cuda-error",
+                5: "device-timeout"}
+UF_OK = 0
+UF_DEVICE_TIMEOUT = 5
+
+
+class UfError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, 'unknown')} ({status})")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the shared library (built by ``__graft_entry__.build()``); raise if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise ImportError(f"the uf_contrastive CUDA library is not built ({p} is missing); "
+                          "run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    P, I64, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.uf_status_name.argtypes = [I32]
+    lib.uf_status_name.restype = ctypes.c_char_p
+    lib.uf_contrastive_version.argtypes = []
+    lib.uf_contrastive_version.restype = I32
+    lib.uf_contrastive_init.argtypes = [I32]
+    lib.uf_contrastive_init.restype = I32
+    lib.uf_contrastive_workspace_size.argtypes = [I64, I64, I32, P, I32, I32, I32]
+    lib.uf_contrastive_workspace_size.restype = SZ
+    lib.uf_contrastive_fwd_bwd.argtypes = [P, P, I64, I64, I32, P, I32, I32, F32, F32, P, P, P, P, P, P, P, SZ,
+                                           P, P]
+    lib.uf_contrastive_fwd_bwd.restype = I32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _int_array(values, ctype=ctypes.c_int):
+    arr = (ctype * len(values))(*values)
+    return arr
+
+
+# ---- the C entry points, same names ------------------------------------------------
+
+def uf_status_name(status: int) -> str:
+    return load().uf_status_name(int(status)).decode()
+
+
+def uf_contrastive_version() -> int:
+    return int(load().uf_contrastive_version())
+
+
+def uf_contrastive_init(device: int) -> int:
+    return int(load().uf_contrastive_init(int(device)))
+
+
+def uf_contrastive_workspace_size(Na, Nb, D, prefixes, kind, want_grads) -> int:
+    pre = _int_array(list(prefixes))
+    return int(load().uf_contrastive_workspace_size(int(Na), int(Nb), int(D), pre, len(prefixes), int(kind),
+                                                    int(bool(want_grads))))
+
+
+def uf_contrastive_fwd_bwd(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, prefix_weights, loss_per_prefix,
+                           row_terms, col_terms, dA, dB, workspace, workspace_bytes, device_status, stream) -> int:
+    """Raw call: every pointer argument is an int device address (or 0 / None for NULL)."""
+    pre = _int_array(list(prefixes))
+    w = None if prefix_weights is None else (ctypes.c_float * len(prefix_weights))(*prefix_weights)
+    return int(load().uf_contrastive_fwd_bwd(A, B, int(Na), int(Nb), int(D), pre, len(prefixes), int(kind),
+                                             float(logit_scale), float(bias), w, loss_per_prefix, row_terms,
+                                             col_terms, dA, dB, workspace, int(workspace_bytes), device_status,
+                                             stream))
+
+
+# ---- torch convenience ------------------------------------------------------------
+
+def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), logit_scale=1 / 0.07, bias=0.0,
+                        prefix_weights=None, grads=True, terms=False, workspace=None, device_status=None,
+                        stream=None):
+    """Run the loss on bf16 CUDA tensors A (Na x D) and B (Nb x D).
+
+    Returns a dict with ``loss`` (n_prefix fp32), ``dA``/``dB`` (fp32, when grads) and
+    ``row_terms``/``col_terms`` (when terms).  ``workspace`` may be a preallocated uint8
+    CUDA tensor of at least ``uf_contrastive_workspace_size`` bytes.
+    """
+    import torch
+
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or not A.is_cuda or not B.is_cuda:
+        raise TypeError("A and B must be bf16 CUDA tensors")
+    A = A.contiguous()
+    B = B.contiguous()
+    Na, D = A.shape
+    Nb = B.shape[0]
+    k = KINDS[kind] if isinstance(kind, str) else int(kind)
+    dev = A.device
+    n = len(prefixes)
+    need = uf_contrastive_workspace_size(Na, Nb, D, prefixes, k, grads)
+    if need == 0:
+        raise UfError(1, "uf_contrastive_workspace_size")
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = {"loss": torch.empty(n, dtype=torch.float32, device=dev)}
+    if grads:
+        out["dA"] = torch.empty((Na, D), dtype=torch.float32, device=dev)
+        out["dB"] = torch.empty((Nb, D), dtype=torch.float32, device=dev)
+    if terms:
+        out["row_terms"] = torch.empty((n, Na), dtype=torch.float32, device=dev)
+        out["col_terms"] = torch.empty((n, Nb), dtype=torch.float32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    with torch.cuda.device(dev):
+        st = uf_contrastive_fwd_bwd(A.data_ptr(), B.data_ptr(), Na, Nb, D, prefixes, k, logit_scale, bias,
+                                    prefix_weights, out["loss"].data_ptr(), ptr(out.get("row_terms")),
+                                    ptr(out.get("col_terms")), ptr(out.get("dA")), ptr(out.get("dB")),
+                                    workspace.data_ptr(), workspace.numel(), ptr(device_status), s.cuda_stream)
+    if st != UF_OK:
+        raise UfError(st, "uf_contrastive_fwd_bwd")
+    return out

@@ -1,0 +1,330 @@
+// aux_kernels.cu -- the HBM-streaming steps around the fused score kernel:
+//   prep      per-prefix inverse norms of every row and the positives' cosines
+//   transpose bf16 X (rows x d) -> X^T (d x rows), the K-major operand of the gradient MMA
+//   stats     fixed-shift row/column sums -> row terms, backward factors
+//   finalize  per-prefix loss (fp64, fixed reduction order)
+//   norm_bwd  dX = G - r_c X + q_c Y: the cosine's projection term and the diagonal
+//             (positive-pair) correction, band by band.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "launch.h"
+
+namespace ufc {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ int band_of(int e, const int* pend, int n) {
+  int b = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxPrefix; ++k) b += (k < n && pend[k] <= e) ? 1 : 0;
+  return b;  // == n past the last prefix
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------------------------ prep
+// One warp per item r < max(Na, Nb): rows A_r and B_r together while r < Nmin (so the
+// positive pair's dot products come from the same registers), otherwise the one row.
+__global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_items = p.na > p.nb ? p.na : p.nb;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int n = p.n_prefix;
+  for (int64_t r = warp_id; r < n_items; r += n_warps) {
+    const bool has_a = r < p.na, has_b = r < p.nb, pair = r < p.nmin;
+    float ssa[kMaxPrefix], ssb[kMaxPrefix], dab[kMaxPrefix];
+#pragma unroll
+    for (int k = 0; k < kMaxPrefix; ++k) ssa[k] = ssb[k] = dab[k] = 0.f;
+    const uint4* ra = reinterpret_cast<const uint4*>(p.A + r * p.d);
+    const uint4* rb = reinterpret_cast<const uint4*>(p.B + r * p.d);
+    const int pn = p.prefix_end[n - 1];
+    for (int ch = lane; ch * 8 < pn; ch += 32) {
+      const int b = band_of(ch * 8, p.prefix_end, n);
+      uint4 va = make_uint4(0, 0, 0, 0), vb = make_uint4(0, 0, 0, 0);
+      if (has_a) va = __ldg(ra + ch);
+      if (has_b) vb = __ldg(rb + ch);
+      const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+      float sa = 0.f, sb = 0.f, sd = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a0 = bf16_lo(wa[q]), a1 = bf16_hi(wa[q]);
+        const float b0 = bf16_lo(wb[q]), b1 = bf16_hi(wb[q]);
+        sa = fmaf(a0, a0, fmaf(a1, a1, sa));
+        sb = fmaf(b0, b0, fmaf(b1, b1, sb));
+        sd = fmaf(a0, b0, fmaf(a1, b1, sd));
+      }
+#pragma unroll
+      for (int k = 0; k < kMaxPrefix; ++k)
+        if (k == b) {
+          ssa[k] += sa;
+          ssb[k] += sb;
+          dab[k] += sd;
+        }
+    }
+    float ca = 0.f, cb = 0.f, cd = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxPrefix; ++k) {
+      if (k >= n) break;
+      ca += warp_sum(ssa[k]);
+      cb += warp_sum(ssb[k]);
+      cd += warp_sum(dab[k]);
+      if (lane == 0) {
+        const float rA = 1.f / fmaxf(sqrtf(ca), 1e-30f);
+        const float rB = 1.f / fmaxf(sqrtf(cb), 1e-30f);
+        if (has_a) p.rinv_a[k * p.na + r] = rA;
+        if (has_b) p.rinv_b[k * p.nb + r] = rB;
+        if (pair) p.pos_cos[k * p.nmin + r] = cd * rA * rB;
+      }
+    }
+  }
+}
+
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
+  const int64_t items = p.na > p.nb ? p.na : p.nb;
+  int64_t blocks = (items * 32 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------ transpose
+__global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restrict__ X, uint16_t* __restrict__ Xt,
+                                                        int64_t rows, int d, int64_t ld) {
+  __shared__ uint16_t tile[64][66];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 64;
+  const int c0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
+  for (int y = ty; y < 64; y += 4) {
+    const int64_t r = r0 + y;
+    tile[y][tx] = (r < rows) ? X[r * d + c0 + tx] : uint16_t(0);
+  }
+  __syncthreads();
+  for (int y = ty; y < 64; y += 4) {
+    const int64_t r = r0 + tx;
+    if (r < rows) Xt[static_cast<int64_t>(c0 + y) * ld + r] = tile[tx][y];
+  }
+}
+
+cudaError_t launch_transpose(const uint16_t* X, uint16_t* Xt, int64_t rows, int d, int64_t ld, cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>((rows + 63) / 64), static_cast<unsigned>(d / 64));
+  transpose_kernel<<<grid, 256, 0, stream>>>(X, Xt, rows, d, ld);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------ stats
+// Elementwise over (prefix, row) of A and then of B.
+__global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
+  const int n = p.n_prefix;
+  const int64_t total_a = static_cast<int64_t>(n) * p.na;
+  const int64_t total = total_a + static_cast<int64_t>(n) * p.nb;
+  const int64_t nmin = p.na < p.nb ? p.na : p.nb;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool side_a = e < total_a;
+    const int64_t nrows = side_a ? p.na : p.nb;
+    const int64_t ee = side_a ? e : e - total_a;
+    const int k = static_cast<int>(ee / nrows);
+    const int64_t i = ee % nrows;
+    const float* acc = side_a ? p.rowacc_a : p.rowacc_b;
+    const int slots = side_a ? p.slots_a : p.slots_b;
+    const float w = p.weight[k];
+    if (p.kind == KIND_SIGLIP) {
+      if (!side_a) {
+        p.terms_b[ee] = 0.f;
+        continue;
+      }
+      double s = 0.0;  // log2 units, fixed order over slots
+      for (int sl = 0; sl < slots; ++sl) s += acc[(static_cast<int64_t>(sl) * n + k) * nrows + i];
+      const float x_ii = p.tau_or_t * p.pos_cos[k * nmin + i] + p.bias;
+      p.terms_a[ee] = static_cast<float>(s * 0.6931471805599453) - x_ii;
+      continue;
+    }
+    if (p.kind == KIND_ROWS && !side_a) {
+      p.terms_b[ee] = 0.f;
+      continue;
+    }
+    float z = 0.f;  // sum_j exp(s_ij - tau), fixed order over slots
+    for (int sl = 0; sl < slots; ++sl) z += acc[(static_cast<int64_t>(sl) * n + k) * nrows + i];
+    const float tau = p.tau_or_t;
+    const float s_ii = tau * p.pos_cos[k * nmin + i];
+    const float term = logf(z) + tau - s_ii;
+    const double N = static_cast<double>(p.na);
+    const float coef = (p.kind == KIND_CLIP) ? static_cast<float>(w * tau / (2.0 * N)) : static_cast<float>(w * tau / N);
+    const float rho = side_a ? p.rinv_a[k * p.na + i] : p.rinv_b[k * p.nb + i];
+    if (side_a) {
+      p.zr[ee] = z;
+      p.fa[ee] = rho * coef / z;
+      p.terms_a[ee] = term;
+    } else {
+      p.zc[ee] = z;
+      p.fb[ee] = rho * coef / z;
+      p.terms_b[ee] = term;
+    }
+  }
+}
+
+// One block per prefix: L_k from the row (and column) terms, fp64, fixed order.
+__global__ void __launch_bounds__(1024) finalize_kernel(const StatsParams p) {
+  __shared__ double red[32];
+  const int k = blockIdx.x;
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < p.na; i += blockDim.x) s += p.terms_a[k * p.na + i];
+  if (p.kind == KIND_CLIP)
+    for (int64_t j = threadIdx.x; j < p.nb; j += blockDim.x) s += p.terms_b[k * p.nb + j];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    double v = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) {
+      const double denom = (p.kind == KIND_CLIP) ? 2.0 * p.na : static_cast<double>(p.na);
+      p.loss[k] = static_cast<float>(v / denom);
+    }
+  }
+}
+
+cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(p.n_prefix) * (p.na + p.nb);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  stats_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  finalize_kernel<<<p.n_prefix, 1024, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------ norm_bwd
+// One warp per row of X.  Lanes k < n first form, for prefix k, the row's diagonal
+// weight W_ii = W'_ii + w (the positive pair, in fp32), its full row scalar
+// C_k = sum_j W_ij cos_ij, and from them the band coefficients
+//   r_c = sum_{k>=c} rho_k^2 C_k,  q_c = sum_{k>=c} rho_k sigma_k W_ii,k.
+// Then the warp streams the row: dX[d] = sum_s G_s[d] - r_c X[d] + q_c Y[d].
+__global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int n = p.n_prefix;
+  const int pn = p.prefix_end[n - 1];
+  for (int64_t i = warp_id; i < p.nx; i += n_warps) {
+    const bool diag = i < p.nmin;
+    float rk = 0.f, qk = 0.f;
+    if (lane < n) {
+      const int k = lane;
+      const float rho = p.rinv_x[k * p.nx + i];
+      float C = 0.f;
+      for (int s = 0; s < p.crow_slots; ++s) C += p.crow[(static_cast<int64_t>(s) * n + k) * p.nx + i];
+      float Wd = 0.f;
+      if (diag) {
+        const float cosd = p.pos_cos[k * p.nmin + i];
+        const float sig = p.rinv_y[k * p.ny + i];
+        const float w = p.weight[k];
+        const double N = static_cast<double>(p.n_total);
+        if (p.kind == KIND_SIGLIP) {
+          const float x = p.tau_or_t * cosd + p.bias;
+          const float sg = 1.f / (1.f + expf(-x));
+          Wd = static_cast<float>(w * p.tau_or_t / N) * (sg - 1.f);
+        } else {
+          const float tau = p.tau_or_t;
+          const float e = expf(tau * cosd - tau);
+          if (p.kind == KIND_CLIP) {
+            const float c = static_cast<float>(w * tau / (2.0 * N));
+            Wd = e * (c / p.z_x[k * p.nx + i] + c / p.z_y[k * p.ny + i]) - 2.f * c;
+          } else {
+            const float c = static_cast<float>(w * tau / N);
+            const float zq = p.x_is_query ? p.z_x[k * p.nx + i] : p.z_y[k * p.ny + i];
+            Wd = e * c / zq - c;
+          }
+        }
+        C += Wd * cosd;
+        qk = rho * sig * Wd;
+      }
+      rk = rho * rho * C;
+    }
+    // suffix sums over prefixes: band c uses every prefix k >= c
+    float rc[kMaxPrefix], qc[kMaxPrefix];
+    float ar = 0.f, aq = 0.f;
+#pragma unroll
+    for (int k = kMaxPrefix - 1; k >= 0; --k) {
+      const float r_k = __shfl_sync(0xffffffffu, rk, k);
+      const float q_k = __shfl_sync(0xffffffffu, qk, k);
+      if (k < n) {
+        ar += r_k;
+        aq += q_k;
+      }
+      rc[k] = ar;
+      qc[k] = aq;
+    }
+    const uint16_t* xr = p.X + i * p.d;
+    const uint16_t* yr = p.Y + (diag ? i : 0) * p.d;
+    float* out = p.dX + i * p.d;
+    for (int c4 = lane * 4; c4 < p.d; c4 += 128) {
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c4 < pn) {
+        const int b = band_of(c4, p.prefix_end, n);
+        float r_c = 0.f, q_c = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxPrefix; ++k)
+          if (k == b) {
+            r_c = rc[k];
+            q_c = qc[k];
+          }
+        float g[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s = 0; s < p.g_splits; ++s) {
+          const float4 v = *reinterpret_cast<const float4*>(p.G + (static_cast<int64_t>(s) * p.nx + i) * p.d + c4);
+          g[0] += v.x;
+          g[1] += v.y;
+          g[2] += v.z;
+          g[3] += v.w;
+        }
+        const uint2 xv = *reinterpret_cast<const uint2*>(xr + c4);
+        const float x[4] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y)};
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        if (diag) {
+          const uint2 yv = *reinterpret_cast<const uint2*>(yr + c4);
+          y[0] = bf16_lo(yv.x);
+          y[1] = bf16_hi(yv.x);
+          y[2] = bf16_lo(yv.y);
+          y[3] = bf16_hi(yv.y);
+        }
+        o.x = g[0] - r_c * x[0] + q_c * y[0];
+        o.y = g[1] - r_c * x[1] + q_c * y[1];
+        o.z = g[2] - r_c * x[2] + q_c * y[2];
+        o.w = g[3] - r_c * x[3] + q_c * y[3];
+      }
+      *reinterpret_cast<float4*>(out + c4) = o;
+    }
+  }
+}
+
+cudaError_t launch_norm_bwd(const NormBwdParams& p, cudaStream_t stream) {
+  int64_t blocks = (p.nx * 32 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  norm_bwd_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Force the module holding these kernels to load now (no lazy loading on the hot path).
+cudaError_t aux_kernels_setup() {
+  cudaFuncAttributes fa;
+  cudaError_t e;
+  if ((e = cudaFuncGetAttributes(&fa, prep_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, transpose_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, stats_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, finalize_kernel)) != cudaSuccess) return e;
+  return cudaFuncGetAttributes(&fa, norm_bwd_kernel);
+}
+
+}  // namespace ufc

@@ -1,0 +1,85 @@
+// launch.h -- host-side launchers of the kernels (internal to the library).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace ufc {
+
+// Load every auxiliary kernel now (aux_kernels.cu).
+cudaError_t aux_kernels_setup();
+
+// Fused score kernel (tile_kernel.cu).
+cudaError_t tile_kernel_setup();
+cudaError_t launch_tile(int mode, int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y,
+                        const CUtensorMap& tm_yt, const TileParams& p, dim3 grid, cudaStream_t stream);
+
+// Per-row inverse norms of every prefix for A and B, plus the positives' cosines
+// cos_ii for i < min(Na, Nb).  Layouts [n][rows].
+struct PrepParams {
+  const uint16_t* A;
+  const uint16_t* B;
+  int64_t na, nb, nmin;
+  int d, n_prefix;
+  int prefix_end[kMaxPrefix];
+  float* rinv_a;
+  float* rinv_b;
+  float* pos_cos;
+};
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
+
+// X (rows x d, bf16) -> Xt (d x ld, bf16): Xt[c][r] = X[r][c].
+cudaError_t launch_transpose(const uint16_t* X, uint16_t* Xt, int64_t rows, int d, int64_t ld, cudaStream_t stream);
+
+// Loss statistics after the forward (CLIP / ROWS) or the A-side backward (SigLIP).
+struct StatsParams {
+  int kind;
+  int64_t na, nb;
+  int n_prefix;
+  int prefix_end[kMaxPrefix];
+  float tau_or_t, bias;
+  float weight[kMaxPrefix];
+  const float* rinv_a;
+  const float* rinv_b;
+  const float* pos_cos;
+  const float* rowacc_a;   // [slots_a][n][na]
+  int slots_a;
+  const float* rowacc_b;   // [slots_b][n][nb] (CLIP)
+  int slots_b;
+  float* zr;               // [n][na]  fixed-shift row sums (CLIP/ROWS)
+  float* zc;               // [n][nb]
+  float* fa;               // [n][na]  rho_i * u_i  (backward factor)
+  float* fb;               // [n][nb]  sigma_j * v_j
+  float* terms_a;          // [n][na]  row terms
+  float* terms_b;          // [n][nb]  column terms (CLIP; 0 otherwise)
+  float* loss;             // [n]
+};
+cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream);
+
+// dX = sum_s G[s] - r_c * X + q_c * Y (diagonal rows), 0 past the last prefix.
+struct NormBwdParams {
+  int kind;
+  int64_t nx, ny, nmin, n_total;  // n_total: batch size used by the loss normaliser
+  int d, n_prefix;
+  int prefix_end[kMaxPrefix];
+  float tau_or_t, bias;
+  float weight[kMaxPrefix];
+  const uint16_t* X;
+  const uint16_t* Y;
+  const float* rinv_x;
+  const float* rinv_y;
+  const float* pos_cos;
+  const float* z_x;        // CLIP/ROWS fixed-shift sums of X's rows (ROWS: the queries')
+  const float* z_y;        // CLIP: of Y's rows
+  int x_is_query;          // ROWS: 1 when X holds the queries
+  const float* crow;       // [slots][n][nx]
+  int crow_slots;
+  const float* G;          // [splits][nx][d]
+  int g_splits;
+  float* dX;               // [nx][d]
+};
+cudaError_t launch_norm_bwd(const NormBwdParams& p, cudaStream_t stream);
+
+}  // namespace ufc

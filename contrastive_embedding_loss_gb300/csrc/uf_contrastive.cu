@@ -1,0 +1,416 @@
+// uf_contrastive.cu -- the C ABI: argument checks, the workspace plan, TMA tensor maps
+// and the launch sequence on the caller's stream.  No allocation, no synchronisation.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/uf_contrastive.h"
+#include "launch.h"
+
+using namespace ufc;
+
+namespace {
+
+constexpr int kTargetCtas = 600;  // about four waves of one CTA per SM on a 152-SM GB300
+
+struct Split {
+  int splits = 1;
+  int tiles_per_split = 1;
+};
+
+Split plan_split(int64_t row_blocks, int64_t slices, int64_t tiles) {
+  Split s;
+  int64_t want = (kTargetCtas + row_blocks * slices - 1) / (row_blocks * slices);
+  if (want < 1) want = 1;
+  if (want > tiles) want = tiles;
+  s.tiles_per_split = static_cast<int>((tiles + want - 1) / want);
+  s.splits = static_cast<int>((tiles + s.tiles_per_split - 1) / s.tiles_per_split);
+  return s;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Sizes and offsets of every scratch array of one call.
+struct Plan {
+  int64_t na = 0, nb = 0, nmin = 0;
+  int d = 0, n = 0;
+  int kind = 0;
+  bool grads = false;
+  int64_t rb_a = 0, rb_b = 0, tiles_a = 0, tiles_b = 0;  // row blocks / column tiles with X = A or X = B
+  int slices = 0;
+  Split fwd_a, fwd_b, bwd_a, bwd_b;
+  int64_t lda = 0, ldb = 0;  // padded leading dimensions of A^T and B^T
+  // offsets
+  size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
+      o_terms_b, o_loss, o_at, o_bt, o_ga, o_gb, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int kind, bool grads, Plan& P) {
+  if (Na < 1 || Nb < 1 || D < 64 || D > 4096 || D % 64 != 0 || n < 1 || n > kMaxPrefix || !prefixes) return false;
+  if (kind != KIND_CLIP && kind != KIND_SIGLIP && kind != KIND_ROWS) return false;
+  if ((kind == KIND_CLIP || kind == KIND_SIGLIP) && Na != Nb) return false;
+  if (kind == KIND_ROWS && Nb < Na) return false;
+  if (Na > (int64_t(1) << 31) || Nb > (int64_t(1) << 31)) return false;
+  for (int k = 0; k < n; ++k) {
+    if (prefixes[k] <= 0 || prefixes[k] % 64 != 0 || prefixes[k] > D) return false;
+    if (k && prefixes[k] <= prefixes[k - 1]) return false;
+  }
+  P.na = Na;
+  P.nb = Nb;
+  P.nmin = Na < Nb ? Na : Nb;
+  P.d = D;
+  P.n = n;
+  P.kind = kind;
+  P.grads = grads;
+  P.rb_a = cdiv(Na, kTileRows);
+  P.rb_b = cdiv(Nb, kTileRows);
+  P.tiles_a = cdiv(Nb, kTileCols);  // X = A walks B's rows
+  P.tiles_b = cdiv(Na, kTileCols);  // X = B walks A's rows
+  P.slices = static_cast<int>(cdiv(prefixes[n - 1], kSliceDims));
+  P.fwd_a = plan_split(P.rb_a, 1, P.tiles_a);
+  P.fwd_b = plan_split(P.rb_b, 1, P.tiles_b);
+  P.bwd_a = plan_split(P.rb_a, P.slices, P.tiles_a);
+  P.bwd_b = plan_split(P.rb_b, P.slices, P.tiles_b);
+  P.lda = cdiv(Na, 64) * 64;
+  P.ldb = cdiv(Nb, 64) * 64;
+
+  const size_t f = sizeof(float);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  P.o_rinv_a = take(f * n * Na);
+  P.o_rinv_b = take(f * n * Nb);
+  P.o_pos = take(f * n * P.nmin);
+  P.o_zr = take(f * n * Na);
+  P.o_zc = take(f * n * Nb);
+  P.o_fa = take(f * n * Na);
+  P.o_fb = take(f * n * Nb);
+  // row-statistic partials: forward (CLIP/ROWS), or the SigLIP loss sums
+  int slots_a = 2 * P.fwd_a.splits;
+  if (kind == KIND_SIGLIP && grads) slots_a = 2 * P.bwd_a.splits;
+  P.o_acc_a = take(f * n * Na * slots_a);
+  P.o_acc_b = take(kind == KIND_CLIP ? f * n * Nb * 2 * P.fwd_b.splits : 0);
+  P.o_crow_a = take(grads ? f * n * Na * 2 * P.bwd_a.splits : 0);
+  P.o_crow_b = take(grads ? f * n * Nb * 2 * P.bwd_b.splits : 0);
+  P.o_terms_a = take(f * n * Na);
+  P.o_terms_b = take(f * n * Nb);
+  P.o_loss = take(f * kMaxPrefix);
+  P.o_at = take(grads ? sizeof(uint16_t) * D * P.lda : 0);
+  P.o_bt = take(grads ? sizeof(uint16_t) * D * P.ldb : 0);
+  P.o_ga = take(grads && P.bwd_a.splits > 1 ? f * D * Na * P.bwd_a.splits : 0);
+  P.o_gb = take(grads && P.bwd_b.splits > 1 ? f * D * Nb * P.bwd_b.splits : 0);
+  P.total = o;
+  return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 2-D bf16 tensor map over a row-major [rows x cols] matrix with row stride ld
+// elements, 128-byte swizzle, box = [box_rows x 64 columns].
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+std::mutex g_init_mu;
+uint64_t g_init_mask = 0;  // devices already set up (device ordinal < 64)
+
+}  // namespace
+
+extern "C" {
+
+const char* uf_status_name(int status) {
+  switch (status) {
+    case UF_OK: return "ok";
+    case UF_INVALID_ARGUMENT: return "invalid-argument";
+    case UF_UNSUPPORTED: return "unsupported";
+    case UF_WORKSPACE_TOO_SMALL: return "workspace-too-small";
+    case UF_CUDA_ERROR: return "cuda-error";
+    case UF_DEVICE_TIMEOUT: return "device-timeout";
+    default: return "unknown";
+  }
+}
+
+int uf_contrastive_version(void) { return 100; }
+
+uf_status_t uf_contrastive_init(int device) {
+  std::lock_guard<std::mutex> lock(g_init_mu);
+  if (device < 0 || device >= 64) return UF_INVALID_ARGUMENT;
+  if (g_init_mask & (uint64_t(1) << device)) return UF_OK;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return UF_CUDA_ERROR;
+  if (cudaSetDevice(device) != cudaSuccess) return UF_CUDA_ERROR;
+  cudaDeviceProp prop;
+  uf_status_t st = UF_OK;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
+    st = UF_CUDA_ERROR;
+  } else if (tile_kernel_setup() != cudaSuccess || aux_kernels_setup() != cudaSuccess || !get_encode()) {
+    st = UF_CUDA_ERROR;
+  }
+  cudaSetDevice(prev);
+  if (st == UF_OK) g_init_mask |= uint64_t(1) << device;
+  return st;
+}
+
+size_t uf_contrastive_workspace_size(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix, int kind,
+                                     int want_grads) {
+  Plan P;
+  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, want_grads != 0, P)) return 0;
+  return P.total;
+}
+
+uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int64_t Nb, int D, const int* prefixes,
+                                   int n_prefix, int kind, float logit_scale, float bias,
+                                   const float* prefix_weights, float* loss_per_prefix, float* row_terms,
+                                   float* col_terms, float* dA, float* dB, void* workspace, size_t workspace_bytes,
+                                   int* device_status, void* stream_handle) {
+  // ---- argument checks (nothing is enqueued on failure)
+  if (!A || !B || !loss_per_prefix || !workspace) return UF_INVALID_ARGUMENT;
+  if ((dA == nullptr) != (dB == nullptr)) return UF_INVALID_ARGUMENT;
+  const bool grads = dA != nullptr;
+  Plan P;
+  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, grads, P)) return UF_INVALID_ARGUMENT;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(workspace, 256) || !aligned(loss_per_prefix, 4))
+    return UF_INVALID_ARGUMENT;
+  if (grads && (!aligned(dA, 16) || !aligned(dB, 16))) return UF_INVALID_ARGUMENT;
+  if ((row_terms && !aligned(row_terms, 4)) || (col_terms && !aligned(col_terms, 4))) return UF_INVALID_ARGUMENT;
+  if (!std::isfinite(logit_scale) || !std::isfinite(bias)) return UF_INVALID_ARGUMENT;
+  float w[kMaxPrefix];
+  for (int k = 0; k < kMaxPrefix; ++k) w[k] = 0.f;
+  for (int k = 0; k < n_prefix; ++k) {
+    w[k] = prefix_weights ? prefix_weights[k] : 1.f;
+    if (!std::isfinite(w[k])) return UF_INVALID_ARGUMENT;
+  }
+  if (kind == KIND_SIGLIP) {
+    if (std::fabs(logit_scale) + std::fabs(bias) > 80.f) return UF_UNSUPPORTED;
+  } else {
+    if (!(logit_scale > 0.f)) return UF_INVALID_ARGUMENT;
+    if (logit_scale > 40.f) return UF_UNSUPPORTED;
+  }
+  if (workspace_bytes < P.total) return UF_WORKSPACE_TOO_SMALL;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UF_CUDA_ERROR;
+  if (uf_contrastive_init(dev) != UF_OK) return UF_CUDA_ERROR;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  const uint16_t* A16 = static_cast<const uint16_t*>(A);
+  const uint16_t* B16 = static_cast<const uint16_t*>(B);
+  const int n = n_prefix;
+  const float log2e = 1.4426950408889634f;
+  const bool siglip = kind == KIND_SIGLIP;
+
+  // ---- tensor maps
+  CUtensorMap tmA, tmB, tmAt, tmBt;
+  if (!encode_map(&tmA, A, Na, D, D, kTileRows) || !encode_map(&tmB, B, Nb, D, D, kTileRows))
+    return UF_CUDA_ERROR;
+  uint16_t* At = reinterpret_cast<uint16_t*>(ws + P.o_at);
+  uint16_t* Bt = reinterpret_cast<uint16_t*>(ws + P.o_bt);
+  if (grads) {
+    if (!encode_map(&tmAt, At, D, Na, P.lda, kSliceDims) || !encode_map(&tmBt, Bt, D, Nb, P.ldb, kSliceDims))
+      return UF_CUDA_ERROR;
+  } else {
+    tmAt = tmA;
+    tmBt = tmB;
+  }
+
+  cudaError_t e;
+#define UF_CHECK(x)                 \
+  do {                              \
+    e = (x);                        \
+    if (e != cudaSuccess) return UF_CUDA_ERROR; \
+  } while (0)
+
+  // ---- 1. inverse norms, positives' cosines, transposed copies
+  PrepParams pp{};
+  pp.A = A16;
+  pp.B = B16;
+  pp.na = Na;
+  pp.nb = Nb;
+  pp.nmin = P.nmin;
+  pp.d = D;
+  pp.n_prefix = n;
+  for (int k = 0; k < n; ++k) pp.prefix_end[k] = prefixes[k];
+  pp.rinv_a = F(P.o_rinv_a);
+  pp.rinv_b = F(P.o_rinv_b);
+  pp.pos_cos = F(P.o_pos);
+  UF_CHECK(launch_prep(pp, stream));
+  if (grads) {
+    UF_CHECK(launch_transpose(A16, At, Na, D, P.lda, stream));
+    UF_CHECK(launch_transpose(B16, Bt, Nb, D, P.ldb, stream));
+  }
+
+  auto base_tile = [&](bool x_is_a) {
+    TileParams t{};
+    t.nx = x_is_a ? Na : Nb;
+    t.ny = x_is_a ? Nb : Na;
+    t.d = D;
+    t.n_prefix = n;
+    for (int k = 0; k < n; ++k) t.prefix_end[k] = prefixes[k];
+    t.n_col_tiles = static_cast<int>(x_is_a ? P.tiles_a : P.tiles_b);
+    t.L = logit_scale * log2e;
+    t.b2 = bias * log2e;
+    t.rinv_x = F(x_is_a ? P.o_rinv_a : P.o_rinv_b);
+    t.rinv_y = F(x_is_a ? P.o_rinv_b : P.o_rinv_a);
+    t.status = device_status;
+    return t;
+  };
+
+  float* terms_a = row_terms ? row_terms : F(P.o_terms_a);
+  float* terms_b = col_terms ? col_terms : F(P.o_terms_b);
+  StatsParams sp{};
+  sp.kind = kind;
+  sp.na = Na;
+  sp.nb = Nb;
+  sp.n_prefix = n;
+  for (int k = 0; k < n; ++k) {
+    sp.prefix_end[k] = prefixes[k];
+    sp.weight[k] = w[k];
+  }
+  sp.tau_or_t = logit_scale;
+  sp.bias = bias;
+  sp.rinv_a = F(P.o_rinv_a);
+  sp.rinv_b = F(P.o_rinv_b);
+  sp.pos_cos = F(P.o_pos);
+  sp.zr = F(P.o_zr);
+  sp.zc = F(P.o_zc);
+  sp.fa = F(P.o_fa);
+  sp.fb = F(P.o_fb);
+  sp.terms_a = terms_a;
+  sp.terms_b = terms_b;
+  sp.loss = loss_per_prefix;
+
+  // ---- 2. forward row statistics (all kinds without gradients; CLIP/ROWS with them)
+  if (!siglip || !grads) {
+    TileParams t = base_tile(true);
+    t.tiles_per_split = P.fwd_a.tiles_per_split;
+    t.rowacc = F(P.o_acc_a);
+    UF_CHECK(launch_tile(MODE_FWD, kind, tmA, tmB, tmB, t,
+                         dim3(static_cast<unsigned>(P.rb_a), P.fwd_a.splits, 1), stream));
+    sp.rowacc_a = t.rowacc;
+    sp.slots_a = 2 * P.fwd_a.splits;
+    if (kind == KIND_CLIP) {
+      TileParams tb = base_tile(false);
+      tb.tiles_per_split = P.fwd_b.tiles_per_split;
+      tb.rowacc = F(P.o_acc_b);
+      UF_CHECK(launch_tile(MODE_FWD, kind, tmB, tmA, tmA, tb,
+                           dim3(static_cast<unsigned>(P.rb_b), P.fwd_b.splits, 1), stream));
+      sp.rowacc_b = tb.rowacc;
+      sp.slots_b = 2 * P.fwd_b.splits;
+    }
+    UF_CHECK(launch_stats(sp, stream));
+  }
+  if (!grads) {
+    if (col_terms && kind != KIND_CLIP) UF_CHECK(cudaMemsetAsync(col_terms, 0, sizeof(float) * n * Nb, stream));
+    return UF_OK;
+  }
+
+  // ---- 3. backward: A side (X = A), then B side (X = B)
+  float* ga = P.bwd_a.splits > 1 ? F(P.o_ga) : dA;
+  float* gb = P.bwd_b.splits > 1 ? F(P.o_gb) : dB;
+  {
+    TileParams t = base_tile(true);
+    t.tiles_per_split = P.bwd_a.tiles_per_split;
+    t.alpha_x = siglip ? nullptr : F(P.o_fa);
+    t.beta_y = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
+    for (int k = 0; k < n; ++k) t.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
+    t.rowacc = F(P.o_acc_a);
+    t.crow = F(P.o_crow_a);
+    t.grad = ga;
+    UF_CHECK(launch_tile(MODE_BWD, kind, tmA, tmB, tmBt, t,
+                         dim3(static_cast<unsigned>(P.rb_a), P.bwd_a.splits, P.slices), stream));
+  }
+  if (siglip) {
+    sp.rowacc_a = F(P.o_acc_a);
+    sp.slots_a = 2 * P.bwd_a.splits;
+    UF_CHECK(launch_stats(sp, stream));
+  }
+  {
+    TileParams t = base_tile(false);
+    t.tiles_per_split = P.bwd_b.tiles_per_split;
+    t.alpha_x = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
+    t.beta_y = siglip ? nullptr : F(P.o_fa);
+    for (int k = 0; k < n; ++k) t.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
+    t.rowacc = F(P.o_acc_b);  // unused by the B side
+    t.crow = F(P.o_crow_b);
+    t.grad = gb;
+    UF_CHECK(launch_tile(MODE_BWD, kind, tmB, tmA, tmAt, t,
+                         dim3(static_cast<unsigned>(P.rb_b), P.bwd_b.splits, P.slices), stream));
+  }
+
+  // ---- 4. projection term and diagonal correction
+  for (int side = 0; side < 2; ++side) {
+    const bool xa = side == 0;
+    NormBwdParams q{};
+    q.kind = kind;
+    q.nx = xa ? Na : Nb;
+    q.ny = xa ? Nb : Na;
+    q.nmin = P.nmin;
+    q.n_total = Na;
+    q.d = D;
+    q.n_prefix = n;
+    for (int k = 0; k < n; ++k) {
+      q.prefix_end[k] = prefixes[k];
+      q.weight[k] = w[k];
+    }
+    q.tau_or_t = logit_scale;
+    q.bias = bias;
+    q.X = xa ? A16 : B16;
+    q.Y = xa ? B16 : A16;
+    q.rinv_x = F(xa ? P.o_rinv_a : P.o_rinv_b);
+    q.rinv_y = F(xa ? P.o_rinv_b : P.o_rinv_a);
+    q.pos_cos = F(P.o_pos);
+    q.z_x = F(xa ? P.o_zr : P.o_zc);
+    q.z_y = F(xa ? P.o_zc : P.o_zr);
+    if (kind == KIND_ROWS) {
+      q.x_is_query = xa ? 1 : 0;
+      q.z_x = F(P.o_zr);
+      q.z_y = F(P.o_zr);
+    }
+    q.crow = F(xa ? P.o_crow_a : P.o_crow_b);
+    q.crow_slots = 2 * (xa ? P.bwd_a.splits : P.bwd_b.splits);
+    q.G = xa ? ga : gb;
+    q.g_splits = xa ? P.bwd_a.splits : P.bwd_b.splits;
+    q.dX = xa ? dA : dB;
+    UF_CHECK(launch_norm_bwd(q, stream));
+  }
+  if (col_terms && kind != KIND_CLIP) UF_CHECK(cudaMemsetAsync(col_terms, 0, sizeof(float) * n * Nb, stream));
+#undef UF_CHECK
+  return UF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,130 @@
+/*
+ * uf_contrastive.h -- C ABI of a GB300 (sm_103a) library for the batched Matryoshka
+ * contrastive loss, forward and backward, on one GPU.
+ *
+ * What it computes.  Two bf16 embedding matrices A (Na x D) and B (Nb x D), row-major
+ * with row stride D, are scored all-against-all at nested prefixes p_1 < ... < p_n of
+ * the embedding (the Matryoshka ladder {64, 128, 256, 512, 1024}: UForm README,
+ * "Matryoshka" paragraph; blog "Scaling-Up Contrastive Learning over NVLink
+ * Multicast", section "One Set or Two").  For each prefix p every row is
+ * L2-normalised on its first p dimensions, cos_ij = <a_i[:p], b_j[:p]> / (|a_i[:p]| |b_j[:p]|),
+ * and one of three losses is applied:
+ *   UF_LOSS_CLIP_SYMMETRIC  s = scale * cos; L_p = 1/2 (mean_i CE_row(i) + mean_j CE_col(j)),
+ *                           positives on the diagonal (Na == Nb).  The blog, section
+ *                           "One Set or Two": CLIP turns each row of cosines into a
+ *                           softmax over the batch; the symmetric form adds the columns.
+ *   UF_LOSS_SIGLIP          x = scale * cos + bias; L_p = -(1/N) sum_ij log sigmoid(z_ij x_ij),
+ *                           z = +1 on the diagonal, -1 elsewhere (Na == Nb).  The blog's
+ *                           SigLIP equation, same section.
+ *   UF_LOSS_INFONCE_ROWS    L_p = mean_{i<Na} CE over all Nb keys of row i, the positive
+ *                           of query i being key i (Nb >= Na).
+ * The gradients returned are those of sum_p w_p L_p (w_p = 1 unless given).
+ * Precision policy (UForm README, "Training is BF16"): operands bf16, products and
+ * every accumulation fp32, gradients fp32.  The Na x Nb logits are never stored.
+ *
+ * Conventions (UForm Swift binding page, sections "Errors" and "Design": one C verb per
+ * operation named <lib>_<noun>_<verb>, an enum status with a name function; section
+ * "Arenas": the caller owns every output and the scratch, and nothing is allocated on
+ * the call path).  All entry points are thread-safe; a call only enqueues work on the
+ * caller's stream and returns without synchronising, so it can be captured in a CUDA
+ * graph.  Calls on different streams are independent as long as each has its own
+ * workspace and outputs.
+ */
+#ifndef UF_CONTRASTIVE_H_
+#define UF_CONTRASTIVE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define UF_API __attribute__((visibility("default")))
+#else
+#define UF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  UF_DEVICE_TIMEOUT is only ever written to *device_status by a kernel
+ * whose bounded wait ran out; the host-side call itself never returns it. */
+typedef enum uf_status {
+  UF_OK = 0,
+  UF_INVALID_ARGUMENT = 1,    /* null pointer, bad size, misaligned pointer, bad prefix ladder */
+  UF_UNSUPPORTED = 2,         /* valid request this build does not implement (e.g. scale > 40) */
+  UF_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < uf_contrastive_workspace_size(...) */
+  UF_CUDA_ERROR = 4,          /* a CUDA runtime call or kernel launch failed */
+  UF_DEVICE_TIMEOUT = 5       /* a kernel gave up a bounded wait (read from *device_status) */
+} uf_status_t;
+
+typedef enum uf_loss_kind {
+  UF_LOSS_CLIP_SYMMETRIC = 0,
+  UF_LOSS_SIGLIP = 1,
+  UF_LOSS_INFONCE_ROWS = 2
+} uf_loss_kind_t;
+
+/* Static spelling of a status ("ok", "invalid-argument", ...); "unknown" otherwise. */
+UF_API const char* uf_status_name(int status);
+
+/* Version of this library as major*10000 + minor*100 + patch. */
+UF_API int uf_contrastive_version(void);
+
+/*
+ * Load every kernel of the library on `device` and set their shared-memory limits.
+ * Idempotent.  Calling it once per device before the first uf_contrastive_fwd_bwd (and
+ * before any stream capture) keeps lazy module loading off the hot path; the blog's
+ * section "Across the Box" describes the host blocking on lazy loading inside a step.
+ * Returns UF_CUDA_ERROR when the device is absent or is not sm_103.
+ */
+UF_API uf_status_t uf_contrastive_init(int device);
+
+/*
+ * Bytes of device scratch that uf_contrastive_fwd_bwd needs for these arguments
+ * (a pure function of the arguments; 0 when they are invalid).  want_grads != 0 sizes
+ * the workspace for the backward as well.
+ */
+UF_API size_t uf_contrastive_workspace_size(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix,
+                                     int kind, int want_grads);
+
+/*
+ * Forward and (optionally) backward of the Matryoshka contrastive loss.
+ *
+ *   A, B            device, bf16, row-major Na x D and Nb x D, 16-byte aligned.
+ *   Na, Nb, D       rows and width.  D is a multiple of 64 and <= 4096; Na, Nb >= 1.
+ *                   CLIP and SigLIP need Na == Nb; ROWS needs Nb >= Na.
+ *   prefixes        host, n_prefix strictly increasing multiples of 64, last <= D.
+ *   n_prefix        1..8.
+ *   kind            a uf_loss_kind_t.
+ *   logit_scale     CLIP/ROWS: tau in s = tau * cos, 0 < tau <= 40 (the forward uses the
+ *                   fixed shift s - tau, exact while e^{-2 tau} is a normal float; larger
+ *                   tau returns UF_UNSUPPORTED).  SigLIP: t in x = t cos + b, |t| + |b| <= 80.
+ *   bias            SigLIP b; ignored otherwise.
+ *   prefix_weights  host, n_prefix weights w_p of the gradient, or NULL for all 1.
+ *   loss_per_prefix device fp32 [n_prefix]: the unweighted L_p.
+ *   row_terms       device fp32 [n_prefix][Na] or NULL: per-row terms whose mean is the
+ *                   row half of L_p (CLIP: LSE_j s_ij - s_ii; ROWS: the same; SigLIP:
+ *                   sum_j softplus(-z_ij x_ij), so L_p = mean_i row_terms).
+ *   col_terms       device fp32 [n_prefix][Nb] or NULL: CLIP only (LSE_i s_ij - s_jj);
+ *                   written as 0 for the other kinds.
+ *   dA, dB          device fp32 Na x D / Nb x D, 16-byte aligned, or both NULL for a
+ *                   forward-only call.  Columns at or past the last prefix are written 0.
+ *   workspace       device scratch of workspace_bytes >= uf_contrastive_workspace_size(),
+ *                   256-byte aligned.  Owned by the caller; one call at a time per workspace.
+ *   device_status   device int or NULL.  Kernels that give up a bounded wait store
+ *                   UF_DEVICE_TIMEOUT there (it is never cleared by the library).
+ *   stream          a cudaStream_t (0 = legacy default stream).
+ * Zero-norm prefixes use 1/max(|x|, 1e-30) as their inverse norm.
+ * Argument errors are found on the host before anything is enqueued; the outputs are then
+ * untouched.  Launch failures return UF_CUDA_ERROR; outputs are then unspecified.
+ */
+UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
+                                   const int* prefixes, int n_prefix, int kind, float logit_scale, float bias,
+                                   const float* prefix_weights, float* loss_per_prefix, float* row_terms,
+                                   float* col_terms, float* dA, float* dB, void* workspace,
+                                   size_t workspace_bytes, int* device_status, void* stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* UF_CONTRASTIVE_H_ */

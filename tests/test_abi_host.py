@@ -1,0 +1,110 @@
+"""Host-side tests of the C ABI (no GPU needed): exports, workspace sizing, argument checks."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from contrastive_embedding_loss_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LADDER = (64, 128, 256, 512, 1024)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            txt = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"UF_API\s+[\w\s\*]+?\b(uf_\w+)\s*\(", txt))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"uf_contrastive_fwd_bwd", "uf_contrastive_workspace_size", "uf_contrastive_init",
+            "uf_status_name", "uf_contrastive_version"} <= names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_names(lib):
+    assert binding.uf_status_name(0) == "ok"
+    assert binding.uf_status_name(1) == "invalid-argument"
+    assert binding.uf_status_name(5) == "device-timeout"
+    assert binding.uf_status_name(99) == "unknown"
+    assert binding.uf_contrastive_version() == 100
+
+
+def test_workspace_size(lib):
+    ws = binding.uf_contrastive_workspace_size
+    assert ws(256, 256, 1024, LADDER, 0, 1) > 0
+    assert ws(256, 256, 1024, LADDER, 0, 1) >= ws(256, 256, 1024, LADDER, 0, 0)
+    # invalid requests size to 0
+    assert ws(256, 255, 1024, LADDER, 0, 1) == 0      # CLIP needs Na == Nb
+    assert ws(256, 100, 1024, LADDER, 2, 1) == 0      # ROWS needs Nb >= Na
+    assert ws(256, 256, 1000, LADDER, 0, 1) == 0      # D not a multiple of 64
+    assert ws(256, 256, 1024, (64, 100), 0, 1) == 0   # prefix not a multiple of 64
+    assert ws(256, 256, 1024, (128, 64), 0, 1) == 0   # not increasing
+    assert ws(256, 256, 512, LADDER, 0, 1) == 0       # last prefix > D
+    assert ws(256, 256, 1024, tuple(range(64, 64 * 10, 64)), 0, 1) == 0  # > 8 prefixes
+    assert ws(0, 0, 1024, LADDER, 0, 1) == 0
+    assert ws(256, 256, 1024, LADDER, 7, 1) == 0      # unknown kind
+    # pure function of the arguments, and it grows with the batch
+    assert ws(4096, 4096, 1024, LADDER, 0, 1) == ws(4096, 4096, 1024, LADDER, 0, 1)
+    assert ws(65536, 65536, 1024, LADDER, 0, 1) > ws(4096, 4096, 1024, LADDER, 0, 1)
+    # the N=65536 backward fits comfortably in HBM
+    assert ws(65536, 65536, 1024, LADDER, 0, 1) < 2 << 30
+
+
+FAKE = 1 << 20  # a 256-byte aligned fake device address; these calls return before any CUDA call
+
+
+def _call(**kw):
+    args = dict(A=FAKE, B=FAKE, Na=256, Nb=256, D=1024, prefixes=LADDER, kind=0, logit_scale=1 / 0.07, bias=0.0,
+                prefix_weights=None, loss_per_prefix=FAKE, row_terms=None, col_terms=None, dA=FAKE, dB=FAKE,
+                workspace=FAKE, workspace_bytes=1 << 40, device_status=None, stream=None)
+    args.update(kw)
+    return binding.uf_contrastive_fwd_bwd(**args)
+
+
+def test_argument_errors_are_found_on_the_host(lib):
+    INV, UNS, WS = 1, 2, 3
+    assert _call(A=None) == INV
+    assert _call(loss_per_prefix=None) == INV
+    assert _call(workspace=None) == INV
+    assert _call(dB=None) == INV                      # dA and dB go together
+    assert _call(A=FAKE + 2) == INV                   # misaligned
+    assert _call(workspace=FAKE + 16) == INV          # workspace must be 256-byte aligned
+    assert _call(dA=FAKE + 4) == INV
+    assert _call(Nb=255) == INV
+    assert _call(prefixes=(64, 64)) == INV
+    assert _call(kind=3) == INV
+    assert _call(logit_scale=-1.0) == INV
+    assert _call(logit_scale=float("nan")) == INV
+    assert _call(prefix_weights=[1, 1, float("inf"), 1, 1]) == INV
+    assert _call(logit_scale=100.0) == UNS            # beyond the fixed-shift range
+    assert _call(kind=1, logit_scale=70.0, bias=-20.0) == UNS
+    assert _call(workspace_bytes=1024) == WS
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call() == 4  # UF_CUDA_ERROR, raised by the first CUDA runtime call
+    assert binding.uf_contrastive_init(0) == 4
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(ImportError):
+        binding.load(str(tmp_path / "nope.so"))

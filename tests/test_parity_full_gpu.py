@@ -1,0 +1,137 @@
+"""Parity at the full benchmark sizes, in the launch configuration the benchmark times.
+
+Where the oracle can compute an output one row at a time, it does so on seeded samples
+(per-row loss terms of 512 rows / columns, SigLIP and row-InfoNCE gradient rows, whose
+normalisers are row-local).  Outputs that need every normaliser of the batch at once
+(CLIP gradients at N = 65536) are checked through properties that hold at any size:
+the per-row Euler identity sum_d x_d dL/dx_d = 0 of a scale-invariant loss, the mean of
+the row terms equalling the loss, and A <-> B swap symmetry.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from contrastive_embedding_loss_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+LADDER = (64, 128, 256, 512, 1024)
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from contrastive_embedding_loss_gb300 import binding
+
+    assert binding.uf_contrastive_init(0) == 0
+    return binding
+
+
+def dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run(binding, kind, A16, B16, scale, bias):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = binding.contrastive_fwd_bwd(dev(A16), dev(B16), kind, LADDER, scale, bias, grads=True, terms=True,
+                                      device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out
+
+
+def sample(n, k, seed):
+    return np.sort(np.random.default_rng(seed).choice(n, size=min(k, n), replace=False))
+
+
+def check_terms(got, ref, what):
+    err = np.abs(got - ref).max()
+    assert err <= 2e-3 * np.abs(ref).max(), f"{what}: err {err:.3e} vs max {np.abs(ref).max():.3e}"
+
+
+def check_grad_rows(got, ref, what):
+    err = np.abs(got - ref).max()
+    assert err <= 1e-2 * np.abs(ref).max(), f"{what}: err {err:.3e} vs max {np.abs(ref).max():.3e}"
+
+
+def check_loss_is_mean_of_terms(out, kind):
+    loss = out["loss"].double().cpu().numpy()
+    rt = out["row_terms"].double().mean(dim=1).cpu().numpy()
+    if kind == "clip":
+        rt = 0.5 * (rt + out["col_terms"].double().mean(dim=1).cpu().numpy())
+    np.testing.assert_allclose(loss, rt, rtol=1e-5)
+
+
+def check_euler(X16, G, what):
+    x = torch.from_numpy(synth.bf16_bits_to_float(X16)).cuda().double()
+    g = G.double()
+    dot = (x * g).sum(dim=1).abs()
+    bound = 2e-3 * x.norm(dim=1) * g.norm(dim=1) + 1e-30
+    frac = (dot / bound).max().item()
+    assert frac <= 1.0, f"{what}: Euler identity off by {frac:.2f} x tolerance"
+
+
+def test_clip_n4096_full_oracle(ctx):
+    kind, A16, B16, s, b = synth.workload("clip_n4096")
+    out = run(ctx, kind, A16, B16, s, b)
+    ref = oracle.fwd_bwd(kind, A16, B16, LADDER, s, b)
+    got = {k: v.double().cpu().numpy() for k, v in out.items()}
+    assert (np.abs(got["loss"] - ref["loss"]) / ref["loss"]).max() <= 2e-3
+    check_terms(got["row_terms"], ref["row_terms"], "row terms")
+    check_terms(got["col_terms"], ref["col_terms"], "col terms")
+    check_grad_rows(got["dA"], ref["dA"], "dA")
+    check_grad_rows(got["dB"], ref["dB"], "dB")
+
+
+def test_siglip_n16384_sampled(ctx):
+    kind, A16, B16, s, b = synth.workload("siglip_n16384")
+    out = run(ctx, kind, A16, B16, s, b)
+    check_loss_is_mean_of_terms(out, kind)
+    rows = sample(A16.shape[0], 512, 1)
+    ref_terms = oracle.row_terms_sampled(kind, A16, B16, LADDER, s, b, rows)
+    check_terms(out["row_terms"][:, rows].double().cpu().numpy(), ref_terms, "row terms")
+    gA = oracle.grad_rows(kind, True, A16, B16, LADDER, s, b, rows)
+    check_grad_rows(out["dA"][rows].double().cpu().numpy(), gA, "dA rows")
+    cols = sample(B16.shape[0], 512, 2)
+    gB = oracle.grad_rows(kind, False, B16, A16, LADDER, s, b, cols)
+    check_grad_rows(out["dB"][cols].double().cpu().numpy(), gB, "dB rows")
+
+
+def test_clip_n65536_sampled_and_properties(ctx):
+    kind, A16, B16, s, b = synth.workload("clip_n65536_hardneg")
+    out = run(ctx, kind, A16, B16, s, b)
+    check_loss_is_mean_of_terms(out, kind)
+    rows = sample(A16.shape[0], 512, 3)
+    check_terms(out["row_terms"][:, rows].double().cpu().numpy(),
+                oracle.row_terms_sampled(kind, A16, B16, LADDER, s, b, rows), "row terms")
+    cols = sample(B16.shape[0], 512, 4)
+    check_terms(out["col_terms"][:, cols].double().cpu().numpy(),
+                oracle.row_terms_sampled(kind, B16, A16, LADDER, s, b, cols), "col terms")
+    check_euler(A16, out["dA"], "dA")
+    check_euler(B16, out["dB"], "dB")
+    assert torch.all(out["dA"][:, LADDER[-1]:] == 0) if A16.shape[1] > LADDER[-1] else True
+    # swap symmetry: CLIP(B, A) has the same loss and exchanges the gradients
+    sw = run(ctx, kind, B16, A16, s, b)
+    np.testing.assert_allclose(sw["loss"].cpu().numpy(), out["loss"].cpu().numpy(), rtol=1e-4)
+    for g1, g2, what in ((sw["dA"], out["dB"], "dA<->dB"), (sw["dB"], out["dA"], "dB<->dA")):
+        err = (g1 - g2).abs().max().item()
+        assert err <= 1e-2 * g2.abs().max().item(), what
+
+
+def test_rows_q8192_k262144_sampled(ctx):
+    kind, Q16, K16, s, b = synth.workload("rows_q8192_k262144")
+    out = run(ctx, kind, Q16, K16, s, b)
+    check_loss_is_mean_of_terms(out, kind)
+    assert torch.all(out["col_terms"] == 0)
+    rows = sample(Q16.shape[0], 128, 5)
+    lse, pos = oracle.row_stats(kind, Q16, K16, LADDER, s, b, rows)
+    check_terms(out["row_terms"][:, rows].double().cpu().numpy(), (lse - pos).T, "query terms")
+    grows = rows[:64]
+    lse_full = np.zeros((len(LADDER), Q16.shape[0]))
+    lse_full[:, grows] = lse[:64].T
+    gQ = oracle.grad_rows(kind, True, Q16, K16, LADDER, s, b, grows, lse_x=lse_full)
+    check_grad_rows(out["dA"][grows].double().cpu().numpy(), gQ, "query gradient rows")
+    check_euler(Q16, out["dA"], "dA")
+    check_euler(K16, out["dB"], "dB")

@@ -1,0 +1,128 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Tolerances (the acceptance bar of the Matryoshka loss build): per-prefix loss relative
+error <= 2e-3; gradient max-abs error <= 1e-2 * max|grad|.  Per-row terms are held to
+2e-3 of the largest term.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from contrastive_embedding_loss_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+LADDER = (64, 128, 256, 512, 1024)
+LOSS_RTOL = 2e-3
+GRAD_FRAC = 1e-2
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from contrastive_embedding_loss_gb300 import binding
+
+    assert binding.uf_contrastive_init(0) == 0
+    return binding
+
+
+def dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run(binding, kind, A16, B16, pre, scale, bias, weights=None, grads=True):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = binding.contrastive_fwd_bwd(dev(A16), dev(B16), kind, pre, scale, bias, weights, grads=grads, terms=True,
+                                      device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "a kernel reported a timeout"
+    return {k: v.double().cpu().numpy() for k, v in out.items()}
+
+
+def check_loss(got, ref):
+    rel = np.abs(got - ref) / np.abs(ref)
+    assert rel.max() <= LOSS_RTOL, f"loss {got} vs oracle {ref} (rel {rel})"
+
+
+def check_grad(got, ref, what):
+    err = np.abs(got - ref).max()
+    scale = np.abs(ref).max()
+    assert err <= GRAD_FRAC * scale, f"{what}: max-abs err {err:.3e} > {GRAD_FRAC} * {scale:.3e}"
+
+
+def check_terms(got, ref, what):
+    err = np.abs(got - ref).max()
+    assert err <= LOSS_RTOL * max(np.abs(ref).max(), 1e-30), f"{what}: err {err:.3e}"
+
+
+def make(kind, Na, Nb, D, seed, noise):
+    if kind == "rows":
+        return synth.queries_keys(Na, Nb, D, noise, seed)
+    return synth.paired(Na, D, noise, seed)
+
+
+SMALL = [
+    # kind, Na, Nb, D, prefixes, scale, bias, noise, seed
+    ("clip", 256, 256, 1024, LADDER, 1 / 0.07, 0.0, 1.0, 0),     # the N=256 benchmark configuration itself
+    ("clip", 300, 300, 1024, LADDER, 1 / 0.07, 0.0, 1.0, 11),    # ragged tail (300 = 2*128 + 44)
+    ("clip", 640, 640, 1024, LADDER, 1 / 0.07, 0.0, 1.0, 12),    # five tiles per row
+    ("siglip", 300, 300, 1024, LADDER, 10.0, -10.0, 0.7, 13),
+    ("siglip", 512, 512, 1024, LADDER, 10.0, -10.0, 0.7, 14),
+    ("rows", 200, 700, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 15),     # ragged queries and keys
+    ("clip", 257, 257, 384, (64, 192, 384), 5.0, 0.0, 1.0, 16),   # another ladder; partial gradient slice
+    ("clip", 130, 130, 1024, (1024,), 1 / 0.07, 0.0, 1.0, 17),    # one prefix
+    ("siglip", 200, 200, 640, (128, 320, 512), 4.0, -2.0, 0.7, 18),  # last prefix < D: zero tail columns
+    ("rows", 1, 300, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 19),       # one query
+    ("clip", 192, 192, 1024, LADDER, 40.0, 0.0, 3.0, 21),         # the largest supported tau
+]
+
+
+@pytest.mark.parametrize("kind,Na,Nb,D,pre,scale,bias,noise,seed", SMALL)
+def test_parity_small(ctx, kind, Na, Nb, D, pre, scale, bias, noise, seed):
+    A16, B16 = make(kind, Na, Nb, D, seed, noise)
+    w = np.linspace(0.5, 1.5, len(pre))
+    got = run(ctx, kind, A16, B16, pre, scale, bias, weights=list(w))
+    ref = oracle.fwd_bwd(kind, A16, B16, pre, scale, bias, w)
+    check_loss(got["loss"], ref["loss"])
+    check_terms(got["row_terms"], ref["row_terms"], "row terms")
+    check_terms(got["col_terms"], ref["col_terms"], "col terms")
+    check_grad(got["dA"], ref["dA"], "dA")
+    check_grad(got["dB"], ref["dB"], "dB")
+    assert np.all(got["dA"][:, pre[-1]:] == 0) and np.all(got["dB"][:, pre[-1]:] == 0)
+
+
+def test_forward_only_matches(ctx):
+    A16, B16 = make("clip", 300, 300, 1024, 31, 1.0)
+    full = run(ctx, "clip", A16, B16, LADDER, 1 / 0.07, 0.0)
+    fwd = run(ctx, "clip", A16, B16, LADDER, 1 / 0.07, 0.0, grads=False)
+    assert np.array_equal(full["loss"], fwd["loss"])
+    S16, T16 = make("siglip", 300, 300, 1024, 32, 0.7)
+    ref = oracle.fwd_bwd("siglip", S16, T16, LADDER, 10.0, -10.0, grads=False)
+    check_loss(run(ctx, "siglip", S16, T16, LADDER, 10.0, -10.0, grads=False)["loss"], ref["loss"])
+
+
+def test_identical_embeddings_give_ln_n(ctx):
+    v = np.random.default_rng(0).standard_normal(1024)
+    A16 = synth.round_to_bf16_bits(np.tile(v, (384, 1)))
+    got = run(ctx, "clip", A16, A16, LADDER, 1 / 0.07, 0.0)
+    np.testing.assert_allclose(got["loss"], np.log(384), rtol=LOSS_RTOL)
+    scale = np.abs(run(ctx, "clip", *make("clip", 384, 384, 1024, 3, 1.0), LADDER, 1 / 0.07, 0.0)["dA"]).max()
+    assert np.abs(got["dA"]).max() <= GRAD_FRAC * scale
+
+
+def test_single_pair(ctx):
+    """N = 1: the only logit is the positive, so L = 0 and every gradient vanishes."""
+    A16, B16 = make("clip", 1, 1, 128, 20, 1.0)
+    got = run(ctx, "clip", A16, B16, (64, 128), 1 / 0.07, 0.0)
+    assert np.abs(got["loss"]).max() < 1e-5
+    assert np.abs(got["dA"]).max() < 1e-6 and np.abs(got["dB"]).max() < 1e-6
+
+
+def test_deterministic(ctx):
+    A16, B16 = make("clip", 640, 640, 1024, 40, 1.0)
+    r1 = run(ctx, "clip", A16, B16, LADDER, 1 / 0.07, 0.0)
+    r2 = run(ctx, "clip", A16, B16, LADDER, 1 / 0.07, 0.0)
+    for k in r1:
+        assert np.array_equal(r1[k], r2[k]), k
