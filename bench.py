@@ -1,0 +1,350 @@
+"""Benchmark: Matryoshka contrastive loss forward+backward on one GB300 (or N replicas).
+
+A step is one call of uf_contrastive_fwd_bwd over one batch: inverse norms, forward row
+statistics, loss, backward score recompute + gradient GEMMs, projection -- every step of
+the path.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the float64 CPU oracle on the host cores instead (the reference
+arm: there is no runnable reference implementation of this path).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd pairs/s at 5 prefixes (N=65536, D=1024 bf16); TFLOP/s vs bf16 peak"
+LADDER = (64, 128, 256, 512, 1024)
+DEFAULT_WORKLOAD = "clip_n65536_hardneg"
+ORACLE_SAMPLE_PAIRS = 2048      # cpu_baseline: oracle on the first 2048 pairs (about 10-30 s)
+REFERENCE_STEP_PAIRS = 1024     # --impl reference: oracle on the first 1024 pairs per step
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def pairs_of(w, A16):
+    return A16.shape[0]  # CLIP/SigLIP: N pairs; ROWS: Nq queries
+
+
+def credited_flops(kind, Na, Nb, D):
+    # forward S + backward S + dA + dB for InfoNCE (S is needed twice); SigLIP skips the forward
+    return (6 if kind == "siglip" else 8) * Na * Nb * D
+
+
+def executed_flops(kind, Na, Nb, D):
+    return (8 if kind == "siglip" else 10) * Na * Nb * D
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def sub_batch(kind, A16, B16, n):
+    # the first n pairs (for ROWS: the first n queries and their n positive keys)
+    return A16[:n], B16[:n]
+
+
+def oracle_rate(kind, A16, B16, scale, bias, n_sample):
+    """Time the oracle on a sub-batch and scale its time to the full batch by cells (N^2)."""
+    import oracle
+
+    a, b = sub_batch(kind, A16, B16, n_sample)
+    t0 = time.perf_counter()
+    oracle.fwd_bwd(kind, a, b, LADDER, scale, bias)
+    dt = time.perf_counter() - t0
+    full_cells = A16.shape[0] * B16.shape[0]
+    cells = a.shape[0] * b.shape[0]
+    t_full = dt * full_cells / cells
+    return pairs_of(None, A16) / t_full, dt, a.shape[0], b.shape[0]
+
+
+def omp_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v else (os.cpu_count() or 1)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.out = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            txt, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            txt = ""
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in txt.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def csrc_digest():
+    h = hashlib.sha1()
+    d = os.path.join(ROOT, "contrastive_embedding_loss_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """Per-launch DRAM bytes of the dominant kernel from a committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("csrc_digest") != csrc_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def dist_setup(n_gpus):
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier_max(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the float64 oracle on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    from contrastive_embedding_loss_gb300 import synth
+
+    kind, A16, B16, scale, bias = synth.workload(args.workload)
+    rates = []
+    for i in range(args.warmup + args.steps):
+        r, dt, na, nb = oracle_rate(kind, A16, B16, scale, bias, REFERENCE_STEP_PAIRS)
+        if i >= args.warmup:
+            rates.append((r, dt))
+    value = float(np.mean([r for r, _ in rates]))
+    N, D = A16.shape[0], A16.shape[1]
+    full_t = pairs_of(None, A16) / value
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * full_t, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "kind": kind, "Na": int(N), "Nb": int(B16.shape[0]), "D": int(D),
+                   "prefixes": list(LADDER)},
+        "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": omp_threads(), "kind": "oracle",
+                         "sample": f"float64 oracle fwd+bwd on the first {REFERENCE_STEP_PAIRS} pairs per step; "
+                                   f"time scaled to the full batch by cells ({N}x{B16.shape[0]})"},
+        "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+
+    from contrastive_embedding_loss_gb300 import binding, synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    assert binding.uf_contrastive_init(local) == binding.UF_OK
+
+    kind, A16, B16, scale, bias = synth.workload(args.workload)
+    Na, D = A16.shape
+    Nb = B16.shape[0]
+    k = binding.KINDS[kind]
+    n = len(LADDER)
+    to_t = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    A_h, B_h = to_t(A16).pin_memory(), to_t(B16).pin_memory()
+    A_d, B_d = A_h.to(dev), B_h.to(dev)
+    ws_bytes = binding.uf_contrastive_workspace_size(Na, Nb, D, LADDER, k, True)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    loss = torch.empty(n, dtype=torch.float32, device=dev)
+    dA = torch.empty((Na, D), dtype=torch.float32, device=dev)
+    dB = torch.empty((Nb, D), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    loss_h = torch.empty(n, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def step(a_ptr, b_ptr):
+        st = binding.uf_contrastive_fwd_bwd(a_ptr, b_ptr, Na, Nb, D, LADDER, k, scale, bias, None, loss.data_ptr(),
+                                            None, None, dA.data_ptr(), dB.data_ptr(), ws.data_ptr(), ws_bytes,
+                                            status.data_ptr(), stream.cuda_stream)
+        if st != binding.UF_OK:
+            raise binding.UfError(st, "uf_contrastive_fwd_bwd")
+
+    # ---- device-resident timing (inputs 2 x Na*D*2 bytes, larger than the 129 MB L2 at N=65536)
+    for _ in range(args.warmup):
+        step(A_d.data_ptr(), B_d.data_ptr())
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    binding.uf_contrastive_profile(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(A_d.data_ptr(), B_d.data_ptr())
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms_local = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    prof = {binding.KERNEL_GROUPS[g]: binding.uf_contrastive_profile_read(g) for g in range(len(binding.KERNEL_GROUPS))}
+    binding.uf_contrastive_profile(False)
+    assert int(status.item()) == 0, "a kernel reported a timeout"
+    ms = barrier_max(ms_local, world)
+    ms_step = ms / args.steps
+    units = pairs_of(None, A16)
+    value = units * world * args.steps / (ms / 1e3)
+
+    # ---- end to end through the public API with host buffers: H2D inputs, D2H loss, every step
+    for _ in range(2):
+        A_d.copy_(A_h, non_blocking=True)
+        B_d.copy_(B_h, non_blocking=True)
+        step(A_d.data_ptr(), B_d.data_ptr())
+        loss_h.copy_(loss, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        A_d.copy_(A_h, non_blocking=True)
+        B_d.copy_(B_h, non_blocking=True)
+        step(A_d.data_ptr(), B_d.data_ptr())
+        loss_h.copy_(loss, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = barrier_max(ev0.elapsed_time(ev1), world)
+    e2e_value = units * world * args.steps / (ms_e2e / 1e3)
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    # dominant kernel by device time
+    dom = max(prof, key=lambda g: prof[g][0])
+    dom_ms, dom_pairs, dom_launches = prof[dom]
+    per_launch_ms = dom_ms / max(dom_pairs, 1)
+    if dom == "bwd_tile":
+        alg = 4.0 * Na * Nb * D  # score recompute (2 Nx Ny D) + gradient GEMM (2 Nx Ny D) per side
+    elif dom == "fwd_tile":
+        alg = 2.0 * Na * Nb * D
+    else:
+        alg = None
+    roof = None
+    if alg is not None:
+        achieved = alg / (per_launch_ms / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": ncu_traffic(args.workload),
+                "peak_source": f"{peak_src} bf16_tflops_sustained",
+                "algorithmic_flops_per_launch": alg, "ms_per_launch": per_launch_ms,
+                "share_of_step": dom_ms / ms_local}
+    cflops = credited_flops(kind, Na, Nb, D)
+    line = {
+        "metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "kind": kind, "Na": int(Na), "Nb": int(Nb), "D": int(D),
+                   "prefixes": list(LADDER), "logit_scale": scale, "bias": bias,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "tflops_credited": cflops / (ms_step / 1e3) / 1e12,
+        "tflops_executed": executed_flops(kind, Na, Nb, D) / (ms_step / 1e3) / 1e12,
+        "frac_credited_of_bf16_peak": cflops / (ms_step / 1e3) / 1e12 / peak_tf,
+        "roofline": roof,
+        "kernels_ms_per_step": {g: prof[g][0] / args.steps for g in prof},
+        "gpu_launches": int(sum(prof[g][2] for g in prof)),
+        "e2e": {"value": e2e_value, "unit": "pairs/s", "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
+                "d2h_bytes_per_step": int(loss_h.numel() * 4), "ms_per_step": ms_e2e / args.steps},
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        r, dt, na, nb = oracle_rate(kind, A16, B16, scale, bias, ORACLE_SAMPLE_PAIRS)
+        line["cpu_baseline"] = {"value": r, "unit": "pairs/s", "cores": omp_threads(), "kind": "oracle",
+                                "sample": f"float64 oracle fwd+bwd on the first {na}x{nb} pairs ({dt:.1f} s); "
+                                          f"time scaled to {Na}x{Nb} by cells"}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

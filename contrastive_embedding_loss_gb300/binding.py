@@ -56,6 +56,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.uf_contrastive_fwd_bwd.argtypes = [P, P, I64, I64, I32, P, I32, I32, F32, F32, P, P, P, P, P, P, P, SZ,
                                            P, P]
     lib.uf_contrastive_fwd_bwd.restype = I32
+    lib.uf_contrastive_profile.argtypes = [I32]
+    lib.uf_contrastive_profile.restype = I32
+    lib.uf_contrastive_profile_read.argtypes = [I32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64),
+                                                ctypes.POINTER(I64)]
+    lib.uf_contrastive_profile_read.restype = I32
+    lib.uf_contrastive_profile_name.argtypes = [I32]
+    lib.uf_contrastive_profile_name.restype = ctypes.c_char_p
     if path is None:
         _lib = lib
     return lib
@@ -95,6 +102,27 @@ def uf_contrastive_fwd_bwd(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, p
                                              float(logit_scale), float(bias), w, loss_per_prefix, row_terms,
                                              col_terms, dA, dB, workspace, int(workspace_bytes), device_status,
                                              stream))
+
+
+KERNEL_GROUPS = ("prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd")
+
+
+def uf_contrastive_profile(enable: bool) -> int:
+    return int(load().uf_contrastive_profile(int(bool(enable))))
+
+
+def uf_contrastive_profile_name(group: int) -> str:
+    return load().uf_contrastive_profile_name(int(group)).decode()
+
+
+def uf_contrastive_profile_read(group: int):
+    """(total_ms, timed_pairs, launches) of one kernel group since profiling was enabled."""
+    ms, pairs, launches = ctypes.c_double(), ctypes.c_int64(), ctypes.c_int64()
+    st = int(load().uf_contrastive_profile_read(int(group), ctypes.byref(ms), ctypes.byref(pairs),
+                                                ctypes.byref(launches)))
+    if st != UF_OK:
+        raise UfError(st, "uf_contrastive_profile_read")
+    return ms.value, pairs.value, launches.value
 
 
 # ---- torch convenience ------------------------------------------------------------

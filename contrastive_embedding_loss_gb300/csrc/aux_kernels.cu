@@ -121,7 +121,12 @@ cudaError_t launch_transpose(const uint16_t* X, uint16_t* Xt, int64_t rows, int 
 }
 
 // ------------------------------------------------------------------------------ stats
-// Elementwise over (prefix, row) of A and then of B.
+// Elementwise over (prefix, row) of A and then of B.  The forward sums cover the
+// negatives only (Zneg); the positive's share is handled here in float64:
+//   CLIP/ROWS  term = -log P_ii = softplus(log Zneg + tau - s_ii),  Z = Zneg + e^{s_ii - tau}
+//   SigLIP     term = ln2 * (sum of negatives' softplus in log2 units) + softplus(-x_ii)
+__device__ __forceinline__ double softplus_d(double y) { return y > 0 ? y + log1p(exp(-y)) : log1p(exp(y)); }
+
 __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
   const int n = p.n_prefix;
   const int64_t total_a = static_cast<int64_t>(n) * p.na;
@@ -136,7 +141,9 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
     const int64_t i = ee % nrows;
     const float* acc = side_a ? p.rowacc_a : p.rowacc_b;
     const int slots = side_a ? p.slots_a : p.slots_b;
-    const float w = p.weight[k];
+    const double w = p.weight[k];
+    const bool has_pos = i < nmin;
+    const double cos_ii = has_pos ? static_cast<double>(p.pos_cos[k * nmin + i]) : 0.0;
     if (p.kind == KIND_SIGLIP) {
       if (!side_a) {
         p.terms_b[ee] = 0.f;
@@ -144,30 +151,32 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
       }
       double s = 0.0;  // log2 units, fixed order over slots
       for (int sl = 0; sl < slots; ++sl) s += acc[(static_cast<int64_t>(sl) * n + k) * nrows + i];
-      const float x_ii = p.tau_or_t * p.pos_cos[k * nmin + i] + p.bias;
-      p.terms_a[ee] = static_cast<float>(s * 0.6931471805599453) - x_ii;
+      const double x_ii = static_cast<double>(p.tau_or_t) * cos_ii + static_cast<double>(p.bias);
+      p.terms_a[ee] = static_cast<float>(s * 0.6931471805599453 + (has_pos ? softplus_d(-x_ii) : 0.0));
       continue;
     }
     if (p.kind == KIND_ROWS && !side_a) {
       p.terms_b[ee] = 0.f;
       continue;
     }
-    float z = 0.f;  // sum_j exp(s_ij - tau), fixed order over slots
-    for (int sl = 0; sl < slots; ++sl) z += acc[(static_cast<int64_t>(sl) * n + k) * nrows + i];
-    const float tau = p.tau_or_t;
-    const float s_ii = tau * p.pos_cos[k * nmin + i];
-    const float term = logf(z) + tau - s_ii;
+    double zneg = 0.0;  // sum over negatives of exp(s_ij - tau), fixed order over slots
+    for (int sl = 0; sl < slots; ++sl) zneg += acc[(static_cast<int64_t>(sl) * n + k) * nrows + i];
+    const double tau = p.tau_or_t;
+    const double s_ii = tau * cos_ii;
+    const double e_ii = has_pos ? exp(s_ii - tau) : 0.0;
+    const double z = zneg + e_ii;
+    const double term = has_pos ? softplus_d(log(zneg) + tau - s_ii) : log(zneg) + tau;
     const double N = static_cast<double>(p.na);
-    const float coef = (p.kind == KIND_CLIP) ? static_cast<float>(w * tau / (2.0 * N)) : static_cast<float>(w * tau / N);
-    const float rho = side_a ? p.rinv_a[k * p.na + i] : p.rinv_b[k * p.nb + i];
+    const double coef = (p.kind == KIND_CLIP) ? w * tau / (2.0 * N) : w * tau / N;
+    const double rho = side_a ? p.rinv_a[k * p.na + i] : p.rinv_b[k * p.nb + i];
     if (side_a) {
-      p.zr[ee] = z;
-      p.fa[ee] = rho * coef / z;
-      p.terms_a[ee] = term;
+      p.zr[ee] = static_cast<float>(zneg);
+      p.fa[ee] = static_cast<float>(rho * coef / z);
+      p.terms_a[ee] = static_cast<float>(term);
     } else {
-      p.zc[ee] = z;
-      p.fb[ee] = rho * coef / z;
-      p.terms_b[ee] = term;
+      p.zc[ee] = static_cast<float>(zneg);
+      p.fb[ee] = static_cast<float>(rho * coef / z);
+      p.terms_b[ee] = static_cast<float>(term);
     }
   }
 }
@@ -232,20 +241,23 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
         const float sig = p.rinv_y[k * p.ny + i];
         const float w = p.weight[k];
         const double N = static_cast<double>(p.n_total);
+        // W_ii = W'_ii + w, written without cancellation: 1 - P_ii = Zneg / Z and
+        // sigmoid(x) - 1 = -sigmoid(-x).
         if (p.kind == KIND_SIGLIP) {
           const float x = p.tau_or_t * cosd + p.bias;
-          const float sg = 1.f / (1.f + expf(-x));
-          Wd = static_cast<float>(w * p.tau_or_t / N) * (sg - 1.f);
+          const float sg_neg = 1.f / (1.f + expf(x));
+          Wd = -static_cast<float>(w * p.tau_or_t / N) * sg_neg;
         } else {
           const float tau = p.tau_or_t;
           const float e = expf(tau * cosd - tau);
           if (p.kind == KIND_CLIP) {
             const float c = static_cast<float>(w * tau / (2.0 * N));
-            Wd = e * (c / p.z_x[k * p.nx + i] + c / p.z_y[k * p.ny + i]) - 2.f * c;
+            const float zx = p.z_x[k * p.nx + i], zy = p.z_y[k * p.ny + i];
+            Wd = -c * (zx / (zx + e) + zy / (zy + e));
           } else {
             const float c = static_cast<float>(w * tau / N);
             const float zq = p.x_is_query ? p.z_x[k * p.nx + i] : p.z_y[k * p.ny + i];
-            Wd = e * c / zq - c;
+            Wd = -c * (zq / (zq + e));
           }
         }
         C += Wd * cosd;

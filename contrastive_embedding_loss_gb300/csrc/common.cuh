@@ -36,7 +36,8 @@ struct TileParams {
   const float* beta_y;            // backward CLIP/ROWS: sigma_j * beta_j
   float m_scale[kMaxPrefix];      // backward SigLIP: w_k * t / N
   // outputs (slot = split*2 + column half)
-  float* rowacc;                  // [slot][n_prefix][nx]: forward row sums; SigLIP backward: loss sums
+  float* rowacc;                  // [slot][n_prefix][nx]: forward row sums; SigLIP backward: loss
+                                  // sums (NULL: not wanted)
   float* crow;                    // [slot][n_prefix][nx]: backward sum_j m_ij dot_ij (off-diagonal)
   float* grad;                    // [split][nx][d]: backward sum_j m_ij y_j over this CTA's columns
   int* status;

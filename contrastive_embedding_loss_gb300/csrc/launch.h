@@ -48,7 +48,7 @@ struct StatsParams {
   int slots_a;
   const float* rowacc_b;   // [slots_b][n][nb] (CLIP)
   int slots_b;
-  float* zr;               // [n][na]  fixed-shift row sums (CLIP/ROWS)
+  float* zr;               // [n][na]  fixed-shift row sums over the negatives (CLIP/ROWS)
   float* zc;               // [n][nb]
   float* fa;               // [n][na]  rho_i * u_i  (backward factor)
   float* fb;               // [n][nb]  sigma_j * v_j
@@ -71,7 +71,7 @@ struct NormBwdParams {
   const float* rinv_x;
   const float* rinv_y;
   const float* pos_cos;
-  const float* z_x;        // CLIP/ROWS fixed-shift sums of X's rows (ROWS: the queries')
+  const float* z_x;        // CLIP/ROWS fixed-shift sums of X's rows over negatives (ROWS: the queries')
   const float* z_y;        // CLIP: of Y's rows
   int x_is_query;          // ROWS: 1 when X holds the queries
   const float* crow;       // [slots][n][nx]

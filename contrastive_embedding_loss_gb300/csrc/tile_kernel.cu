@@ -12,9 +12,11 @@
 // bands with the negate-A bit of the instruction descriptor; accumulating each band on
 // its own avoids the extra 1984/1024 MMA work that needs).
 //
-// Forward (MODE_FWD): per row and prefix, CLIP/ROWS: sum_j exp(s_ij - tau) with the
-// fixed shift tau (|cos| <= 1 bounds every logit, so no running maximum is needed);
-// SigLIP: sum_j softplus(x_ij) in log2 units.
+// Forward (MODE_FWD): per row and prefix, over the negatives j != i only, CLIP/ROWS:
+// sum_j exp(s_ij - tau) with the fixed shift tau (|cos| <= 1 bounds every logit, so no
+// running maximum is needed); SigLIP: sum_j softplus(x_ij) in log2 units.  The positive
+// cell is added back in float64 by the statistics kernel, which keeps nearly converged
+// rows (loss ~1e-4) free of cancellation.
 //
 // Backward (MODE_BWD): per cell and prefix the epilogue forms
 //     m_ij = rho_i sigma_j W'_ij,   W' = dL/dcos off the diagonal,
@@ -135,7 +137,7 @@ __device__ __forceinline__ void epi_cells(const TileParams& p, const float (&run
         const float e = ex2_approx(-fabsf(x2));
         if constexpr (MODE == MODE_FWD) {
           const float l = fmaxf(x2, 0.f) + lg2_approx(1.f + e);
-          acc_row += valid ? l : 0.f;
+          acc_row += (valid && !(DIAG && jj == diag_col)) ? l : 0.f;
           mv[u] = 0.f;
         } else {
           const float d = 1.f + e;
@@ -146,7 +148,7 @@ __device__ __forceinline__ void epi_cells(const TileParams& p, const float (&run
           acc_c = fmaf(m, run[jj], acc_c);
           if (R3 != 0.f) {  // R3 != 0 marks the CTA that also sums the SigLIP loss
             const float l = fmaxf(x2, 0.f) + lg2_approx(d);
-            acc_row += valid ? l : 0.f;
+            acc_row += (valid && !(DIAG && jj == diag_col)) ? l : 0.f;
           }
           mv[u] = m;
         }
@@ -154,7 +156,7 @@ __device__ __forceinline__ void epi_cells(const TileParams& p, const float (&run
         const float x = fmaf(t, run[jj], -L);
         const float e = ex2_approx(x);
         if constexpr (MODE == MODE_FWD) {
-          acc_row += valid ? e : 0.f;
+          acc_row += (valid && !(DIAG && jj == diag_col)) ? e : 0.f;
           mv[u] = 0.f;
         } else {
           // m = e * rho_i * sigma_j * (alpha_i + beta_j) = e * (R2 * s1 + R3 * s2)
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t left = p.ny - j0;
       const int ncols_valid = left < kTileCols ? static_cast<int>(left) : kTileCols;
       const bool masked = ncols_valid < kTileCols;
-      const bool diag_tile = (MODE == MODE_BWD) && (j0 == i0);
+      const bool diag_tile = j0 == i0;  // the tile holds the positive pairs (i, i)
       const int diag_col = r - h * 64;  // local column (within my 64) of the diagonal cell
       float run[64];
       for (int b = 0; b < n && ok; ++b, ++ait) {
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (MODE == MODE_BWD) {
           if constexpr (KIND == KIND_SIGLIP) {
             R2 = rho * p.m_scale[k];
-            R3 = (slice == 0) ? 1.f : 0.f;
+            R3 = (slice == 0 && p.rowacc) ? 1.f : 0.f;
           } else {
             R2 = (row_ok && p.alpha_x) ? p.alpha_x[k * p.nx + gi] : 0.f;
             R3 = rho;
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- outputs
     if (row_ok && ok) {
       const int slot = split * 2 + h;
-      if (MODE == MODE_FWD || (KIND == KIND_SIGLIP && slice == 0)) {
+      if (p.rowacc && (MODE == MODE_FWD || (KIND == KIND_SIGLIP && slice == 0))) {
         for (int k = 0; k < n; ++k) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi] = acc_row[k];
       }
       if (MODE == MODE_BWD && slice == 0) {

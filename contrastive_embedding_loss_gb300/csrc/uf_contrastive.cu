@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/uf_contrastive.h"
 #include "launch.h"
@@ -147,6 +148,52 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 std::mutex g_init_mu;
 uint64_t g_init_mask = 0;  // devices already set up (device ordinal < 64)
 
+// ---- optional per-kernel timing (uf_contrastive_profile)
+struct ProfRecord {
+  int group;
+  int launches;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::atomic<bool> g_prof_on{false};
+std::vector<ProfRecord> g_prof_pending;
+std::vector<cudaEvent_t> g_prof_pool;
+double g_prof_ms[UF_KERNEL_GROUPS];
+int64_t g_prof_pairs[UF_KERNEL_GROUPS], g_prof_launches[UF_KERNEL_GROUPS];
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Records a start event on construction and a stop event on destruction (profiling only).
+struct ProfScope {
+  bool on;
+  ProfRecord rec{};
+  cudaStream_t stream;
+  ProfScope(int group, int launches, cudaStream_t s) : on(g_prof_on.load()), stream(s) {
+    if (!on) return;
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    rec.group = group;
+    rec.launches = launches;
+    rec.start = prof_event();
+    rec.stop = prof_event();
+    cudaEventRecord(rec.start, stream);
+  }
+  ~ProfScope() {
+    if (!on) return;
+    cudaEventRecord(rec.stop, stream);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_pending.push_back(rec);
+  }
+};
+
 }  // namespace
 
 extern "C" {
@@ -268,9 +315,16 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
   pp.rinv_a = F(P.o_rinv_a);
   pp.rinv_b = F(P.o_rinv_b);
   pp.pos_cos = F(P.o_pos);
-  UF_CHECK(launch_prep(pp, stream));
+  {
+    ProfScope ps(UF_KERNEL_PREP, 1, stream);
+    UF_CHECK(launch_prep(pp, stream));
+  }
   if (grads) {
-    UF_CHECK(launch_transpose(A16, At, Na, D, P.lda, stream));
+    {
+      ProfScope ps(UF_KERNEL_TRANSPOSE, 1, stream);
+      UF_CHECK(launch_transpose(A16, At, Na, D, P.lda, stream));
+    }
+    ProfScope ps(UF_KERNEL_TRANSPOSE, 1, stream);
     UF_CHECK(launch_transpose(B16, Bt, Nb, D, P.ldb, stream));
   }
 
@@ -319,19 +373,24 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     TileParams t = base_tile(true);
     t.tiles_per_split = P.fwd_a.tiles_per_split;
     t.rowacc = F(P.o_acc_a);
-    UF_CHECK(launch_tile(MODE_FWD, kind, tmA, tmB, tmB, t,
-                         dim3(static_cast<unsigned>(P.rb_a), P.fwd_a.splits, 1), stream));
+    {
+      ProfScope ps(UF_KERNEL_FWD_TILE, 1, stream);
+      UF_CHECK(launch_tile(MODE_FWD, kind, tmA, tmB, tmB, t,
+                           dim3(static_cast<unsigned>(P.rb_a), P.fwd_a.splits, 1), stream));
+    }
     sp.rowacc_a = t.rowacc;
     sp.slots_a = 2 * P.fwd_a.splits;
     if (kind == KIND_CLIP) {
       TileParams tb = base_tile(false);
       tb.tiles_per_split = P.fwd_b.tiles_per_split;
       tb.rowacc = F(P.o_acc_b);
+      ProfScope ps(UF_KERNEL_FWD_TILE, 1, stream);
       UF_CHECK(launch_tile(MODE_FWD, kind, tmB, tmA, tmA, tb,
                            dim3(static_cast<unsigned>(P.rb_b), P.fwd_b.splits, 1), stream));
       sp.rowacc_b = tb.rowacc;
       sp.slots_b = 2 * P.fwd_b.splits;
     }
+    ProfScope ps(UF_KERNEL_STATS, 2, stream);
     UF_CHECK(launch_stats(sp, stream));
   }
   if (!grads) {
@@ -351,12 +410,14 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     t.rowacc = F(P.o_acc_a);
     t.crow = F(P.o_crow_a);
     t.grad = ga;
+    ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
     UF_CHECK(launch_tile(MODE_BWD, kind, tmA, tmB, tmBt, t,
                          dim3(static_cast<unsigned>(P.rb_a), P.bwd_a.splits, P.slices), stream));
   }
   if (siglip) {
     sp.rowacc_a = F(P.o_acc_a);
     sp.slots_a = 2 * P.bwd_a.splits;
+    ProfScope ps(UF_KERNEL_STATS, 2, stream);
     UF_CHECK(launch_stats(sp, stream));
   }
   {
@@ -365,9 +426,10 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     t.alpha_x = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
     t.beta_y = siglip ? nullptr : F(P.o_fa);
     for (int k = 0; k < n; ++k) t.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
-    t.rowacc = F(P.o_acc_b);  // unused by the B side
+    t.rowacc = nullptr;  // the B side sums no loss
     t.crow = F(P.o_crow_b);
     t.grad = gb;
+    ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
     UF_CHECK(launch_tile(MODE_BWD, kind, tmB, tmA, tmAt, t,
                          dim3(static_cast<unsigned>(P.rb_b), P.bwd_b.splits, P.slices), stream));
   }
@@ -406,11 +468,54 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     q.G = xa ? ga : gb;
     q.g_splits = xa ? P.bwd_a.splits : P.bwd_b.splits;
     q.dX = xa ? dA : dB;
+    ProfScope ps(UF_KERNEL_NORM_BWD, 1, stream);
     UF_CHECK(launch_norm_bwd(q, stream));
   }
   if (col_terms && kind != KIND_CLIP) UF_CHECK(cudaMemsetAsync(col_terms, 0, sizeof(float) * n * Nb, stream));
 #undef UF_CHECK
   return UF_OK;
+}
+
+uf_status_t uf_contrastive_profile(int enable) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (enable) {
+    for (auto& r : g_prof_pending) {
+      g_prof_pool.push_back(r.start);
+      g_prof_pool.push_back(r.stop);
+    }
+    g_prof_pending.clear();
+    for (int g = 0; g < UF_KERNEL_GROUPS; ++g) {
+      g_prof_ms[g] = 0.0;
+      g_prof_pairs[g] = g_prof_launches[g] = 0;
+    }
+  }
+  g_prof_on.store(enable != 0);
+  return UF_OK;
+}
+
+uf_status_t uf_contrastive_profile_read(int group, double* total_ms, int64_t* pairs, int64_t* launches) {
+  if (group < 0 || group >= UF_KERNEL_GROUPS) return UF_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (auto& r : g_prof_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      return UF_CUDA_ERROR;
+    g_prof_ms[r.group] += ms;
+    g_prof_pairs[r.group] += 1;
+    g_prof_launches[r.group] += r.launches;
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof_pending.clear();
+  if (total_ms) *total_ms = g_prof_ms[group];
+  if (pairs) *pairs = g_prof_pairs[group];
+  if (launches) *launches = g_prof_launches[group];
+  return UF_OK;
+}
+
+const char* uf_contrastive_profile_name(int group) {
+  static const char* names[UF_KERNEL_GROUPS] = {"prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd"};
+  return (group >= 0 && group < UF_KERNEL_GROUPS) ? names[group] : "unknown";
 }
 
 }  // extern "C"

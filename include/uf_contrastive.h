@@ -123,6 +123,32 @@ UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t 
                                    float* col_terms, float* dA, float* dB, void* workspace,
                                    size_t workspace_bytes, int* device_status, void* stream);
 
+/*
+ * Optional per-kernel timing, for benchmarks and profiling (not part of the loss).
+ * While enabled, every uf_contrastive_fwd_bwd records a pair of CUDA events on its
+ * stream around each group of internal kernel launches and keeps the pairs in a host
+ * list (this list grows, so do not enable it under stream capture or on a hot path that
+ * must not allocate).  uf_contrastive_profile_read() waits for the recorded events,
+ * folds them into per-kernel totals and returns them.  Kernel groups:
+ */
+typedef enum uf_kernel_group {
+  UF_KERNEL_PREP = 0,       /* per-prefix inverse norms and positives' cosines (1 launch) */
+  UF_KERNEL_TRANSPOSE = 1,  /* bf16 transposes for the gradient operand (1 launch each) */
+  UF_KERNEL_FWD_TILE = 2,   /* fused tcgen05 forward: row sums of every prefix */
+  UF_KERNEL_STATS = 3,      /* loss statistics and per-prefix loss (2 launches) */
+  UF_KERNEL_BWD_TILE = 4,   /* fused tcgen05 backward: score recompute + gradient GEMM */
+  UF_KERNEL_NORM_BWD = 5,   /* projection term and positive-pair correction */
+  UF_KERNEL_GROUPS = 6
+} uf_kernel_group_t;
+
+/* enable != 0: start timing (clears the totals); 0: stop.  Process-wide. */
+UF_API uf_status_t uf_contrastive_profile(int enable);
+/* Totals of one group since the last enable: summed milliseconds, timed event pairs,
+ * and kernel launches.  Synchronises with the recorded events. */
+UF_API uf_status_t uf_contrastive_profile_read(int group, double* total_ms, int64_t* pairs, int64_t* launches);
+/* Static name of a group ("bwd_tile", ...), or "unknown". */
+UF_API const char* uf_contrastive_profile_name(int group);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif
