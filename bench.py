@@ -26,7 +26,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fwd+bwd pairs/s at 5 prefixes (N=65536, D=1024 bf16); TFLOP/s vs bf16 peak"
 LADDER = (64, 128, 256, 512, 1024)
 DEFAULT_WORKLOAD = "clip_n65536_hardneg"
-ORACLE_SAMPLE_PAIRS = 2048      # cpu_baseline: oracle on the first 2048 pairs (about 10-30 s)
+ORACLE_SAMPLE_PAIRS = 8192      # cpu_baseline: oracle on the first 8192 pairs (about 10-30 s on 16 cores)
 REFERENCE_STEP_PAIRS = 1024     # --impl reference: oracle on the first 1024 pairs per step
 
 
