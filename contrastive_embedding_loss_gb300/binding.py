@@ -169,3 +169,27 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
     if st != UF_OK:
         raise UfError(st, "uf_contrastive_fwd_bwd")
     return out
+
+
+# ---- the entry point for callers that cannot allocate device memory -----------------
+
+UF_STATIC_WORKSPACE_BYTES = 96 << 20
+
+
+def uf_contrastive_fwd_bwd_static(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, prefix_weights,
+                                  loss_per_prefix, row_terms, col_terms, dA, dB, device_status, stream) -> int:
+    """Raw call of the library-owned-scratch variant: like ``uf_contrastive_fwd_bwd`` but
+    without a workspace.  For callers that must not allocate device memory; calls whose GPU
+    work overlaps share one scratch array and race.  Pointers are int device addresses."""
+    lib = load()
+    if not getattr(lib, "_static_bound", False):
+        P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        lib.uf_contrastive_fwd_bwd_static.argtypes = [P, P, I64, I64, I32, P, I32, I32, F32, F32, P, P, P, P, P, P,
+                                                      P, P]
+        lib.uf_contrastive_fwd_bwd_static.restype = I32
+        lib._static_bound = True
+    pre = _int_array(list(prefixes))
+    w = None if prefix_weights is None else (ctypes.c_float * len(prefix_weights))(*prefix_weights)
+    return int(lib.uf_contrastive_fwd_bwd_static(A, B, int(Na), int(Nb), int(D), pre, len(prefixes), int(kind),
+                                                 float(logit_scale), float(bias), w, loss_per_prefix, row_terms,
+                                                 col_terms, dA, dB, device_status, stream))

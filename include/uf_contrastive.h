@@ -124,6 +124,35 @@ UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t 
                                    size_t workspace_bytes, int* device_status, void* stream);
 
 /*
+ * uf_contrastive_fwd_bwd without a workspace argument, for callers that cannot allocate
+ * device memory: hosts that reserve all of their memory at start-up and forbid
+ * allocation afterwards, plugins whose host application owns every device buffer, or
+ * processes whose allocator is a fixed pool.  (The pages describe no such entry point;
+ * it exists for these callers only.)
+ *
+ * The scratch is one device array of UF_STATIC_WORKSPACE_BYTES inside the library, which
+ * every GPU that loads the library keeps until the process exits.  The caller still
+ * passes inputs and outputs, with the same meaning and rules as uf_contrastive_fwd_bwd.
+ *   - A request whose uf_contrastive_workspace_size() exceeds UF_STATIC_WORKSPACE_BYTES
+ *     returns UF_WORKSPACE_TOO_SMALL before anything is enqueued (for instance CLIP or
+ *     SigLIP with gradients fits up to about N = 1024 at D = 1024, forward-only calls up
+ *     to far larger batches).
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array, and it keeps whatever the last call left
+ *     there (nothing in it needs clearing: every element is written before it is read).
+ *     Calls whose GPU work overlaps -- on different streams, or from different threads --
+ *     race on it and give wrong results; serialise them.
+ *   - It calls no allocator: no cudaMalloc, no cudaFree, no allocating library routine.
+ */
+#define UF_STATIC_WORKSPACE_BYTES (96u << 20)
+UF_API uf_status_t uf_contrastive_fwd_bwd_static(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
+                                                  const int* prefixes, int n_prefix, int kind, float logit_scale,
+                                                  float bias, const float* prefix_weights, float* loss_per_prefix,
+                                                  float* row_terms, float* col_terms, float* dA, float* dB,
+                                                  int* device_status, void* stream);
+
+/*
  * Optional per-kernel timing, for benchmarks and profiling (not part of the loss).
  * While enabled, every uf_contrastive_fwd_bwd records a pair of CUDA events on its
  * stream around each group of internal kernel launches and keeps the pairs in a host
