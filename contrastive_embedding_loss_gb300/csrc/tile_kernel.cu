@@ -69,10 +69,12 @@ struct Layout {
   static constexpr int off_m = off_yt + (MODE == MODE_BWD ? 2 * kYtBytes : 0);
   static constexpr int off_colf = off_m + (MODE == MODE_BWD ? 2 * kMBytes : 0);
   static constexpr int colf_bytes = 2 * kMaxPrefix * Cfg<MODE>::NCOLF * kTileCols * 4;
-  static constexpr int off_bar = off_colf + colf_bytes;
+  static constexpr int off_rowf = off_colf + colf_bytes;
+  static constexpr int rowf_bytes = kMaxPrefix * 3 * kTileRows * 4;
+  static constexpr int off_bar = off_rowf + rowf_bytes;
   static constexpr int n_bars = 2 * NS + 2 * Cfg<MODE>::NB + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int off_misc = off_bar + n_bars * 8;
-  static constexpr int bytes = off_misc + 16;
+  static constexpr int bytes = off_misc + 16 + 4 * kMaxPrefix;
   static constexpr int alloc_bytes = bytes + 1024;  // slack for 1024-byte alignment
 };
 static_assert(Layout<MODE_FWD>::alloc_bytes <= 232448, "forward shared memory");
@@ -115,40 +117,40 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 }
 
 // ------------------------------------------------------------------------------------
-// Epilogue math for one band-end (prefix k) over this thread's 64 cells.
-// run[]: prefix-k dot products of row i with the thread's 64 columns.
+// Epilogue math for one band end (prefix k) over 32 of this thread's cells.
+// run[]: prefix-k dot products of row i with those 32 columns; cf1/cf2: the columns'
+// factors; col0: their first column within the tile; R1..R3: the row's factors.
 template <int MODE, int KIND, bool MASK, bool DIAG>
-__device__ __forceinline__ void epi_cells(const TileParams& p, const float (&run)[64], const float* colf1,
-                                          const float* colf2, float R1, float R2, float R3, int col_base,
-                                          int ncols_valid, int diag_col, float& acc_row, float& acc_c,
-                                          uint32_t (&packed)[32]) {
-  const float L = p.L;
+__device__ __forceinline__ void epi_cells32(const float* run, const float* cf1, const float* cf2, float R1, float R2,
+                                            float R3, float L, float b2, int col0, int ncols_valid, int diag_col,
+                                            float& acc_row, float& acc_c, uint32_t (&packed)[16]) {
 #pragma unroll
-  for (int j = 0; j < 64; j += 2) {
+  for (int j = 0; j < 32; j += 2) {
     float mv[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int jj = j + u;
-      const float s1 = colf1[jj];
+      const float s1 = cf1[jj];
       const float t = R1 * s1;
-      const bool valid = !MASK || (col_base + jj < ncols_valid);
+      const bool valid = !MASK || (col0 + jj < ncols_valid);
+      const bool diag = DIAG && (col0 + jj == diag_col);
       if constexpr (KIND == KIND_SIGLIP) {
-        const float x2 = fmaf(t, run[jj], p.b2);
+        const float x2 = fmaf(t, run[jj], b2);
         const float e = ex2_approx(-fabsf(x2));
         if constexpr (MODE == MODE_FWD) {
           const float l = fmaxf(x2, 0.f) + lg2_approx(1.f + e);
-          acc_row += (valid && !(DIAG && jj == diag_col)) ? l : 0.f;
+          acc_row += (valid && !diag) ? l : 0.f;
           mv[u] = 0.f;
         } else {
           const float d = 1.f + e;
           const float r = rcp_approx(d);
           const float sig = x2 >= 0.f ? r : e * r;
           float m = sig * (R2 * s1);  // R2 = rho_i * w t / N; s1 = 0 on padded columns
-          if (DIAG && jj == diag_col) m = 0.f;
+          if (diag) m = 0.f;
           acc_c = fmaf(m, run[jj], acc_c);
           if (R3 != 0.f) {  // R3 != 0 marks the CTA that also sums the SigLIP loss
             const float l = fmaxf(x2, 0.f) + lg2_approx(d);
-            acc_row += (valid && !(DIAG && jj == diag_col)) ? l : 0.f;
+            acc_row += (valid && !diag) ? l : 0.f;
           }
           mv[u] = m;
         }
@@ -156,12 +158,12 @@ __device__ __forceinline__ void epi_cells(const TileParams& p, const float (&run
         const float x = fmaf(t, run[jj], -L);
         const float e = ex2_approx(x);
         if constexpr (MODE == MODE_FWD) {
-          acc_row += (valid && !(DIAG && jj == diag_col)) ? e : 0.f;
+          acc_row += (valid && !diag) ? e : 0.f;
           mv[u] = 0.f;
         } else {
           // m = e * rho_i * sigma_j * (alpha_i + beta_j) = e * (R2 * s1 + R3 * s2)
-          float m = e * fmaf(R2, s1, R3 * colf2[jj]);
-          if (DIAG && jj == diag_col) m = 0.f;
+          float m = e * fmaf(R2, s1, R3 * cf2[jj]);
+          if (diag) m = 0.f;
           acc_c = fmaf(m, run[jj], acc_c);
           mv[u] = m;
         }
@@ -198,8 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.yt_empty = B.yt_full + 2;
   B.grad_done = B.yt_empty + 2;
   B.drain = B.grad_done + 1;
+  float* rowf = reinterpret_cast<float*>(smem + LO::off_rowf);
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + LO::off_misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LO::off_misc + 4);
+  int* pend = reinterpret_cast<int*>(smem + LO::off_misc + 16);  // prefix ends (kernel parameter copy)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -211,11 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_begin = split * p.tiles_per_split;
   const int t_end = min(p.n_col_tiles, t_begin + p.tiles_per_split);
   const int T = t_end - t_begin;
-  const int nchunk = p.prefix_end[n - 1] / kChunk;
-  // prefixes that reach this CTA's gradient slice
-  int k_first = 0;
-  if constexpr (MODE == MODE_BWD) {
-    while (k_first < n && p.prefix_end[k_first] <= d0) ++k_first;
+  int nchunk = 0, k_first = 0;  // K chunks of the widest prefix; first prefix reaching the slice
+#pragma unroll
+  for (int k = 0; k < kMaxPrefix; ++k) {
+    if (k < n) nchunk = p.prefix_end[k] / kChunk;
+    if (MODE == MODE_BWD && k < n && p.prefix_end[k] <= d0) k_first = k + 1;
   }
 
   if (threadIdx.x == 0) {
@@ -236,6 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(B.grad_done, 1);
     mbar_init(B.drain, 1);
     *abort_flag = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxPrefix; ++k) pend[k] = p.prefix_end[k];
     fence_mbar_init();
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_y);
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + ab * kTileCols;
-        const int c_end = p.prefix_end[b] / kChunk;
+        const int c_end = pend[b] / kChunk;
         const int c_first = c;
         for (; c < c_end; ++c, ++it) {
           const uint32_t s = it % NS, ph = (it / NS) & 1;
@@ -333,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
       for (int k = k_first; k < n && ok; ++k, ++cnt) {
-        const int nk = min(p.prefix_end[k], d0 + kSliceDims) - d0;  // multiple of 64, <= 256
+        const int nk = min(pend[k], d0 + kSliceDims) - d0;  // multiple of 64, <= 256
         const uint32_t idesc = idesc_bf16_f32(kTileRows, static_cast<uint32_t>(nk));
         for (int h = 0; h < 2; ++h) {
           if (!wait_or_abort(&B.m_full[h], cnt & 1, abort_flag) ||
@@ -383,61 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int etid = threadIdx.x - kEpiWarp0 * 32;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     constexpr int NCF = Cfg<MODE>::NCOLF;
-    float acc_row[kMaxPrefix], acc_c[kMaxPrefix];
-#pragma unroll
-    for (int k = 0; k < kMaxPrefix; ++k) acc_row[k] = acc_c[k] = 0.f;
-    uint32_t ait = 0, mcnt = 0;
-    bool ok = true;
-    // every epilogue warp runs all T iterations (an aborted warp skips the work but still
-    // meets the named barriers, so the others cannot hang on them)
-    for (int t = 0; t < T; ++t) {
-      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kTileCols;
-      // column factors of this tile -> shared memory (double-buffered by tile parity)
-      named_bar_sync(1, kEpiThreads);
-      float* cf = colf + (t & 1) * kMaxPrefix * NCF * kTileCols;
-      for (int e = etid; e < n * kTileCols; e += kEpiThreads) {
-        const int k = e / kTileCols, c = e % kTileCols;
-        const int64_t gj = j0 + c;
-        const bool v = gj < p.ny;
-        cf[(k * NCF + 0) * kTileCols + c] = v ? p.rinv_y[k * p.ny + gj] : 0.f;
-        if constexpr (NCF > 1) {
-          cf[(k * NCF + 1) * kTileCols + c] = (v && p.beta_y) ? p.beta_y[k * p.ny + gj] : 0.f;
-        }
-      }
-      named_bar_sync(1, kEpiThreads);
-      if (!ok) continue;
-      const int64_t left = p.ny - j0;
-      const int ncols_valid = left < kTileCols ? static_cast<int>(left) : kTileCols;
-      const bool masked = ncols_valid < kTileCols;
-      const bool diag_tile = j0 == i0;  // the tile holds the positive pairs (i, i)
-      const int diag_col = r - h * 64;  // local column (within my 64) of the diagonal cell
-      float run[64];
-      for (int b = 0; b < n && ok; ++b, ++ait) {
-        const uint32_t ab = ait % NB, aph = (ait / NB) & 1;
-        if (!wait_or_abort(&B.acc_full[ab], aph, abort_flag)) {
-          record_timeout(p, abort_flag);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        {
-          float v[32];
-          const uint32_t a = tmem + lane_addr + ab * kTileCols + h * 64;
-          tmem_ld32(a, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) run[j] = (b == 0) ? v[j] : run[j] + v[j];
-          tmem_ld32(a + 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) run[32 + j] = (b == 0) ? v[j] : run[32 + j] + v[j];
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.acc_empty[ab]);
+    constexpr int CF_STRIDE = kMaxPrefix * NCF * kTileCols;  // floats per column-factor buffer
 
-        if (MODE == MODE_BWD && b < k_first) continue;  // prefix does not reach this slice
-        const int k = b;
+    // Row factors of this CTA's rows, once: R1 = L rho, and for the backward
+    // CLIP/ROWS: R2 = rho alpha (prescaled), R3 = rho; SigLIP: R2 = rho w t / N, R3 = loss flag.
+    if (h == 0) {
+#pragma unroll
+      for (int k = 0; k < kMaxPrefix; ++k) {
+        if (k >= n) break;
         const float rho = row_ok ? p.rinv_x[k * p.nx + gi] : 0.f;
-        const float R1 = p.L * rho;
         float R2 = 0.f, R3 = 0.f;
         if constexpr (MODE == MODE_BWD) {
           if constexpr (KIND == KIND_SIGLIP) {
@@ -448,21 +408,115 @@ __global__ void __launch_bounds__(kThreads, 1)
             R3 = rho;
           }
         }
+        rowf[(k * 3 + 0) * kTileRows + r] = p.L * rho;
+        rowf[(k * 3 + 1) * kTileRows + r] = R2;
+        rowf[(k * 3 + 2) * kTileRows + r] = R3;
+      }
+    }
+    // Column factors of tile t land in colf[t & 1] by cp.async, one tile ahead.
+    auto prefetch_colf = [&](int t) {
+      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kTileCols;
+      float* cf = colf + (t & 1) * CF_STRIDE;
+      for (int e = etid; e < n * kTileCols; e += kEpiThreads) {
+        const int k = e / kTileCols, c = e % kTileCols;
+        const int64_t gj = j0 + c;
+        const bool v = gj < p.ny;
+        const int64_t idx = v ? k * p.ny + gj : 0;
+        cp_async4(cf + (k * NCF + 0) * kTileCols + c, p.rinv_y + idx, v ? 4u : 0u);
+        if constexpr (NCF > 1) {
+          const bool vb = v && p.beta_y;
+          cp_async4(cf + (k * NCF + 1) * kTileCols + c, vb ? p.beta_y + idx : p.rinv_y, vb ? 4u : 0u);
+        }
+      }
+    };
+    if (T > 0) prefetch_colf(0);
+    cp_async_commit();
+
+    float acc_row[kMaxPrefix], acc_c[kMaxPrefix];
+#pragma unroll
+    for (int k = 0; k < kMaxPrefix; ++k) acc_row[k] = acc_c[k] = 0.f;
+    uint32_t ait = 0, mcnt = 0;
+    bool ok = true;
+    // every epilogue warp runs all T iterations (an aborted warp skips the work but still
+    // meets the named barriers, so the others cannot hang on them)
+    for (int t = 0; t < T; ++t) {
+      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kTileCols;
+      named_bar_sync(1, kEpiThreads);  // everyone is done with tile t-1: colf[(t+1) & 1] is free
+      if (t + 1 < T) prefetch_colf(t + 1);
+      cp_async_commit();
+      cp_async_wait<1>();               // this thread's copies for tile t have landed
+      named_bar_sync(1, kEpiThreads);  // ... and everyone else's
+      if (!ok) continue;
+      const float* cf = colf + (t & 1) * CF_STRIDE;
+      const int64_t left = p.ny - j0;
+      const int ncols_valid = left < kTileCols ? static_cast<int>(left) : kTileCols;
+      const bool masked = ncols_valid < kTileCols;
+      const bool diag_tile = j0 == i0;  // the tile holds the positive pairs (i, i)
+      const int diag_col = r - h * 64;  // column (within my 64) of the diagonal cell
+      float run[64];
+      for (int b = 0; b < n && ok; ++b, ++ait) {
+        const uint32_t ab = ait % NB, aph = (ait / NB) & 1;
+        if (!wait_or_abort(&B.acc_full[ab], aph, abort_flag)) {
+          record_timeout(p, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
+          float v[64];
+          tmem_ld64(tmem + lane_addr + ab * kTileCols + h * 64, v);
+#pragma unroll
+          for (int j = 0; j < 64; ++j) run[j] = (b == 0) ? v[j] : run[j] + v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.acc_empty[ab]);
+
+        if (MODE == MODE_BWD && b < k_first) continue;  // prefix does not reach this slice
+        const int k = b;
+        const float R1 = rowf[(k * 3 + 0) * kTileRows + r];
+        const float R2 = rowf[(k * 3 + 1) * kTileRows + r];
+        const float R3 = rowf[(k * 3 + 2) * kTileRows + r];
         const float* c1 = cf + (k * NCF + 0) * kTileCols + h * 64;
         const float* c2 = cf + (k * NCF + (NCF > 1 ? 1 : 0)) * kTileCols + h * 64;
-        uint32_t packed[32];
+        uint8_t* mt = sm + h * kMBytes + (r >> 3) * 1024 + (r & 7) * 128;
+        if constexpr (MODE == MODE_BWD) {
+          // the gradient MMA must have consumed the previous weights of this half
+          if (!wait_or_abort(&B.m_empty[h], (mcnt & 1) ^ 1, abort_flag)) {
+            record_timeout(p, abort_flag);
+            ok = false;
+            break;
+          }
+        }
         float ar = 0.f, ac = 0.f;
-        const int cb = h * 64;
-        if (masked) {
-          if (diag_tile)
-            epi_cells<MODE, KIND, true, true>(p, run, c1, c2, R1, R2, R3, cb, ncols_valid, diag_col, ar, ac, packed);
-          else
-            epi_cells<MODE, KIND, true, false>(p, run, c1, c2, R1, R2, R3, cb, ncols_valid, diag_col, ar, ac, packed);
-        } else {
-          if (diag_tile)
-            epi_cells<MODE, KIND, false, true>(p, run, c1, c2, R1, R2, R3, cb, ncols_valid, diag_col, ar, ac, packed);
-          else
-            epi_cells<MODE, KIND, false, false>(p, run, c1, c2, R1, R2, R3, cb, ncols_valid, diag_col, ar, ac, packed);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t packed[16];
+          const int col0 = h * 64 + hh * 32;
+          const float* rr = run + hh * 32;
+          if (masked) {
+            if (diag_tile)
+              epi_cells32<MODE, KIND, true, true>(rr, c1 + hh * 32, c2 + hh * 32, R1, R2, R3, p.L, p.b2, col0 - h * 64,
+                                                  ncols_valid - h * 64, diag_col, ar, ac, packed);
+            else
+              epi_cells32<MODE, KIND, true, false>(rr, c1 + hh * 32, c2 + hh * 32, R1, R2, R3, p.L, p.b2, col0 - h * 64,
+                                                   ncols_valid - h * 64, diag_col, ar, ac, packed);
+          } else {
+            if (diag_tile)
+              epi_cells32<MODE, KIND, false, true>(rr, c1 + hh * 32, c2 + hh * 32, R1, R2, R3, p.L, p.b2, col0 - h * 64,
+                                                   ncols_valid - h * 64, diag_col, ar, ac, packed);
+            else
+              epi_cells32<MODE, KIND, false, false>(rr, c1 + hh * 32, c2 + hh * 32, R1, R2, R3, p.L, p.b2,
+                                                    col0 - h * 64, ncols_valid - h * 64, diag_col, ar, ac, packed);
+          }
+          if constexpr (MODE == MODE_BWD) {
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+              const int chunk = hh * 4 + qd;  // 16-byte chunk of the 128-byte swizzled row
+              *reinterpret_cast<uint4*>(mt + ((chunk ^ (r & 7)) << 4)) =
+                  make_uint4(packed[4 * qd], packed[4 * qd + 1], packed[4 * qd + 2], packed[4 * qd + 3]);
+            }
+          }
         }
 #pragma unroll
         for (int kk = 0; kk < kMaxPrefix; ++kk)
@@ -471,18 +525,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc_c[kk] += ac;
           }
         if constexpr (MODE == MODE_BWD) {
-          // hand the bf16 weights to the gradient MMA: wait until the previous ones are consumed
-          if (!wait_or_abort(&B.m_empty[h], (mcnt & 1) ^ 1, abort_flag)) {
-            record_timeout(p, abort_flag);
-            ok = false;
-            break;
-          }
-          uint8_t* mt = sm + h * kMBytes + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-          for (int qd = 0; qd < 8; ++qd) {
-            const uint4 v = make_uint4(packed[4 * qd], packed[4 * qd + 1], packed[4 * qd + 2], packed[4 * qd + 3]);
-            *reinterpret_cast<uint4*>(mt + ((qd ^ (r & 7)) << 4)) = v;
-          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.m_full[h]);
@@ -490,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    cp_async_wait<0>();
     // ---- outputs
     if (row_ok && ok) {
       const int slot = split * 2 + h;
