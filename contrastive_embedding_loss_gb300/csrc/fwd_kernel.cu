@@ -1,0 +1,395 @@
+// fwd_kernel.cu -- forward statistics of the Matryoshka contrastive loss in one pass:
+// per row i of X and prefix k the sum over the negatives of exp(s_ij - tau) (CLIP, ROWS)
+// or of softplus(x_ij) (SigLIP, log2 units), and for CLIP also the same sums per column
+// j of Y (so the column softmax needs no second pass over the grid).
+//
+// Tiles.  A CTA owns 128 rows of X and walks 256-row tiles of Y.  The score tile is one
+// 128 x 256 tcgen05 MMA per K step (N = 256 keeps the tensor pipe at full rate; 128-wide
+// tiles ran at about half rate on this part).  The K walk goes band by band (a band is
+// the dimensions between consecutive prefix ends) and accumulates into one TMEM
+// accumulator, so after band k the accumulator holds the prefix-k dot products: the
+// epilogue reads that snapshot, releases the accumulator for the next band, and
+// evaluates prefix k.  Two accumulators (512 TMEM columns) let the MMA run the next tile's
+// band while the epilogue reads this one's.
+//
+// Epilogue.  16 warps: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows) and one
+// quarter (64 columns) of the tile.  Column sums: each warp reduces its 32 rows per
+// column by a shuffle reduce-scatter (lane l ends with column l of each 32-column group),
+// the four row-quadrant warps of a column quarter combine through shared memory, and one
+// of them writes the 128-row partial of every column to global memory (one slot per row
+// block; a reduction kernel adds the slots in a fixed order).
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace ufc {
+
+namespace fwd {
+
+constexpr int kCols = 256;                         // score tile N
+constexpr int kThreads = 576;                      // warp 0 TMA, warp 1 MMA, warps 2..17 epilogue
+constexpr int kEpiWarp0 = 2;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kNS = 3;                             // operand stages
+constexpr int kXBytes = kTileRows * kChunk * 2;    // 16 KB
+constexpr int kYBytes = kCols * kChunk * 2;        // 32 KB
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+constexpr int off_x = 0;
+constexpr int off_y = off_x + kNS * kXBytes;
+constexpr int off_colf = off_y + kNS * kYBytes;                    // [4][kMaxPrefix][256] sigma_j
+constexpr int off_rowf = off_colf + 4 * kMaxPrefix * kCols * 4;    // [kMaxPrefix][128] L rho_i
+constexpr int off_cpart = off_rowf + kMaxPrefix * kTileRows * 4;   // [2][4 quarters][4 quadrants][64]
+constexpr int off_bar = off_cpart + 2 * 4 * 4 * 64 * 4;
+constexpr int n_bars = 2 * kNS + 2 + 2 + 1;
+constexpr int off_misc = off_bar + n_bars * 8;
+constexpr int smem_bytes = off_misc + 16 + 1024;  // + slack for 1024-byte alignment
+static_assert(smem_bytes <= 232448, "forward shared memory");
+
+struct Params {
+  int64_t nx, ny;
+  int n_prefix;
+  int prefix_end[kMaxPrefix];
+  int n_col_tiles;      // ceil(ny / 256)
+  int tiles_per_split;
+  float L, b2;          // see TileParams
+  const float* rinv_x;  // [n][nx]
+  const float* rinv_y;  // [n][ny]
+  float* rowacc;        // [split * 4 + quarter][n][nx]
+  float* colacc;        // [row block][n][ny] (CLIP) or NULL
+  int* status;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  if (p.status) atomicExch(p.status, kStatusTimeout);
+}
+
+// Sum of 32 values over the warp's 32 lanes, scattered: lane l returns the sum of v[l].
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float lo = v[i], hi = v[i + m];
+      const float send = upper ? lo : hi;
+      const float keep = upper ? hi : lo;
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  return v[0];
+}
+
+// The order in which tiles and bands are fed to the MMA: tiles in pairs (t even in
+// accumulator 0, t + 1 in accumulator 1), band by band, alternating within a pair.
+// Step index s -> (tile, band); the producer, the MMA issuer and the epilogue all walk it.
+struct Schedule {
+  int T, n;
+  __device__ int steps() const { return T * n; }
+  __device__ void at(int s, int& t, int& b) const {
+    const int pair = s / (2 * n);
+    const int rem = s - pair * 2 * n;
+    const int tp = 2 * pair;
+    const int width = (tp + 1 < T) ? 2 : 1;  // the last pair may hold one tile
+    b = rem / width;
+    t = tp + rem % width;
+  }
+};
+
+template <int KIND, bool COLS>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sx = smem + off_x;
+  uint8_t* sy = smem + off_y;
+  float* colf = reinterpret_cast<float*>(smem + off_colf);
+  float* rowf = reinterpret_cast<float*>(smem + off_rowf);
+  float* cpart = reinterpret_cast<float*>(smem + off_cpart);
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + off_bar);
+  uint64_t* s_empty = s_full + kNS;
+  uint64_t* acc_full = s_empty + kNS;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_misc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
+  const int split = blockIdx.y;
+  const int n = p.n_prefix;
+  const int t_begin = split * p.tiles_per_split;
+  const int T = min(p.n_col_tiles, t_begin + p.tiles_per_split) - t_begin;
+  const Schedule sched{T, n};
+  int pend[kMaxPrefix];
+#pragma unroll
+  for (int k = 0; k < kMaxPrefix; ++k) pend[k] = p.prefix_end[k];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_y);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (T > 0 && warp == 0 && lane == 0) {
+    // ------------------------------------------------------------- operand producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int s = 0; s < sched.steps() && ok; ++s) {
+      int t, b;
+      sched.at(s, t, b);
+      const int j0 = (t_begin + t) * kCols;
+      const int c0 = b == 0 ? 0 : pend[b - 1] / kChunk, c1 = pend[b] / kChunk;
+      for (int c = c0; c < c1; ++c, ++it) {
+        const uint32_t st = it % kNS, ph = (it / kNS) & 1;
+        if (!wait_bounded(&s_empty[st], ph ^ 1, abort_flag)) {
+          fail(p, abort_flag);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&s_full[st], kXBytes + kYBytes);
+        tma_load_2d(sx + st * kXBytes, &tm_x, &s_full[st], c * kChunk, static_cast<int>(i0));
+        tma_load_2d(sy + st * kYBytes, &tm_y, &s_full[st], c * kChunk, j0);
+      }
+    }
+    for (uint32_t k = 0; k < kNS && k < it; ++k) {  // let the last copies land
+      const uint32_t q = it - 1 - k;
+      mbar_wait(&s_full[q % kNS], (q / kNS) & 1, kWaitLimitNs);
+    }
+  } else if (T > 0 && warp == 1 && lane == 0) {
+    // ------------------------------------------------------------- MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(kTileRows, kCols);
+    uint32_t it = 0;
+    uint32_t uses[2] = {0, 0};
+    bool ok = true;
+    for (int s = 0; s < sched.steps() && ok; ++s) {
+      int t, b;
+      sched.at(s, t, b);
+      const int a = t & 1;
+      if (uses[a] > 0 && !wait_bounded(&acc_empty[a], (uses[a] - 1) & 1, abort_flag)) {
+        fail(p, abort_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + a * kCols;
+      const int c0 = b == 0 ? 0 : pend[b - 1] / kChunk, c1 = pend[b] / kChunk;
+      for (int c = c0; c < c1; ++c, ++it) {
+        const uint32_t st = it % kNS, ph = (it / kNS) & 1;
+        if (!wait_bounded(&s_full[st], ph, abort_flag)) {
+          fail(p, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ax = smem_u32(sx + st * kXBytes), ay = smem_u32(sy + st * kYBytes);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk)  // bands accumulate: only a tile's first step starts fresh
+          umma_bf16(d, sdesc_kmajor_sw128(ax + kk * 32), sdesc_kmajor_sw128(ay + kk * 32), idesc,
+                    (c != 0 || kk != 0) ? 1u : 0u);
+        umma_commit(&s_empty[st]);
+      }
+      if (ok) umma_commit(&acc_full[a]);
+      ++uses[a];
+    }
+    umma_commit(drain);
+    mbar_wait(drain, 0, kWaitLimitNs);
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;                       // TMEM lane quadrant (rows 32q..32q+31)
+    const int cq = (warp - kEpiWarp0) >> 2;       // column quarter (64 columns)
+    const int r = q * 32 + lane;
+    const int64_t gi = i0 + r;
+    const bool row_ok = gi < p.nx;
+    const int etid = threadIdx.x - kEpiWarp0 * 32;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    constexpr int CF = kMaxPrefix * kCols;  // floats per column-factor buffer
+    if (cq == 0) {
+#pragma unroll
+      for (int k = 0; k < kMaxPrefix; ++k)
+        if (k < n) rowf[k * kTileRows + r] = row_ok ? p.L * p.rinv_x[k * p.nx + gi] : 0.f;
+    }
+    // column factors of tile t live in colf[t & 3]; a tile pair's factors are fetched by
+    // cp.async while the previous pair is processed
+    auto prefetch_colf = [&](int t) {
+      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
+      float* cf = colf + (t & 3) * CF;
+      for (int e = etid; e < n * kCols; e += kEpiThreads) {
+        const int k = e / kCols, c = e % kCols;
+        const int64_t gj = j0 + c;
+        const bool v = gj < p.ny;
+        cp_async4(cf + k * kCols + c, p.rinv_y + (v ? k * p.ny + gj : 0), v ? 4u : 0u);
+      }
+    };
+    for (int t = 0; t < 2 && t < T; ++t) prefetch_colf(t);
+    cp_async_commit();
+    float acc_row[kMaxPrefix];
+#pragma unroll
+    for (int k = 0; k < kMaxPrefix; ++k) acc_row[k] = 0.f;
+    uint32_t uses[2] = {0, 0};
+    uint32_t snap = 0;  // snapshots processed (selects the column-partial buffer)
+    bool ok = true;
+    for (int s = 0; s < sched.steps(); ++s) {
+      int t, b;
+      sched.at(s, t, b);
+      if ((t & 1) == 0 && b == 0) {
+        // a tile pair begins (every warp reaches this point at the same step)
+        named_bar_sync(1, kEpiThreads);          // all are done with the previous pair
+        for (int u = 2; u < 4 && t + u < T; ++u) prefetch_colf(t + u);
+        cp_async_commit();
+        cp_async_wait<1>();                      // this pair's factors (fetched a pair ago) are in
+        named_bar_sync(1, kEpiThreads);
+      }
+      const int a = t & 1;
+      const int k = b;
+      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
+      if (ok && !wait_bounded(&acc_full[a], uses[a] & 1, abort_flag)) {
+        fail(p, abort_flag);
+        ok = false;
+      }
+      if (ok) {
+        tc_fence_after();
+        float v[64];
+        tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[a]);
+
+        const float* cf = colf + (t & 3) * CF + k * kCols + cq * 64;
+        const float R1 = rowf[k * kTileRows + r];
+        const int64_t left = p.ny - j0;
+        const int ncols = left < kCols ? static_cast<int>(left) : kCols;
+        const int dcol = static_cast<int>(i0 - j0) + r;  // tile column of this row's positive, if any
+        float rs = 0.f;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          float e[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = cq * 64 + g * 32 + j;
+            const float tt = R1 * cf[g * 32 + j];
+            float val;
+            if constexpr (KIND == KIND_SIGLIP) {
+              const float x2 = fmaf(tt, v[g * 32 + j], p.b2);
+              val = fmaxf(x2, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(x2)));
+            } else {
+              val = ex2_approx(fmaf(tt, v[g * 32 + j], -p.L));
+            }
+            const bool keep = row_ok && col < ncols && col != dcol;
+            e[j] = keep ? val : 0.f;
+            rs += e[j];
+          }
+          if constexpr (COLS) {
+            const float colsum = reduce_scatter32(e, lane);  // this warp's rows, column cq*64 + g*32 + lane
+            cpart[(((snap & 1) * 4 + cq) * 4 + q) * 64 + g * 32 + lane] = colsum;
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < kMaxPrefix; ++kk)
+          if (kk == k) acc_row[kk] += rs;
+      }
+      ++uses[a];
+      if constexpr (COLS) {
+        // combine the four row quadrants of this column quarter; one warp writes the partial
+        named_bar_sync(2 + cq, 128);
+        if (ok && q == 0) {
+          const float* cp = cpart + (((snap & 1) * 4 + cq) * 4) * 64;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int c = g * 32 + lane;
+            const float sum = cp[c] + cp[64 + c] + cp[128 + c] + cp[192 + c];
+            const int64_t gj = j0 + cq * 64 + c;
+            if (gj < p.ny) p.colacc[(static_cast<int64_t>(blockIdx.x) * n + k) * p.ny + gj] = sum;
+          }
+        }
+      }
+      ++snap;
+    }
+    cp_async_wait<0>();
+    if (row_ok && ok) {
+      const int slot = split * 4 + cq;
+      for (int k = 0; k < n; ++k) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi] = acc_row[k];
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int KIND, bool COLS>
+static cudaError_t setup_one() {
+  return cudaFuncSetAttribute(fwd_kernel<KIND, COLS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+}  // namespace fwd
+
+cudaError_t fwd_kernel_setup() {
+  cudaError_t e;
+  if ((e = fwd::setup_one<KIND_CLIP, true>()) != cudaSuccess) return e;
+  if ((e = fwd::setup_one<KIND_ROWS, false>()) != cudaSuccess) return e;
+  return fwd::setup_one<KIND_SIGLIP, false>();
+}
+
+cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const FwdParams& q, dim3 grid,
+                       cudaStream_t stream) {
+  fwd::Params p;
+  p.nx = q.nx;
+  p.ny = q.ny;
+  p.n_prefix = q.n_prefix;
+  for (int k = 0; k < kMaxPrefix; ++k) p.prefix_end[k] = q.prefix_end[k];
+  p.n_col_tiles = q.n_col_tiles;
+  p.tiles_per_split = q.tiles_per_split;
+  p.L = q.L;
+  p.b2 = q.b2;
+  p.rinv_x = q.rinv_x;
+  p.rinv_y = q.rinv_y;
+  p.rowacc = q.rowacc;
+  p.colacc = q.colacc;
+  p.status = q.status;
+  if (kind == KIND_CLIP)
+    fwd::fwd_kernel<KIND_CLIP, true><<<grid, fwd::kThreads, fwd::smem_bytes, stream>>>(tm_x, tm_y, p);
+  else if (kind == KIND_ROWS)
+    fwd::fwd_kernel<KIND_ROWS, false><<<grid, fwd::kThreads, fwd::smem_bytes, stream>>>(tm_x, tm_y, p);
+  else
+    fwd::fwd_kernel<KIND_SIGLIP, false><<<grid, fwd::kThreads, fwd::smem_bytes, stream>>>(tm_x, tm_y, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ufc

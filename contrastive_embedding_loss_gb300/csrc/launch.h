@@ -11,6 +11,26 @@ namespace ufc {
 // Load every auxiliary kernel now (aux_kernels.cu).
 cudaError_t aux_kernels_setup();
 
+// Forward statistics with 128 x 256 score tiles (fwd_kernel.cu): row sums of every
+// prefix over the negatives, and (CLIP) 128-row partial column sums.
+struct FwdParams {
+  int64_t nx, ny;
+  int n_prefix;
+  int prefix_end[kMaxPrefix];
+  int n_col_tiles;          // ceil(ny / 256)
+  int tiles_per_split;
+  float L, b2;
+  const float* rinv_x;
+  const float* rinv_y;
+  float* rowacc;            // [split * 4 + column quarter][n][nx]
+  float* colacc;            // [row block][n][ny] (CLIP only)
+  int* status;
+};
+constexpr int kFwdCols = 256;
+cudaError_t fwd_kernel_setup();
+cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const FwdParams& p, dim3 grid,
+                       cudaStream_t stream);
+
 // Fused score kernel (tile_kernel.cu).
 cudaError_t tile_kernel_setup();
 cudaError_t launch_tile(int mode, int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y,

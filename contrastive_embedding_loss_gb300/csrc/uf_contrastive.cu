@@ -43,8 +43,9 @@ struct Plan {
   int kind = 0;
   bool grads = false;
   int64_t rb_a = 0, rb_b = 0, tiles_a = 0, tiles_b = 0;  // row blocks / column tiles with X = A or X = B
+  int64_t ftiles = 0;                                     // forward: 256-column tiles of B
   int slices = 0;
-  Split fwd_a, fwd_b, bwd_a, bwd_b;
+  Split fwd_a, bwd_a, bwd_b;
   int64_t lda = 0, ldb = 0;  // padded leading dimensions of A^T and B^T
   // offsets
   size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
@@ -75,8 +76,8 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.tiles_a = cdiv(Nb, kTileCols);  // X = A walks B's rows
   P.tiles_b = cdiv(Na, kTileCols);  // X = B walks A's rows
   P.slices = static_cast<int>(cdiv(prefixes[n - 1], kSliceDims));
-  P.fwd_a = plan_split(P.rb_a, 1, P.tiles_a);
-  P.fwd_b = plan_split(P.rb_b, 1, P.tiles_b);
+  P.ftiles = cdiv(Nb, kFwdCols);
+  P.fwd_a = plan_split(P.rb_a, 1, P.ftiles);
   P.bwd_a = plan_split(P.rb_a, P.slices, P.tiles_a);
   P.bwd_b = plan_split(P.rb_b, P.slices, P.tiles_b);
   P.lda = cdiv(Na, 64) * 64;
@@ -97,10 +98,10 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.o_fa = take(f * n * Na);
   P.o_fb = take(f * n * Nb);
   // row-statistic partials: forward (CLIP/ROWS), or the SigLIP loss sums
-  int slots_a = 2 * P.fwd_a.splits;
+  int slots_a = 4 * P.fwd_a.splits;  // forward: one slot per split and column quarter
   if (kind == KIND_SIGLIP && grads) slots_a = 2 * P.bwd_a.splits;
   P.o_acc_a = take(f * n * Na * slots_a);
-  P.o_acc_b = take(kind == KIND_CLIP ? f * n * Nb * 2 * P.fwd_b.splits : 0);
+  P.o_acc_b = take(kind == KIND_CLIP ? f * n * Nb * P.rb_a : 0);  // CLIP: 128-row column partials
   P.o_crow_a = take(grads ? f * n * Na * 2 * P.bwd_a.splits : 0);
   P.o_crow_b = take(grads ? f * n * Nb * 2 * P.bwd_b.splits : 0);
   P.o_terms_a = take(f * n * Na);
@@ -223,7 +224,8 @@ uf_status_t uf_contrastive_init(int device) {
   uf_status_t st = UF_OK;
   if (cudaGetDeviceProperties(&prop, device) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
     st = UF_CUDA_ERROR;
-  } else if (tile_kernel_setup() != cudaSuccess || aux_kernels_setup() != cudaSuccess || !get_encode()) {
+  } else if (tile_kernel_setup() != cudaSuccess || fwd_kernel_setup() != cudaSuccess ||
+             aux_kernels_setup() != cudaSuccess || !get_encode()) {
     st = UF_CUDA_ERROR;
   }
   cudaSetDevice(prev);
@@ -282,8 +284,9 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
   const bool siglip = kind == KIND_SIGLIP;
 
   // ---- tensor maps
-  CUtensorMap tmA, tmB, tmAt, tmBt;
-  if (!encode_map(&tmA, A, Na, D, D, kTileRows) || !encode_map(&tmB, B, Nb, D, D, kTileRows))
+  CUtensorMap tmA, tmB, tmAt, tmBt, tmBf;
+  if (!encode_map(&tmA, A, Na, D, D, kTileRows) || !encode_map(&tmB, B, Nb, D, D, kTileRows) ||
+      !encode_map(&tmBf, B, Nb, D, D, kFwdCols))
     return UF_CUDA_ERROR;
   uint16_t* At = reinterpret_cast<uint16_t*>(ws + P.o_at);
   uint16_t* Bt = reinterpret_cast<uint16_t*>(ws + P.o_bt);
@@ -368,27 +371,33 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
   sp.terms_b = terms_b;
   sp.loss = loss_per_prefix;
 
-  // ---- 2. forward row statistics (all kinds without gradients; CLIP/ROWS with them)
+  // ---- 2. forward statistics (all kinds without gradients; CLIP/ROWS with them): one pass
+  // over the grid gives every row sum and, for CLIP, every column sum
   if (!siglip || !grads) {
-    TileParams t = base_tile(true);
-    t.tiles_per_split = P.fwd_a.tiles_per_split;
-    t.rowacc = F(P.o_acc_a);
+    FwdParams fp{};
+    fp.nx = Na;
+    fp.ny = Nb;
+    fp.n_prefix = n;
+    for (int k = 0; k < n; ++k) fp.prefix_end[k] = prefixes[k];
+    fp.n_col_tiles = static_cast<int>(P.ftiles);
+    fp.tiles_per_split = P.fwd_a.tiles_per_split;
+    fp.L = logit_scale * log2e;
+    fp.b2 = bias * log2e;
+    fp.rinv_x = F(P.o_rinv_a);
+    fp.rinv_y = F(P.o_rinv_b);
+    fp.rowacc = F(P.o_acc_a);
+    fp.colacc = kind == KIND_CLIP ? F(P.o_acc_b) : nullptr;
+    fp.status = device_status;
     {
       ProfScope ps(UF_KERNEL_FWD_TILE, 1, stream);
-      UF_CHECK(launch_tile(MODE_FWD, kind, tmA, tmB, tmB, t,
-                           dim3(static_cast<unsigned>(P.rb_a), P.fwd_a.splits, 1), stream));
+      UF_CHECK(launch_fwd(kind, tmA, tmBf, fp, dim3(static_cast<unsigned>(cdiv(Na, kTileRows)), P.fwd_a.splits, 1),
+                          stream));
     }
-    sp.rowacc_a = t.rowacc;
-    sp.slots_a = 2 * P.fwd_a.splits;
+    sp.rowacc_a = fp.rowacc;
+    sp.slots_a = 4 * P.fwd_a.splits;
     if (kind == KIND_CLIP) {
-      TileParams tb = base_tile(false);
-      tb.tiles_per_split = P.fwd_b.tiles_per_split;
-      tb.rowacc = F(P.o_acc_b);
-      ProfScope ps(UF_KERNEL_FWD_TILE, 1, stream);
-      UF_CHECK(launch_tile(MODE_FWD, kind, tmB, tmA, tmA, tb,
-                           dim3(static_cast<unsigned>(P.rb_b), P.fwd_b.splits, 1), stream));
-      sp.rowacc_b = tb.rowacc;
-      sp.slots_b = 2 * P.fwd_b.splits;
+      sp.rowacc_b = fp.colacc;
+      sp.slots_b = static_cast<int>(P.rb_a);
     }
     ProfScope ps(UF_KERNEL_STATS, 2, stream);
     UF_CHECK(launch_stats(sp, stream));
