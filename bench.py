@@ -6,8 +6,8 @@ the path.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
---impl reference times the float64 CPU oracle on the host cores instead (the reference
-arm: there is no runnable reference implementation of this path).
+--impl reference times the float64 CPU oracle on the host cores instead: the pages publish no
+runnable implementation of this path, so the oracle stands in as the reference arm.
 """
 import argparse
 import hashlib
