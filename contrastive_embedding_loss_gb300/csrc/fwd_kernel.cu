@@ -95,6 +95,38 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// One snapshot of this thread's 64 cells: the row sum is returned, and (COLS) the
+// warp's 32-row column partials of the 64 columns go to cp[0..63].  CHECK evaluates the
+// masks (padding columns and rows, the positive's diagonal cell).
+template <int KIND, bool COLS, bool CHECK>
+__device__ __forceinline__ float fwd_cells(const float (&v)[64], const float* cf, float R1, float L, float b2,
+                                           int col_base, int ncols, int dcol, bool row_ok, int lane, float* cp) {
+  float rs = 0.f;
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    float e[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float tt = R1 * cf[g * 32 + j];
+      float val;
+      if constexpr (KIND == KIND_SIGLIP) {
+        const float x2 = fmaf(tt, v[g * 32 + j], b2);
+        val = fmaxf(x2, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(x2)));
+      } else {
+        val = ex2_approx(fmaf(tt, v[g * 32 + j], -L));
+      }
+      if constexpr (CHECK) {
+        const int col = col_base + g * 32 + j;
+        val = (row_ok && col < ncols && col != dcol) ? val : 0.f;
+      }
+      e[j] = val;
+      rs += val;
+    }
+    if constexpr (COLS) cp[g * 32 + lane] = reduce_scatter32(e, lane);  // column col_base + g*32 + lane
+  }
+  return rs;
+}
+
 // The order in which tiles and bands are fed to the MMA: tiles in pairs (t even in
 // accumulator 0, t + 1 in accumulator 1), band by band, alternating within a pair.
 // Step index s -> (tile, band); the producer, the MMA issuer and the epilogue all walk it.
@@ -293,30 +325,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t left = p.ny - j0;
         const int ncols = left < kCols ? static_cast<int>(left) : kCols;
         const int dcol = static_cast<int>(i0 - j0) + r;  // tile column of this row's positive, if any
-        float rs = 0.f;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          float e[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = cq * 64 + g * 32 + j;
-            const float tt = R1 * cf[g * 32 + j];
-            float val;
-            if constexpr (KIND == KIND_SIGLIP) {
-              const float x2 = fmaf(tt, v[g * 32 + j], p.b2);
-              val = fmaxf(x2, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(x2)));
-            } else {
-              val = ex2_approx(fmaf(tt, v[g * 32 + j], -p.L));
-            }
-            const bool keep = row_ok && col < ncols && col != dcol;
-            e[j] = keep ? val : 0.f;
-            rs += e[j];
-          }
-          if constexpr (COLS) {
-            const float colsum = reduce_scatter32(e, lane);  // this warp's rows, column cq*64 + g*32 + lane
-            cpart[(((snap & 1) * 4 + cq) * 4 + q) * 64 + g * 32 + lane] = colsum;
-          }
-        }
+        // masks are only evaluated in the few tiles that need them (padding columns, the
+        // positives' diagonal, padding rows); every other tile takes the unmasked path
+        const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
+        const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (i0 + kTileRows > p.nx);
+        float* cp = cpart + (((snap & 1) * 4 + cq) * 4 + q) * 64;
+        const float rs = check ? fwd_cells<KIND, COLS, true>(v, cf, R1, p.L, p.b2, cq * 64, ncols, dcol, row_ok, lane, cp)
+                               : fwd_cells<KIND, COLS, false>(v, cf, R1, p.L, p.b2, cq * 64, ncols, dcol, row_ok, lane, cp);
 #pragma unroll
         for (int kk = 0; kk < kMaxPrefix; ++kk)
           if (kk == k) acc_row[kk] += rs;
