@@ -108,9 +108,11 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restri
     tile[y][tx] = (r < rows) ? X[r * d + c0 + tx] : uint16_t(0);
   }
   __syncthreads();
+  // the grid spans ld = rows rounded up to 64, so the padding columns get the zeros
+  // loaded above: the gradient GEMM reads them (with zero weights) and must not meet NaNs
   for (int y = ty; y < 64; y += 4) {
     const int64_t r = r0 + tx;
-    if (r < rows) Xt[static_cast<int64_t>(c0 + y) * ld + r] = tile[tx][y];
+    Xt[static_cast<int64_t>(c0 + y) * ld + r] = tile[tx][y];
   }
 }
 

@@ -31,10 +31,14 @@ cudaError_t fwd_kernel_setup();
 cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const FwdParams& p, dim3 grid,
                        cudaStream_t stream);
 
-// Fused score kernel (tile_kernel.cu).
-cudaError_t tile_kernel_setup();
-cudaError_t launch_tile(int mode, int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y,
-                        const CUtensorMap& tm_yt, const TileParams& p, dim3 grid, cudaStream_t stream);
+// Backward with 128 x 256 score tiles and a 256-dimension gradient slice per CTA
+// (bwd_kernel.cu).  tm_x: [128 x 64] boxes of X; tm_y: [256 x 64] boxes of Y; tm_yt:
+// [64 x 64] boxes of Y^T.  grid = (row blocks of X, splits of the column tiles, slices).
+constexpr int kBwdCols = 256;
+constexpr int kBwdYtBox = 64;
+cudaError_t bwd_kernel_setup();
+cudaError_t launch_bwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const CUtensorMap& tm_yt,
+                       const TileParams& p, dim3 grid, cudaStream_t stream);
 
 // Per-row inverse norms of every prefix for A and B, plus the positives' cosines
 // cos_ii for i < min(Na, Nb).  Layouts [n][rows].

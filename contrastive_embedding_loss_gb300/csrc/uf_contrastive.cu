@@ -73,8 +73,8 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.grads = grads;
   P.rb_a = cdiv(Na, kTileRows);
   P.rb_b = cdiv(Nb, kTileRows);
-  P.tiles_a = cdiv(Nb, kTileCols);  // X = A walks B's rows
-  P.tiles_b = cdiv(Na, kTileCols);  // X = B walks A's rows
+  P.tiles_a = cdiv(Nb, kBwdCols);  // backward, X = A: 256-row tiles of B
+  P.tiles_b = cdiv(Na, kBwdCols);  // backward, X = B: 256-row tiles of A
   P.slices = static_cast<int>(cdiv(prefixes[n - 1], kSliceDims));
   P.ftiles = cdiv(Nb, kFwdCols);
   P.fwd_a = plan_split(P.rb_a, 1, P.ftiles);
@@ -99,11 +99,11 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.o_fb = take(f * n * Nb);
   // row-statistic partials: forward (CLIP/ROWS), or the SigLIP loss sums
   int slots_a = 4 * P.fwd_a.splits;  // forward: one slot per split and column quarter
-  if (kind == KIND_SIGLIP && grads) slots_a = 2 * P.bwd_a.splits;
+  if (kind == KIND_SIGLIP && grads) slots_a = 4 * P.bwd_a.splits;
   P.o_acc_a = take(f * n * Na * slots_a);
   P.o_acc_b = take(kind == KIND_CLIP ? f * n * Nb * P.rb_a : 0);  // CLIP: 128-row column partials
-  P.o_crow_a = take(grads ? f * n * Na * 2 * P.bwd_a.splits : 0);
-  P.o_crow_b = take(grads ? f * n * Nb * 2 * P.bwd_b.splits : 0);
+  P.o_crow_a = take(grads ? f * n * Na * 4 * P.bwd_a.splits : 0);  // one slot per split and column quarter
+  P.o_crow_b = take(grads ? f * n * Nb * 4 * P.bwd_b.splits : 0);
   P.o_terms_a = take(f * n * Na);
   P.o_terms_b = take(f * n * Nb);
   P.o_loss = take(f * kMaxPrefix);
@@ -224,7 +224,7 @@ uf_status_t uf_contrastive_init(int device) {
   uf_status_t st = UF_OK;
   if (cudaGetDeviceProperties(&prop, device) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
     st = UF_CUDA_ERROR;
-  } else if (tile_kernel_setup() != cudaSuccess || fwd_kernel_setup() != cudaSuccess ||
+  } else if (bwd_kernel_setup() != cudaSuccess || fwd_kernel_setup() != cudaSuccess ||
              aux_kernels_setup() != cudaSuccess || !get_encode()) {
     st = UF_CUDA_ERROR;
   }
@@ -284,14 +284,16 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
   const bool siglip = kind == KIND_SIGLIP;
 
   // ---- tensor maps
-  CUtensorMap tmA, tmB, tmAt, tmBt, tmBf;
+  // [128 x 64] boxes for the owner rows, [256 x 64] for the walked rows, [64 dims x 64] for
+  // the transposed operand of the gradient GEMM
+  CUtensorMap tmA, tmB, tmAt, tmBt, tmAf, tmBf;
   if (!encode_map(&tmA, A, Na, D, D, kTileRows) || !encode_map(&tmB, B, Nb, D, D, kTileRows) ||
-      !encode_map(&tmBf, B, Nb, D, D, kFwdCols))
+      !encode_map(&tmAf, A, Na, D, D, kBwdCols) || !encode_map(&tmBf, B, Nb, D, D, kFwdCols))
     return UF_CUDA_ERROR;
   uint16_t* At = reinterpret_cast<uint16_t*>(ws + P.o_at);
   uint16_t* Bt = reinterpret_cast<uint16_t*>(ws + P.o_bt);
   if (grads) {
-    if (!encode_map(&tmAt, At, D, Na, P.lda, kSliceDims) || !encode_map(&tmBt, Bt, D, Nb, P.ldb, kSliceDims))
+    if (!encode_map(&tmAt, At, D, Na, P.lda, kBwdYtBox) || !encode_map(&tmBt, Bt, D, Nb, P.ldb, kBwdYtBox))
       return UF_CUDA_ERROR;
   } else {
     tmAt = tmA;
@@ -420,12 +422,12 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     t.crow = F(P.o_crow_a);
     t.grad = ga;
     ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-    UF_CHECK(launch_tile(MODE_BWD, kind, tmA, tmB, tmBt, t,
-                         dim3(static_cast<unsigned>(P.rb_a), P.bwd_a.splits, P.slices), stream));
+    UF_CHECK(launch_bwd(kind, tmA, tmBf, tmBt, t, dim3(static_cast<unsigned>(P.rb_a), P.bwd_a.splits, P.slices),
+                        stream));
   }
   if (siglip) {
     sp.rowacc_a = F(P.o_acc_a);
-    sp.slots_a = 2 * P.bwd_a.splits;
+    sp.slots_a = 4 * P.bwd_a.splits;
     ProfScope ps(UF_KERNEL_STATS, 2, stream);
     UF_CHECK(launch_stats(sp, stream));
   }
@@ -439,8 +441,8 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     t.crow = F(P.o_crow_b);
     t.grad = gb;
     ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-    UF_CHECK(launch_tile(MODE_BWD, kind, tmB, tmA, tmAt, t,
-                         dim3(static_cast<unsigned>(P.rb_b), P.bwd_b.splits, P.slices), stream));
+    UF_CHECK(launch_bwd(kind, tmB, tmAf, tmAt, t, dim3(static_cast<unsigned>(P.rb_b), P.bwd_b.splits, P.slices),
+                        stream));
   }
 
   // ---- 4. projection term and diagonal correction
@@ -473,7 +475,7 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
       q.z_y = F(P.o_zr);
     }
     q.crow = F(xa ? P.o_crow_a : P.o_crow_b);
-    q.crow_slots = 2 * (xa ? P.bwd_a.splits : P.bwd_b.splits);
+    q.crow_slots = 4 * (xa ? P.bwd_a.splits : P.bwd_b.splits);
     q.G = xa ? ga : gb;
     q.g_splits = xa ? P.bwd_a.splits : P.bwd_b.splits;
     q.dX = xa ? dA : dB;
