@@ -104,7 +104,7 @@ def uf_contrastive_fwd_bwd(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, p
                                              stream))
 
 
-KERNEL_GROUPS = ("prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd")
+KERNEL_GROUPS = ("prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd", "gemm")
 
 
 def uf_contrastive_profile(enable: bool) -> int:

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libuf_contrastive.so"
-SOURCES = ["bwd_kernel.cu", "fwd_kernel.cu", "aux_kernels.cu", "uf_contrastive.cu", "uf_static.cu"]
+SOURCES = ["wgt_kernel.cu", "gemm_kernel.cu", "fwd_kernel.cu", "aux_kernels.cu", "uf_contrastive.cu", "uf_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

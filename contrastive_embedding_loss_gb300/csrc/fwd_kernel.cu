@@ -54,7 +54,7 @@ struct Params {
   int prefix_end[kMaxPrefix];
   int n_col_tiles;      // ceil(ny / 256)
   int tiles_per_split;
-  float L, b2;          // see TileParams
+  float L, b2;          // CLIP/ROWS: tau*log2(e) (also the fixed shift); SigLIP: t*log2(e), bias*log2(e)
   const float* rinv_x;  // [n][nx]
   const float* rinv_y;  // [n][ny]
   float* rowacc;        // [split * 4 + quarter][n][nx]

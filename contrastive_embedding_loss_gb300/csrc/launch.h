@@ -31,14 +31,54 @@ cudaError_t fwd_kernel_setup();
 cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const FwdParams& p, dim3 grid,
                        cudaStream_t stream);
 
-// Backward with 128 x 256 score tiles and a 256-dimension gradient slice per CTA
-// (bwd_kernel.cu).  tm_x: [128 x 64] boxes of X; tm_y: [256 x 64] boxes of Y; tm_yt:
-// [64 x 64] boxes of Y^T.  grid = (row blocks of X, splits of the column tiles, slices).
-constexpr int kBwdCols = 256;
+// Backward weights (wgt_kernel.cu): m^k_ij = rho_i sigma_j dL/dcos^k_ij as bf16 into a
+// [prefix][row][column] array (row stride in elements fixed by tm_w), plus the row
+// scalars sum_j m_ij dot_ij and (SigLIP) the row loss sums.  One launch covers rows
+// [row0, row0 + rows) of X; grid = (ceil(rows / 128), splits of the 256-column tiles).
+// tm_x: [128 x 64] boxes of X; tm_y: [256 x 64] boxes of Y; tm_w: [32 x 64] boxes of the
+// weight array viewed as [n * w_rows_per_prefix rows][ny columns].
+struct WgtParams {
+  int64_t nx, ny;                 // full sizes of X and Y
+  int64_t row0, rows;             // this launch's rows of X
+  int n_prefix;
+  int prefix_end[kMaxPrefix];
+  int n_col_tiles;                // ceil(ny / 256)
+  int tiles_per_split;
+  float L, b2;                    // CLIP/ROWS: tau*log2(e) (also the fixed shift); SigLIP: t*log2(e), bias*log2(e)
+  const float* rinv_x;            // [n][nx]
+  const float* alpha_x;           // [n][nx] rho_i alpha_i (CLIP/ROWS) or NULL
+  const float* rinv_y;            // [n][ny]
+  const float* beta_y;            // [n][ny] sigma_j beta_j (CLIP/ROWS) or NULL
+  float m_scale[kMaxPrefix];      // SigLIP: w_k t / N
+  int64_t w_rows_per_prefix;      // rows between prefixes in the weight array (multiple of 128)
+  float* crow;                    // [split * 4 + quarter][n][nx]
+  float* rowacc;                  // SigLIP: [split * 4 + quarter][n][nx] loss sums (log2 units), or NULL
+  int* status;
+};
+constexpr int kWgtCols = 256;
+constexpr int kWgtStoreRows = 32;
+cudaError_t wgt_kernel_setup();
+cudaError_t launch_wgt(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const CUtensorMap& tm_w,
+                       const WgtParams& p, dim3 grid, cudaStream_t stream);
+
+// Gradient contraction (gemm_kernel.cu): G[i, d] (+)= sum_k [d < p_k] sum_j m^k[i, j] Y[j, d]
+// for rows i < m_rows and d < p_n, dims d < d of G past p_n untouched.  tm_w: [128 x 64]
+// boxes of the weight array ([n * w_rows_per_prefix rows][kdim columns]); tm_yt: [64 x 64]
+// boxes of Y^T ([d rows][kdim columns]).
+struct GemmParams {
+  int64_t m_rows;                 // rows of G computed by this launch
+  int64_t kdim;                   // contraction length (columns of m^k)
+  int64_t w_rows_per_prefix;
+  int d;                          // row stride of G in elements
+  int n_prefix;
+  int prefix_end[kMaxPrefix];
+  float* G;                       // first row of this launch
+  int* status;
+};
 constexpr int kBwdYtBox = 64;
-cudaError_t bwd_kernel_setup();
-cudaError_t launch_bwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const CUtensorMap& tm_yt,
-                       const TileParams& p, dim3 grid, cudaStream_t stream);
+cudaError_t gemm_kernel_setup();
+cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool accumulate,
+                        cudaStream_t stream);
 
 // Per-row inverse norms of every prefix for A and B, plus the positives' cosines
 // cos_ii for i < min(Na, Nb).  Layouts [n][rows].

@@ -36,25 +36,34 @@ Split plan_split(int64_t row_blocks, int64_t slices, int64_t tiles) {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Default size of the backward weight array (bf16 m^k of every prefix for a chunk of
+// rows): a GB300 has 288 GB of HBM, so the N = 65536 workloads keep every row in one chunk.
+constexpr size_t kDefaultWeightBytes = size_t(48) << 30;
+
 // Sizes and offsets of every scratch array of one call.
 struct Plan {
   int64_t na = 0, nb = 0, nmin = 0;
   int d = 0, n = 0;
   int kind = 0;
   bool grads = false;
-  int64_t rb_a = 0, rb_b = 0, tiles_a = 0, tiles_b = 0;  // row blocks / column tiles with X = A or X = B
-  int64_t ftiles = 0;                                     // forward: 256-column tiles of B
-  int slices = 0;
-  Split fwd_a, bwd_a, bwd_b;
-  int64_t lda = 0, ldb = 0;  // padded leading dimensions of A^T and B^T
+  int64_t rb_a = 0;                  // 128-row blocks of A
+  int64_t ftiles = 0;                // forward: 256-column tiles of B
+  Split fwd_a, wgt_a, wgt_b;         // column splits of the forward and of the two weight passes
+  int64_t lda = 0, ldb = 0;          // padded leading dimensions of A^T and B^T
+  int64_t ldw = 0;                   // row stride of the weight array (elements)
+  int64_t chunk = 0;                 // rows of X per weight chunk (multiple of 128)
+  size_t fixed = 0;                  // bytes of everything but the weight array
   // offsets
   size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
-      o_terms_b, o_loss, o_at, o_bt, o_ga, o_gb, total;
+      o_terms_b, o_loss, o_at, o_bt, o_w, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int kind, bool grads, Plan& P) {
+// ws_limit: the workspace the caller provides (0: plan the default weight array).  The
+// weight array takes what is left after the fixed part, in chunks of 128 rows.
+bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int kind, bool grads, size_t ws_limit,
+               Plan& P) {
   if (Na < 1 || Nb < 1 || D < 64 || D > 4096 || D % 64 != 0 || n < 1 || n > kMaxPrefix || !prefixes) return false;
   if (kind != KIND_CLIP && kind != KIND_SIGLIP && kind != KIND_ROWS) return false;
   if ((kind == KIND_CLIP || kind == KIND_SIGLIP) && Na != Nb) return false;
@@ -72,16 +81,13 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.kind = kind;
   P.grads = grads;
   P.rb_a = cdiv(Na, kTileRows);
-  P.rb_b = cdiv(Nb, kTileRows);
-  P.tiles_a = cdiv(Nb, kBwdCols);  // backward, X = A: 256-row tiles of B
-  P.tiles_b = cdiv(Na, kBwdCols);  // backward, X = B: 256-row tiles of A
-  P.slices = static_cast<int>(cdiv(prefixes[n - 1], kSliceDims));
   P.ftiles = cdiv(Nb, kFwdCols);
   P.fwd_a = plan_split(P.rb_a, 1, P.ftiles);
-  P.bwd_a = plan_split(P.rb_a, P.slices, P.tiles_a);
-  P.bwd_b = plan_split(P.rb_b, P.slices, P.tiles_b);
+  P.wgt_a = plan_split(P.rb_a, 1, cdiv(Nb, kWgtCols));          // X = A walks B's rows
+  P.wgt_b = plan_split(cdiv(Nb, kTileRows), 1, cdiv(Na, kWgtCols));  // X = B walks A's rows
   P.lda = cdiv(Na, 64) * 64;
   P.ldb = cdiv(Nb, 64) * 64;
+  P.ldw = P.lda > P.ldb ? P.lda : P.ldb;
 
   const size_t f = sizeof(float);
   size_t o = 0;
@@ -97,20 +103,31 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.o_zc = take(f * n * Nb);
   P.o_fa = take(f * n * Na);
   P.o_fb = take(f * n * Nb);
-  // row-statistic partials: forward (CLIP/ROWS), or the SigLIP loss sums
-  int slots_a = 4 * P.fwd_a.splits;  // forward: one slot per split and column quarter
-  if (kind == KIND_SIGLIP && grads) slots_a = 4 * P.bwd_a.splits;
+  // row-statistic partials: forward (CLIP/ROWS), or the SigLIP loss sums of the A-side weight pass
+  int slots_a = 4 * P.fwd_a.splits;  // one slot per split and column quarter
+  if (kind == KIND_SIGLIP && grads) slots_a = 4 * P.wgt_a.splits;
   P.o_acc_a = take(f * n * Na * slots_a);
   P.o_acc_b = take(kind == KIND_CLIP ? f * n * Nb * P.rb_a : 0);  // CLIP: 128-row column partials
-  P.o_crow_a = take(grads ? f * n * Na * 4 * P.bwd_a.splits : 0);  // one slot per split and column quarter
-  P.o_crow_b = take(grads ? f * n * Nb * 4 * P.bwd_b.splits : 0);
+  P.o_crow_a = take(grads ? f * n * Na * 4 * P.wgt_a.splits : 0);
+  P.o_crow_b = take(grads ? f * n * Nb * 4 * P.wgt_b.splits : 0);
   P.o_terms_a = take(f * n * Na);
   P.o_terms_b = take(f * n * Nb);
   P.o_loss = take(f * kMaxPrefix);
   P.o_at = take(grads ? sizeof(uint16_t) * D * P.lda : 0);
   P.o_bt = take(grads ? sizeof(uint16_t) * D * P.ldb : 0);
-  P.o_ga = take(grads && P.bwd_a.splits > 1 ? f * D * Na * P.bwd_a.splits : 0);
-  P.o_gb = take(grads && P.bwd_b.splits > 1 ? f * D * Nb * P.bwd_b.splits : 0);
+  P.fixed = o;
+  P.o_w = o;
+  P.chunk = 0;
+  if (grads) {
+    const int64_t rows_max = cdiv(Na > Nb ? Na : Nb, kTileRows) * kTileRows;
+    const size_t row_bytes = sizeof(uint16_t) * static_cast<size_t>(n) * static_cast<size_t>(P.ldw);
+    const size_t budget = ws_limit ? (ws_limit > o ? ws_limit - o : 0) : kDefaultWeightBytes;
+    int64_t rows = static_cast<int64_t>(budget / row_bytes) / kTileRows * kTileRows;
+    if (rows > rows_max) rows = rows_max;
+    if (rows < kTileRows) rows = kTileRows;  // the minimum; a smaller workspace is rejected by the caller
+    P.chunk = rows;
+    o = align256(o + row_bytes * static_cast<size_t>(rows));
+  }
   P.total = o;
   return true;
 }
@@ -224,7 +241,8 @@ uf_status_t uf_contrastive_init(int device) {
   uf_status_t st = UF_OK;
   if (cudaGetDeviceProperties(&prop, device) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
     st = UF_CUDA_ERROR;
-  } else if (bwd_kernel_setup() != cudaSuccess || fwd_kernel_setup() != cudaSuccess ||
+  } else if (wgt_kernel_setup() != cudaSuccess || gemm_kernel_setup() != cudaSuccess ||
+             fwd_kernel_setup() != cudaSuccess ||
              aux_kernels_setup() != cudaSuccess || !get_encode()) {
     st = UF_CUDA_ERROR;
   }
@@ -236,7 +254,7 @@ uf_status_t uf_contrastive_init(int device) {
 size_t uf_contrastive_workspace_size(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix, int kind,
                                      int want_grads) {
   Plan P;
-  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, want_grads != 0, P)) return 0;
+  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, want_grads != 0, 0, P)) return 0;
   return P.total;
 }
 
@@ -250,7 +268,7 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
   if ((dA == nullptr) != (dB == nullptr)) return UF_INVALID_ARGUMENT;
   const bool grads = dA != nullptr;
   Plan P;
-  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, grads, P)) return UF_INVALID_ARGUMENT;
+  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, grads, workspace_bytes, P)) return UF_INVALID_ARGUMENT;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(workspace, 256) || !aligned(loss_per_prefix, 4))
     return UF_INVALID_ARGUMENT;
   if (grads && (!aligned(dA, 16) || !aligned(dB, 16))) return UF_INVALID_ARGUMENT;
@@ -288,7 +306,7 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
   // the transposed operand of the gradient GEMM
   CUtensorMap tmA, tmB, tmAt, tmBt, tmAf, tmBf;
   if (!encode_map(&tmA, A, Na, D, D, kTileRows) || !encode_map(&tmB, B, Nb, D, D, kTileRows) ||
-      !encode_map(&tmAf, A, Na, D, D, kBwdCols) || !encode_map(&tmBf, B, Nb, D, D, kFwdCols))
+      !encode_map(&tmAf, A, Na, D, D, kWgtCols) || !encode_map(&tmBf, B, Nb, D, D, kFwdCols))
     return UF_CUDA_ERROR;
   uint16_t* At = reinterpret_cast<uint16_t*>(ws + P.o_at);
   uint16_t* Bt = reinterpret_cast<uint16_t*>(ws + P.o_bt);
@@ -332,22 +350,6 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     ProfScope ps(UF_KERNEL_TRANSPOSE, 1, stream);
     UF_CHECK(launch_transpose(B16, Bt, Nb, D, P.ldb, stream));
   }
-
-  auto base_tile = [&](bool x_is_a) {
-    TileParams t{};
-    t.nx = x_is_a ? Na : Nb;
-    t.ny = x_is_a ? Nb : Na;
-    t.d = D;
-    t.n_prefix = n;
-    for (int k = 0; k < n; ++k) t.prefix_end[k] = prefixes[k];
-    t.n_col_tiles = static_cast<int>(x_is_a ? P.tiles_a : P.tiles_b);
-    t.L = logit_scale * log2e;
-    t.b2 = bias * log2e;
-    t.rinv_x = F(x_is_a ? P.o_rinv_a : P.o_rinv_b);
-    t.rinv_y = F(x_is_a ? P.o_rinv_b : P.o_rinv_a);
-    t.status = device_status;
-    return t;
-  };
 
   float* terms_a = row_terms ? row_terms : F(P.o_terms_a);
   float* terms_b = col_terms ? col_terms : F(P.o_terms_b);
@@ -409,40 +411,69 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     return UF_OK;
   }
 
-  // ---- 3. backward: A side (X = A), then B side (X = B)
-  float* ga = P.bwd_a.splits > 1 ? F(P.o_ga) : dA;
-  float* gb = P.bwd_b.splits > 1 ? F(P.o_gb) : dB;
-  {
-    TileParams t = base_tile(true);
-    t.tiles_per_split = P.bwd_a.tiles_per_split;
-    t.alpha_x = siglip ? nullptr : F(P.o_fa);
-    t.beta_y = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
-    for (int k = 0; k < n; ++k) t.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
-    t.rowacc = F(P.o_acc_a);
-    t.crow = F(P.o_crow_a);
-    t.grad = ga;
-    ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-    UF_CHECK(launch_bwd(kind, tmA, tmBf, tmBt, t, dim3(static_cast<unsigned>(P.rb_a), P.bwd_a.splits, P.slices),
-                        stream));
-  }
-  if (siglip) {
-    sp.rowacc_a = F(P.o_acc_a);
-    sp.slots_a = 4 * P.bwd_a.splits;
-    ProfScope ps(UF_KERNEL_STATS, 2, stream);
-    UF_CHECK(launch_stats(sp, stream));
-  }
-  {
-    TileParams t = base_tile(false);
-    t.tiles_per_split = P.bwd_b.tiles_per_split;
-    t.alpha_x = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
-    t.beta_y = siglip ? nullptr : F(P.o_fa);
-    for (int k = 0; k < n; ++k) t.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
-    t.rowacc = nullptr;  // the B side sums no loss
-    t.crow = F(P.o_crow_b);
-    t.grad = gb;
-    ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-    UF_CHECK(launch_bwd(kind, tmB, tmAf, tmAt, t, dim3(static_cast<unsigned>(P.rb_b), P.bwd_b.splits, P.slices),
-                        stream));
+  // ---- 3. backward, A side (X = A, Y = B) then B side (X = B, Y = A): per chunk of X's
+  // rows, the weight pass writes m^k (bf16) and the row scalars, and the GEMM contracts the
+  // weights with Y into G = dX before its projection (written in place into dA / dB)
+  uint16_t* W = reinterpret_cast<uint16_t*>(ws + P.o_w);
+  for (int side = 0; side < 2; ++side) {
+    const bool xa = side == 0;
+    const int64_t nx = xa ? Na : Nb, ny = xa ? Nb : Na;
+    const Split& sp_w = xa ? P.wgt_a : P.wgt_b;
+    CUtensorMap tmWs, tmWl;  // the weight array as [n * chunk rows][ny columns]: store / load boxes
+    if (!encode_map(&tmWs, W, static_cast<int64_t>(n) * P.chunk, ny, P.ldw, kWgtStoreRows) ||
+        !encode_map(&tmWl, W, static_cast<int64_t>(n) * P.chunk, ny, P.ldw, kTileRows))
+      return UF_CUDA_ERROR;
+    WgtParams wp{};
+    wp.nx = nx;
+    wp.ny = ny;
+    wp.n_prefix = n;
+    for (int k = 0; k < n; ++k) wp.prefix_end[k] = prefixes[k];
+    wp.n_col_tiles = static_cast<int>(cdiv(ny, kWgtCols));
+    wp.tiles_per_split = sp_w.tiles_per_split;
+    wp.L = logit_scale * log2e;
+    wp.b2 = bias * log2e;
+    wp.rinv_x = F(xa ? P.o_rinv_a : P.o_rinv_b);
+    wp.rinv_y = F(xa ? P.o_rinv_b : P.o_rinv_a);
+    if (xa) {
+      wp.alpha_x = siglip ? nullptr : F(P.o_fa);
+      wp.beta_y = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
+    } else {
+      wp.alpha_x = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
+      wp.beta_y = siglip ? nullptr : F(P.o_fa);
+    }
+    for (int k = 0; k < n; ++k) wp.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
+    wp.w_rows_per_prefix = P.chunk;
+    wp.crow = F(xa ? P.o_crow_a : P.o_crow_b);
+    wp.rowacc = (xa && siglip) ? F(P.o_acc_a) : nullptr;  // the A side also sums the SigLIP loss
+    wp.status = device_status;
+    GemmParams gp{};
+    gp.kdim = ny;
+    gp.w_rows_per_prefix = P.chunk;
+    gp.d = D;
+    gp.n_prefix = n;
+    for (int k = 0; k < n; ++k) gp.prefix_end[k] = prefixes[k];
+    gp.status = device_status;
+    float* G = xa ? dA : dB;
+    for (int64_t r0 = 0; r0 < nx; r0 += P.chunk) {
+      const int64_t rows = nx - r0 < P.chunk ? nx - r0 : P.chunk;
+      wp.row0 = r0;
+      wp.rows = rows;
+      {
+        ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
+        UF_CHECK(launch_wgt(kind, xa ? tmA : tmB, xa ? tmBf : tmAf, tmWs, wp,
+                            dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), sp_w.splits), stream));
+      }
+      gp.m_rows = rows;
+      gp.G = G + r0 * D;
+      ProfScope ps(UF_KERNEL_GEMM, 1, stream);
+      UF_CHECK(launch_gemm(tmWl, xa ? tmBt : tmAt, gp, false, stream));
+    }
+    if (xa && siglip) {
+      sp.rowacc_a = F(P.o_acc_a);
+      sp.slots_a = 4 * P.wgt_a.splits;
+      ProfScope ps(UF_KERNEL_STATS, 2, stream);
+      UF_CHECK(launch_stats(sp, stream));
+    }
   }
 
   // ---- 4. projection term and diagonal correction
@@ -475,9 +506,9 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
       q.z_y = F(P.o_zr);
     }
     q.crow = F(xa ? P.o_crow_a : P.o_crow_b);
-    q.crow_slots = 4 * (xa ? P.bwd_a.splits : P.bwd_b.splits);
-    q.G = xa ? ga : gb;
-    q.g_splits = xa ? P.bwd_a.splits : P.bwd_b.splits;
+    q.crow_slots = 4 * (xa ? P.wgt_a.splits : P.wgt_b.splits);
+    q.G = xa ? dA : dB;
+    q.g_splits = 1;
     q.dX = xa ? dA : dB;
     ProfScope ps(UF_KERNEL_NORM_BWD, 1, stream);
     UF_CHECK(launch_norm_bwd(q, stream));
@@ -525,7 +556,8 @@ uf_status_t uf_contrastive_profile_read(int group, double* total_ms, int64_t* pa
 }
 
 const char* uf_contrastive_profile_name(int group) {
-  static const char* names[UF_KERNEL_GROUPS] = {"prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd"};
+  static const char* names[UF_KERNEL_GROUPS] = {"prep",     "transpose", "fwd_tile", "stats",
+                                                "bwd_tile", "norm_bwd",  "gemm"};
   return (group >= 0 && group < UF_KERNEL_GROUPS) ? names[group] : "unknown";
 }
 

@@ -1,0 +1,428 @@
+// wgt_kernel.cu -- the backward weights of the Matryoshka contrastive loss, written to HBM.
+//
+// For every cell (i, j) off the diagonal and every prefix k the gradient of the loss
+// with respect to the cosine, times the two inverse norms, is
+//     m^k_ij = rho_i sigma_j dL/dcos^k_ij
+// (CLIP/ROWS: e^{s_ij - tau} rho_i sigma_j (alpha_i + beta_j) with the softmax
+// normalisers folded into alpha, beta; SigLIP: sigma(x_ij) rho_i sigma_j w_k t / N).
+// This kernel recomputes the scores tile by tile exactly like the forward pass (128 x 256
+// tcgen05 tiles, the K walk band by band into a cumulative TMEM accumulator, two
+// accumulators so the MMA of one tile overlaps the epilogue of the other) and writes m^k
+// as bf16 into a [prefix][row][column] array, 32 x 64 blocks per warp through TMA stores.
+// It also sums, per row and prefix, sum_j m_ij dot_ij (the projection term of the norm
+// backward) and, for SigLIP, the loss over the negatives.  The gradient contraction
+// G = sum_k m^k Y[:, :p_k] is then a dense GEMM over these weights (gemm_kernel.cu), so
+// the scores are computed once per side of the backward instead of once per gradient slice.
+//
+// Warps (576 threads): 0 TMA, 1 MMA, 2..17 epilogue (warp w reads TMEM lanes 32 (w % 4)..
+// and one 64-column quarter of the tile).
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace ufc {
+namespace wgt {
+
+constexpr int kCols = 256;
+constexpr int kThreads = 576;
+constexpr int kEpiWarp0 = 2;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kNS = 2;                              // operand stages
+constexpr int kXBytes = kTileRows * kChunk * 2;     // 16 KB
+constexpr int kYBytes = kCols * kChunk * 2;         // 32 KB
+constexpr int kStageRows = 32;                      // one warp's rows of a weight block
+constexpr int kStageBytes = kStageRows * kChunk * 2;  // 4 KB: [32 rows x 64 columns] bf16, 128-byte swizzle
+constexpr int kColfBytes = kMaxPrefix * 2 * kCols * 4;  // [prefix][sigma, sigma*beta][256 columns]
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+constexpr int off_x = 0;
+constexpr int off_y = off_x + kNS * kXBytes;
+constexpr int off_stage = off_y + kNS * kYBytes;           // [16 warps][4 KB]
+constexpr int off_colf = off_stage + kEpiWarps * kStageBytes;  // four buffers: two tile pairs
+constexpr int off_bar = off_colf + 4 * kColfBytes;
+constexpr int n_bars = 2 * kNS + 2 + 2 + 1;
+constexpr int off_pend = off_bar + n_bars * 8;
+constexpr int off_misc = off_pend + 4 * kMaxPrefix;
+constexpr int smem_bytes = off_misc + 16 + 1024;
+static_assert(smem_bytes <= 232448, "weight kernel shared memory");
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fail(const WgtParams& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  if (p.status) atomicExch(p.status, kStatusTimeout);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 8 cells: their weights as four packed bf16 pairs; adds to the row scalar and (SigLIP,
+// loss != 0) to the loss over the negatives.  c1, c2: shared addresses of the columns'
+// factors.  CHECK evaluates the masks (padding rows and columns, the positive's cell).
+template <int KIND, bool CHECK>
+__device__ __forceinline__ uint4 cells8(const float* dot, uint32_t c1, uint32_t c2, float R1, float R2, float R3,
+                                        float L, float b2, int col0, int ncols, int dcol, bool row_ok, float& acc_c,
+                                        float& acc_l) {
+  const float4 s1a = ld_shared_v4f(c1), s1b = ld_shared_v4f(c1 + 16);
+  const float s1v[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
+  float s2v[8];
+  if constexpr (KIND != KIND_SIGLIP) {
+    const float4 s2a = ld_shared_v4f(c2), s2b = ld_shared_v4f(c2 + 16);
+    s2v[0] = s2a.x; s2v[1] = s2a.y; s2v[2] = s2a.z; s2v[3] = s2a.w;
+    s2v[4] = s2b.x; s2v[5] = s2b.y; s2v[6] = s2b.z; s2v[7] = s2b.w;
+  }
+  uint32_t packed[4];
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    float mv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int jj = j + u;
+      const float s1 = s1v[jj];
+      const float t = R1 * s1;
+      float m;
+      bool keep = true;
+      if constexpr (CHECK) {
+        const int col = col0 + jj;
+        keep = row_ok && col < ncols && col != dcol;
+      }
+      if constexpr (KIND == KIND_SIGLIP) {
+        const float x2 = fmaf(t, dot[jj], b2);
+        const float e = ex2_approx(-fabsf(x2));
+        const float d = 1.f + e;
+        const float r = rcp_approx(d);
+        const float sig = x2 >= 0.f ? r : e * r;
+        m = sig * (R2 * s1);
+        if (R3 != 0.f) {  // this launch also sums the SigLIP loss
+          const float l = fmaxf(x2, 0.f) + lg2_approx(d);
+          acc_l += keep ? l : 0.f;
+        }
+      } else {
+        const float e = ex2_approx(fmaf(t, dot[jj], -L));
+        m = e * fmaf(R2, s1, R3 * s2v[jj]);
+      }
+      if constexpr (CHECK) m = keep ? m : 0.f;
+      acc_c = fmaf(m, dot[jj], acc_c);
+      mv[u] = m;
+    }
+    packed[j / 2] = pack_bf16x2(mv[0], mv[1]);
+  }
+  return make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+// Tiles in pairs (t even in accumulator 0, t + 1 in accumulator 1), band by band,
+// alternating within a pair.  Step s -> (tile, band); producer, MMA and epilogue all walk it.
+struct Schedule {
+  int T, n;
+  __device__ int steps() const { return T * n; }
+  __device__ void at(int s, int& t, int& b) const {
+    const int pair = s / (2 * n);
+    const int rem = s - pair * 2 * n;
+    const int tp = 2 * pair;
+    const int width = (tp + 1 < T) ? 2 : 1;  // the last pair may hold one tile
+    b = rem / width;
+    t = tp + rem % width;
+  }
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    wgt_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+               const __grid_constant__ CUtensorMap tm_w, const WgtParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sx = smem + off_x;
+  uint8_t* sy = smem + off_y;
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + off_bar);
+  uint64_t* s_empty = s_full + kNS;
+  uint64_t* acc_full = s_empty + kNS;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  int* pend = reinterpret_cast<int*>(smem + off_pend);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_misc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t il0 = static_cast<int64_t>(blockIdx.x) * kTileRows;  // first row within this launch
+  const int64_t i0 = p.row0 + il0;                                    // first row of X
+  const int split = blockIdx.y;
+  const int n = p.n_prefix;
+  const int t_begin = split * p.tiles_per_split;
+  const int T = min(p.n_col_tiles, t_begin + p.tiles_per_split) - t_begin;
+  const Schedule sched{T, n};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxPrefix; ++k) pend[k] = p.prefix_end[k];
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_y);
+    tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (T > 0 && warp == 0 && lane == 0) {
+    // ------------------------------------------------------------- operand producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int s = 0; s < sched.steps() && ok; ++s) {
+      int t, b;
+      sched.at(s, t, b);
+      const int j0 = (t_begin + t) * kCols;
+      const int c0 = b == 0 ? 0 : pend[b - 1] / kChunk, c1 = pend[b] / kChunk;
+      for (int c = c0; c < c1; ++c, ++it) {
+        const uint32_t st = it % kNS, ph = (it / kNS) & 1;
+        if (!wait_bounded(&s_empty[st], ph ^ 1, abort_flag)) {
+          fail(p, abort_flag);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&s_full[st], kXBytes + kYBytes);
+        tma_load_2d(sx + st * kXBytes, &tm_x, &s_full[st], c * kChunk, static_cast<int>(i0));
+        tma_load_2d(sy + st * kYBytes, &tm_y, &s_full[st], c * kChunk, j0);
+      }
+    }
+    for (uint32_t k = 0; k < kNS && k < it; ++k) {  // let the last copies land
+      const uint32_t q = it - 1 - k;
+      mbar_wait(&s_full[q % kNS], (q / kNS) & 1, kWaitLimitNs);
+    }
+  } else if (T > 0 && warp == 1 && lane == 0) {
+    // ------------------------------------------------------------- MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(kTileRows, kCols);
+    uint32_t it = 0;
+    uint32_t uses[2] = {0, 0};
+    bool ok = true;
+    for (int s = 0; s < sched.steps() && ok; ++s) {
+      int t, b;
+      sched.at(s, t, b);
+      const int a = t & 1;
+      if (uses[a] > 0 && !wait_bounded(&acc_empty[a], (uses[a] - 1) & 1, abort_flag)) {
+        fail(p, abort_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + a * kCols;
+      const int c0 = b == 0 ? 0 : pend[b - 1] / kChunk, c1 = pend[b] / kChunk;
+      for (int c = c0; c < c1; ++c, ++it) {
+        const uint32_t st = it % kNS, ph = (it / kNS) & 1;
+        if (!wait_bounded(&s_full[st], ph, abort_flag)) {
+          fail(p, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ax = smem_u32(sx + st * kXBytes), ay = smem_u32(sy + st * kYBytes);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk)  // bands accumulate: only a tile's first step starts fresh
+          umma_bf16(d, sdesc_kmajor_sw128(ax + kk * 32), sdesc_kmajor_sw128(ay + kk * 32), idesc,
+                    (c != 0 || kk != 0) ? 1u : 0u);
+        umma_commit(&s_empty[st]);
+      }
+      if (ok) umma_commit(&acc_full[a]);
+      ++uses[a];
+    }
+    umma_commit(drain);
+    mbar_wait(drain, 0, kWaitLimitNs);
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;                       // TMEM lane quadrant (rows 32q..32q+31)
+    const int ew = warp - kEpiWarp0;
+    const int cq = ew >> 2;                       // column quarter (64 columns)
+    const int r = q * 32 + lane;
+    const int64_t gi = i0 + r;
+    const bool row_ok = il0 + r < p.rows;
+    const int etid = threadIdx.x - kEpiWarp0 * 32;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t colf_s = smem_u32(smem + off_colf);
+    uint8_t* stage = smem + off_stage + ew * kStageBytes;
+    const uint32_t stage_row = smem_u32(stage) + (lane >> 3) * 1024 + (lane & 7) * 128;  // row `lane` of the block
+    const uint32_t swz = lane & 7;
+    // column factors of tile t live in buffer t & 3; a tile pair's factors are fetched by
+    // cp.async while the previous pair is processed
+    auto prefetch_colf = [&](int t) {
+      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
+      const uint32_t dst = colf_s + (t & 3) * kColfBytes;
+      for (int e = etid; e < n * 2 * kCols; e += kEpiThreads) {
+        const int k = e / (2 * kCols), f = (e / kCols) & 1, c = e % kCols;
+        const int64_t gj = j0 + c;
+        const float* src = f == 0 ? p.rinv_y : p.beta_y;
+        const bool v = src != nullptr && gj < p.ny;
+        cp_async4_u32(dst + e * 4, v ? src + static_cast<int64_t>(k) * p.ny + gj : p.rinv_y, v ? 4u : 0u);
+      }
+    };
+    for (int t = 0; t < 2 && t < T; ++t) prefetch_colf(t);
+    cp_async_commit();
+    // raw row factors of the next step's prefix (rho_i, and rho_i alpha_i for CLIP/ROWS),
+    // loaded one step ahead
+    float n_rho = 0.f, n_alpha = 0.f;
+    auto load_row = [&](int k) {
+      n_rho = row_ok ? p.rinv_x[static_cast<int64_t>(k) * p.nx + gi] : 0.f;
+      if constexpr (KIND != KIND_SIGLIP)
+        n_alpha = (row_ok && p.alpha_x) ? p.alpha_x[static_cast<int64_t>(k) * p.nx + gi] : 0.f;
+    };
+    if (T > 0) load_row(0);
+    const int64_t slot_off = static_cast<int64_t>(split * 4 + cq) * n * p.nx + gi;
+    const float siglip_loss = (KIND == KIND_SIGLIP && p.rowacc) ? 1.f : 0.f;
+    const int64_t wrow = static_cast<int64_t>(il0) + q * 32;  // this warp's first row in the weight array
+    uint32_t uses[2] = {0, 0};
+    bool ok = true;
+    for (int s = 0; s < sched.steps(); ++s) {
+      int t, b;
+      sched.at(s, t, b);
+      if ((t & 1) == 0 && b == 0) {
+        // a tile pair begins (every warp reaches this point at the same step)
+        named_bar_sync(1, kEpiThreads);          // all are done with the previous pair
+        for (int u = 2; u < 4 && t + u < T; ++u) prefetch_colf(t + u);
+        cp_async_commit();
+        cp_async_wait<1>();                      // this pair's factors (fetched a pair ago) are in
+        named_bar_sync(1, kEpiThreads);
+      }
+      const int a = t & 1;
+      const int k = b;
+      ++uses[a];
+      if (!ok) continue;
+      if (!wait_bounded(&acc_full[a], (uses[a] - 1) & 1, abort_flag)) {
+        fail(p, abort_flag);
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+      float v[64];
+      tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
+
+      const float rho = n_rho;
+      float R2, R3;
+      if constexpr (KIND == KIND_SIGLIP) {
+        float ms = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < kMaxPrefix; ++kk)
+          if (kk == k) ms = p.m_scale[kk];
+        R2 = rho * ms;  // rho_i w_k t / N
+        R3 = siglip_loss;
+      } else {
+        R2 = n_alpha;   // rho_i alpha_i
+        R3 = rho;
+      }
+      const float R1 = p.L * rho;
+      if (s + 1 < sched.steps()) {
+        int tn, bn;
+        sched.at(s + 1, tn, bn);
+        load_row(bn);
+      }
+      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
+      const int64_t left = p.ny - j0;
+      const int ncols = left < kCols ? static_cast<int>(left) : kCols;
+      const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
+      const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (il0 + kTileRows > p.rows);
+      const int diag_col = static_cast<int>(dtile) + r;  // tile column of this row's positive
+      const uint32_t cf = colf_s + (t & 3) * kColfBytes + cq * 64 * 4;
+      const uint32_t c1 = cf + (k * 2 + 0) * kCols * 4;
+      const uint32_t c2 = cf + (k * 2 + 1) * kCols * 4;
+      // the previous TMA store of this warp must have read its staging block
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+      float ac = 0.f, al = 0.f;
+      if (check) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(stage_row + ((ch ^ swz) << 4),
+                       cells8<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, p.L, p.b2,
+                                          cq * 64 + ch * 8, ncols, diag_col, row_ok, ac, al));
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(stage_row + ((ch ^ swz) << 4), cells8<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32,
+                                                                           R1, R2, R3, p.L, p.b2, 0, 0, 0, true,
+                                                                           ac, al));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && j0 + cq * 64 < p.ny) {  // a quarter wholly past the last column stores nothing
+        tma_store_2d(&tm_w, stage, static_cast<int>(j0 + cq * 64),
+                     static_cast<int>(static_cast<int64_t>(k) * p.w_rows_per_prefix + wrow));
+        bulk_commit();
+      }
+      if (row_ok) {
+        float* pc = p.crow + slot_off + static_cast<int64_t>(k) * p.nx;
+        if (t == 0) *pc = ac;
+        else atomicAdd(pc, ac);
+        if (KIND == KIND_SIGLIP && p.rowacc) {
+          float* pl = p.rowacc + slot_off + static_cast<int64_t>(k) * p.nx;
+          if (t == 0) *pl = al;
+          else atomicAdd(pl, al);
+        }
+      }
+    }
+    cp_async_wait<0>();
+    if (lane == 0) bulk_wait0();  // the weights are in global memory before the CTA exits
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int KIND>
+static cudaError_t setup_one() {
+  return cudaFuncSetAttribute(wgt_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+}  // namespace wgt
+
+cudaError_t wgt_kernel_setup() {
+  cudaError_t e;
+  if ((e = wgt::setup_one<KIND_CLIP>()) != cudaSuccess) return e;
+  if ((e = wgt::setup_one<KIND_SIGLIP>()) != cudaSuccess) return e;
+  return wgt::setup_one<KIND_ROWS>();
+}
+
+cudaError_t launch_wgt(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const CUtensorMap& tm_w,
+                       const WgtParams& p, dim3 grid, cudaStream_t stream) {
+  if (kind == KIND_CLIP)
+    wgt::wgt_kernel<KIND_CLIP><<<grid, wgt::kThreads, wgt::smem_bytes, stream>>>(tm_x, tm_y, tm_w, p);
+  else if (kind == KIND_SIGLIP)
+    wgt::wgt_kernel<KIND_SIGLIP><<<grid, wgt::kThreads, wgt::smem_bytes, stream>>>(tm_x, tm_y, tm_w, p);
+  else
+    wgt::wgt_kernel<KIND_ROWS><<<grid, wgt::kThreads, wgt::smem_bytes, stream>>>(tm_x, tm_y, tm_w, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ufc

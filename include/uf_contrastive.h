@@ -165,9 +165,10 @@ typedef enum uf_kernel_group {
   UF_KERNEL_TRANSPOSE = 1,  /* bf16 transposes for the gradient operand (1 launch each) */
   UF_KERNEL_FWD_TILE = 2,   /* fused tcgen05 forward: row sums of every prefix */
   UF_KERNEL_STATS = 3,      /* loss statistics and per-prefix loss (2 launches) */
-  UF_KERNEL_BWD_TILE = 4,   /* fused tcgen05 backward: score recompute + gradient GEMM */
+  UF_KERNEL_BWD_TILE = 4,   /* tcgen05 backward weight pass: score recompute, bf16 weights to HBM */
   UF_KERNEL_NORM_BWD = 5,   /* projection term and positive-pair correction */
-  UF_KERNEL_GROUPS = 6
+  UF_KERNEL_GEMM = 6,       /* tcgen05 gradient contraction over the bf16 weights */
+  UF_KERNEL_GROUPS = 7
 } uf_kernel_group_t;
 
 /* enable != 0: start timing (clears the totals); 0: stop.  Process-wide. */

@@ -61,8 +61,15 @@ def test_workspace_size(lib):
     # pure function of the arguments, and it grows with the batch
     assert ws(4096, 4096, 1024, LADDER, 0, 1) == ws(4096, 4096, 1024, LADDER, 0, 1)
     assert ws(65536, 65536, 1024, LADDER, 0, 1) > ws(4096, 4096, 1024, LADDER, 0, 1)
-    # the N=65536 backward fits comfortably in HBM
-    assert ws(65536, 65536, 1024, LADDER, 0, 1) < 2 << 30
+    # the forward alone needs little scratch
+    assert ws(65536, 65536, 1024, LADDER, 0, 0) < 2 << 30
+    # the backward keeps the bf16 weights of every prefix: at N=65536 all rows fit in one
+    # chunk (5 x 65536^2 x 2 bytes = 40 GiB) within the default 48 GiB weight budget
+    full = 5 * 65536 * 65536 * 2
+    assert full <= ws(65536, 65536, 1024, LADDER, 0, 1) - ws(65536, 65536, 1024, LADDER, 0, 0) < full + (2 << 30)
+    # larger batches are cut into row chunks: the weight array stays within its budget
+    big = 262144
+    assert ws(big, big, 1024, LADDER, 0, 1) - ws(big, big, 1024, LADDER, 0, 0) < (48 << 30) + (1 << 30)
 
 
 FAKE = 1 << 20  # a 256-byte aligned fake device address; these calls return before any CUDA call
