@@ -1,36 +1,41 @@
 // gemm_kernel.cu -- the gradient contraction of the Matryoshka loss as a dense tcgen05 GEMM
-// over the bf16 weights m^k written by the weight kernel:
+// over the bf16 weights m^k written by the weight kernel, for both sides of the pair:
 //
-//     G[i, d] (+)= sum_k [d < p_k] sum_j m^k[i, j] * Y[j, d]
+//     A side:  G[i, d] = sum_k [d < p_k] sum_j m^k[i, j] B[j, d]      (weights K-major)
+//     B side:  G[j, d] = sum_k [d < p_k] sum_i m^k[i, j] A[i, d]      (weights MN-major)
 //
-// (prefix-expanded: prefix k contributes to the first p_k dimensions only).  A CTA owns
-// 128 rows of G and one 256-dimension slice [d0, d0 + 256); for every prefix reaching the
-// slice it streams 64-column chunks of m^k (A operand, K-major) and of Y^T restricted to
-// the slice (B operand, K-major, N = min(p_k, d0 + 256) - d0 rows) through a 4-stage TMA
-// ring into one TMEM accumulator of 256 columns.  Prefixes are walked from the widest
-// down, so the CTAs of the slices of one row block, which run side by side, read the same
-// rows of m^4 first and share them through L2.
+// (prefix-expanded: prefix k contributes to its first p_k dimensions).  A CTA owns 128
+// rows of G and one 256-dimension slice [d0, d0 + 256).  For each prefix reaching the slice,
+// from the widest down, it streams 64-long K chunks of m^k (A operand) and of the other
+// side's transposed embeddings restricted to the slice (B operand, K-major, N = min(p_k,
+// d0 + 256) - d0 rows) through a 4-stage TMA ring into one of two TMEM accumulators, so
+// the MMA of prefix k - 1 overlaps the epilogue of prefix k.  The epilogue adds G^k into G
+// in global memory and forms the projection scalar of the norm backward,
+//     r^k_row = sum_j m^k dot^k = x_row[:p_k] . G^k_row,
+// as this slice's partial sum (one slot per slice).  The CTAs of the slices of one row
+// block are adjacent in the grid and start on the same rows of m^k, so they share them
+// through L2.
 //
-// Warps (128 threads): lane 0 of warp 0 issues the TMA loads, lane 0 of warp 1 the MMAs;
-// afterwards all four warps move the accumulator (thread = row) to global memory.
+// Warps (192 threads): lane 0 of warp 0 issues the TMA loads, lane 0 of warp 1 the MMAs,
+// warps 2..5 are the epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31).
 #include "launch.h"
 #include "ptx.cuh"
 
 namespace ufc {
 namespace gemm {
 
-constexpr int kThreads = 128;
-constexpr int kN = 256;                         // gradient slice width = TMEM columns
-constexpr int kNS = 4;                          // operand stages
-constexpr int kABytes = kTileRows * kChunk * 2;  // 16 KB: 128 rows of m^k x 64 columns
-constexpr int kBBytes = kN * kChunk * 2;         // 32 KB: up to 256 dims of Y^T x 64 columns
-constexpr int kBox = kBwdYtBox;                  // dims per Y^T TMA box
+constexpr int kThreads = 192;
+constexpr int kN = 256;                          // gradient slice width = TMEM columns per accumulator
+constexpr int kNS = 4;                           // operand stages
+constexpr int kABytes = kTileRows * kChunk * 2;  // 16 KB: 128 rows of G x 64 of K
+constexpr int kBBytes = kN * kChunk * 2;         // 32 KB: up to 256 dims x 64 of K
+constexpr int kBox = kBwdYtBox;                  // rows per B-operand TMA box (and per MN-major A box)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 constexpr int off_a = 0;
 constexpr int off_b = off_a + kNS * kABytes;
 constexpr int off_bar = off_b + kNS * kBBytes;
-constexpr int n_bars = 2 * kNS + 1;
+constexpr int n_bars = 2 * kNS + 4;
 constexpr int off_misc = off_bar + n_bars * 8;
 constexpr int smem_bytes = off_misc + 16 + 1024;
 static_assert(smem_bytes <= 232448, "gemm shared memory");
@@ -52,7 +57,19 @@ __device__ __forceinline__ void fail(const GemmParams& p, volatile int* abort_fl
   if (p.status) atomicExch(p.status, kStatusTimeout);
 }
 
-template <bool ACC>
+__device__ __forceinline__ int prefix_end_of(const GemmParams& p, int k) {
+  int pk = 0;
+#pragma unroll
+  for (int kk = 0; kk < kMaxPrefix; ++kk)
+    if (kk == k) pk = p.prefix_end[kk];
+  return pk;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// AMN: the weights are the MN-major A operand (B side: rows of G are columns of m^k).
+template <bool AMN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_yt,
                 const GemmParams p) {
@@ -62,60 +79,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sb = smem + off_b;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + off_bar);
   uint64_t* empty = full + kNS;
-  uint64_t* done = empty + kNS;
+  uint64_t* acc_full = empty + kNS;   // [2]
+  uint64_t* acc_empty = acc_full + 2;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_misc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // slices are the fast grid dimension: the CTAs of one row block run side by side
-  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * kTileRows;
-  const int d0 = blockIdx.x * kN;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileRows;  // first row of G in this launch
+  const int slice = blockIdx.x;
+  const int d0 = slice * kN;
   const int n = p.n_prefix;
   int k_first = 0;  // prefixes k_first .. n-1 reach this slice
 #pragma unroll
   for (int k = 0; k < kMaxPrefix; ++k)
     if (k < n && p.prefix_end[k] <= d0) k_first = k + 1;
-  const int nj = static_cast<int>((p.kdim + kChunk - 1) / kChunk);
+  const int nkc = static_cast<int>((p.kdim + kChunk - 1) / kChunk);  // K chunks per prefix
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(done, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);  // the four epilogue warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_yt);
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, kN);
+    tmem_alloc(tmem_slot, 2 * kN);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-  // zero the accumulator: every MMA accumulates onto it (prefixes differ in width)
-#pragma unroll
-  for (int c = 0; c < kN; c += 32) tmem_st32_zero(tmem + lane_addr + c);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
 
-  bool ok = true;
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------- TMA producer
     uint32_t it = 0;
+    bool ok = true;
     for (int k = n - 1; k >= k_first && ok; --k) {
-      int pk = 0;
-#pragma unroll
-      for (int kk = 0; kk < kMaxPrefix; ++kk)
-        if (kk == k) pk = p.prefix_end[kk];
-      const int nk = min(pk, d0 + kN) - d0;
-      const int arow = static_cast<int>(k * p.w_rows_per_prefix + i0);
-      for (int jc = 0; jc < nj; ++jc, ++it) {
+      const int nk = min(prefix_end_of(p, k), d0 + kN) - d0;
+      const int64_t wrow = static_cast<int64_t>(k) * p.w_rows_per_prefix;
+      for (int c = 0; c < nkc; ++c, ++it) {
         const uint32_t st = it % kNS, ph = (it / kNS) & 1;
         if (!wait_bounded(&empty[st], ph ^ 1, abort_flag)) {
           fail(p, abort_flag);
@@ -123,9 +134,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&full[st], kABytes + nk * kChunk * 2);
-        tma_load_2d(sa + st * kABytes, &tm_w, &full[st], jc * kChunk, arow);
+        if constexpr (AMN) {
+          // [64 K rows x 64 M columns] twice: M blocks 0..63 and 64..127 of this row block
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(sa + st * kABytes + h * (kABytes / 2), &tm_w, &full[st],
+                        static_cast<int>(m0 + h * 64), static_cast<int>(wrow + c * kChunk));
+        } else {
+          tma_load_2d(sa + st * kABytes, &tm_w, &full[st], c * kChunk, static_cast<int>(wrow + m0));
+        }
         for (int r0 = 0; r0 < nk; r0 += kBox)
-          tma_load_2d(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, &full[st], jc * kChunk, d0 + r0);
+          tma_load_2d(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, &full[st],
+                      static_cast<int>(p.b_col0 + c * kChunk), d0 + r0);
       }
     }
     for (uint32_t q = 0; q < kNS && q < it; ++q) {  // let the last copies land
@@ -134,15 +153,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------- MMA issuer
-    uint32_t it = 0;
-    for (int k = n - 1; k >= k_first && ok; --k) {
-      int pk = 0;
-#pragma unroll
-      for (int kk = 0; kk < kMaxPrefix; ++kk)
-        if (kk == k) pk = p.prefix_end[kk];
-      const int nk = min(pk, d0 + kN) - d0;
-      const uint32_t idesc = idesc_bf16_f32(kTileRows, static_cast<uint32_t>(nk));
-      for (int jc = 0; jc < nj; ++jc, ++it) {
+    uint32_t it = 0, pi = 0;
+    bool ok = true;
+    for (int k = n - 1; k >= k_first && ok; --k, ++pi) {
+      const int nk = min(prefix_end_of(p, k), d0 + kN) - d0;
+      const uint32_t a = pi & 1;
+      // the epilogue must have read this accumulator's previous prefix
+      if (pi >= 2 && !wait_bounded(&acc_empty[a], ((pi - 2) >> 1) & 1, abort_flag)) {
+        fail(p, abort_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + a * kN;
+      const uint32_t idesc = AMN ? idesc_bf16_f32_amn(kTileRows, static_cast<uint32_t>(nk))
+                                 : idesc_bf16_f32(kTileRows, static_cast<uint32_t>(nk));
+      for (int c = 0; c < nkc; ++c, ++it) {
         const uint32_t st = it % kNS, ph = (it / kNS) & 1;
         if (!wait_bounded(&full[st], ph, abort_flag)) {
           fail(p, abort_flag);
@@ -150,55 +176,96 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a = smem_u32(sa + st * kABytes), b = smem_u32(sb + st * kBBytes);
+        const uint32_t as = smem_u32(sa + st * kABytes), bs = smem_u32(sb + st * kBBytes);
 #pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk)
-          umma_bf16(tmem, sdesc_kmajor_sw128(a + kk * 32), sdesc_kmajor_sw128(b + kk * 32), idesc, 1u);
+        for (int kk = 0; kk < kChunk / 16; ++kk) {
+          // K = 16 per MMA: MN-major A advances 16 K rows (two 1024-byte atoms), K-major 32 bytes
+          const uint64_t adesc = AMN ? sdesc_mnmajor_sw128(as + kk * 2048, kABytes / 2, 1024)
+                                     : sdesc_kmajor_sw128(as + kk * 32);
+          umma_bf16(d, adesc, sdesc_kmajor_sw128(bs + kk * 32), idesc, (c != 0 || kk != 0) ? 1u : 0u);
+        }
         umma_commit(&empty[st]);
       }
+      if (ok) umma_commit(&acc_full[a]);
     }
-    umma_commit(done);
-  }
-  __syncwarp();
-  // ------------------------------------------------------------- epilogue (all 128 threads)
-  if (!wait_bounded(done, 0, abort_flag)) {
-    fail(p, abort_flag);
-  } else if (!*abort_flag) {
-    tc_fence_after();
-    const int r = warp * 32 + lane;
-    const int64_t gi = i0 + r;
-    float* g = p.G + gi * p.d + d0;
-#pragma unroll 1
-    for (int c = 0; c < kN; c += 32) {
-      float v[32];
-      tmem_ld32(tmem + lane_addr + c, v);
-      if (gi < p.m_rows && d0 + c < p.d) {
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int64_t gl = m0 + r;              // row within this launch
+    const int64_t g = p.row0 + gl;          // row of G / X / crow
+    const bool row_ok = gl < p.m_rows;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    float* grow = p.G + g * p.d + d0;
+    const uint16_t* xrow = p.X + g * p.d + d0;
+    // prefixes that do not reach this slice contribute nothing to its slot
+    if (row_ok && !p.accumulate)
+      for (int k = 0; k < k_first; ++k) p.crow[(static_cast<int64_t>(slice) * n + k) * p.crow_rows + g] = 0.f;
+    uint32_t pi = 0;
+    bool ok = true;
+    for (int k = n - 1; k >= k_first; --k, ++pi) {
+      if (!ok) continue;
+      const int nk = min(prefix_end_of(p, k), d0 + kN) - d0;
+      const uint32_t a = pi & 1;
+      if (!wait_bounded(&acc_full[a], (pi >> 1) & 1, abort_flag)) {
+        fail(p, abort_flag);
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+      const bool first = pi == 0 && !p.accumulate;  // the widest prefix writes G, the others add
+      float rk = 0.f;
+      for (int c = 0; c < nk; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + lane_addr + a * kN + c, v);
+        if (row_ok) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-          if constexpr (ACC) {
-            const float4 prev = *reinterpret_cast<const float4*>(g + c + j);
-            o.x += prev.x;
-            o.y += prev.y;
-            o.z += prev.z;
-            o.w += prev.w;
+          for (int j = 0; j < 32; j += 8) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + c + j);
+            rk = fmaf(bf16_lo(xv.x), v[j + 0], rk);
+            rk = fmaf(bf16_hi(xv.x), v[j + 1], rk);
+            rk = fmaf(bf16_lo(xv.y), v[j + 2], rk);
+            rk = fmaf(bf16_hi(xv.y), v[j + 3], rk);
+            rk = fmaf(bf16_lo(xv.z), v[j + 4], rk);
+            rk = fmaf(bf16_hi(xv.z), v[j + 5], rk);
+            rk = fmaf(bf16_lo(xv.w), v[j + 6], rk);
+            rk = fmaf(bf16_hi(xv.w), v[j + 7], rk);
           }
-          *reinterpret_cast<float4*>(g + c + j) = o;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            if (!first) {
+              const float4 prev = *reinterpret_cast<const float4*>(grow + c + j);
+              o.x += prev.x;
+              o.y += prev.y;
+              o.z += prev.z;
+              o.w += prev.w;
+            }
+            *reinterpret_cast<float4*>(grow + c + j) = o;
+          }
         }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
+      if (row_ok) {
+        float* pc = p.crow + (static_cast<int64_t>(slice) * n + k) * p.crow_rows + g;
+        *pc = p.accumulate ? *pc + rk : rk;
       }
     }
   }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kN);
+    tmem_dealloc(tmem, 2 * kN);
   }
 }
 
-template <bool ACC>
+template <bool AMN>
 static cudaError_t setup_one() {
-  return cudaFuncSetAttribute(gemm_kernel<ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  return cudaFuncSetAttribute(gemm_kernel<AMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 }  // namespace gemm
@@ -209,12 +276,12 @@ cudaError_t gemm_kernel_setup() {
   return gemm::setup_one<true>();
 }
 
-cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool accumulate,
+cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool weights_mn,
                         cudaStream_t stream) {
-  int pn = p.prefix_end[p.n_prefix - 1];
+  const int pn = p.prefix_end[p.n_prefix - 1];
   dim3 grid(static_cast<unsigned>((pn + gemm::kN - 1) / gemm::kN),
             static_cast<unsigned>((p.m_rows + kTileRows - 1) / kTileRows));
-  if (accumulate)
+  if (weights_mn)
     gemm::gemm_kernel<true><<<grid, gemm::kThreads, gemm::smem_bytes, stream>>>(tm_w, tm_yt, p);
   else
     gemm::gemm_kernel<false><<<grid, gemm::kThreads, gemm::smem_bytes, stream>>>(tm_w, tm_yt, p);

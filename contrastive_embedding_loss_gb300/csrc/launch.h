@@ -32,8 +32,8 @@ cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
                        cudaStream_t stream);
 
 // Backward weights (wgt_kernel.cu): m^k_ij = rho_i sigma_j dL/dcos^k_ij as bf16 into a
-// [prefix][row][column] array (row stride in elements fixed by tm_w), plus the row
-// scalars sum_j m_ij dot_ij and (SigLIP) the row loss sums.  One launch covers rows
+// [prefix][row][column] array (row stride in elements fixed by tm_w), plus (SigLIP) the
+// row loss sums.  One launch covers rows
 // [row0, row0 + rows) of X; grid = (ceil(rows / 128), splits of the 256-column tiles).
 // tm_x: [128 x 64] boxes of X; tm_y: [256 x 64] boxes of Y; tm_w: [32 x 64] boxes of the
 // weight array viewed as [n * w_rows_per_prefix rows][ny columns].
@@ -51,7 +51,6 @@ struct WgtParams {
   const float* beta_y;            // [n][ny] sigma_j beta_j (CLIP/ROWS) or NULL
   float m_scale[kMaxPrefix];      // SigLIP: w_k t / N
   int64_t w_rows_per_prefix;      // rows between prefixes in the weight array (multiple of 128)
-  float* crow;                    // [split * 4 + quarter][n][nx]
   float* rowacc;                  // SigLIP: [split * 4 + quarter][n][nx] loss sums (log2 units), or NULL
   int* status;
 };
@@ -61,23 +60,32 @@ cudaError_t wgt_kernel_setup();
 cudaError_t launch_wgt(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const CUtensorMap& tm_w,
                        const WgtParams& p, dim3 grid, cudaStream_t stream);
 
-// Gradient contraction (gemm_kernel.cu): G[i, d] (+)= sum_k [d < p_k] sum_j m^k[i, j] Y[j, d]
-// for rows i < m_rows and d < p_n, dims d < d of G past p_n untouched.  tm_w: [128 x 64]
-// boxes of the weight array ([n * w_rows_per_prefix rows][kdim columns]); tm_yt: [64 x 64]
-// boxes of Y^T ([d rows][kdim columns]).
+// Gradient contraction (gemm_kernel.cu), for rows g = row0 + [0, m_rows) of G:
+//   weights K-major (A side):  G[g, d] = sum_k [d < p_k] sum_c m^k[g - row0, c] Y[c, d]
+//   weights MN-major (B side): G[g, d] = sum_k [d < p_k] sum_c m^k[c, g] Y[b_col0 + c, d]
+// with c over [0, kdim), and the projection scalars crow[slice][k][g] = X[g, slice] . G^k[g, slice]
+// (partial over each 256-dimension slice).  accumulate: add into G and crow instead of
+// writing them.  tm_w: the weight array [n * w_rows_per_prefix rows][columns], boxes of
+// [128 x 64] (K-major) or [64 x 64] (MN-major); tm_yt: [64 x 64] boxes of Y^T ([d rows][rows of Y]).
 struct GemmParams {
   int64_t m_rows;                 // rows of G computed by this launch
-  int64_t kdim;                   // contraction length (columns of m^k)
+  int64_t row0;                   // their first row in G, X and crow
+  int64_t kdim;                   // contraction length
+  int64_t b_col0;                 // first column of Y^T for this launch's contraction range
   int64_t w_rows_per_prefix;
-  int d;                          // row stride of G in elements
+  int d;                          // row stride of G and X in elements
   int n_prefix;
   int prefix_end[kMaxPrefix];
-  float* G;                       // first row of this launch
+  int accumulate;
+  float* G;
+  const uint16_t* X;              // bf16 rows of the side G belongs to
+  float* crow;                    // [slice][n][crow_rows]
+  int64_t crow_rows;
   int* status;
 };
 constexpr int kBwdYtBox = 64;
 cudaError_t gemm_kernel_setup();
-cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool accumulate,
+cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool weights_mn,
                         cudaStream_t stream);
 
 // Per-row inverse norms of every prefix for A and B, plus the positives' cosines

@@ -208,6 +208,20 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Descriptor for an MN-major operand tile in the 128-byte swizzled layout: each 128-byte
+// row holds 64 consecutive M (or N) elements of one K index, 8 rows (8 K indices) form a
+// 1024-byte swizzle atom.  lbo: bytes between consecutive 64-element blocks along M/N;
+// sbo: bytes between consecutive 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulator, both
 // operands K-major, dense, no negation:
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
@@ -215,6 +229,10 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 //   bits 17-22 N >> 3, bits 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// Same with the A operand MN-major (bit 15).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(uint32_t M, uint32_t N) {
+  return idesc_bf16_f32(M, N) | (1u << 15);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

@@ -48,7 +48,8 @@ struct Plan {
   bool grads = false;
   int64_t rb_a = 0;                  // 128-row blocks of A
   int64_t ftiles = 0;                // forward: 256-column tiles of B
-  Split fwd_a, wgt_a, wgt_b;         // column splits of the forward and of the two weight passes
+  Split fwd_a, wgt;                  // column splits of the forward and of the weight pass
+  int slices = 0;                    // 256-dimension slices of the gradient GEMMs
   int64_t lda = 0, ldb = 0;          // padded leading dimensions of A^T and B^T
   int64_t ldw = 0;                   // row stride of the weight array (elements)
   int64_t chunk = 0;                 // rows of X per weight chunk (multiple of 128)
@@ -83,11 +84,11 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.rb_a = cdiv(Na, kTileRows);
   P.ftiles = cdiv(Nb, kFwdCols);
   P.fwd_a = plan_split(P.rb_a, 1, P.ftiles);
-  P.wgt_a = plan_split(P.rb_a, 1, cdiv(Nb, kWgtCols));          // X = A walks B's rows
-  P.wgt_b = plan_split(cdiv(Nb, kTileRows), 1, cdiv(Na, kWgtCols));  // X = B walks A's rows
+  P.wgt = plan_split(P.rb_a, 1, cdiv(Nb, kWgtCols));  // rows of A against 256-row tiles of B
+  P.slices = static_cast<int>(cdiv(prefixes[n - 1], 256));
   P.lda = cdiv(Na, 64) * 64;
   P.ldb = cdiv(Nb, 64) * 64;
-  P.ldw = P.lda > P.ldb ? P.lda : P.ldb;
+  P.ldw = P.ldb;
 
   const size_t f = sizeof(float);
   size_t o = 0;
@@ -103,13 +104,13 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.o_zc = take(f * n * Nb);
   P.o_fa = take(f * n * Na);
   P.o_fb = take(f * n * Nb);
-  // row-statistic partials: forward (CLIP/ROWS), or the SigLIP loss sums of the A-side weight pass
+  // row-statistic partials: forward (CLIP/ROWS), or the SigLIP loss sums of the weight pass
   int slots_a = 4 * P.fwd_a.splits;  // one slot per split and column quarter
-  if (kind == KIND_SIGLIP && grads) slots_a = 4 * P.wgt_a.splits;
+  if (kind == KIND_SIGLIP && grads) slots_a = 4 * P.wgt.splits;
   P.o_acc_a = take(f * n * Na * slots_a);
   P.o_acc_b = take(kind == KIND_CLIP ? f * n * Nb * P.rb_a : 0);  // CLIP: 128-row column partials
-  P.o_crow_a = take(grads ? f * n * Na * 4 * P.wgt_a.splits : 0);
-  P.o_crow_b = take(grads ? f * n * Nb * 4 * P.wgt_b.splits : 0);
+  P.o_crow_a = take(grads ? f * n * Na * P.slices : 0);  // projection scalars, one slot per slice
+  P.o_crow_b = take(grads ? f * n * Nb * P.slices : 0);
   P.o_terms_a = take(f * n * Na);
   P.o_terms_b = take(f * n * Nb);
   P.o_loss = take(f * kMaxPrefix);
@@ -119,7 +120,7 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.o_w = o;
   P.chunk = 0;
   if (grads) {
-    const int64_t rows_max = cdiv(Na > Nb ? Na : Nb, kTileRows) * kTileRows;
+    const int64_t rows_max = cdiv(Na, kTileRows) * kTileRows;
     const size_t row_bytes = sizeof(uint16_t) * static_cast<size_t>(n) * static_cast<size_t>(P.ldw);
     const size_t budget = ws_limit ? (ws_limit > o ? ws_limit - o : 0) : kDefaultWeightBytes;
     int64_t rows = static_cast<int64_t>(budget / row_bytes) / kTileRows * kTileRows;
@@ -411,66 +412,75 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     return UF_OK;
   }
 
-  // ---- 3. backward, A side (X = A, Y = B) then B side (X = B, Y = A): per chunk of X's
-  // rows, the weight pass writes m^k (bf16) and the row scalars, and the GEMM contracts the
-  // weights with Y into G = dX before its projection (written in place into dA / dB)
-  uint16_t* W = reinterpret_cast<uint16_t*>(ws + P.o_w);
-  for (int side = 0; side < 2; ++side) {
-    const bool xa = side == 0;
-    const int64_t nx = xa ? Na : Nb, ny = xa ? Nb : Na;
-    const Split& sp_w = xa ? P.wgt_a : P.wgt_b;
-    CUtensorMap tmWs, tmWl;  // the weight array as [n * chunk rows][ny columns]: store / load boxes
-    if (!encode_map(&tmWs, W, static_cast<int64_t>(n) * P.chunk, ny, P.ldw, kWgtStoreRows) ||
-        !encode_map(&tmWl, W, static_cast<int64_t>(n) * P.chunk, ny, P.ldw, kTileRows))
+  // ---- 3. backward: per chunk of A's rows, the weight pass writes m^k (bf16, [k][i][j]);
+  // one GEMM contracts the chunk's weights with B into dA's rows, another contracts their
+  // transpose with the chunk of A into all of dB (added over chunks).  Both write G = dX
+  // before its projection in place into dA / dB, and the projection scalars.
+  {
+    uint16_t* W = reinterpret_cast<uint16_t*>(ws + P.o_w);
+    const int64_t wrows = static_cast<int64_t>(n) * P.chunk;
+    // the weight array as [n * chunk rows][Nb columns]: store, K-major and MN-major load boxes
+    CUtensorMap tmWs, tmWk, tmWm;
+    if (!encode_map(&tmWs, W, wrows, Nb, P.ldw, kWgtStoreRows) || !encode_map(&tmWk, W, wrows, Nb, P.ldw, kTileRows) ||
+        !encode_map(&tmWm, W, wrows, Nb, P.ldw, 64))
       return UF_CUDA_ERROR;
     WgtParams wp{};
-    wp.nx = nx;
-    wp.ny = ny;
+    wp.nx = Na;
+    wp.ny = Nb;
     wp.n_prefix = n;
     for (int k = 0; k < n; ++k) wp.prefix_end[k] = prefixes[k];
-    wp.n_col_tiles = static_cast<int>(cdiv(ny, kWgtCols));
-    wp.tiles_per_split = sp_w.tiles_per_split;
+    wp.n_col_tiles = static_cast<int>(cdiv(Nb, kWgtCols));
+    wp.tiles_per_split = P.wgt.tiles_per_split;
     wp.L = logit_scale * log2e;
     wp.b2 = bias * log2e;
-    wp.rinv_x = F(xa ? P.o_rinv_a : P.o_rinv_b);
-    wp.rinv_y = F(xa ? P.o_rinv_b : P.o_rinv_a);
-    if (xa) {
-      wp.alpha_x = siglip ? nullptr : F(P.o_fa);
-      wp.beta_y = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
-    } else {
-      wp.alpha_x = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
-      wp.beta_y = siglip ? nullptr : F(P.o_fa);
-    }
+    wp.rinv_x = F(P.o_rinv_a);
+    wp.rinv_y = F(P.o_rinv_b);
+    wp.alpha_x = siglip ? nullptr : F(P.o_fa);
+    wp.beta_y = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
     for (int k = 0; k < n; ++k) wp.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
     wp.w_rows_per_prefix = P.chunk;
-    wp.crow = F(xa ? P.o_crow_a : P.o_crow_b);
-    wp.rowacc = (xa && siglip) ? F(P.o_acc_a) : nullptr;  // the A side also sums the SigLIP loss
+    wp.rowacc = siglip ? F(P.o_acc_a) : nullptr;  // the SigLIP loss sums
     wp.status = device_status;
-    GemmParams gp{};
-    gp.kdim = ny;
-    gp.w_rows_per_prefix = P.chunk;
-    gp.d = D;
-    gp.n_prefix = n;
-    for (int k = 0; k < n; ++k) gp.prefix_end[k] = prefixes[k];
-    gp.status = device_status;
-    float* G = xa ? dA : dB;
-    for (int64_t r0 = 0; r0 < nx; r0 += P.chunk) {
-      const int64_t rows = nx - r0 < P.chunk ? nx - r0 : P.chunk;
+    GemmParams ga{}, gb{};
+    for (GemmParams* g : {&ga, &gb}) {
+      g->w_rows_per_prefix = P.chunk;
+      g->d = D;
+      g->n_prefix = n;
+      for (int k = 0; k < n; ++k) g->prefix_end[k] = prefixes[k];
+      g->status = device_status;
+    }
+    ga.kdim = Nb;
+    ga.G = dA;
+    ga.X = A16;
+    ga.crow = F(P.o_crow_a);
+    ga.crow_rows = Na;
+    gb.m_rows = Nb;
+    gb.row0 = 0;
+    gb.G = dB;
+    gb.X = B16;
+    gb.crow = F(P.o_crow_b);
+    gb.crow_rows = Nb;
+    for (int64_t r0 = 0; r0 < Na; r0 += P.chunk) {
+      const int64_t rows = Na - r0 < P.chunk ? Na - r0 : P.chunk;
       wp.row0 = r0;
       wp.rows = rows;
       {
         ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-        UF_CHECK(launch_wgt(kind, xa ? tmA : tmB, xa ? tmBf : tmAf, tmWs, wp,
-                            dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), sp_w.splits), stream));
+        UF_CHECK(launch_wgt(kind, tmA, tmBf, tmWs, wp, dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), P.wgt.splits),
+                            stream));
       }
-      gp.m_rows = rows;
-      gp.G = G + r0 * D;
-      ProfScope ps(UF_KERNEL_GEMM, 1, stream);
-      UF_CHECK(launch_gemm(tmWl, xa ? tmBt : tmAt, gp, false, stream));
+      ProfScope ps(UF_KERNEL_GEMM, 2, stream);
+      ga.m_rows = rows;
+      ga.row0 = r0;
+      UF_CHECK(launch_gemm(tmWk, tmBt, ga, false, stream));
+      gb.kdim = rows;
+      gb.b_col0 = r0;
+      gb.accumulate = r0 > 0;
+      UF_CHECK(launch_gemm(tmWm, tmAt, gb, true, stream));
     }
-    if (xa && siglip) {
+    if (siglip) {
       sp.rowacc_a = F(P.o_acc_a);
-      sp.slots_a = 4 * P.wgt_a.splits;
+      sp.slots_a = 4 * P.wgt.splits;
       ProfScope ps(UF_KERNEL_STATS, 2, stream);
       UF_CHECK(launch_stats(sp, stream));
     }
@@ -506,7 +516,7 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
       q.z_y = F(P.o_zr);
     }
     q.crow = F(xa ? P.o_crow_a : P.o_crow_b);
-    q.crow_slots = 4 * (xa ? P.wgt_a.splits : P.wgt_b.splits);
+    q.crow_slots = P.slices;
     q.G = xa ? dA : dB;
     q.g_splits = 1;
     q.dX = xa ? dA : dB;

@@ -9,10 +9,9 @@
 // tcgen05 tiles, the K walk band by band into a cumulative TMEM accumulator, two
 // accumulators so the MMA of one tile overlaps the epilogue of the other) and writes m^k
 // as bf16 into a [prefix][row][column] array, 32 x 64 blocks per warp through TMA stores.
-// It also sums, per row and prefix, sum_j m_ij dot_ij (the projection term of the norm
-// backward) and, for SigLIP, the loss over the negatives.  The gradient contraction
-// G = sum_k m^k Y[:, :p_k] is then a dense GEMM over these weights (gemm_kernel.cu), so
-// the scores are computed once per side of the backward instead of once per gradient slice.
+// For SigLIP it also sums the loss over the negatives.  Both gradient contractions,
+// G_A = sum_k m^k B[:, :p_k] and G_B = sum_k (m^k)^T A[:, :p_k], are then dense GEMMs over
+// these weights (gemm_kernel.cu): the backward computes the scores once.
 //
 // Warps (576 threads): 0 TMA, 1 MMA, 2..17 epilogue (warp w reads TMEM lanes 32 (w % 4)..
 // and one 64-column quarter of the tile).
@@ -70,13 +69,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 8 cells: their weights as four packed bf16 pairs; adds to the row scalar and (SigLIP,
-// loss != 0) to the loss over the negatives.  c1, c2: shared addresses of the columns'
+// 8 cells: their weights as four packed bf16 pairs; (SigLIP, R3 != 0) adds to the loss
+// over the negatives.  c1, c2: shared addresses of the columns'
 // factors.  CHECK evaluates the masks (padding rows and columns, the positive's cell).
 template <int KIND, bool CHECK>
 __device__ __forceinline__ uint4 cells8(const float* dot, uint32_t c1, uint32_t c2, float R1, float R2, float R3,
-                                        float L, float b2, int col0, int ncols, int dcol, bool row_ok, float& acc_c,
-                                        float& acc_l) {
+                                        float L, float b2, int col0, int ncols, int dcol, bool row_ok, float& acc_l) {
   const float4 s1a = ld_shared_v4f(c1), s1b = ld_shared_v4f(c1 + 16);
   const float s1v[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
   float s2v[8];
@@ -116,7 +114,6 @@ __device__ __forceinline__ uint4 cells8(const float* dot, uint32_t c1, uint32_t 
         m = e * fmaf(R2, s1, R3 * s2v[jj]);
       }
       if constexpr (CHECK) m = keep ? m : 0.f;
-      acc_c = fmaf(m, dot[jj], acc_c);
       mv[u] = m;
     }
     packed[j / 2] = pack_bf16x2(mv[0], mv[1]);
@@ -356,19 +353,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the previous TMA store of this warp must have read its staging block
       if (lane == 0) bulk_wait_read0();
       __syncwarp();
-      float ac = 0.f, al = 0.f;
+      float al = 0.f;
       if (check) {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           st_shared_v4(stage_row + ((ch ^ swz) << 4),
                        cells8<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, p.L, p.b2,
-                                          cq * 64 + ch * 8, ncols, diag_col, row_ok, ac, al));
+                                          cq * 64 + ch * 8, ncols, diag_col, row_ok, al));
       } else {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           st_shared_v4(stage_row + ((ch ^ swz) << 4), cells8<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32,
                                                                            R1, R2, R3, p.L, p.b2, 0, 0, 0, true,
-                                                                           ac, al));
+                                                                           al));
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -377,15 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      static_cast<int>(static_cast<int64_t>(k) * p.w_rows_per_prefix + wrow));
         bulk_commit();
       }
-      if (row_ok) {
-        float* pc = p.crow + slot_off + static_cast<int64_t>(k) * p.nx;
-        if (t == 0) *pc = ac;
-        else atomicAdd(pc, ac);
-        if (KIND == KIND_SIGLIP && p.rowacc) {
-          float* pl = p.rowacc + slot_off + static_cast<int64_t>(k) * p.nx;
-          if (t == 0) *pl = al;
-          else atomicAdd(pl, al);
-        }
+      if (KIND == KIND_SIGLIP && p.rowacc && row_ok) {
+        float* pl = p.rowacc + slot_off + static_cast<int64_t>(k) * p.nx;
+        if (t == 0) *pl = al;
+        else atomicAdd(pl, al);
       }
     }
     cp_async_wait<0>();
