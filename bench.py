@@ -50,8 +50,24 @@ def credited_flops(kind, Na, Nb, D):
     return (6 if kind == "siglip" else 8) * Na * Nb * D
 
 
-def executed_flops(kind, Na, Nb, D):
-    return (8 if kind == "siglip" else 10) * Na * Nb * D
+def executed_flops(kind, Na, Nb, D, prefixes=None):
+    """Tensor-core flops the library runs per step: the forward score pass (not for SigLIP,
+    whose loss comes out of the weight pass), the weight pass, and the two prefix-expanded
+    gradient GEMMs (prefix k contributes p_k dimensions)."""
+    pre = list(prefixes) if prefixes else [D]
+    score = 2.0 * Na * Nb * pre[-1]
+    gemms = 2 * 2.0 * Na * Nb * sum(pre)
+    return (0.0 if kind == "siglip" else score) + score + gemms
+
+
+def group_flops(group, kind, Na, Nb, D, prefixes):
+    """Algorithmic tensor flops of one kernel group per step (None: not a tensor kernel)."""
+    pre = list(prefixes)
+    if group in ("fwd_tile", "bwd_tile"):
+        return 2.0 * Na * Nb * pre[-1]  # one score pass over every prefix (cumulative bands)
+    if group == "gemm":
+        return 2 * 2.0 * Na * Nb * sum(pre)  # dA and dB contractions, prefix-expanded
+    return None
 
 
 def load_peaks():
@@ -302,24 +318,20 @@ def main():
         return
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    # dominant kernel by device time
+    # dominant kernel by device time; its algorithmic flops over its own device time
     dom = max(prof, key=lambda g: prof[g][0])
     dom_ms, dom_pairs, dom_launches = prof[dom]
-    per_launch_ms = dom_ms / max(dom_pairs, 1)
-    if dom == "bwd_tile":
-        alg = 4.0 * Na * Nb * D  # score recompute (2 Nx Ny D) + gradient GEMM (2 Nx Ny D) per side
-    elif dom == "fwd_tile":
-        alg = 2.0 * Na * Nb * D
-    else:
-        alg = None
+    per_launch_ms = dom_ms / max(dom_launches, 1)
+    alg_step = group_flops(dom, kind, Na, Nb, D, LADDER)
     roof = None
-    if alg is not None:
-        achieved = alg / (per_launch_ms / 1e3) / 1e12
+    if alg_step is not None:
+        alg_launch = alg_step * args.steps / max(dom_launches, 1)
+        achieved = alg_launch / (per_launch_ms / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf, "traffic": ncu_traffic(args.workload),
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
-                "algorithmic_flops_per_launch": alg, "ms_per_launch": per_launch_ms,
-                "share_of_step": dom_ms / ms_local}
+                "algorithmic_flops_per_launch": alg_launch, "launches_per_step": dom_launches / args.steps,
+                "ms_per_launch": per_launch_ms, "share_of_step": dom_ms / ms_local}
     cflops = credited_flops(kind, Na, Nb, D)
     line = {
         "metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": world, "steps": args.steps,
@@ -329,7 +341,7 @@ def main():
                    "prefixes": list(LADDER), "logit_scale": scale, "bias": bias,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "tflops_credited": cflops / (ms_step / 1e3) / 1e12,
-        "tflops_executed": executed_flops(kind, Na, Nb, D) / (ms_step / 1e3) / 1e12,
+        "tflops_executed": executed_flops(kind, Na, Nb, D, LADDER) / (ms_step / 1e3) / 1e12,
         "frac_credited_of_bf16_peak": cflops / (ms_step / 1e3) / 1e12 / peak_tf,
         "roofline": roof,
         "kernels_ms_per_step": {g: prof[g][0] / args.steps for g in prof},

@@ -8,34 +8,36 @@
 // rows of G and one 256-dimension slice [d0, d0 + 256).  For each prefix reaching the slice,
 // from the widest down, it streams 64-long K chunks of m^k (A operand) and of the other
 // side's transposed embeddings restricted to the slice (B operand, K-major, N = min(p_k,
-// d0 + 256) - d0 rows) through a 4-stage TMA ring into one of two TMEM accumulators, so
-// the MMA of prefix k - 1 overlaps the epilogue of prefix k.  The epilogue adds G^k into G
+// d0 + 256) - d0 rows) into one of two TMEM accumulators, so the MMA of prefix k - 1
+// overlaps the epilogue of prefix k.  The weights come from HBM and the other operand
+// mostly from L2, so each has its own TMA ring and producer: 6 stages of weights (about
+// 2500 MMA cycles of latency cover) and 4 of the other operand.  The epilogue adds G^k into G
 // in global memory and forms the projection scalar of the norm backward,
 //     r^k_row = sum_j m^k dot^k = x_row[:p_k] . G^k_row,
-// as this slice's partial sum (one slot per slice).  The CTAs of the slices of one row
-// block are adjacent in the grid and start on the same rows of m^k, so they share them
-// through L2.
+// as this slice's partial sum (one slot per slice).
 //
-// Warps (192 threads): lane 0 of warp 0 issues the TMA loads, lane 0 of warp 1 the MMAs,
-// warps 2..5 are the epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31).
+// Warps (224 threads): lane 0 of warp 0 loads the weights, lane 0 of warp 6 the other
+// operand, lane 0 of warp 1 issues the MMAs, warps 2..5 are the epilogue (warp w reads
+// TMEM lanes 32 (w % 4) .. + 31).
 #include "launch.h"
 #include "ptx.cuh"
 
 namespace ufc {
 namespace gemm {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kN = 256;                          // gradient slice width = TMEM columns per accumulator
-constexpr int kNS = 4;                           // operand stages
+constexpr int kNA = 6;                           // weight stages
+constexpr int kNB = 4;                           // stages of the other operand
 constexpr int kABytes = kTileRows * kChunk * 2;  // 16 KB: 128 rows of G x 64 of K
 constexpr int kBBytes = kN * kChunk * 2;         // 32 KB: up to 256 dims x 64 of K
 constexpr int kBox = kBwdYtBox;                  // rows per B-operand TMA box (and per MN-major A box)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 constexpr int off_a = 0;
-constexpr int off_b = off_a + kNS * kABytes;
-constexpr int off_bar = off_b + kNS * kBBytes;
-constexpr int n_bars = 2 * kNS + 4;
+constexpr int off_b = off_a + kNA * kABytes;
+constexpr int off_bar = off_b + kNB * kBBytes;
+constexpr int n_bars = 2 * kNA + 2 * kNB + 4;
 constexpr int off_misc = off_bar + n_bars * 8;
 constexpr int smem_bytes = off_misc + 16 + 1024;
 static_assert(smem_bytes <= 232448, "gemm shared memory");
@@ -77,17 +79,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem + off_a;
   uint8_t* sb = smem + off_b;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + off_bar);
-  uint64_t* empty = full + kNS;
-  uint64_t* acc_full = empty + kNS;   // [2]
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + off_bar);
+  uint64_t* a_empty = a_full + kNA;
+  uint64_t* b_full = a_empty + kNA;
+  uint64_t* b_empty = b_full + kNB;
+  uint64_t* acc_full = b_empty + kNB;  // [2]
   uint64_t* acc_empty = acc_full + 2;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_misc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // slices are the fast grid dimension: the CTAs of one row block run side by side
-  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileRows;  // first row of G in this launch
-  const int slice = blockIdx.x;
+  // row blocks are the fast grid dimension: the heavy first slice (every prefix reaches it)
+  // is scheduled before the light ones, which keeps the tail of the launch short
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kTileRows;  // first row of G in this launch
+  const int slice = blockIdx.y;
   const int d0 = slice * kN;
   const int n = p.n_prefix;
   int k_first = 0;  // prefixes k_first .. n-1 reach this slice
@@ -97,9 +102,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkc = static_cast<int>((p.kdim + kChunk - 1) / kChunk);  // K chunks per prefix
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kNA; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < kNB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -119,37 +128,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------- TMA producer
+  if ((warp == 0 || warp == 6) && lane == 0) {
+    // ------------------------------------------------------------- TMA producers
+    // warp 0: the weights (A operand); warp 6: the other side's transposed rows (B operand)
+    const bool wa = warp == 0;
+    const int ns = wa ? kNA : kNB;
+    uint64_t* fullb = wa ? a_full : b_full;
+    uint64_t* emptyb = wa ? a_empty : b_empty;
     uint32_t it = 0;
     bool ok = true;
     for (int k = n - 1; k >= k_first && ok; --k) {
       const int nk = min(prefix_end_of(p, k), d0 + kN) - d0;
       const int64_t wrow = static_cast<int64_t>(k) * p.w_rows_per_prefix;
       for (int c = 0; c < nkc; ++c, ++it) {
-        const uint32_t st = it % kNS, ph = (it / kNS) & 1;
-        if (!wait_bounded(&empty[st], ph ^ 1, abort_flag)) {
+        const uint32_t st = it % ns, ph = (it / ns) & 1;
+        if (!wait_bounded(&emptyb[st], ph ^ 1, abort_flag)) {
           fail(p, abort_flag);
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[st], kABytes + nk * kChunk * 2);
-        if constexpr (AMN) {
-          // [64 K rows x 64 M columns] twice: M blocks 0..63 and 64..127 of this row block
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d(sa + st * kABytes + h * (kABytes / 2), &tm_w, &full[st],
-                        static_cast<int>(m0 + h * 64), static_cast<int>(wrow + c * kChunk));
+        if (wa) {
+          mbar_arrive_expect_tx(&fullb[st], kABytes);
+          if constexpr (AMN) {
+            // [64 K rows x 64 M columns] twice: M blocks 0..63 and 64..127 of this row block
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(sa + st * kABytes + h * (kABytes / 2), &tm_w, &fullb[st],
+                          static_cast<int>(m0 + h * 64), static_cast<int>(wrow + c * kChunk));
+          } else {
+            tma_load_2d(sa + st * kABytes, &tm_w, &fullb[st], c * kChunk, static_cast<int>(wrow + m0));
+          }
         } else {
-          tma_load_2d(sa + st * kABytes, &tm_w, &full[st], c * kChunk, static_cast<int>(wrow + m0));
+          mbar_arrive_expect_tx(&fullb[st], nk * kChunk * 2);
+          for (int r0 = 0; r0 < nk; r0 += kBox)
+            tma_load_2d(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, &fullb[st],
+                        static_cast<int>(p.b_col0 + c * kChunk), d0 + r0);
         }
-        for (int r0 = 0; r0 < nk; r0 += kBox)
-          tma_load_2d(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, &full[st],
-                      static_cast<int>(p.b_col0 + c * kChunk), d0 + r0);
       }
     }
-    for (uint32_t q = 0; q < kNS && q < it; ++q) {  // let the last copies land
+    for (uint32_t q = 0; q < static_cast<uint32_t>(ns) && q < it; ++q) {  // let the last copies land
       const uint32_t u = it - 1 - q;
-      mbar_wait(&full[u % kNS], (u / kNS) & 1, kWaitLimitNs);
+      mbar_wait(&fullb[u % ns], (u / ns) & 1, kWaitLimitNs);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------- MMA issuer
@@ -169,14 +187,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = AMN ? idesc_bf16_f32_amn(kTileRows, static_cast<uint32_t>(nk))
                                  : idesc_bf16_f32(kTileRows, static_cast<uint32_t>(nk));
       for (int c = 0; c < nkc; ++c, ++it) {
-        const uint32_t st = it % kNS, ph = (it / kNS) & 1;
-        if (!wait_bounded(&full[st], ph, abort_flag)) {
+        const uint32_t sta = it % kNA, pha = (it / kNA) & 1;
+        const uint32_t stb = it % kNB, phb = (it / kNB) & 1;
+        if (!wait_bounded(&a_full[sta], pha, abort_flag) || !wait_bounded(&b_full[stb], phb, abort_flag)) {
           fail(p, abort_flag);
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t as = smem_u32(sa + st * kABytes), bs = smem_u32(sb + st * kBBytes);
+        const uint32_t as = smem_u32(sa + sta * kABytes), bs = smem_u32(sb + stb * kBBytes);
 #pragma unroll
         for (int kk = 0; kk < kChunk / 16; ++kk) {
           // K = 16 per MMA: MN-major A advances 16 K rows (two 1024-byte atoms), K-major 32 bytes
@@ -184,11 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : sdesc_kmajor_sw128(as + kk * 32);
           umma_bf16(d, adesc, sdesc_kmajor_sw128(bs + kk * 32), idesc, (c != 0 || kk != 0) ? 1u : 0u);
         }
-        umma_commit(&empty[st]);
+        umma_commit(&a_empty[sta]);
+        umma_commit(&b_empty[stb]);
       }
       if (ok) umma_commit(&acc_full[a]);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -279,8 +299,8 @@ cudaError_t gemm_kernel_setup() {
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool weights_mn,
                         cudaStream_t stream) {
   const int pn = p.prefix_end[p.n_prefix - 1];
-  dim3 grid(static_cast<unsigned>((pn + gemm::kN - 1) / gemm::kN),
-            static_cast<unsigned>((p.m_rows + kTileRows - 1) / kTileRows));
+  dim3 grid(static_cast<unsigned>((p.m_rows + kTileRows - 1) / kTileRows),
+            static_cast<unsigned>((pn + gemm::kN - 1) / gemm::kN));
   if (weights_mn)
     gemm::gemm_kernel<true><<<grid, gemm::kThreads, gemm::smem_bytes, stream>>>(tm_w, tm_yt, p);
   else
