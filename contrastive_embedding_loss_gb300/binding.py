@@ -53,6 +53,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.uf_contrastive_init.restype = I32
     lib.uf_contrastive_workspace_size.argtypes = [I64, I64, I32, P, I32, I32, I32]
     lib.uf_contrastive_workspace_size.restype = SZ
+    lib.uf_contrastive_workspace_min.argtypes = [I64, I64, I32, P, I32, I32, I32]
+    lib.uf_contrastive_workspace_min.restype = SZ
     lib.uf_contrastive_fwd_bwd.argtypes = [P, P, I64, I64, I32, P, I32, I32, F32, F32, P, P, P, P, P, P, P, SZ,
                                            P, P]
     lib.uf_contrastive_fwd_bwd.restype = I32
@@ -91,6 +93,12 @@ def uf_contrastive_workspace_size(Na, Nb, D, prefixes, kind, want_grads) -> int:
     pre = _int_array(list(prefixes))
     return int(load().uf_contrastive_workspace_size(int(Na), int(Nb), int(D), pre, len(prefixes), int(kind),
                                                     int(bool(want_grads))))
+
+
+def uf_contrastive_workspace_min(Na, Nb, D, prefixes, kind, want_grads) -> int:
+    pre = _int_array(list(prefixes))
+    return int(load().uf_contrastive_workspace_min(int(Na), int(Nb), int(D), pre, len(prefixes), int(kind),
+                                                   int(bool(want_grads))))
 
 
 def uf_contrastive_fwd_bwd(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, prefix_weights, loss_per_prefix,
@@ -134,7 +142,9 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
 
     Returns a dict with ``loss`` (n_prefix fp32), ``dA``/``dB`` (fp32, when grads) and
     ``row_terms``/``col_terms`` (when terms).  ``workspace`` may be a preallocated uint8
-    CUDA tensor of at least ``uf_contrastive_workspace_size`` bytes.
+    CUDA tensor of at least ``uf_contrastive_workspace_min`` bytes (its size sets how many
+    rows of backward weights the library keeps at once); by default one of the
+    recommended ``uf_contrastive_workspace_size`` bytes is allocated.
     """
     import torch
 
@@ -150,7 +160,7 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
     need = uf_contrastive_workspace_size(Na, Nb, D, prefixes, k, grads)
     if need == 0:
         raise UfError(1, "uf_contrastive_workspace_size")
-    if workspace is None or workspace.numel() < need:
+    if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     out = {"loss": torch.empty(n, dtype=torch.float32, device=dev)}
     if grads:

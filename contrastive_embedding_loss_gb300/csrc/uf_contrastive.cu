@@ -259,6 +259,13 @@ size_t uf_contrastive_workspace_size(int64_t Na, int64_t Nb, int D, const int* p
   return P.total;
 }
 
+size_t uf_contrastive_workspace_min(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix, int kind,
+                                    int want_grads) {
+  Plan P;
+  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, want_grads != 0, 1, P)) return 0;  // one 128-row chunk
+  return P.total;
+}
+
 uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int64_t Nb, int D, const int* prefixes,
                                    int n_prefix, int kind, float logit_scale, float bias,
                                    const float* prefix_weights, float* loss_per_prefix, float* row_terms,

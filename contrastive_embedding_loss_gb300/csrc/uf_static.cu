@@ -44,7 +44,7 @@ extern "C" uf_status_t uf_contrastive_fwd_bwd_static(const void* A, const void* 
                                                       float logit_scale, float bias, const float* prefix_weights,
                                                       float* loss_per_prefix, float* row_terms, float* col_terms,
                                                       float* dA, float* dB, int* device_status, void* stream) {
-  const size_t need = uf_contrastive_workspace_size(Na, Nb, D, prefixes, n_prefix, kind, dA != nullptr);
+  const size_t need = uf_contrastive_workspace_min(Na, Nb, D, prefixes, n_prefix, kind, dA != nullptr);
   if (need == 0) return UF_INVALID_ARGUMENT;
   if (need > static_cast<size_t>(UF_STATIC_WORKSPACE_BYTES)) return UF_WORKSPACE_TOO_SMALL;
   int device = 0;

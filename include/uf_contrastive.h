@@ -52,7 +52,7 @@ typedef enum uf_status {
   UF_OK = 0,
   UF_INVALID_ARGUMENT = 1,    /* null pointer, bad size, misaligned pointer, bad prefix ladder */
   UF_UNSUPPORTED = 2,         /* valid request this build does not implement (e.g. scale > 40) */
-  UF_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < uf_contrastive_workspace_size(...) */
+  UF_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < uf_contrastive_workspace_min(...) */
   UF_CUDA_ERROR = 4,          /* a CUDA runtime call or kernel launch failed */
   UF_DEVICE_TIMEOUT = 5       /* a kernel gave up a bounded wait (read from *device_status) */
 } uf_status_t;
@@ -79,12 +79,21 @@ UF_API int uf_contrastive_version(void);
 UF_API uf_status_t uf_contrastive_init(int device);
 
 /*
- * Bytes of device scratch that uf_contrastive_fwd_bwd needs for these arguments
- * (a pure function of the arguments; 0 when they are invalid).  want_grads != 0 sizes
- * the workspace for the backward as well.
+ * Recommended bytes of device scratch for uf_contrastive_fwd_bwd with these arguments (a
+ * pure function of the arguments; 0 when they are invalid).  want_grads != 0 sizes the
+ * workspace for the backward as well.  The backward keeps the bf16 weights of every
+ * prefix for a chunk of A's rows in the workspace (n_prefix x rows x Nb x 2 bytes); the
+ * recommended size holds all rows in one chunk unless that exceeds 48 GiB of weights, in
+ * which case the rows are cut into equal chunks.  Any workspace of at least
+ * uf_contrastive_workspace_min() bytes works: a smaller one only means more chunks.
  */
 UF_API size_t uf_contrastive_workspace_size(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix,
                                      int kind, int want_grads);
+
+/* The smallest workspace that uf_contrastive_fwd_bwd accepts for these arguments (one
+ * 128-row chunk of weights); 0 when they are invalid. */
+UF_API size_t uf_contrastive_workspace_min(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix,
+                                    int kind, int want_grads);
 
 /*
  * Forward and (optionally) backward of the Matryoshka contrastive loss.
@@ -108,8 +117,9 @@ UF_API size_t uf_contrastive_workspace_size(int64_t Na, int64_t Nb, int D, const
  *                   written as 0 for the other kinds.
  *   dA, dB          device fp32 Na x D / Nb x D, 16-byte aligned, or both NULL for a
  *                   forward-only call.  Columns at or past the last prefix are written 0.
- *   workspace       device scratch of workspace_bytes >= uf_contrastive_workspace_size(),
- *                   256-byte aligned.  Owned by the caller; one call at a time per workspace.
+ *   workspace       device scratch of workspace_bytes >= uf_contrastive_workspace_min(),
+ *                   256-byte aligned (uf_contrastive_workspace_size() bytes recommended).
+ *                   Owned by the caller; one call at a time per workspace.
  *   device_status   device int or NULL.  Kernels that give up a bounded wait store
  *                   UF_DEVICE_TIMEOUT there (it is never cleared by the library).
  *   stream          a cudaStream_t (0 = legacy default stream).
@@ -133,10 +143,11 @@ UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t 
  * The scratch is one device array of UF_STATIC_WORKSPACE_BYTES inside the library, which
  * every GPU that loads the library keeps until the process exits.  The caller still
  * passes inputs and outputs, with the same meaning and rules as uf_contrastive_fwd_bwd.
- *   - A request whose uf_contrastive_workspace_size() exceeds UF_STATIC_WORKSPACE_BYTES
- *     returns UF_WORKSPACE_TOO_SMALL before anything is enqueued (for instance CLIP or
- *     SigLIP with gradients fits up to about N = 1024 at D = 1024, forward-only calls up
- *     to far larger batches).
+ *   - A request whose uf_contrastive_workspace_min() exceeds UF_STATIC_WORKSPACE_BYTES
+ *     returns UF_WORKSPACE_TOO_SMALL before anything is enqueued (at D = 1024 with the
+ *     five-prefix ladder, CLIP with gradients fits up to about N = 10240, SigLIP to a
+ *     larger N); inside that bound the backward cuts A's rows into as many weight chunks
+ *     as the array needs.
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture.
  *   - All calls on a device share the one array, and it keeps whatever the last call left

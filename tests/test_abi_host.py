@@ -67,6 +67,13 @@ def test_workspace_size(lib):
     # chunk (5 x 65536^2 x 2 bytes = 40 GiB) within the default 48 GiB weight budget
     full = 5 * 65536 * 65536 * 2
     assert full <= ws(65536, 65536, 1024, LADDER, 0, 1) - ws(65536, 65536, 1024, LADDER, 0, 0) < full + (2 << 30)
+    # the minimum holds one 128-row chunk of weights and never exceeds the recommendation
+    wmin = binding.uf_contrastive_workspace_min
+    for N in (1, 300, 4096, 65536):
+        assert 0 < wmin(N, N, 1024, LADDER, 0, 1) <= ws(N, N, 1024, LADDER, 0, 1)
+    assert wmin(65536, 65536, 1024, LADDER, 0, 1) < (3 << 29)  # vs 40 GiB of weights for one chunk
+    assert wmin(256, 255, 1024, LADDER, 0, 1) == 0
+    assert wmin(4096, 4096, 1024, LADDER, 0, 0) == ws(4096, 4096, 1024, LADDER, 0, 0)  # no weights forward-only
     # larger batches are cut into row chunks: the weight array stays within its budget
     big = 262144
     assert ws(big, big, 1024, LADDER, 0, 1) - ws(big, big, 1024, LADDER, 0, 0) < (48 << 30) + (1 << 30)
@@ -81,6 +88,13 @@ def _call(**kw):
                 workspace=FAKE, workspace_bytes=1 << 40, device_status=None, stream=None)
     args.update(kw)
     return binding.uf_contrastive_fwd_bwd(**args)
+
+
+def test_workspace_below_the_minimum_is_rejected_on_the_host(lib):
+    WS = 3
+    need = binding.uf_contrastive_workspace_min(256, 256, 1024, LADDER, 0, 1)
+    assert _call(workspace_bytes=need - 256) == WS
+    assert _call(workspace_bytes=0) == WS
 
 
 def test_argument_errors_are_found_on_the_host(lib):

@@ -32,10 +32,10 @@ def dev(bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def run(binding, kind, A16, B16, pre, scale, bias, weights=None, grads=True):
+def run(binding, kind, A16, B16, pre, scale, bias, weights=None, grads=True, workspace=None):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = binding.contrastive_fwd_bwd(dev(A16), dev(B16), kind, pre, scale, bias, weights, grads=grads, terms=True,
-                                      device_status=status)
+                                      workspace=workspace, device_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "a kernel reported a timeout"
     return {k: v.double().cpu().numpy() for k, v in out.items()}
@@ -94,6 +94,32 @@ def test_parity_small(ctx, kind, Na, Nb, D, pre, scale, bias, noise, seed):
     check_grad(got["dA"], ref["dA"], "dA")
     check_grad(got["dB"], ref["dB"], "dB")
     assert np.all(got["dA"][:, pre[-1]:] == 0) and np.all(got["dB"][:, pre[-1]:] == 0)
+
+
+CHUNKED = [
+    # kind, Na, Nb, D, prefixes, scale, bias, noise, seed: the smallest workspace, so the
+    # backward weights are cut into 128-row chunks (the dB contraction adds over chunks)
+    ("clip", 640, 640, 1024, LADDER, 1 / 0.07, 0.0, 1.0, 51),
+    ("siglip", 300, 300, 1024, LADDER, 10.0, -10.0, 0.7, 52),
+    ("rows", 200, 700, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 53),
+    ("clip", 257, 257, 384, (64, 192, 384), 5.0, 0.0, 1.0, 54),
+]
+
+
+@pytest.mark.parametrize("kind,Na,Nb,D,pre,scale,bias,noise,seed", CHUNKED)
+def test_parity_smallest_workspace(ctx, kind, Na, Nb, D, pre, scale, bias, noise, seed):
+    A16, B16 = make(kind, Na, Nb, D, seed, noise)
+    k = ctx.KINDS[kind]
+    wmin = ctx.uf_contrastive_workspace_min(Na, Nb, D, pre, k, True)
+    assert wmin < ctx.uf_contrastive_workspace_size(Na, Nb, D, pre, k, True)  # more than one chunk
+    ws = torch.empty(wmin, dtype=torch.uint8, device="cuda")
+    got = run(ctx, kind, A16, B16, pre, scale, bias, workspace=ws)
+    ref = oracle.fwd_bwd(kind, A16, B16, pre, scale, bias)
+    check_loss(got["loss"], ref["loss"])
+    check_grad(got["dA"], ref["dA"], "dA")
+    check_grad(got["dB"], ref["dB"], "dB")
+    full = run(ctx, kind, A16, B16, pre, scale, bias)  # one chunk: the same loss bits
+    assert np.array_equal(got["loss"], full["loss"])
 
 
 def test_forward_only_matches(ctx):

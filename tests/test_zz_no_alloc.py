@@ -55,7 +55,7 @@ def _static_call(b, kind, A, B, scale, bias, grads):
 
 
 CASES = [
-    ("clip", 1024, 1024, 1 / 0.07, 0.0, True),    # the largest CLIP batch with gradients that fits
+    ("clip", 4096, 4096, 1 / 0.07, 0.0, True),    # the backward weights take several row chunks
     ("siglip", 700, 700, 10.0, -10.0, True),      # ragged tiles
     ("rows", 300, 9000, 1 / 0.05, 0.0, False),    # forward only
 ]
@@ -84,14 +84,15 @@ def test_static_entry_matches_workspace_entry(binding, kind, Na, Nb, scale, bias
 
 
 def test_static_entry_rejects_batches_beyond_its_scratch(binding):
-    A16, B16 = synth.paired(4096, 1024, 1.0, 8)
-    need = binding.uf_contrastive_workspace_size(4096, 4096, 1024, LADDER, 0, True)
+    N = 16384
+    A16, B16 = synth.paired(N, 1024, 1.0, 8)
+    need = binding.uf_contrastive_workspace_min(N, N, 1024, LADDER, 0, True)
     assert need > binding.UF_STATIC_WORKSPACE_BYTES
     A, B = _dev(A16), _dev(B16)
     loss = torch.zeros(len(LADDER), device="cuda")
-    dA = torch.zeros((4096, 1024), device="cuda")
-    dB = torch.zeros((4096, 1024), device="cuda")
-    st = binding.uf_contrastive_fwd_bwd_static(A.data_ptr(), B.data_ptr(), 4096, 4096, 1024, LADDER, 0, 1 / 0.07, 0.0,
+    dA = torch.zeros((N, 1024), device="cuda")
+    dB = torch.zeros((N, 1024), device="cuda")
+    st = binding.uf_contrastive_fwd_bwd_static(A.data_ptr(), B.data_ptr(), N, N, 1024, LADDER, 0, 1 / 0.07, 0.0,
                                                None, loss.data_ptr(), None, None, dA.data_ptr(), dB.data_ptr(), None,
                                                torch.cuda.current_stream().cuda_stream)
     assert binding.uf_status_name(st) == "workspace-too-small"
