@@ -84,39 +84,52 @@ __device__ __forceinline__ uint4 cells8(const float* dot, uint32_t c1, uint32_t 
     s2v[4] = s2b.x; s2v[5] = s2b.y; s2v[6] = s2b.z; s2v[7] = s2b.w;
   }
   uint32_t packed[4];
+  if constexpr (KIND == KIND_SIGLIP) {
 #pragma unroll
-  for (int j = 0; j < 8; j += 2) {
-    float mv[2];
+    for (int j = 0; j < 8; j += 2) {
+      float mv[2];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int jj = j + u;
-      const float s1 = s1v[jj];
-      const float t = R1 * s1;
-      float m;
-      bool keep = true;
-      if constexpr (CHECK) {
-        const int col = col0 + jj;
-        keep = row_ok && col < ncols && col != dcol;
-      }
-      if constexpr (KIND == KIND_SIGLIP) {
-        const float x2 = fmaf(t, dot[jj], b2);
+      for (int u = 0; u < 2; ++u) {
+        const int jj = j + u;
+        const float s1 = s1v[jj];
+        bool keep = true;
+        if constexpr (CHECK) {
+          const int col = col0 + jj;
+          keep = row_ok && col < ncols && col != dcol;
+        }
+        const float x2 = fmaf(R1 * s1, dot[jj], b2);
         const float e = ex2_approx(-fabsf(x2));
         const float d = 1.f + e;
         const float r = rcp_approx(d);
         const float sig = x2 >= 0.f ? r : e * r;
-        m = sig * (R2 * s1);
+        float m = sig * (R2 * s1);
         if (R3 != 0.f) {  // this launch also sums the SigLIP loss
           const float l = fmaxf(x2, 0.f) + lg2_approx(d);
           acc_l += keep ? l : 0.f;
         }
-      } else {
-        const float e = ex2_approx(fmaf(t, dot[jj], -L));
-        m = e * fmaf(R2, s1, R3 * s2v[jj]);
+        if constexpr (CHECK) m = keep ? m : 0.f;
+        mv[u] = m;
       }
-      if constexpr (CHECK) m = keep ? m : 0.f;
-      mv[u] = m;
+      packed[j / 2] = pack_bf16x2(mv[0], mv[1]);
     }
-    packed[j / 2] = pack_bf16x2(mv[0], mv[1]);
+  } else {
+    // two cells per packed instruction: x = R1 sigma dot - L, e = 2^x, m = e (R2 sigma + R3 sigma beta)
+    const float2 r1 = make_float2(R1, R1), r2 = make_float2(R2, R2), r3 = make_float2(R3, R3);
+    const float2 nl = make_float2(-L, -L);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const float2 s1 = make_float2(s1v[j], s1v[j + 1]);
+      const float2 s2 = make_float2(s2v[j], s2v[j + 1]);
+      const float2 x = fma2(mul2(r1, s1), make_float2(dot[j], dot[j + 1]), nl);
+      const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      float2 m = mul2(e, fma2(r2, s1, mul2(r3, s2)));
+      if constexpr (CHECK) {
+        const int col = col0 + j;
+        if (!(row_ok && col < ncols && col != dcol)) m.x = 0.f;
+        if (!(row_ok && col + 1 < ncols && col + 1 != dcol)) m.y = 0.f;
+      }
+      packed[j / 2] = pack_bf16x2(m.x, m.y);
+    }
   }
   return make_uint4(packed[0], packed[1], packed[2], packed[3]);
 }
@@ -281,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int t = 0; t < 2 && t < T; ++t) prefetch_colf(t);
     cp_async_commit();
-    // raw row factors of the next step's prefix (rho_i, and rho_i alpha_i for CLIP/ROWS),
-    // loaded one step ahead
+    // raw row factors of the next band (rho_i, and rho_i alpha_i for CLIP/ROWS), loaded one
+    // band ahead
     float n_rho = 0.f, n_alpha = 0.f;
     auto load_row = [&](int k) {
       n_rho = row_ok ? p.rinv_x[static_cast<int64_t>(k) * p.nx + gi] : 0.f;
@@ -293,91 +306,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t slot_off = static_cast<int64_t>(split * 4 + cq) * n * p.nx + gi;
     const float siglip_loss = (KIND == KIND_SIGLIP && p.rowacc) ? 1.f : 0.f;
     const int64_t wrow = static_cast<int64_t>(il0) + q * 32;  // this warp's first row in the weight array
-    uint32_t uses[2] = {0, 0};
+    const uint64_t l2_evict_first = l2_policy_evict_first();
+    uint32_t uses = 0;  // uses of each accumulator so far (both advance together)
     bool ok = true;
-    for (int s = 0; s < sched.steps(); ++s) {
-      int t, b;
-      sched.at(s, t, b);
-      if ((t & 1) == 0 && b == 0) {
-        // a tile pair begins (every warp reaches this point at the same step)
-        named_bar_sync(1, kEpiThreads);          // all are done with the previous pair
-        for (int u = 2; u < 4 && t + u < T; ++u) prefetch_colf(t + u);
-        cp_async_commit();
-        cp_async_wait<1>();                      // this pair's factors (fetched a pair ago) are in
-        named_bar_sync(1, kEpiThreads);
-      }
-      const int a = t & 1;
-      const int k = b;
-      ++uses[a];
-      if (!ok) continue;
-      if (!wait_bounded(&acc_full[a], (uses[a] - 1) & 1, abort_flag)) {
-        fail(p, abort_flag);
-        ok = false;
-        continue;
-      }
-      tc_fence_after();
-      float v[64];
-      tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[a]);
+    // the schedule of Schedule::at as nested loops: tile pairs, bands, the pair's tiles
+    for (int tp = 0; tp < T; tp += 2) {
+      const int width = tp + 1 < T ? 2 : 1;
+      // a tile pair begins (every warp reaches this point at the same step)
+      named_bar_sync(1, kEpiThreads);          // all are done with the previous pair
+      for (int u = 2; u < 4 && tp + u < T; ++u) prefetch_colf(tp + u);
+      cp_async_commit();
+      cp_async_wait<1>();                      // this pair's factors (fetched a pair ago) are in
+      named_bar_sync(1, kEpiThreads);
+      for (int b = 0; b < n; ++b, ++uses) {
+        const int k = b;
+        // this band's row factors, then the next band's (or the next pair's first) in flight
+        const float rho = n_rho;
+        float R2, R3;
+        if constexpr (KIND == KIND_SIGLIP) {
+          float ms = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < kMaxPrefix; ++kk)
+            if (kk == k) ms = p.m_scale[kk];
+          R2 = rho * ms;  // rho_i w_k t / N
+          R3 = siglip_loss;
+        } else {
+          R2 = n_alpha;   // rho_i alpha_i
+          R3 = rho;
+        }
+        const float R1 = p.L * rho;
+        load_row(b + 1 < n ? b + 1 : 0);
+        for (int u = 0; u < width; ++u) {
+          const int t = tp + u;
+          const int a = u;
+          if (!ok) continue;
+          if (!wait_bounded(&acc_full[a], uses & 1, abort_flag)) {
+            fail(p, abort_flag);
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          float v[64];
+          tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
 
-      const float rho = n_rho;
-      float R2, R3;
-      if constexpr (KIND == KIND_SIGLIP) {
-        float ms = 0.f;
+          const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
+          const int64_t left = p.ny - j0;
+          const int ncols = left < kCols ? static_cast<int>(left) : kCols;
+          const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
+          const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (il0 + kTileRows > p.rows);
+          const int diag_col = static_cast<int>(dtile) + r;  // tile column of this row's positive
+          const uint32_t cf = colf_s + (t & 3) * kColfBytes + cq * 64 * 4;
+          const uint32_t c1 = cf + (k * 2 + 0) * kCols * 4;
+          const uint32_t c2 = cf + (k * 2 + 1) * kCols * 4;
+          // the previous TMA store of this warp must have read its staging block
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          float al = 0.f;
+          if (check) {
 #pragma unroll
-        for (int kk = 0; kk < kMaxPrefix; ++kk)
-          if (kk == k) ms = p.m_scale[kk];
-        R2 = rho * ms;  // rho_i w_k t / N
-        R3 = siglip_loss;
-      } else {
-        R2 = n_alpha;   // rho_i alpha_i
-        R3 = rho;
-      }
-      const float R1 = p.L * rho;
-      if (s + 1 < sched.steps()) {
-        int tn, bn;
-        sched.at(s + 1, tn, bn);
-        load_row(bn);
-      }
-      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
-      const int64_t left = p.ny - j0;
-      const int ncols = left < kCols ? static_cast<int>(left) : kCols;
-      const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
-      const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (il0 + kTileRows > p.rows);
-      const int diag_col = static_cast<int>(dtile) + r;  // tile column of this row's positive
-      const uint32_t cf = colf_s + (t & 3) * kColfBytes + cq * 64 * 4;
-      const uint32_t c1 = cf + (k * 2 + 0) * kCols * 4;
-      const uint32_t c2 = cf + (k * 2 + 1) * kCols * 4;
-      // the previous TMA store of this warp must have read its staging block
-      if (lane == 0) bulk_wait_read0();
-      __syncwarp();
-      float al = 0.f;
-      if (check) {
+            for (int ch = 0; ch < 8; ++ch)
+              st_shared_v4(stage_row + ((ch ^ swz) << 4),
+                           cells8<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, p.L, p.b2,
+                                              cq * 64 + ch * 8, ncols, diag_col, row_ok, al));
+          } else {
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(stage_row + ((ch ^ swz) << 4),
-                       cells8<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, p.L, p.b2,
-                                          cq * 64 + ch * 8, ncols, diag_col, row_ok, al));
-      } else {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(stage_row + ((ch ^ swz) << 4), cells8<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32,
-                                                                           R1, R2, R3, p.L, p.b2, 0, 0, 0, true,
-                                                                           al));
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && j0 + cq * 64 < p.ny) {  // a quarter wholly past the last column stores nothing
-        tma_store_2d(&tm_w, stage, static_cast<int>(j0 + cq * 64),
-                     static_cast<int>(static_cast<int64_t>(k) * p.w_rows_per_prefix + wrow));
-        bulk_commit();
-      }
-      if (KIND == KIND_SIGLIP && p.rowacc && row_ok) {
-        float* pl = p.rowacc + slot_off + static_cast<int64_t>(k) * p.nx;
-        if (t == 0) *pl = al;
-        else atomicAdd(pl, al);
+            for (int ch = 0; ch < 8; ++ch)
+              st_shared_v4(stage_row + ((ch ^ swz) << 4),
+                           cells8<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, p.L, p.b2, 0, 0,
+                                               0, true, al));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && j0 + cq * 64 < p.ny) {  // a quarter wholly past the last column stores nothing
+            // the weights are written once here and read back by the GEMMs much later: keep
+            // them from evicting the score operands, which every CTA re-reads
+            tma_store_2d_hint(&tm_w, stage, static_cast<int>(j0 + cq * 64),
+                              static_cast<int>(static_cast<int64_t>(k) * p.w_rows_per_prefix + wrow),
+                              l2_evict_first);
+            bulk_commit();
+          }
+          if (KIND == KIND_SIGLIP && p.rowacc && row_ok) {
+            float* pl = p.rowacc + slot_off + static_cast<int64_t>(k) * p.nx;
+            if (t == 0) *pl = al;
+            else atomicAdd(pl, al);
+          }
+        }
       }
     }
     cp_async_wait<0>();
