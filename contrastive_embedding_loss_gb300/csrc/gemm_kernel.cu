@@ -4,21 +4,22 @@
 //     A side:  G[i, d] = sum_k [d < p_k] sum_j m^k[i, j] B[j, d]      (weights K-major)
 //     B side:  G[j, d] = sum_k [d < p_k] sum_i m^k[i, j] A[i, d]      (weights MN-major)
 //
-// (prefix-expanded: prefix k contributes to its first p_k dimensions).  A CTA owns 128
-// rows of G and one 256-dimension slice [d0, d0 + 256).  For each prefix reaching the slice,
-// from the widest down, it streams 64-long K chunks of m^k (A operand) and of the other
-// side's transposed embeddings restricted to the slice (B operand, K-major, N = min(p_k,
-// d0 + 256) - d0 rows) into one of two TMEM accumulators, so the MMA of prefix k - 1
-// overlaps the epilogue of prefix k.  The weights come from HBM and the other operand
-// mostly from L2, so each has its own TMA ring and producer: 6 stages of weights (about
-// 2500 MMA cycles of latency cover) and 4 of the other operand.  The epilogue adds G^k into G
-// in global memory and forms the projection scalar of the norm backward,
-//     r^k_row = sum_j m^k dot^k = x_row[:p_k] . G^k_row,
-// as this slice's partial sum (one slot per slice).
+// (prefix-expanded: prefix k contributes to its first p_k dimensions).  Two CTAs on two SMs
+// form a pair (a cluster of 2, cta_group::2): together they own 256 rows of G (128 each)
+// and one 256-dimension slice [d0, d0 + 256).  For each prefix reaching the slice, from the
+// widest down, they stream 64-long K chunks of m^k (A operand: each CTA its own 128 rows)
+// and of the other side's transposed embeddings restricted to the slice (B operand, K-major,
+// N = min(p_k, d0 + 256) - d0 rows, each CTA holding half of them); the leader CTA issues
+// 256 x N x 16 MMAs that read both halves, so each SM loads half of the B operand a
+// single-SM 128-row tile would need.  Accumulators: two per CTA in TMEM (256 columns each),
+// alternating between prefixes, so the epilogue of prefix k (add G^k into G in global
+// memory; r^k = x_row . G^k_row, the projection scalar of the norm backward, as this
+// slice's partial) overlaps the MMAs of prefix k - 1.  The weights come from HBM and the
+// other operand mostly from L2: each has its own TMA ring and producer.
 //
-// Warps (224 threads): lane 0 of warp 0 loads the weights, lane 0 of warp 6 the other
-// operand, lane 0 of warp 1 issues the MMAs, warps 2..5 are the epilogue (warp w reads
-// TMEM lanes 32 (w % 4) .. + 31).
+// Warps (224 threads per CTA): lane 0 of warp 0 loads the weights, lane 0 of warp 6 the
+// other operand, lane 0 of warp 1 (leader CTA only) issues the MMAs, warps 2..5 are the
+// epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31).
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -27,11 +28,11 @@ namespace gemm {
 
 constexpr int kThreads = 224;
 constexpr int kN = 256;                          // gradient slice width = TMEM columns per accumulator
-constexpr int kNA = 6;                           // weight stages
-constexpr int kNB = 4;                           // stages of the other operand
-constexpr int kABytes = kTileRows * kChunk * 2;  // 16 KB: 128 rows of G x 64 of K
-constexpr int kBBytes = kN * kChunk * 2;         // 32 KB: up to 256 dims x 64 of K
-constexpr int kBox = kBwdYtBox;                  // rows per B-operand TMA box (and per MN-major A box)
+constexpr int kNA = 7;                           // weight stages
+constexpr int kNB = 6;                           // stages of the other operand
+constexpr int kABytes = kTileRows * kChunk * 2;  // 16 KB: this CTA's 128 rows of G x 64 of K
+constexpr int kBBytes = kN / 2 * kChunk * 2;     // 16 KB: this CTA's half of up to 256 dims x 64 of K
+constexpr int kBox = kGemmBBox;                  // rows per B-operand TMA box
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 constexpr int off_a = 0;
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_misc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
   // row blocks are the fast grid dimension: the heavy first slice (every prefix reaches it)
   // is scheduled before the light ones, which keeps the tail of the launch short
   const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kTileRows;  // first row of G in this launch
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);  // the four epilogue warps
+      mbar_init(&acc_empty[a], 8);  // the four epilogue warps of each CTA of the pair (leader's copy)
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -120,17 +122,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_yt);
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 2 * kN);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, 2 * kN);  // the same columns in both SMs of the pair
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ------------------------------------------------------------- TMA producers
-    // warp 0: the weights (A operand); warp 6: the other side's transposed rows (B operand)
+    // warp 0: the weights (A operand); warp 6: the other side's transposed rows (B operand).
+    // Both CTAs load their own parts into their own shared memory; completion is counted on
+    // the leader's barrier, which the leader arms for the bytes of both.
     const bool wa = warp == 0;
     const int ns = wa ? kNA : kNB;
     uint64_t* fullb = wa ? a_full : b_full;
@@ -139,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = n - 1; k >= k_first && ok; --k) {
       const int nk = min(prefix_end_of(p, k), d0 + kN) - d0;
+      const int half = nk / 2;  // B rows held by each CTA
       const int64_t wrow = static_cast<int64_t>(k) * p.w_rows_per_prefix;
       for (int c = 0; c < nkc; ++c, ++it) {
         const uint32_t st = it % ns, ph = (it / ns) & 1;
@@ -147,30 +152,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        const uint32_t bar = mapa_shared(smem_u32(&fullb[st]), 0);
+        if (rank == 0) mbar_arrive_expect_tx(&fullb[st], 2 * (wa ? kABytes : half * kChunk * 2));
         if (wa) {
-          mbar_arrive_expect_tx(&fullb[st], kABytes);
           if constexpr (AMN) {
-            // [64 K rows x 64 M columns] twice: M blocks 0..63 and 64..127 of this row block
+            // [64 K rows x 64 M columns] twice: M blocks 0..63 and 64..127 of this CTA's rows
             for (int h = 0; h < 2; ++h)
-              tma_load_2d(sa + st * kABytes + h * (kABytes / 2), &tm_w, &fullb[st],
-                          static_cast<int>(m0 + h * 64), static_cast<int>(wrow + c * kChunk));
+              tma_load_2d_pair(sa + st * kABytes + h * (kABytes / 2), &tm_w, bar, static_cast<int>(m0 + h * 64),
+                               static_cast<int>(wrow + c * kChunk));
           } else {
-            tma_load_2d(sa + st * kABytes, &tm_w, &fullb[st], c * kChunk, static_cast<int>(wrow + m0));
+            tma_load_2d_pair(sa + st * kABytes, &tm_w, bar, c * kChunk, static_cast<int>(wrow + m0));
           }
         } else {
-          mbar_arrive_expect_tx(&fullb[st], nk * kChunk * 2);
-          for (int r0 = 0; r0 < nk; r0 += kBox)
-            tma_load_2d(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, &fullb[st],
-                        static_cast<int>(p.b_col0 + c * kChunk), d0 + r0);
+          for (int r0 = 0; r0 < half; r0 += kBox)
+            tma_load_2d_pair(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, bar,
+                             static_cast<int>(p.b_col0 + c * kChunk), d0 + static_cast<int>(rank) * half + r0);
         }
       }
     }
-    for (uint32_t q = 0; q < static_cast<uint32_t>(ns) && q < it; ++q) {  // let the last copies land
-      const uint32_t u = it - 1 - q;
-      mbar_wait(&fullb[u % ns], (u / ns) & 1, kWaitLimitNs);
+    if (rank == 0) {
+      for (uint32_t q = 0; q < static_cast<uint32_t>(ns) && q < it; ++q) {  // let the last copies land
+        const uint32_t u = it - 1 - q;
+        mbar_wait(&fullb[u % ns], (u / ns) & 1, kWaitLimitNs);
+      }
+    } else {
+      // the follower's copies are counted on the leader's barriers: wait until the MMAs that
+      // read them (hence the copies) are done, i.e. the last stages are released
+      for (uint32_t q = 0; q < static_cast<uint32_t>(ns) && q < it; ++q) {
+        const uint32_t u = it - 1 - q;
+        mbar_wait(&emptyb[u % ns], (u / ns) & 1, kWaitLimitNs);
+      }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ------------------------------------------------------------- MMA issuer (leader)
     uint32_t it = 0, pi = 0;
     bool ok = true;
     for (int k = n - 1; k >= k_first && ok; --k, ++pi) {
@@ -184,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t d = tmem + a * kN;
-      const uint32_t idesc = AMN ? idesc_bf16_f32_amn(kTileRows, static_cast<uint32_t>(nk))
-                                 : idesc_bf16_f32(kTileRows, static_cast<uint32_t>(nk));
+      const uint32_t idesc = AMN ? idesc_bf16_f32_amn(2 * kTileRows, static_cast<uint32_t>(nk))
+                                 : idesc_bf16_f32(2 * kTileRows, static_cast<uint32_t>(nk));
       for (int c = 0; c < nkc; ++c, ++it) {
         const uint32_t sta = it % kNA, pha = (it / kNA) & 1;
         const uint32_t stb = it % kNB, phb = (it / kNB) & 1;
@@ -201,12 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // K = 16 per MMA: MN-major A advances 16 K rows (two 1024-byte atoms), K-major 32 bytes
           const uint64_t adesc = AMN ? sdesc_mnmajor_sw128(as + kk * 2048, kABytes / 2, 1024)
                                      : sdesc_kmajor_sw128(as + kk * 32);
-          umma_bf16(d, adesc, sdesc_kmajor_sw128(bs + kk * 32), idesc, (c != 0 || kk != 0) ? 1u : 0u);
+          umma_bf16_pair(d, adesc, sdesc_kmajor_sw128(bs + kk * 32), idesc, (c != 0 || kk != 0) ? 1u : 0u);
         }
-        umma_commit(&a_empty[sta]);
-        umma_commit(&b_empty[stb]);
+        umma_commit_pair(&a_empty[sta]);  // releases the stage in both CTAs
+        umma_commit_pair(&b_empty[stb]);
       }
-      if (ok) umma_commit(&acc_full[a]);
+      if (ok) umma_commit_pair(&acc_full[a]);
     }
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------- epilogue
@@ -267,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[a]);
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&acc_empty[a]), 0));
       if (row_ok) {
         float* pc = p.crow + (static_cast<int64_t>(slice) * n + k) * p.crow_rows + g;
         *pc = p.accumulate ? *pc + rk : rk;
@@ -276,10 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // no MMA, copy or remote arrive of the pair is still in flight
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * kN);
+    tmem_dealloc_pair(tmem, 2 * kN);
   }
 }
 
@@ -299,13 +313,22 @@ cudaError_t gemm_kernel_setup() {
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool weights_mn,
                         cudaStream_t stream) {
   const int pn = p.prefix_end[p.n_prefix - 1];
-  dim3 grid(static_cast<unsigned>((p.m_rows + kTileRows - 1) / kTileRows),
-            static_cast<unsigned>((pn + gemm::kN - 1) / gemm::kN));
-  if (weights_mn)
-    gemm::gemm_kernel<true><<<grid, gemm::kThreads, gemm::smem_bytes, stream>>>(tm_w, tm_yt, p);
-  else
-    gemm::gemm_kernel<false><<<grid, gemm::kThreads, gemm::smem_bytes, stream>>>(tm_w, tm_yt, p);
-  return cudaGetLastError();
+  const int64_t blocks = (p.m_rows + kTileRows - 1) / kTileRows;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((blocks + 1) / 2 * 2),  // whole pairs: a padding CTA stores nothing
+                     static_cast<unsigned>((pn + gemm::kN - 1) / gemm::kN));
+  cfg.blockDim = dim3(gemm::kThreads);
+  cfg.dynamicSmemBytes = gemm::smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (weights_mn) return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<true>, tm_w, tm_yt, p);
+  return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<false>, tm_w, tm_yt, p);
 }
 
 }  // namespace ufc

@@ -319,7 +319,7 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
   uint16_t* At = reinterpret_cast<uint16_t*>(ws + P.o_at);
   uint16_t* Bt = reinterpret_cast<uint16_t*>(ws + P.o_bt);
   if (grads) {
-    if (!encode_map(&tmAt, At, D, Na, P.lda, kBwdYtBox) || !encode_map(&tmBt, Bt, D, Nb, P.ldb, kBwdYtBox))
+    if (!encode_map(&tmAt, At, D, Na, P.lda, kGemmBBox) || !encode_map(&tmBt, Bt, D, Nb, P.ldb, kGemmBBox))
       return UF_CUDA_ERROR;
   } else {
     tmAt = tmA;
