@@ -129,6 +129,21 @@ cudaError_t launch_transpose(const uint16_t* X, uint16_t* Xt, int64_t rows, int 
 //   SigLIP     term = ln2 * (sum of negatives' softplus in log2 units) + softplus(-x_ii)
 __device__ __forceinline__ double softplus_d(double y) { return y > 0 ? y + log1p(exp(-y)) : log1p(exp(y)); }
 
+// Sum of the slot partials acc[sl * stride] for sl < slots, in one fixed order: eight
+// interleaved fp32 accumulators (eight loads in flight per thread) combined pairwise.  The
+// partials are positive fp32 sums themselves, so fp32 keeps the total to a few ulps (GB300's
+// fp64 pipe is too slow for a 512-term sum per column).
+__device__ __forceinline__ double sum_slots(const float* acc, int slots, int64_t stride) {
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int sl = 0;
+  for (; sl + 8 <= slots; sl += 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s[u] += acc[static_cast<int64_t>(sl + u) * stride];
+  }
+  for (; sl < slots; ++sl) s[0] += acc[static_cast<int64_t>(sl) * stride];
+  return static_cast<double>(((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7])));
+}
+
 __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
   const int n = p.n_prefix;
   const int64_t total_a = static_cast<int64_t>(n) * p.na;
@@ -151,8 +166,8 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
         p.terms_b[ee] = 0.f;
         continue;
       }
-      double s = 0.0;  // log2 units, fixed order over slots
-      for (int sl = 0; sl < slots; ++sl) s += acc[(static_cast<int64_t>(sl) * n + k) * nrows + i];
+      const double s = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
+      // (log2 units)
       const double x_ii = static_cast<double>(p.tau_or_t) * cos_ii + static_cast<double>(p.bias);
       p.terms_a[ee] = static_cast<float>(s * 0.6931471805599453 + (has_pos ? softplus_d(-x_ii) : 0.0));
       continue;
@@ -161,8 +176,8 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
       p.terms_b[ee] = 0.f;
       continue;
     }
-    double zneg = 0.0;  // sum over negatives of exp(s_ij - tau), fixed order over slots
-    for (int sl = 0; sl < slots; ++sl) zneg += acc[(static_cast<int64_t>(sl) * n + k) * nrows + i];
+    // sum over negatives of exp(s_ij - tau)
+    const double zneg = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
     const double tau = p.tau_or_t;
     const double s_ii = tau * cos_ii;
     const double e_ii = has_pos ? exp(s_ii - tau) : 0.0;

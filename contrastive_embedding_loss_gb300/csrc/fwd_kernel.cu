@@ -80,6 +80,7 @@ __device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag) 
 }
 
 // Sum of 32 values over the warp's 32 lanes, scattered: lane l returns the sum of v[l].
+// (fp32 throughout: the summands span e^-2tau .. 1, beyond what fp16 pairs could carry.)
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {
@@ -101,30 +102,40 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 template <int KIND, bool COLS, bool CHECK>
 __device__ __forceinline__ float fwd_cells(const float (&v)[64], const float* cf, float R1, float L, float b2,
                                            int col_base, int ncols, int dcol, bool row_ok, int lane, float* cp) {
-  float rs = 0.f;
+  float2 rs = make_float2(0.f, 0.f);  // two interleaved row sums
+  const float2 r1 = make_float2(R1, R1), nl = make_float2(-L, -L);
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     float e[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float tt = R1 * cf[g * 32 + j];
-      float val;
+    for (int j = 0; j < 32; j += 2) {
+      const int c = g * 32 + j;
+      float2 val;
       if constexpr (KIND == KIND_SIGLIP) {
-        const float x2 = fmaf(tt, v[g * 32 + j], b2);
-        val = fmaxf(x2, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(x2)));
+        float w[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float x2 = fmaf(R1 * cf[c + u], v[c + u], b2);
+          w[u] = fmaxf(x2, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(x2)));
+        }
+        val = make_float2(w[0], w[1]);
       } else {
-        val = ex2_approx(fmaf(tt, v[g * 32 + j], -L));
+        // two cells per packed instruction: 2^(R1 sigma_j dot - L)
+        const float2 x = fma2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[c], v[c + 1]), nl);
+        val = make_float2(ex2_approx(x.x), ex2_approx(x.y));
       }
       if constexpr (CHECK) {
-        const int col = col_base + g * 32 + j;
-        val = (row_ok && col < ncols && col != dcol) ? val : 0.f;
+        const int col = col_base + c;
+        if (!(row_ok && col < ncols && col != dcol)) val.x = 0.f;
+        if (!(row_ok && col + 1 < ncols && col + 1 != dcol)) val.y = 0.f;
       }
-      e[j] = val;
-      rs += val;
+      e[j] = val.x;
+      e[j + 1] = val.y;
+      rs = add2(rs, val);
     }
     if constexpr (COLS) cp[g * 32 + lane] = reduce_scatter32(e, lane);  // column col_base + g*32 + lane
   }
-  return rs;
+  return rs.x + rs.y;
 }
 
 // The order in which tiles and bands are fed to the MMA: tiles in pairs (t even in
