@@ -75,7 +75,7 @@ __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u 
 template <bool AMN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_yt,
-                const GemmParams p) {
+                const __grid_constant__ CUtensorMap tm_yt128, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem + off_a;
@@ -164,9 +164,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(sa + st * kABytes, &tm_w, bar, c * kChunk, static_cast<int>(wrow + m0));
           }
         } else {
-          for (int r0 = 0; r0 < half; r0 += kBox)
-            tma_load_2d_pair(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, bar,
-                             static_cast<int>(p.b_col0 + c * kChunk), d0 + static_cast<int>(rank) * half + r0);
+          // one 128-row box when the half is full (one TMA instruction: the producer's issue
+          // rate limits this loop), else 32-row boxes
+          if (half == kN / 2)
+            tma_load_2d_pair(sb + st * kBBytes, &tm_yt128, bar, static_cast<int>(p.b_col0 + c * kChunk),
+                             d0 + static_cast<int>(rank) * half);
+          else
+            for (int r0 = 0; r0 < half; r0 += kBox)
+              tma_load_2d_pair(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, bar,
+                               static_cast<int>(p.b_col0 + c * kChunk), d0 + static_cast<int>(rank) * half + r0);
         }
       }
     }
@@ -310,8 +316,8 @@ cudaError_t gemm_kernel_setup() {
   return gemm::setup_one<true>();
 }
 
-cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool weights_mn,
-                        cudaStream_t stream) {
+cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const CUtensorMap& tm_yt128,
+                        const GemmParams& p, bool weights_mn, cudaStream_t stream) {
   const int pn = p.prefix_end[p.n_prefix - 1];
   const int64_t blocks = (p.m_rows + kTileRows - 1) / kTileRows;
   cudaLaunchConfig_t cfg = {};
@@ -327,8 +333,8 @@ cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (weights_mn) return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<true>, tm_w, tm_yt, p);
-  return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<false>, tm_w, tm_yt, p);
+  if (weights_mn) return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<true>, tm_w, tm_yt, tm_yt128, p);
+  return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<false>, tm_w, tm_yt, tm_yt128, p);
 }
 
 }  // namespace ufc

@@ -66,7 +66,8 @@ cudaError_t launch_wgt(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
 // with c over [0, kdim), and the projection scalars crow[slice][k][g] = X[g, slice] . G^k[g, slice]
 // (partial over each 256-dimension slice).  accumulate: add into G and crow instead of
 // writing them.  tm_w: the weight array [n * w_rows_per_prefix rows][columns], boxes of
-// [128 x 64] (K-major) or [64 x 64] (MN-major); tm_yt: [32 x 64] boxes of Y^T ([d rows][rows of Y]).
+// [128 x 64] (K-major) or [64 x 64] (MN-major); tm_yt / tm_yt128: [32 x 64] / [128 x 64] boxes
+// of Y^T ([d rows][rows of Y]).
 struct GemmParams {
   int64_t m_rows;                 // rows of G computed by this launch
   int64_t row0;                   // their first row in G, X and crow
@@ -85,8 +86,8 @@ struct GemmParams {
 };
 constexpr int kGemmBBox = 32;   // rows per TMA box of the GEMMs' B operand (Y^T)
 cudaError_t gemm_kernel_setup();
-cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const GemmParams& p, bool weights_mn,
-                        cudaStream_t stream);
+cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const CUtensorMap& tm_yt128,
+                        const GemmParams& p, bool weights_mn, cudaStream_t stream);
 
 // Per-row inverse norms of every prefix for A and B, plus the positives' cosines
 // cos_ii for i < min(Na, Nb).  Layouts [n][rows].

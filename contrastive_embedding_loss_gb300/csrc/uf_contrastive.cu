@@ -427,7 +427,9 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     uint16_t* W = reinterpret_cast<uint16_t*>(ws + P.o_w);
     const int64_t wrows = static_cast<int64_t>(n) * P.chunk;
     // the weight array as [n * chunk rows][Nb columns]: store, K-major and MN-major load boxes
-    CUtensorMap tmWs, tmWk, tmWm;
+    CUtensorMap tmWs, tmWk, tmWm, tmAt128, tmBt128;
+    if (!encode_map(&tmAt128, At, D, Na, P.lda, 128) || !encode_map(&tmBt128, Bt, D, Nb, P.ldb, 128))
+      return UF_CUDA_ERROR;
     if (!encode_map(&tmWs, W, wrows, Nb, P.ldw, kWgtStoreRows) || !encode_map(&tmWk, W, wrows, Nb, P.ldw, kTileRows) ||
         !encode_map(&tmWm, W, wrows, Nb, P.ldw, 64))
       return UF_CUDA_ERROR;
@@ -479,11 +481,11 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
       ProfScope ps(UF_KERNEL_GEMM, 2, stream);
       ga.m_rows = rows;
       ga.row0 = r0;
-      UF_CHECK(launch_gemm(tmWk, tmBt, ga, false, stream));
+      UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
       gb.kdim = rows;
       gb.b_col0 = r0;
       gb.accumulate = r0 > 0;
-      UF_CHECK(launch_gemm(tmWm, tmAt, gb, true, stream));
+      UF_CHECK(launch_gemm(tmWm, tmAt, tmAt128, gb, true, stream));
     }
     if (siglip) {
       sp.rowacc_a = F(P.o_acc_a);
