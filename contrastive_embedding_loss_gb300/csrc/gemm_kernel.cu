@@ -91,16 +91,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
-  // row blocks are the fast grid dimension: the heavy first slice (every prefix reaches it)
-  // is scheduled before the light ones, which keeps the tail of the launch short
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kTileRows;  // first row of G in this launch
-  const int slice = blockIdx.y;
+  // Grid: [slice pair][row-block pair][slice in the pair][rank].  Slices 2s and 2s + 1 of a
+  // row block run side by side and start on the same weights (the widest prefixes reach
+  // both), which they share through L2; the heavy first pair (every prefix reaches slice 0)
+  // runs first, which keeps the tail of the launch short.
+  int n_slices = 0;
+#pragma unroll
+  for (int kk = 0; kk < kMaxPrefix; ++kk)
+    if (kk < p.n_prefix) n_slices = (p.prefix_end[kk] + kN - 1) / kN;
+  const int64_t pairs = (p.m_rows + 2 * kTileRows - 1) / (2 * kTileRows);
+  const int64_t cta = blockIdx.x >> 1;                 // [group][pair][slice in group]
+  const int64_t per_group = pairs * 2;
+  const int grp = static_cast<int>(cta / per_group);
+  const int64_t rem = cta % per_group;
+  const int64_t pair_i = rem / 2;
+  const int slice = grp * 2 + static_cast<int>(rem % 2);
+  const int64_t m0 = (pair_i * 2 + rank) * kTileRows;  // first row of G in this launch
   const int d0 = slice * kN;
   const int n = p.n_prefix;
-  int k_first = 0;  // prefixes k_first .. n-1 reach this slice
+  const bool idle = slice >= n_slices;  // an odd slice count leaves the last group half empty
+  int k_first = idle ? n : 0;  // prefixes k_first .. n-1 reach this slice
 #pragma unroll
   for (int k = 0; k < kMaxPrefix; ++k)
-    if (k < n && p.prefix_end[k] <= d0) k_first = k + 1;
+    if (!idle && k < n && p.prefix_end[k] <= d0) k_first = k + 1;
   const int nkc = static_cast<int>((p.kdim + kChunk - 1) / kChunk);  // K chunks per prefix
 
   if (threadIdx.x == 0) {
@@ -239,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* grow = p.G + g * p.d + d0;
     const uint16_t* xrow = p.X + g * p.d + d0;
     // prefixes that do not reach this slice contribute nothing to its slot
-    if (row_ok && !p.accumulate)
+    if (row_ok && !p.accumulate && !idle)
       for (int k = 0; k < k_first; ++k) p.crow[(static_cast<int64_t>(slice) * n + k) * p.crow_rows + g] = 0.f;
     uint32_t pi = 0;
     bool ok = true;
@@ -321,8 +334,9 @@ cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const
   const int pn = p.prefix_end[p.n_prefix - 1];
   const int64_t blocks = (p.m_rows + kTileRows - 1) / kTileRows;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((blocks + 1) / 2 * 2),  // whole pairs: a padding CTA stores nothing
-                     static_cast<unsigned>((pn + gemm::kN - 1) / gemm::kN));
+  const int64_t n_slices = (pn + gemm::kN - 1) / gemm::kN;
+  const int64_t groups = (n_slices + 1) / 2;
+  cfg.gridDim = dim3(static_cast<unsigned>(groups * ((blocks + 1) / 2) * 2 * 2));
   cfg.blockDim = dim3(gemm::kThreads);
   cfg.dynamicSmemBytes = gemm::smem_bytes;
   cfg.stream = stream;

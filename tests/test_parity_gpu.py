@@ -76,6 +76,7 @@ SMALL = [
     ("siglip", 200, 200, 640, (128, 320, 512), 4.0, -2.0, 0.7, 18),  # last prefix < D: zero tail columns
     ("rows", 1, 300, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 19),       # one query
     ("clip", 192, 192, 1024, LADDER, 40.0, 0.0, 3.0, 21),         # the largest supported tau
+    ("clip", 260, 260, 640, (64, 320, 640), 5.0, 0.0, 1.0, 22),   # an odd number of 256-dimension slices
 ]
 
 
