@@ -15,4 +15,5 @@ from .ref import (  # noqa: F401
     row_stats,
     row_terms_sampled,
     grad_rows,
+    scale_grads,
 )

@@ -252,6 +252,105 @@ int orc_fwd_bwd(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, 
 }
 
 /*
+ * Derivatives of the weighted total sum_k weights[k] * L_k with respect to the logit scale
+ * and (SIGLIP) the bias, taken directly from the loss definitions on float64 inputs:
+ *   CLIP   dL_k/dtau = 1/2 [ (1/N) sum_i (sum_j Prow_ij cos_ij - cos_ii)
+ *                          + (1/N) sum_j (sum_i Pcol_ij cos_ij - cos_jj) ],
+ *          Prow / Pcol the softmax of tau * cos over the row / the column;
+ *   ROWS   dL_k/dtau = (1/Nq) sum_i (sum_j Prow_ij cos_ij - cos_ii);
+ *   SIGLIP with x = t cos + b and d/dx softplus(-z x) = sigmoid(x) - [z = +1]:
+ *          dL_k/dt = (1/N) sum_ij (sigmoid(x_ij) - [i = j]) cos_ij,
+ *          dL_k/db = (1/N) sum_ij (sigmoid(x_ij) - [i = j]);  dbias = 0 for CLIP / ROWS.
+ * Returns 0, or -1 on bad arguments, -2 when out of memory.
+ */
+int orc_scale_grads_f64(int kind, const double* A, const double* B, int64_t Na, int64_t Nb, int D,
+                        const int* prefixes, int n, double scale, double bias, const double* weights,
+                        double* dscale, double* dbias) {
+  if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
+  double* C = (double*)malloc((size_t)Na * Nb * sizeof(double));
+  double* ra = (double*)malloc((size_t)Na * sizeof(double));
+  double* rb = (double*)malloc((size_t)Nb * sizeof(double));
+  if (!C || !ra || !rb) {
+    free(C); free(ra); free(rb);
+    return -2;
+  }
+  double ds = 0, db = 0;
+  for (int k = 0; k < n; ++k) {
+    const int p = prefixes[k];
+    const double w = weights ? weights[k] : 1.0;
+    for (int64_t i = 0; i < Na; ++i) ra[i] = inv_norm(A + i * D, p);
+    for (int64_t j = 0; j < Nb; ++j) rb[j] = inv_norm(B + j * D, p);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t i = 0; i < Na; ++i)
+      for (int64_t j = 0; j < Nb; ++j) {
+        double dot = 0;
+        for (int d = 0; d < p; ++d) dot += B[j * D + d] * A[i * D + d];
+        C[i * Nb + j] = dot * ra[i] * rb[j];
+      }
+    double gk = 0, bk = 0;
+    if (kind == ORC_CLIP || kind == ORC_ROWS) {
+      const double tau = scale;
+      double rows = 0;  /* sum_i (E_row[cos] - cos_ii) */
+      for (int64_t i = 0; i < Na; ++i) {
+        double m = -INFINITY, z = 0, zc = 0;
+        for (int64_t j = 0; j < Nb; ++j) m = fmax(m, tau * C[i * Nb + j]);
+        for (int64_t j = 0; j < Nb; ++j) {
+          const double e = exp(tau * C[i * Nb + j] - m);
+          z += e;
+          zc += e * C[i * Nb + j];
+        }
+        rows += zc / z - C[i * Nb + i];
+      }
+      if (kind == ORC_CLIP) {
+        double cols = 0;
+        for (int64_t j = 0; j < Nb; ++j) {
+          double m = -INFINITY, z = 0, zc = 0;
+          for (int64_t i = 0; i < Na; ++i) m = fmax(m, tau * C[i * Nb + j]);
+          for (int64_t i = 0; i < Na; ++i) {
+            const double e = exp(tau * C[i * Nb + j] - m);
+            z += e;
+            zc += e * C[i * Nb + j];
+          }
+          cols += zc / z - C[j * Nb + j];
+        }
+        gk = 0.5 * (rows / (double)Na + cols / (double)Nb);
+      } else {
+        gk = rows / (double)Na;
+      }
+    } else {
+      const double t = scale, N = (double)Na;
+      for (int64_t i = 0; i < Na; ++i)
+        for (int64_t j = 0; j < Nb; ++j) {
+          const double g = sigmoid(t * C[i * Nb + j] + bias) - (i == j ? 1.0 : 0.0);
+          gk += g * C[i * Nb + j];
+          bk += g;
+        }
+      gk /= N;
+      bk /= N;
+    }
+    ds += w * gk;
+    db += w * bk;
+  }
+  *dscale = ds;
+  *dbias = db;
+  free(C); free(ra); free(rb);
+  return 0;
+}
+
+int orc_scale_grads(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
+                    const int* prefixes, int n, double scale, double bias, const double* weights,
+                    double* dscale, double* dbias) {
+  if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
+  double* A = widen_matrix(A16, Na, D);
+  double* B = widen_matrix(B16, Nb, D);
+  int rc = (A && B) ? orc_scale_grads_f64(kind, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, dscale, dbias)
+                    : -2;
+  free(A);
+  free(B);
+  return rc;
+}
+
+/*
  * Row statistics for selected rows of X against every row of Y, one row at a time
  * (for batches too large for the full grid).  The positive of row i of X is row i
  * of Y.  For each selected row and prefix k:

@@ -46,7 +46,11 @@ def _bind(path):
     lib.orc_grad_rows.argtypes = [ctypes.c_int, ctypes.c_int, P, P, i64, i64, ctypes.c_int, P,
                                   ctypes.c_int, ctypes.c_double, ctypes.c_double, P, P, P, P,
                                   i64, P]
-    for f in (lib.orc_fwd_bwd, lib.orc_fwd_bwd_f64, lib.orc_row_stats, lib.orc_grad_rows):
+    lib.orc_scale_grads.argtypes = [ctypes.c_int, P, P, i64, i64, ctypes.c_int, P, ctypes.c_int,
+                                    ctypes.c_double, ctypes.c_double, P, P, P]
+    lib.orc_scale_grads_f64.argtypes = lib.orc_scale_grads.argtypes
+    for f in (lib.orc_fwd_bwd, lib.orc_fwd_bwd_f64, lib.orc_row_stats, lib.orc_grad_rows, lib.orc_scale_grads,
+              lib.orc_scale_grads_f64):
         f.restype = ctypes.c_int
     return lib
 
@@ -151,3 +155,24 @@ def grad_rows(kind, x_is_a, X, Y, prefixes, scale, bias, rows, lse_x=None, lse_y
     if rc:
         raise ValueError(f"oracle grad_rows failed ({rc})")
     return out
+
+
+def scale_grads(kind, A, B, prefixes, scale, bias=0.0, weights=None):
+    """(dL/dscale, dL/dbias) of sum_k w_k L_k, from the loss definitions; see oracle.c.
+
+    A and B are bf16 bit patterns (uint16) or float64 arrays."""
+    A, B = np.ascontiguousarray(A), np.ascontiguousarray(B)
+    if A.dtype == np.float64 and B.dtype == np.float64:
+        fn = _load().orc_scale_grads_f64
+    else:
+        A, B = _bits(A), _bits(B)
+        fn = _load().orc_scale_grads
+    pre = _prefix_array(prefixes)
+    w = None if weights is None else np.ascontiguousarray(np.asarray(weights, np.float64))
+    ds = np.zeros(1)
+    db = np.zeros(1)
+    rc = fn(KINDS[kind], _ptr(A), _ptr(B), A.shape[0], B.shape[0], A.shape[1], _ptr(pre), pre.size, float(scale),
+            float(bias), _ptr(w), _ptr(ds), _ptr(db))
+    if rc:
+        raise ValueError(f"oracle scale_grads failed ({rc})")
+    return float(ds[0]), float(db[0])

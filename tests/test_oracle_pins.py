@@ -82,6 +82,90 @@ def test_matches_torch_library_and_autograd(kind, Na, Nb, D, prefixes, scale, bi
                                got["loss"], rtol=1e-13)
 
 
+def torch_scale_grads(kind, A, B, prefixes, scale, bias, weights):
+    """d(sum_k w_k L_k)/d(scale) and /d(bias) by torch autograd (float64), the scale and bias
+    as leaves of the graph built from torch's cross_entropy / logsigmoid."""
+    s = torch.tensor(float(scale), dtype=torch.float64, requires_grad=True)
+    b_ = torch.tensor(float(bias), dtype=torch.float64, requires_grad=True)
+    At = torch.tensor(A, dtype=torch.float64)
+    Bt = torch.tensor(B, dtype=torch.float64)
+    Na, Nb = At.shape[0], Bt.shape[0]
+    total = 0.0
+    for p, w in zip(prefixes, weights):
+        cos = F.normalize(At[:, :p], dim=1, eps=1e-30) @ F.normalize(Bt[:, :p], dim=1, eps=1e-30).T
+        if kind == "clip":
+            t = torch.arange(Na)
+            L = 0.5 * (F.cross_entropy(s * cos, t) + F.cross_entropy((s * cos).T, t))
+        elif kind == "rows":
+            L = F.cross_entropy(s * cos, torch.arange(Na))
+        else:
+            z = 2.0 * torch.eye(Na, Nb, dtype=torch.float64) - 1.0
+            L = -F.logsigmoid(z * (s * cos + b_)).sum() / Na
+        total = total + w * L
+    total.backward()
+    return s.grad.item(), (b_.grad.item() if b_.grad is not None else 0.0)
+
+
+@pytest.mark.parametrize("kind,Na,Nb,D,prefixes,scale,bias", CASES)
+def test_scale_grads_match_autograd(kind, Na, Nb, D, prefixes, scale, bias):
+    rng = np.random.default_rng(17)
+    a = rng.standard_normal((Na, D))
+    b = np.concatenate([a, rng.standard_normal((Nb - Na, D))])[:Nb] + 0.8 * rng.standard_normal((Nb, D))
+    A, B = _bits(a), _bits(b)
+    weights = rng.uniform(0.5, 2.0, len(prefixes))
+    ds, db = oracle.scale_grads(kind, A, B, prefixes, scale, bias, weights)
+    ts, tb = torch_scale_grads(kind, _wide(A), _wide(B), prefixes, scale, bias, weights)
+    np.testing.assert_allclose(ds, ts, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(db, tb, rtol=1e-10, atol=1e-13)
+    if kind != "siglip":
+        assert db == 0.0
+
+
+@pytest.mark.parametrize("kind", ["clip", "siglip", "rows"])
+def test_scale_grads_finite_differences(kind):
+    """Central differences of the oracle's own weighted loss in the scale and the bias."""
+    rng = np.random.default_rng(19)
+    Na, Nb, D = 5, (7 if kind == "rows" else 5), 16
+    prefixes = (8, 16)
+    A = rng.standard_normal((Na, D))
+    B = rng.standard_normal((Nb, D))
+    B[:Na] += A
+    scale, bias = (2.5, -1.5) if kind == "siglip" else (3.0, 0.0)
+    w = np.array([0.7, 1.3])
+    ds, db = oracle.scale_grads(kind, A, B, prefixes, scale, bias, w)
+
+    def f(s_, b_):
+        return float(np.dot(w, oracle.fwd_bwd(kind, A, B, prefixes, s_, b_, w, grads=False)["loss"]))
+
+    h = 1e-6
+    np.testing.assert_allclose(ds, (f(scale + h, bias) - f(scale - h, bias)) / (2 * h), rtol=1e-6, atol=1e-9)
+    if kind == "siglip":
+        np.testing.assert_allclose(db, (f(scale, bias + h) - f(scale, bias - h)) / (2 * h), rtol=1e-6, atol=1e-9)
+
+
+def test_scale_grads_closed_forms():
+    N, D = 6, 64
+    pre = (32, 64)
+    # identical rows: every cosine is 1; InfoNCE's expected cosine equals the positive's (0),
+    # SigLIP at t = 10, b = -10 has x = 0 and sigmoid = 1/2 everywhere: 0.5 N - 1 per prefix
+    v = np.random.default_rng(3).standard_normal(D)
+    X = _bits(np.tile(v, (N, 1)))
+    ds, db = oracle.scale_grads("clip", X, X, pre, 5.0, 0.0)
+    assert abs(ds) < 1e-12 and db == 0.0
+    ds, db = oracle.scale_grads("siglip", X, X, pre, 10.0, -10.0)
+    np.testing.assert_allclose([ds, db], [len(pre) * (0.5 * N - 1)] * 2, rtol=1e-12)
+    # one-hot orthogonal rows: cos = [i == j]
+    E = _bits(np.eye(N, D))
+    tau = 4.0
+    ds, _ = oracle.scale_grads("clip", E, E, pre, tau, 0.0)
+    np.testing.assert_allclose(ds, len(pre) * -(N - 1) / (math.exp(tau) + N - 1), rtol=1e-12)
+    t, b = 3.0, -2.0
+    sig = lambda x: 1.0 / (1.0 + math.exp(-x))  # noqa: E731
+    ds, db = oracle.scale_grads("siglip", E, E, pre, t, b)
+    np.testing.assert_allclose(ds, len(pre) * (sig(t + b) - 1.0), rtol=1e-12)
+    np.testing.assert_allclose(db, len(pre) * (sig(t + b) - 1.0 + (N - 1) * sig(b)), rtol=1e-12)
+
+
 @pytest.mark.parametrize("kind", ["clip", "siglip", "rows"])
 def test_finite_differences(kind):
     rng = np.random.default_rng(11)
@@ -305,6 +389,10 @@ MUTATIONS = {
     "clip_normaliser": ("L = 0.5 * (Lr / N + Lc / N);", "L = (Lr / N + Lc / N);"),
     "dB_wrong_norm": ("out[d] += g * (A[i * D + d] * ra[i] - c * B[j * D + d] * rb[j]) * rb[j];",
                       "out[d] += g * (A[i * D + d] * ra[i] - c * B[j * D + d] * rb[j]) * ra[i];"),
+    "dscale_column_half_dropped": ("gk = 0.5 * (rows / (double)Na + cols / (double)Nb);",
+                                   "gk = 0.5 * (rows / (double)Na);"),
+    "dscale_positive_sign": ("const double g = sigmoid(t * C[i * Nb + j] + bias) - (i == j ? 1.0 : 0.0);",
+                             "const double g = sigmoid(t * C[i * Nb + j] + bias) + (i == j ? 1.0 : 0.0);"),
 }
 
 
@@ -315,6 +403,8 @@ def _pins_pass():
         lambda: test_matches_torch_library_and_autograd(*CASES[1]),
         test_identical_embeddings_closed_forms,
         test_one_hot_orthogonal_closed_forms,
+        lambda: test_scale_grads_match_autograd(*CASES[0]),
+        lambda: test_scale_grads_match_autograd(*CASES[1]),
     ]
     for c in checks:
         try:
