@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
   const int pn = p.prefix_end[n - 1];
   for (int64_t i = warp_id; i < p.nx; i += n_warps) {
     const bool diag = i < p.nmin;
-    float rk = 0.f, qk = 0.f;
+    float rk = 0.f, qk = 0.f, Ck = 0.f;
     if (lane < n) {
       const int k = lane;
       const float rho = p.rinv_x[k * p.nx + i];
@@ -281,6 +281,13 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
         qk = rho * sig * Wd;
       }
       rk = rho * rho * C;
+      Ck = C;
+    }
+    if (p.csum) {  // sum_k C_k: this row's share of sum_ij W_ij cos_ij (logit-scale gradient)
+      float cs = Ck;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
+      if (lane == 0) p.csum[i] = cs;
     }
     // suffix sums over prefixes: band c uses every prefix k >= c
     float rc[kMaxPrefix], qc[kMaxPrefix];
@@ -338,6 +345,58 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
   }
 }
 
+__global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams p) {
+  __shared__ double red[2][32];
+  const int n = p.n_prefix;
+  double s = 0.0, sb = 0.0;
+  if (p.csum)
+    for (int64_t i = threadIdx.x; i < p.na; i += blockDim.x) s += p.csum[i];
+  if (p.kind == KIND_SIGLIP && p.rowsig) {  // the sigmoid sums exist only when the bias gradient is asked for
+    const double N = static_cast<double>(p.na);
+    for (int k = 0; k < n; ++k) {
+      const double wk = p.weight[k] / N;
+      for (int64_t i = threadIdx.x; i < p.na; i += blockDim.x) {
+        double neg = 0.0;  // sum over the negatives of row i of sigmoid(x_ij), fixed slot order
+        for (int sl = 0; sl < p.sig_slots; ++sl) neg += p.rowsig[(static_cast<int64_t>(sl) * n + k) * p.na + i];
+        double pos = 0.0;  // the positive's share: sigmoid(x_ii) - 1 = -sigmoid(-x_ii)
+        if (i < p.nmin) {
+          const double x = static_cast<double>(p.scale) * p.pos_cos[k * p.nmin + i] + p.bias;
+          pos = -1.0 / (1.0 + exp(x));
+        }
+        sb += wk * (neg + pos);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    sb += __shfl_xor_sync(0xffffffffu, sb, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = s;
+    red[1][threadIdx.x >> 5] = sb;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    double v = (threadIdx.x < (blockDim.x >> 5)) ? red[0][threadIdx.x] : 0.0;
+    double vb = (threadIdx.x < (blockDim.x >> 5)) ? red[1][threadIdx.x] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      v += __shfl_xor_sync(0xffffffffu, v, o);
+      vb += __shfl_xor_sync(0xffffffffu, vb, o);
+    }
+    if (threadIdx.x == 0) {
+      if (p.d_scale) *p.d_scale = static_cast<float>(v / static_cast<double>(p.scale));
+      if (p.d_bias) *p.d_bias = static_cast<float>(p.kind == KIND_SIGLIP ? vb : 0.0);
+    }
+  }
+}
+
+cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream) {
+  scale_grad_kernel<<<1, 1024, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_norm_bwd(const NormBwdParams& p, cudaStream_t stream) {
   int64_t blocks = (p.nx * 32 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
@@ -353,6 +412,7 @@ cudaError_t aux_kernels_setup() {
   if ((e = cudaFuncGetAttributes(&fa, transpose_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, stats_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, finalize_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, scale_grad_kernel)) != cudaSuccess) return e;
   return cudaFuncGetAttributes(&fa, norm_bwd_kernel);
 }
 

@@ -52,6 +52,8 @@ struct WgtParams {
   float m_scale[kMaxPrefix];      // SigLIP: w_k t / N
   int64_t w_rows_per_prefix;      // rows between prefixes in the weight array (multiple of 128)
   float* rowacc;                  // SigLIP: [split * 4 + quarter][n][nx] loss sums (log2 units), or NULL
+  float* rowsig;                  // SigLIP, with rowacc: the same slots, sums of sigmoid(x_ij) over the
+                                  // negatives (the bias gradient), or NULL
   int* status;
 };
 constexpr int kWgtCols = 256;
@@ -152,7 +154,27 @@ struct NormBwdParams {
   const float* G;          // [splits][nx][d]
   int g_splits;
   float* dX;               // [nx][d]
+  float* csum;             // NULL or [nx]: sum over prefixes of the full row scalar C_k (logit-scale gradient)
 };
 cudaError_t launch_norm_bwd(const NormBwdParams& p, cudaStream_t stream);
+
+// Gradients of the weighted loss in the logit scale and (SigLIP) the bias, from the row
+// scalars: d_scale = (1 / scale) sum_i csum[i]  (sum_ij W_ij cos_ij = scale dL/dscale), and
+// d_bias = sum_k (w_k / N) (sum_i sum_slots rowsig[.][k][i] - sum_i sigmoid(-x_ii)).
+// One block, float64, fixed order.
+struct ScaleGradParams {
+  int kind;
+  int64_t na, nmin;
+  int n_prefix;
+  float scale, bias;
+  float weight[kMaxPrefix];
+  const float* csum;       // [na]
+  const float* rowsig;     // SigLIP: [slots][n][na]
+  int sig_slots;
+  const float* pos_cos;    // [n][nmin]
+  float* d_scale;          // device scalar or NULL
+  float* d_bias;           // device scalar or NULL
+};
+cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream);
 
 }  // namespace ufc

@@ -56,7 +56,7 @@ struct Plan {
   size_t fixed = 0;                  // bytes of everything but the weight array
   // offsets
   size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
-      o_terms_b, o_loss, o_at, o_bt, o_w, total;
+      o_terms_b, o_loss, o_at, o_bt, o_csum, o_sig, o_w, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -116,6 +116,8 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.o_loss = take(f * kMaxPrefix);
   P.o_at = take(grads ? sizeof(uint16_t) * D * P.lda : 0);
   P.o_bt = take(grads ? sizeof(uint16_t) * D * P.ldb : 0);
+  P.o_csum = take(grads ? f * Na : 0);  // per-row sums of the row scalars (logit-scale gradient)
+  P.o_sig = take(grads && kind == KIND_SIGLIP ? f * n * Na * 4 * P.wgt.splits : 0);  // sigmoid sums (bias)
   P.fixed = o;
   P.o_w = o;
   P.chunk = 0;
@@ -271,10 +273,23 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
                                    const float* prefix_weights, float* loss_per_prefix, float* row_terms,
                                    float* col_terms, float* dA, float* dB, void* workspace, size_t workspace_bytes,
                                    int* device_status, void* stream_handle) {
+  return uf_contrastive_fwd_bwd_ex(A, B, Na, Nb, D, prefixes, n_prefix, kind, logit_scale, bias, prefix_weights,
+                                   loss_per_prefix, row_terms, col_terms, dA, dB, nullptr, nullptr, workspace,
+                                   workspace_bytes, device_status, stream_handle);
+}
+
+uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
+                                      const int* prefixes, int n_prefix, int kind, float logit_scale, float bias,
+                                      const float* prefix_weights, float* loss_per_prefix, float* row_terms,
+                                      float* col_terms, float* dA, float* dB, float* d_logit_scale, float* d_bias,
+                                      void* workspace, size_t workspace_bytes, int* device_status,
+                                      void* stream_handle) {
   // ---- argument checks (nothing is enqueued on failure)
   if (!A || !B || !loss_per_prefix || !workspace) return UF_INVALID_ARGUMENT;
   if ((dA == nullptr) != (dB == nullptr)) return UF_INVALID_ARGUMENT;
   const bool grads = dA != nullptr;
+  if ((d_logit_scale || d_bias) && !grads) return UF_INVALID_ARGUMENT;  // they come out of the backward
+  if ((d_logit_scale && !aligned(d_logit_scale, 4)) || (d_bias && !aligned(d_bias, 4))) return UF_INVALID_ARGUMENT;
   Plan P;
   if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, grads, workspace_bytes, P)) return UF_INVALID_ARGUMENT;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(workspace, 256) || !aligned(loss_per_prefix, 4))
@@ -290,6 +305,7 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
   }
   if (kind == KIND_SIGLIP) {
     if (std::fabs(logit_scale) + std::fabs(bias) > 80.f) return UF_UNSUPPORTED;
+    if (d_logit_scale && logit_scale == 0.f) return UF_UNSUPPORTED;  // taken as (sum W cos) / t
   } else {
     if (!(logit_scale > 0.f)) return UF_INVALID_ARGUMENT;
     if (logit_scale > 40.f) return UF_UNSUPPORTED;
@@ -449,6 +465,7 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     for (int k = 0; k < n; ++k) wp.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
     wp.w_rows_per_prefix = P.chunk;
     wp.rowacc = siglip ? F(P.o_acc_a) : nullptr;  // the SigLIP loss sums
+    wp.rowsig = (siglip && d_bias) ? F(P.o_sig) : nullptr;  // and, for the bias gradient, the sigmoid sums
     wp.status = device_status;
     GemmParams ga{}, gb{};
     for (GemmParams* g : {&ga, &gb}) {
@@ -526,11 +543,31 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
     }
     q.crow = F(xa ? P.o_crow_a : P.o_crow_b);
     q.crow_slots = P.slices;
+    q.csum = (xa && d_logit_scale) ? F(P.o_csum) : nullptr;
     q.G = xa ? dA : dB;
     q.g_splits = 1;
     q.dX = xa ? dA : dB;
     ProfScope ps(UF_KERNEL_NORM_BWD, 1, stream);
     UF_CHECK(launch_norm_bwd(q, stream));
+  }
+  // ---- 5. gradients in the logit scale and the bias
+  if (d_logit_scale || d_bias) {
+    ScaleGradParams g{};
+    g.kind = kind;
+    g.na = Na;
+    g.nmin = P.nmin;
+    g.n_prefix = n;
+    g.scale = logit_scale;
+    g.bias = bias;
+    for (int k = 0; k < n; ++k) g.weight[k] = w[k];
+    g.csum = d_logit_scale ? F(P.o_csum) : nullptr;
+    g.rowsig = (siglip && d_bias) ? F(P.o_sig) : nullptr;
+    g.sig_slots = 4 * P.wgt.splits;
+    g.pos_cos = F(P.o_pos);
+    g.d_scale = d_logit_scale;
+    g.d_bias = d_bias;
+    ProfScope ps(UF_KERNEL_NORM_BWD, 1, stream);
+    UF_CHECK(launch_scale_grad(g, stream));
   }
   if (col_terms && kind != KIND_CLIP) UF_CHECK(cudaMemsetAsync(col_terms, 0, sizeof(float) * n * Nb, stream));
 #undef UF_CHECK

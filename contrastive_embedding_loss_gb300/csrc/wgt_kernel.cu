@@ -69,12 +69,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 8 cells: their weights as four packed bf16 pairs; (SigLIP, R3 != 0) adds to the loss
-// over the negatives.  c1, c2: shared addresses of the columns'
+// 8 cells: their weights as four packed bf16 pairs; (SigLIP, R3 != 0) adds the loss and
+// the sigmoid of the negatives to acc (.x, .y).  c1, c2: shared addresses of the columns'
 // factors.  CHECK evaluates the masks (padding rows and columns, the positive's cell).
 template <int KIND, bool CHECK>
 __device__ __forceinline__ uint4 cells8(const float* dot, uint32_t c1, uint32_t c2, float R1, float R2, float R3,
-                                        float L, float b2, int col0, int ncols, int dcol, bool row_ok, float& acc_l) {
+                                        float L, float b2, int col0, int ncols, int dcol, bool row_ok, float2& acc) {
   const float4 s1a = ld_shared_v4f(c1), s1b = ld_shared_v4f(c1 + 16);
   const float s1v[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
   float s2v[8];
@@ -105,7 +105,8 @@ __device__ __forceinline__ uint4 cells8(const float* dot, uint32_t c1, uint32_t 
         float m = sig * (R2 * s1);
         if (R3 != 0.f) {  // this launch also sums the SigLIP loss
           const float l = fmaxf(x2, 0.f) + lg2_approx(d);
-          acc_l += keep ? l : 0.f;
+          acc.x += keep ? l : 0.f;
+          acc.y += keep ? sig : 0.f;
         }
         if constexpr (CHECK) m = keep ? m : 0.f;
         mv[u] = m;
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the previous TMA store of this warp must have read its staging block
           if (lane == 0) bulk_wait_read0();
           __syncwarp();
-          float al = 0.f;
+          float2 al = make_float2(0.f, 0.f);
           if (check) {
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
@@ -390,8 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (KIND == KIND_SIGLIP && p.rowacc && row_ok) {
             float* pl = p.rowacc + slot_off + static_cast<int64_t>(k) * p.nx;
-            if (t == 0) *pl = al;
-            else atomicAdd(pl, al);
+            if (t == 0) *pl = al.x;
+            else atomicAdd(pl, al.x);
+            if (p.rowsig) {
+              float* ps = p.rowsig + slot_off + static_cast<int64_t>(k) * p.nx;
+              if (t == 0) *ps = al.y;
+              else atomicAdd(ps, al.y);
+            }
           }
         }
       }

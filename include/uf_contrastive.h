@@ -134,6 +134,28 @@ UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t 
                                    size_t workspace_bytes, int* device_status, void* stream);
 
 /*
+ * uf_contrastive_fwd_bwd that also differentiates the weighted loss sum_p w_p L_p with
+ * respect to its two scalar parameters, which training learns (blog post "Scaling-Up
+ * Contrastive Learning over NVLink Multicast", section "One Set or Two": SigLIP's learned
+ * temperature t and bias b; CLIP's logit scale likewise):
+ *   d_logit_scale   device fp32 scalar or NULL: dL/d(logit_scale) (tau for CLIP / ROWS,
+ *                   t for SigLIP), computed as (1 / logit_scale) sum_ij dL/dcos_ij cos_ij
+ *                   from the backward's row scalars; SigLIP with logit_scale == 0 returns
+ *                   UF_UNSUPPORTED when it is requested.
+ *   d_bias          device fp32 scalar or NULL: dL/db for SigLIP, from the per-row sums of
+ *                   sigmoid(x_ij) over the negatives and the positives' sigmoid(-x_ii);
+ *                   written 0 for CLIP and ROWS.
+ * Both need the backward (dA and dB non-NULL), else UF_INVALID_ARGUMENT.  Every other
+ * argument means what it means in uf_contrastive_fwd_bwd, which is this call with both NULL.
+ */
+UF_API uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
+                                      const int* prefixes, int n_prefix, int kind, float logit_scale,
+                                      float bias, const float* prefix_weights, float* loss_per_prefix,
+                                      float* row_terms, float* col_terms, float* dA, float* dB,
+                                      float* d_logit_scale, float* d_bias, void* workspace,
+                                      size_t workspace_bytes, int* device_status, void* stream);
+
+/*
  * uf_contrastive_fwd_bwd without a workspace argument, for callers that cannot allocate
  * device memory: hosts that reserve all of their memory at start-up and forbid
  * allocation afterwards, plugins whose host application owns every device buffer, or

@@ -129,3 +129,37 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(ImportError):
         binding.load(str(tmp_path / "nope.so"))
+
+
+def _call_ex(d_logit_scale=FAKE, d_bias=FAKE, **kw):
+    args = dict(A=FAKE, B=FAKE, Na=256, Nb=256, D=1024, prefixes=LADDER, kind=0, logit_scale=1 / 0.07, bias=0.0,
+                prefix_weights=None, loss_per_prefix=FAKE, row_terms=None, col_terms=None, dA=FAKE, dB=FAKE,
+                d_logit_scale=d_logit_scale, d_bias=d_bias, workspace=FAKE, workspace_bytes=1 << 40,
+                device_status=None, stream=None)
+    args.update(kw)
+    return binding.uf_contrastive_fwd_bwd_ex(**args)
+
+
+def test_scale_gradient_argument_errors_are_found_on_the_host(lib):
+    INV, UNS = 1, 2
+    assert _call_ex(dA=None, dB=None) == INV                    # they come out of the backward
+    assert _call_ex(d_bias=None, dA=None, dB=None) == INV
+    assert _call_ex(d_logit_scale=FAKE + 2) == INV              # fp32 scalars: 4-byte aligned
+    assert _call_ex(d_bias=FAKE + 1) == INV
+    assert _call_ex(kind=1, logit_scale=0.0, bias=0.0) == UNS   # SigLIP t = 0: dL/dt is not (sum W cos) / t
+    assert _call_ex(kind=1, logit_scale=0.0, bias=0.0, d_logit_scale=None) != UNS  # the bias alone is fine
+    # the same checks as the plain entry point still apply
+    assert _call_ex(Nb=255) == INV
+    assert _call_ex(logit_scale=100.0) == UNS
+    # the workspace needed is the same with or without the scalar gradients
+    need = binding.uf_contrastive_workspace_min(256, 256, 1024, LADDER, 1, 1)
+    assert _call_ex(kind=1, logit_scale=10.0, bias=-10.0, workspace_bytes=need - 256) == 3
+
+
+def test_valid_scale_gradient_call_without_gpu_reports_cuda_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call_ex() == 4
+    assert _call_ex(kind=1, logit_scale=10.0, bias=-10.0) == 4

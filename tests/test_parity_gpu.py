@@ -32,10 +32,10 @@ def dev(bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def run(binding, kind, A16, B16, pre, scale, bias, weights=None, grads=True, workspace=None):
+def run(binding, kind, A16, B16, pre, scale, bias, weights=None, grads=True, workspace=None, scale_grads=False):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = binding.contrastive_fwd_bwd(dev(A16), dev(B16), kind, pre, scale, bias, weights, grads=grads, terms=True,
-                                      workspace=workspace, device_status=status)
+                                      workspace=workspace, device_status=status, scale_grads=scale_grads)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "a kernel reported a timeout"
     return {k: v.double().cpu().numpy() for k, v in out.items()}
@@ -156,3 +156,70 @@ def test_deterministic(ctx):
     r2 = run(ctx, "clip", A16, B16, LADDER, 1 / 0.07, 0.0)
     for k in r1:
         assert np.array_equal(r1[k], r2[k]), k
+
+
+def logit_grad_l1(kind, A16, B16, pre, scale, bias, w):
+    """(sum_k w_k sum_ij |dL_k/dx_ij| |cos_ij|, sum_k w_k sum_ij |dL_k/dx_ij|), x the logits.
+
+    Only a tolerance: both gradients are sums over the score matrix of dL/dx_ij times cos_ij
+    (logit scale) or times 1 (bias), and the library rounds every dL/dcos_ij to bf16
+    (relative error <= 2^-9) before it sums them, so the error of each sum is at most
+    2^-9 times the matching sum of magnitudes."""
+    A, B = synth.bf16_bits_to_float(A16), synth.bf16_bits_to_float(B16)
+    Na = A.shape[0]
+    m_cos = m_one = 0.0
+    for k, p in enumerate(pre):
+        a = A[:, :p] / np.linalg.norm(A[:, :p], axis=1, keepdims=True)
+        b = B[:, :p] / np.linalg.norm(B[:, :p], axis=1, keepdims=True)
+        cos = a @ b.T
+        x = scale * cos + (bias if kind == "siglip" else 0.0)
+        eye = np.zeros_like(x)
+        eye[np.arange(min(x.shape)), np.arange(min(x.shape))] = 1.0
+        if kind == "siglip":
+            g = (1.0 / (1.0 + np.exp(-x)) - eye) / Na
+        else:
+            pr = np.exp(x - x.max(1, keepdims=True))
+            g = (pr / pr.sum(1, keepdims=True) - eye) / Na
+            if kind == "clip":
+                pc = np.exp(x - x.max(0, keepdims=True))
+                g = 0.5 * (g + (pc / pc.sum(0, keepdims=True) - eye) / Na)
+        m_cos += w[k] * np.sum(np.abs(g) * np.abs(cos))
+        m_one += w[k] * np.sum(np.abs(g))
+    return m_cos, m_one
+
+
+SCALE_GRADS = [
+    # kind, Na, Nb, D, prefixes, scale, bias, noise, seed, smallest workspace
+    ("clip", 300, 300, 1024, LADDER, 1 / 0.07, 0.0, 1.0, 71, False),
+    ("clip", 640, 640, 1024, LADDER, 1 / 0.07, 0.0, 1.0, 72, True),
+    ("clip", 257, 257, 384, (64, 192, 384), 40.0, 0.0, 3.0, 73, False),
+    ("siglip", 300, 300, 1024, LADDER, 10.0, -10.0, 0.7, 74, False),
+    ("siglip", 512, 512, 1024, LADDER, 4.0, -2.0, 0.7, 75, True),     # many negatives with sizeable sigmoid
+    ("siglip", 200, 200, 640, (128, 320, 512), 4.0, 1.0, 0.7, 76, False),
+    ("rows", 200, 700, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 77, False),
+    ("rows", 1, 300, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 78, False),
+]
+
+
+@pytest.mark.parametrize("kind,Na,Nb,D,pre,scale,bias,noise,seed,small_ws", SCALE_GRADS)
+def test_parity_scale_and_bias_gradients(ctx, kind, Na, Nb, D, pre, scale, bias, noise, seed, small_ws):
+    A16, B16 = make(kind, Na, Nb, D, seed, noise)
+    w = list(np.linspace(1.5, 0.5, len(pre)))
+    ws = None
+    if small_ws:
+        wmin = ctx.uf_contrastive_workspace_min(Na, Nb, D, pre, ctx.KINDS[kind], True)
+        ws = torch.empty(wmin, dtype=torch.uint8, device="cuda")
+    got = run(ctx, kind, A16, B16, pre, scale, bias, weights=w, workspace=ws, scale_grads=True)
+    ds, db = oracle.scale_grads(kind, A16, B16, pre, scale, bias, w)
+    m_cos, m_one = logit_grad_l1(kind, A16, B16, pre, scale, bias, w)
+    tol_s = 2.0 ** -8 * m_cos + 1e-5 * abs(ds)   # twice the bf16 rounding bound, plus fp32 sums
+    tol_b = 2.0 ** -8 * m_one + 1e-5 * abs(db)
+    assert abs(got["d_logit_scale"][0] - ds) <= tol_s, f"dL/dscale {got['d_logit_scale'][0]} vs oracle {ds}"
+    if kind == "siglip":
+        assert abs(got["d_bias"][0] - db) <= tol_b, f"dL/dbias {got['d_bias'][0]} vs oracle {db}"
+    else:
+        assert got["d_bias"][0] == 0.0
+    # asking for them changes nothing else
+    plain = run(ctx, kind, A16, B16, pre, scale, bias, weights=w, workspace=ws)
+    for key in ("loss", "dA", "dB", "row_terms"):
+        assert np.array_equal(got[key], plain[key]), key
