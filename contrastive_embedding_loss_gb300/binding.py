@@ -59,7 +59,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                            P, P]
     lib.uf_contrastive_fwd_bwd.restype = I32
     lib.uf_contrastive_fwd_bwd_ex.argtypes = [P, P, I64, I64, I32, P, I32, I32, F32, F32, P, P, P, P, P, P, P, P, P,
-                                              SZ, P, P]
+                                              P, P, SZ, P, P]
     lib.uf_contrastive_fwd_bwd_ex.restype = I32
     lib.uf_contrastive_profile.argtypes = [I32]
     lib.uf_contrastive_profile.restype = I32
@@ -115,16 +115,17 @@ def uf_contrastive_fwd_bwd(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, p
                                              stream))
 
 
-def uf_contrastive_fwd_bwd_ex(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, prefix_weights, loss_per_prefix,
-                              row_terms, col_terms, dA, dB, d_logit_scale, d_bias, workspace, workspace_bytes,
-                              device_status, stream) -> int:
-    """Raw call that also writes dL/d(logit_scale) and dL/d(bias) (device fp32 scalars or None)."""
+def uf_contrastive_fwd_bwd_ex(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, logit_scale_dev, bias_dev,
+                              prefix_weights, loss_per_prefix, row_terms, col_terms, dA, dB, d_logit_scale, d_bias,
+                              workspace, workspace_bytes, device_status, stream) -> int:
+    """Raw call with the scalars optionally on the device (``*_dev``) and their gradients
+    (``d_logit_scale``, ``d_bias``): device fp32 scalar addresses or None."""
     pre = _int_array(list(prefixes))
     w = None if prefix_weights is None else (ctypes.c_float * len(prefix_weights))(*prefix_weights)
     return int(load().uf_contrastive_fwd_bwd_ex(A, B, int(Na), int(Nb), int(D), pre, len(prefixes), int(kind),
-                                                float(logit_scale), float(bias), w, loss_per_prefix, row_terms,
-                                                col_terms, dA, dB, d_logit_scale, d_bias, workspace,
-                                                int(workspace_bytes), device_status, stream))
+                                                float(logit_scale), float(bias), logit_scale_dev, bias_dev, w,
+                                                loss_per_prefix, row_terms, col_terms, dA, dB, d_logit_scale, d_bias,
+                                                workspace, int(workspace_bytes), device_status, stream))
 
 
 KERNEL_GROUPS = ("prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd", "gemm")
@@ -158,7 +159,9 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
     Returns a dict with ``loss`` (n_prefix fp32), ``dA``/``dB`` (fp32, when grads) and
     ``row_terms``/``col_terms`` (when terms), and with ``scale_grads`` the one-element
     fp32 tensors ``d_logit_scale`` and ``d_bias`` (the weighted loss's derivatives in
-    the logit scale and the SigLIP bias; needs grads).  ``workspace`` may be a preallocated uint8
+    the logit scale and the SigLIP bias; needs grads).  ``logit_scale`` and ``bias`` may
+    be floats or one-element fp32 CUDA tensors; a tensor is read by the kernels when they
+    run (graph capture of a learned scale).  ``workspace`` may be a preallocated uint8
     CUDA tensor of at least ``uf_contrastive_workspace_min`` bytes (its size sets how many
     rows of backward weights the library keeps at once); by default one of the
     recommended ``uf_contrastive_workspace_size`` bytes is allocated.
@@ -191,9 +194,19 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
         out["d_bias"] = torch.empty(1, dtype=torch.float32, device=dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+
+    def scalar(v):  # (host value, device pointer)
+        if isinstance(v, torch.Tensor):
+            if v.dtype != torch.float32 or not v.is_cuda or v.numel() != 1:
+                raise TypeError("a device logit scale / bias must be a one-element fp32 CUDA tensor")
+            return 0.0, v.data_ptr()
+        return float(v), None
+
+    ls_host, ls_dev = scalar(logit_scale)
+    b_host, b_dev = scalar(bias)
     with torch.cuda.device(dev):
-        st = uf_contrastive_fwd_bwd_ex(A.data_ptr(), B.data_ptr(), Na, Nb, D, prefixes, k, logit_scale, bias,
-                                       prefix_weights, out["loss"].data_ptr(), ptr(out.get("row_terms")),
+        st = uf_contrastive_fwd_bwd_ex(A.data_ptr(), B.data_ptr(), Na, Nb, D, prefixes, k, ls_host, b_host, ls_dev,
+                                       b_dev, prefix_weights, out["loss"].data_ptr(), ptr(out.get("row_terms")),
                                        ptr(out.get("col_terms")), ptr(out.get("dA")), ptr(out.get("dB")),
                                        ptr(out.get("d_logit_scale")), ptr(out.get("d_bias")), workspace.data_ptr(),
                                        workspace.numel(), ptr(device_status), s.cuda_stream)

@@ -39,6 +39,13 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   const int64_t n_items = p.na > p.nb ? p.na : p.nb;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int n = p.n_prefix;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && (p.sc.scale_ptr || p.sc.bias_ptr)) {
+    // scalars that only the device knows are range-checked here, where the host checks its own
+    const float t = p.sc.t(), b = p.sc.b();
+    const bool ok = p.kind == KIND_SIGLIP ? (isfinite(t) && isfinite(b) && fabsf(t) + fabsf(b) <= kMaxSiglipRange)
+                                          : (t > 0.f && t <= kMaxLogitScale);
+    if (!ok) atomicExch(p.status, kStatusBadScalar);
+  }
   for (int64_t r = warp_id; r < n_items; r += n_warps) {
     const bool has_a = r < p.na, has_b = r < p.nb, pair = r < p.nmin;
     float ssa[kMaxPrefix], ssb[kMaxPrefix], dab[kMaxPrefix];
@@ -124,8 +131,9 @@ cudaError_t launch_transpose(const uint16_t* X, uint16_t* Xt, int64_t rows, int 
 
 // ------------------------------------------------------------------------------ stats
 // Elementwise over (prefix, row) of A and then of B.  The forward sums cover the
-// negatives only (Zneg); the positive's share is handled here in float64:
-//   CLIP/ROWS  term = -log P_ii = softplus(log Zneg + tau - s_ii),  Z = Zneg + e^{s_ii - tau}
+// negatives only (Zneg, relative to the row's shift S: tau, or the row's largest logit on
+// the max-shifted path); the positive's share is handled here in float64:
+//   CLIP/ROWS  term = -log P_ii = softplus(log Zneg + S - s_ii),  Z = Zneg + e^{s_ii - S}
 //   SigLIP     term = ln2 * (sum of negatives' softplus in log2 units) + softplus(-x_ii)
 __device__ __forceinline__ double softplus_d(double y) { return y > 0 ? y + log1p(exp(-y)) : log1p(exp(y)); }
 
@@ -146,6 +154,7 @@ __device__ __forceinline__ double sum_slots(const float* acc, int slots, int64_t
 
 __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
   const int n = p.n_prefix;
+  const double tau = p.sc.t(), bias = p.sc.b();
   const int64_t total_a = static_cast<int64_t>(n) * p.na;
   const int64_t total = total_a + static_cast<int64_t>(n) * p.nb;
   const int64_t nmin = p.na < p.nb ? p.na : p.nb;
@@ -168,7 +177,7 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
       }
       const double s = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
       // (log2 units)
-      const double x_ii = static_cast<double>(p.tau_or_t) * cos_ii + static_cast<double>(p.bias);
+      const double x_ii = tau * cos_ii + bias;
       p.terms_a[ee] = static_cast<float>(s * 0.6931471805599453 + (has_pos ? softplus_d(-x_ii) : 0.0));
       continue;
     }
@@ -176,23 +185,34 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
       p.terms_b[ee] = 0.f;
       continue;
     }
-    // sum over negatives of exp(s_ij - tau)
+    // sum over negatives of exp(s_ij - S), S the shift of this row (column)
     const double zneg = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
-    const double tau = p.tau_or_t;
+    const float* shift = side_a ? p.shift_a : p.shift_b;
+    const double ush = shift ? static_cast<double>(shift[ee]) : tau * 1.4426950408889634;  // log2 units
+    const double S = shift ? ush * 0.6931471805599453 : tau;
     const double s_ii = tau * cos_ii;
-    const double e_ii = has_pos ? exp(s_ii - tau) : 0.0;
+    const double e_ii = has_pos ? exp(s_ii - S) : 0.0;
     const double z = zneg + e_ii;
-    const double term = has_pos ? softplus_d(log(zneg) + tau - s_ii) : log(zneg) + tau;
+    // (zneg = 0 happens on the shifted path when the positive outweighs every negative
+    // beyond fp32's range: log gives -inf and softplus(-inf) = 0, the exact limit)
+    const double term = has_pos ? softplus_d(log(zneg) + S - s_ii) : log(zneg) + S;
     const double N = static_cast<double>(p.na);
-    const double coef = (p.kind == KIND_CLIP) ? w * tau / (2.0 * N) : w * tau / N;
     const double rho = side_a ? p.rinv_a[k * p.na + i] : p.rinv_b[k * p.nb + i];
+    double f;
+    if (shift) {  // log2(rho alpha / w) - u: the weight pass multiplies by w and takes 2^(x + f)
+      const double coef = (p.kind == KIND_CLIP) ? tau / (2.0 * N) : tau / N;
+      f = log2(rho * coef / z) - ush;
+    } else {
+      const double coef = (p.kind == KIND_CLIP) ? w * tau / (2.0 * N) : w * tau / N;
+      f = rho * coef / z;
+    }
     if (side_a) {
       p.zr[ee] = static_cast<float>(zneg);
-      p.fa[ee] = static_cast<float>(rho * coef / z);
+      p.fa[ee] = static_cast<float>(f);
       p.terms_a[ee] = static_cast<float>(term);
     } else {
       p.zc[ee] = static_cast<float>(zneg);
-      p.fb[ee] = static_cast<float>(rho * coef / z);
+      p.fb[ee] = static_cast<float>(f);
       p.terms_b[ee] = static_cast<float>(term);
     }
   }
@@ -244,6 +264,7 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int n = p.n_prefix;
   const int pn = p.prefix_end[n - 1];
+  const float t_sc = p.sc.t(), b_sc = p.sc.b();
   for (int64_t i = warp_id; i < p.nx; i += n_warps) {
     const bool diag = i < p.nmin;
     float rk = 0.f, qk = 0.f, Ck = 0.f;
@@ -261,20 +282,26 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
         // W_ii = W'_ii + w, written without cancellation: 1 - P_ii = Zneg / Z and
         // sigmoid(x) - 1 = -sigmoid(-x).
         if (p.kind == KIND_SIGLIP) {
-          const float x = p.tau_or_t * cosd + p.bias;
+          const float x = t_sc * cosd + b_sc;
           const float sg_neg = 1.f / (1.f + expf(x));
-          Wd = -static_cast<float>(w * p.tau_or_t / N) * sg_neg;
+          Wd = -static_cast<float>(w * t_sc / N) * sg_neg;
         } else {
-          const float tau = p.tau_or_t;
-          const float e = expf(tau * cosd - tau);
+          const float tau = t_sc;
+          // e^{s_ii - S} for the shift S of each normaliser (tau, or the row's / column's
+          // largest logit on the max-shifted path, stored in log2 units)
+          const float ln2 = 0.6931471805599453f;
+          const float sx = p.shift_x ? p.shift_x[k * p.nx + i] * ln2 : tau;
+          const float sy = p.shift_y ? p.shift_y[k * p.ny + i] * ln2 : tau;
+          const float ex = expf(tau * cosd - sx), ey = expf(tau * cosd - sy);
           if (p.kind == KIND_CLIP) {
             const float c = static_cast<float>(w * tau / (2.0 * N));
             const float zx = p.z_x[k * p.nx + i], zy = p.z_y[k * p.ny + i];
-            Wd = -c * (zx / (zx + e) + zy / (zy + e));
+            Wd = -c * (zx / (zx + ex) + zy / (zy + ey));
           } else {
             const float c = static_cast<float>(w * tau / N);
             const float zq = p.x_is_query ? p.z_x[k * p.nx + i] : p.z_y[k * p.ny + i];
-            Wd = -c * (zq / (zq + e));
+            const float eq = p.x_is_query ? ex : ey;
+            Wd = -c * (zq / (zq + eq));
           }
         }
         C += Wd * cosd;
@@ -348,6 +375,7 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
 __global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams p) {
   __shared__ double red[2][32];
   const int n = p.n_prefix;
+  const float scale = p.sc.t(), bias = p.sc.b();
   double s = 0.0, sb = 0.0;
   if (p.csum)
     for (int64_t i = threadIdx.x; i < p.na; i += blockDim.x) s += p.csum[i];
@@ -360,7 +388,7 @@ __global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams 
         for (int sl = 0; sl < p.sig_slots; ++sl) neg += p.rowsig[(static_cast<int64_t>(sl) * n + k) * p.na + i];
         double pos = 0.0;  // the positive's share: sigmoid(x_ii) - 1 = -sigmoid(-x_ii)
         if (i < p.nmin) {
-          const double x = static_cast<double>(p.scale) * p.pos_cos[k * p.nmin + i] + p.bias;
+          const double x = static_cast<double>(scale) * p.pos_cos[k * p.nmin + i] + bias;
           pos = -1.0 / (1.0 + exp(x));
         }
         sb += wk * (neg + pos);
@@ -386,10 +414,40 @@ __global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams 
       vb += __shfl_xor_sync(0xffffffffu, vb, o);
     }
     if (threadIdx.x == 0) {
-      if (p.d_scale) *p.d_scale = static_cast<float>(v / static_cast<double>(p.scale));
+      // (scale = 0, possible only for SigLIP, gives 0/0: the host refuses a host t = 0, a
+      // device one is the caller's to avoid)
+      if (p.d_scale) *p.d_scale = static_cast<float>(v / static_cast<double>(scale));
       if (p.d_bias) *p.d_bias = static_cast<float>(p.kind == KIND_SIGLIP ? vb : 0.0);
     }
   }
+}
+
+// ------------------------------------------------------------------------------ max_reduce
+__global__ void __launch_bounds__(256) max_reduce_kernel(const MaxReduceParams p) {
+  const int n = p.n_prefix;
+  const int64_t total_a = static_cast<int64_t>(n) * p.na;
+  const int64_t total = total_a + (p.v ? static_cast<int64_t>(n) * p.nb : 0);
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float m = -INFINITY;
+    if (e < total_a) {
+      for (int s = 0; s < p.slots_a; ++s) m = fmaxf(m, p.rowmax[static_cast<int64_t>(s) * total_a + e]);
+      p.u[e] = m;
+    } else {
+      const int64_t ee = e - total_a;
+      const int64_t total_b = static_cast<int64_t>(n) * p.nb;
+      for (int s = 0; s < p.blocks; ++s) m = fmaxf(m, p.colmax[static_cast<int64_t>(s) * total_b + ee]);
+      p.v[ee] = m;
+    }
+  }
+}
+
+cudaError_t launch_max_reduce(const MaxReduceParams& p, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(p.n_prefix) * (p.na + (p.v ? p.nb : 0));
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  max_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream) {
@@ -413,6 +471,7 @@ cudaError_t aux_kernels_setup() {
   if ((e = cudaFuncGetAttributes(&fa, stats_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, finalize_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, scale_grad_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, max_reduce_kernel)) != cudaSuccess) return e;
   return cudaFuncGetAttributes(&fa, norm_bwd_kernel);
 }
 

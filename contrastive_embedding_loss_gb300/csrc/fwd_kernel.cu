@@ -18,6 +18,13 @@
 // the four row-quadrant warps of a column quarter combine through shared memory, and one
 // of them writes the 128-row partial of every column to global memory (one slot per row
 // block; a reduction kernel adds the slots in a fixed order).
+//
+// Shifts.  The default sums 2^(x - L) with x = tau log2(e) cos and the fixed shift L =
+// tau log2(e): |cos| <= 1 keeps every term in [2^-2L, 1], normal fp32 while tau <= 40.
+// Beyond that (or when tau is only known on the device) the same kernel runs twice: a
+// max pass (kFwdMax) finds every row's and column's largest x, then a shifted pass
+// (kFwdShifted) sums 2^(x - u_i) for the row and 2^(x - v_j) for the column, u and v
+// those maxima, so the largest term of every sum is 1 whatever the scale.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -40,8 +47,10 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr int off_x = 0;
 constexpr int off_y = off_x + kNS * kXBytes;
 constexpr int off_colf = off_y + kNS * kYBytes;                    // [4][kMaxPrefix][256] sigma_j
-constexpr int off_rowf = off_colf + 4 * kMaxPrefix * kCols * 4;    // [kMaxPrefix][128] L rho_i
-constexpr int off_cpart = off_rowf + kMaxPrefix * kTileRows * 4;   // [2][4 quarters][4 quadrants][64]
+constexpr int off_colsh = off_colf + 4 * kMaxPrefix * kCols * 4;   // [4][kMaxPrefix][256] v_j (shifted, CLIP)
+constexpr int off_rowf = off_colsh + 4 * kMaxPrefix * kCols * 4;   // [kMaxPrefix][128] L rho_i
+constexpr int off_rowsh = off_rowf + kMaxPrefix * kTileRows * 4;   // [kMaxPrefix][128] u_i (shifted)
+constexpr int off_cpart = off_rowsh + kMaxPrefix * kTileRows * 4;  // [2][4 quarters][4 quadrants][64]
 constexpr int off_bar = off_cpart + 2 * 4 * 4 * 64 * 4;
 constexpr int n_bars = 2 * kNS + 2 + 2 + 1;
 constexpr int off_misc = off_bar + n_bars * 8;
@@ -54,9 +63,11 @@ struct Params {
   int prefix_end[kMaxPrefix];
   int n_col_tiles;      // ceil(ny / 256)
   int tiles_per_split;
-  float L, b2;          // CLIP/ROWS: tau*log2(e) (also the fixed shift); SigLIP: t*log2(e), bias*log2(e)
+  Scalars sc;           // tau or t, and b: L = scale log2(e) (also the fixed shift), b2 = bias log2(e)
   const float* rinv_x;  // [n][nx]
   const float* rinv_y;  // [n][ny]
+  const float* shift_x; // kFwdShifted: [n][nx]
+  const float* shift_y; // kFwdShifted, CLIP: [n][ny]
   float* rowacc;        // [split * 4 + quarter][n][nx]
   float* colacc;        // [row block][n][ny] (CLIP) or NULL
   int* status;
@@ -79,8 +90,10 @@ __device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag) 
   if (p.status) atomicExch(p.status, kStatusTimeout);
 }
 
-// Sum of 32 values over the warp's 32 lanes, scattered: lane l returns the sum of v[l].
-// (fp32 throughout: the summands span e^-2tau .. 1, beyond what fp16 pairs could carry.)
+// Sum (or MAX: maximum) of 32 values over the warp's 32 lanes, scattered: lane l returns
+// the sum of v[l].  (fp32 throughout: the summands span e^-2tau .. 1, beyond what fp16
+// pairs could carry.)
+template <bool MAX = false>
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {
@@ -90,7 +103,8 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
       const float lo = v[i], hi = v[i + m];
       const float send = upper ? lo : hi;
       const float keep = upper ? hi : lo;
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+      const float got = __shfl_xor_sync(0xffffffffu, send, m);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
     }
   }
   return v[0];
@@ -138,6 +152,71 @@ __device__ __forceinline__ float fwd_cells(const float (&v)[64], const float* cf
   return rs.x + rs.y;
 }
 
+// kFwdMax: the row maximum of x = R1 sigma_j dot over this thread's 64 cells is returned,
+// the warp's 32-row column maxima go to cp (COLS).  Only padding is masked (to -inf).
+template <bool COLS, bool CHECK>
+__device__ __forceinline__ float fwd_cells_max(const float (&v)[64], const float* cf, float R1, int col_base,
+                                               int ncols, bool row_ok, int lane, float* cp) {
+  float2 rm = make_float2(-INFINITY, -INFINITY);
+  const float2 r1 = make_float2(R1, R1);
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const int c = g * 32 + j;
+      // the same two roundings as fwd_cells_shifted, so that x - u_i <= 0 holds exactly there
+      float2 val = mul2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[c], v[c + 1]));
+      if constexpr (CHECK) {
+        const int col = col_base + c;
+        if (!(row_ok && col < ncols)) val.x = -INFINITY;
+        if (!(row_ok && col + 1 < ncols)) val.y = -INFINITY;
+      }
+      x[j] = val.x;
+      x[j + 1] = val.y;
+      rm = make_float2(fmaxf(rm.x, val.x), fmaxf(rm.y, val.y));
+    }
+    if constexpr (COLS) cp[g * 32 + lane] = reduce_scatter32<true>(x, lane);
+  }
+  return fmaxf(rm.x, rm.y);
+}
+
+// kFwdShifted: the row sum of 2^(x - U) is returned (U the row's shift), and (COLS) the
+// warp's column partials of 2^(x - vs[c]) go to cp.  Masks as in fwd_cells.
+template <bool COLS, bool CHECK>
+__device__ __forceinline__ float fwd_cells_shifted(const float (&v)[64], const float* cf, const float* vs, float R1,
+                                                   float U, int col_base, int ncols, int dcol, bool row_ok, int lane,
+                                                   float* cp) {
+  float2 rs = make_float2(0.f, 0.f);
+  const float2 r1 = make_float2(R1, R1), nu = make_float2(-U, -U);
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    float e[32];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const int c = g * 32 + j;
+      const float2 x = mul2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[c], v[c + 1]));
+      const float2 xr = add2(x, nu);
+      float2 er = make_float2(ex2_approx(xr.x), ex2_approx(xr.y));
+      float2 ec = make_float2(0.f, 0.f);
+      if constexpr (COLS) {
+        const float2 xc = add2(x, make_float2(-vs[c], -vs[c + 1]));
+        ec = make_float2(ex2_approx(xc.x), ex2_approx(xc.y));
+      }
+      if constexpr (CHECK) {
+        const int col = col_base + c;
+        if (!(row_ok && col < ncols && col != dcol)) er.x = ec.x = 0.f;
+        if (!(row_ok && col + 1 < ncols && col + 1 != dcol)) er.y = ec.y = 0.f;
+      }
+      e[j] = ec.x;
+      e[j + 1] = ec.y;
+      rs = add2(rs, er);
+    }
+    if constexpr (COLS) cp[g * 32 + lane] = reduce_scatter32(e, lane);
+  }
+  return rs.x + rs.y;
+}
+
 // The order in which tiles and bands are fed to the MMA: tiles in pairs (t even in
 // accumulator 0, t + 1 in accumulator 1), band by band, alternating within a pair.
 // Step index s -> (tile, band); the producer, the MMA issuer and the epilogue all walk it.
@@ -154,7 +233,7 @@ struct Schedule {
   }
 };
 
-template <int KIND, bool COLS>
+template <int KIND, bool COLS, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -163,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sy = smem + off_y;
   float* colf = reinterpret_cast<float*>(smem + off_colf);
   float* rowf = reinterpret_cast<float*>(smem + off_rowf);
+  float* rowsh = reinterpret_cast<float*>(smem + off_rowsh);
+  float* colsh = reinterpret_cast<float*>(smem + off_colsh);
   float* cpart = reinterpret_cast<float*>(smem + off_cpart);
   uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + off_bar);
   uint64_t* s_empty = s_full + kNS;
@@ -171,6 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_misc + 4);
+  // L = scale log2(e) and b2 = bias log2(e), read once from the host value or the device
+  // scalar; the epilogue reloads them per snapshot (volatile) instead of pinning registers
+  volatile float* s_scal = reinterpret_cast<volatile float*>(smem + off_misc + 8);
+  const uint32_t scal_s = smem_u32(smem + off_misc + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
@@ -194,6 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    s_scal[0] = p.sc.t() * 1.4426950408889634f;
+    s_scal[1] = p.sc.b() * 1.4426950408889634f;
     fence_mbar_init();
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_y);
@@ -281,9 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     constexpr int CF = kMaxPrefix * kCols;  // floats per column-factor buffer
     if (cq == 0) {
+      const float L = s_scal[0];
 #pragma unroll
       for (int k = 0; k < kMaxPrefix; ++k)
-        if (k < n) rowf[k * kTileRows + r] = row_ok ? p.L * p.rinv_x[k * p.nx + gi] : 0.f;
+        if (k < n) {
+          rowf[k * kTileRows + r] = row_ok ? L * p.rinv_x[k * p.nx + gi] : 0.f;
+          if constexpr (MODE == kFwdShifted) rowsh[k * kTileRows + r] = row_ok ? p.shift_x[k * p.nx + gi] : 0.f;
+        }
     }
     // column factors of tile t live in colf[t & 3]; a tile pair's factors are fetched by
     // cp.async while the previous pair is processed
@@ -295,13 +386,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t gj = j0 + c;
         const bool v = gj < p.ny;
         cp_async4(cf + k * kCols + c, p.rinv_y + (v ? k * p.ny + gj : 0), v ? 4u : 0u);
+        if constexpr (MODE == kFwdShifted && COLS)
+          cp_async4(colsh + (t & 3) * CF + k * kCols + c, p.shift_y + (v ? k * p.ny + gj : 0), v ? 4u : 0u);
       }
     };
     for (int t = 0; t < 2 && t < T; ++t) prefetch_colf(t);
     cp_async_commit();
     float acc_row[kMaxPrefix];
 #pragma unroll
-    for (int k = 0; k < kMaxPrefix; ++k) acc_row[k] = 0.f;
+    for (int k = 0; k < kMaxPrefix; ++k) acc_row[k] = MODE == kFwdMax ? -INFINITY : 0.f;
     uint32_t uses[2] = {0, 0};
     uint32_t snap = 0;  // snapshots processed (selects the column-partial buffer)
     bool ok = true;
@@ -341,11 +434,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
         const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (i0 + kTileRows > p.nx);
         float* cp = cpart + (((snap & 1) * 4 + cq) * 4 + q) * 64;
-        const float rs = check ? fwd_cells<KIND, COLS, true>(v, cf, R1, p.L, p.b2, cq * 64, ncols, dcol, row_ok, lane, cp)
-                               : fwd_cells<KIND, COLS, false>(v, cf, R1, p.L, p.b2, cq * 64, ncols, dcol, row_ok, lane, cp);
+        float rs;
+        if constexpr (MODE == kFwdMax) {
+          rs = check ? fwd_cells_max<COLS, true>(v, cf, R1, cq * 64, ncols, row_ok, lane, cp)
+                     : fwd_cells_max<COLS, false>(v, cf, R1, cq * 64, ncols, row_ok, lane, cp);
+        } else if constexpr (MODE == kFwdShifted) {
+          const float* vs = colsh + (t & 3) * CF + k * kCols + cq * 64;
+          const float U = rowsh[k * kTileRows + r];
+          rs = check ? fwd_cells_shifted<COLS, true>(v, cf, vs, R1, U, cq * 64, ncols, dcol, row_ok, lane, cp)
+                     : fwd_cells_shifted<COLS, false>(v, cf, vs, R1, U, cq * 64, ncols, dcol, row_ok, lane, cp);
+        } else {
+          float L, b2;  // (a 32-bit shared address keeps the epilogue within its 96 registers)
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(L), "=f"(b2) : "r"(scal_s));
+          rs = check ? fwd_cells<KIND, COLS, true>(v, cf, R1, L, b2, cq * 64, ncols, dcol, row_ok, lane, cp)
+                     : fwd_cells<KIND, COLS, false>(v, cf, R1, L, b2, cq * 64, ncols, dcol, row_ok, lane, cp);
+        }
 #pragma unroll
         for (int kk = 0; kk < kMaxPrefix; ++kk)
-          if (kk == k) acc_row[kk] += rs;
+          if (kk == k) acc_row[kk] = MODE == kFwdMax ? fmaxf(acc_row[kk], rs) : acc_row[kk] + rs;
       }
       ++uses[a];
       if constexpr (COLS) {
@@ -356,7 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
             const int c = g * 32 + lane;
-            const float sum = cp[c] + cp[64 + c] + cp[128 + c] + cp[192 + c];
+            const float sum = MODE == kFwdMax ? fmaxf(fmaxf(cp[c], cp[64 + c]), fmaxf(cp[128 + c], cp[192 + c]))
+                                              : cp[c] + cp[64 + c] + cp[128 + c] + cp[192 + c];
             const int64_t gj = j0 + cq * 64 + c;
             if (gj < p.ny) p.colacc[(static_cast<int64_t>(blockIdx.x) * n + k) * p.ny + gj] = sum;
           }
@@ -379,18 +486,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int KIND, bool COLS>
+template <int KIND, bool COLS, int MODE>
 static cudaError_t setup_one() {
-  return cudaFuncSetAttribute(fwd_kernel<KIND, COLS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  return cudaFuncSetAttribute(fwd_kernel<KIND, COLS, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes);
 }
 
 }  // namespace fwd
 
 cudaError_t fwd_kernel_setup() {
   cudaError_t e;
-  if ((e = fwd::setup_one<KIND_CLIP, true>()) != cudaSuccess) return e;
-  if ((e = fwd::setup_one<KIND_ROWS, false>()) != cudaSuccess) return e;
-  return fwd::setup_one<KIND_SIGLIP, false>();
+  if ((e = fwd::setup_one<KIND_CLIP, true, kFwdSum>()) != cudaSuccess) return e;
+  if ((e = fwd::setup_one<KIND_CLIP, true, kFwdMax>()) != cudaSuccess) return e;
+  if ((e = fwd::setup_one<KIND_CLIP, true, kFwdShifted>()) != cudaSuccess) return e;
+  if ((e = fwd::setup_one<KIND_ROWS, false, kFwdSum>()) != cudaSuccess) return e;
+  if ((e = fwd::setup_one<KIND_ROWS, false, kFwdMax>()) != cudaSuccess) return e;
+  if ((e = fwd::setup_one<KIND_ROWS, false, kFwdShifted>()) != cudaSuccess) return e;
+  return fwd::setup_one<KIND_SIGLIP, false, kFwdSum>();
 }
 
 cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const FwdParams& q, dim3 grid,
@@ -402,19 +514,30 @@ cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
   for (int k = 0; k < kMaxPrefix; ++k) p.prefix_end[k] = q.prefix_end[k];
   p.n_col_tiles = q.n_col_tiles;
   p.tiles_per_split = q.tiles_per_split;
-  p.L = q.L;
-  p.b2 = q.b2;
+  p.sc = q.sc;
   p.rinv_x = q.rinv_x;
   p.rinv_y = q.rinv_y;
+  p.shift_x = q.shift_x;
+  p.shift_y = q.shift_y;
   p.rowacc = q.rowacc;
   p.colacc = q.colacc;
   p.status = q.status;
-  if (kind == KIND_CLIP)
-    fwd::fwd_kernel<KIND_CLIP, true><<<grid, fwd::kThreads, fwd::smem_bytes, stream>>>(tm_x, tm_y, p);
-  else if (kind == KIND_ROWS)
-    fwd::fwd_kernel<KIND_ROWS, false><<<grid, fwd::kThreads, fwd::smem_bytes, stream>>>(tm_x, tm_y, p);
-  else
-    fwd::fwd_kernel<KIND_SIGLIP, false><<<grid, fwd::kThreads, fwd::smem_bytes, stream>>>(tm_x, tm_y, p);
+  using fwd::fwd_kernel;
+  constexpr int T = fwd::kThreads, S = fwd::smem_bytes;
+  if (kind == KIND_SIGLIP && q.mode != kFwdSum) return cudaErrorInvalidValue;
+  if (q.mode == kFwdShifted && (q.shift_x == nullptr || (kind == KIND_CLIP && q.shift_y == nullptr)))
+    return cudaErrorInvalidValue;
+  if (kind == KIND_CLIP) {
+    if (q.mode == kFwdMax) fwd_kernel<KIND_CLIP, true, kFwdMax><<<grid, T, S, stream>>>(tm_x, tm_y, p);
+    else if (q.mode == kFwdShifted) fwd_kernel<KIND_CLIP, true, kFwdShifted><<<grid, T, S, stream>>>(tm_x, tm_y, p);
+    else fwd_kernel<KIND_CLIP, true, kFwdSum><<<grid, T, S, stream>>>(tm_x, tm_y, p);
+  } else if (kind == KIND_ROWS) {
+    if (q.mode == kFwdMax) fwd_kernel<KIND_ROWS, false, kFwdMax><<<grid, T, S, stream>>>(tm_x, tm_y, p);
+    else if (q.mode == kFwdShifted) fwd_kernel<KIND_ROWS, false, kFwdShifted><<<grid, T, S, stream>>>(tm_x, tm_y, p);
+    else fwd_kernel<KIND_ROWS, false, kFwdSum><<<grid, T, S, stream>>>(tm_x, tm_y, p);
+  } else {
+    fwd_kernel<KIND_SIGLIP, false, kFwdSum><<<grid, T, S, stream>>>(tm_x, tm_y, p);
+  }
   return cudaGetLastError();
 }
 

@@ -12,16 +12,25 @@ namespace ufc {
 cudaError_t aux_kernels_setup();
 
 // Forward statistics with 128 x 256 score tiles (fwd_kernel.cu): row sums of every
-// prefix over the negatives, and (CLIP) 128-row partial column sums.
+// prefix over the negatives, and (CLIP) 128-row partial column sums.  Modes:
+//   kFwdSum      sums of 2^(x - L), x = tau log2(e) cos (the fixed shift L = tau log2(e))
+//   kFwdMax      maxima of x over the row / the 128 rows of the column (padding excluded,
+//                the positive included): the shifts of the max-shifted path
+//   kFwdShifted  sums of 2^(x - u_i) per row and 2^(x - v_j) per column, u and v the
+//                maxima of a kFwdMax pass (log2 units)
+enum FwdMode : int { kFwdSum = 0, kFwdMax = 1, kFwdShifted = 2 };
 struct FwdParams {
   int64_t nx, ny;
   int n_prefix;
   int prefix_end[kMaxPrefix];
   int n_col_tiles;          // ceil(ny / 256)
   int tiles_per_split;
-  float L, b2;
+  int mode;                 // FwdMode (SigLIP: kFwdSum only)
+  Scalars sc;
   const float* rinv_x;
   const float* rinv_y;
+  const float* shift_x;     // kFwdShifted: u [n][nx]
+  const float* shift_y;     // kFwdShifted, CLIP: v [n][ny]
   float* rowacc;            // [split * 4 + column quarter][n][nx]
   float* colacc;            // [row block][n][ny] (CLIP only)
   int* status;
@@ -44,12 +53,13 @@ struct WgtParams {
   int prefix_end[kMaxPrefix];
   int n_col_tiles;                // ceil(ny / 256)
   int tiles_per_split;
-  float L, b2;                    // CLIP/ROWS: tau*log2(e) (also the fixed shift); SigLIP: t*log2(e), bias*log2(e)
+  Scalars sc;
+  int shifted;                    // CLIP/ROWS: the max-shifted statistics (alpha_x, beta_y in log2 form)
   const float* rinv_x;            // [n][nx]
-  const float* alpha_x;           // [n][nx] rho_i alpha_i (CLIP/ROWS) or NULL
+  const float* alpha_x;           // [n][nx] rho_i alpha_i (CLIP/ROWS) or NULL; shifted: log2(rho_i alpha_i / w_k) - u_i
   const float* rinv_y;            // [n][ny]
-  const float* beta_y;            // [n][ny] sigma_j beta_j (CLIP/ROWS) or NULL
-  float m_scale[kMaxPrefix];      // SigLIP: w_k t / N
+  const float* beta_y;            // [n][ny] sigma_j beta_j (CLIP) or NULL; shifted: log2(sigma_j beta_j / w_k) - v_j
+  float m_scale[kMaxPrefix];      // SigLIP: w_k / N (times t in the kernel); shifted CLIP/ROWS: w_k
   int64_t w_rows_per_prefix;      // rows between prefixes in the weight array (multiple of 128)
   float* rowacc;                  // SigLIP: [split * 4 + quarter][n][nx] loss sums (log2 units), or NULL
   float* rowsig;                  // SigLIP, with rowacc: the same slots, sums of sigmoid(x_ij) over the
@@ -94,6 +104,9 @@ cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const
 // Per-row inverse norms of every prefix for A and B, plus the positives' cosines
 // cos_ii for i < min(Na, Nb).  Layouts [n][rows].
 struct PrepParams {
+  int kind;
+  Scalars sc;              // device scalars are range-checked here (status = kStatusBadScalar)
+  int* status;
   const uint16_t* A;
   const uint16_t* B;
   int64_t na, nb, nmin;
@@ -114,19 +127,21 @@ struct StatsParams {
   int64_t na, nb;
   int n_prefix;
   int prefix_end[kMaxPrefix];
-  float tau_or_t, bias;
+  Scalars sc;
   float weight[kMaxPrefix];
   const float* rinv_a;
   const float* rinv_b;
   const float* pos_cos;
+  const float* shift_a;    // NULL: the fixed shift tau; else the rows' shifts u [n][na] (log2 units)
+  const float* shift_b;    // CLIP, with shift_a: the columns' shifts v [n][nb]
   const float* rowacc_a;   // [slots_a][n][na]
   int slots_a;
   const float* rowacc_b;   // [slots_b][n][nb] (CLIP)
   int slots_b;
-  float* zr;               // [n][na]  fixed-shift row sums over the negatives (CLIP/ROWS)
+  float* zr;               // [n][na]  row sums over the negatives, relative to the row's shift (CLIP/ROWS)
   float* zc;               // [n][nb]
-  float* fa;               // [n][na]  rho_i * u_i  (backward factor)
-  float* fb;               // [n][nb]  sigma_j * v_j
+  float* fa;               // [n][na]  rho_i alpha_i (backward factor); shifted: log2(rho_i alpha_i / w_k) - u_i
+  float* fb;               // [n][nb]  sigma_j beta_j; shifted: log2(sigma_j beta_j / w_k) - v_j
   float* terms_a;          // [n][na]  row terms
   float* terms_b;          // [n][nb]  column terms (CLIP; 0 otherwise)
   float* loss;             // [n]
@@ -139,15 +154,17 @@ struct NormBwdParams {
   int64_t nx, ny, nmin, n_total;  // n_total: batch size used by the loss normaliser
   int d, n_prefix;
   int prefix_end[kMaxPrefix];
-  float tau_or_t, bias;
+  Scalars sc;
   float weight[kMaxPrefix];
   const uint16_t* X;
   const uint16_t* Y;
   const float* rinv_x;
   const float* rinv_y;
   const float* pos_cos;
-  const float* z_x;        // CLIP/ROWS fixed-shift sums of X's rows over negatives (ROWS: the queries')
+  const float* z_x;        // CLIP/ROWS sums of X's rows over negatives (ROWS: the queries')
   const float* z_y;        // CLIP: of Y's rows
+  const float* shift_x;    // NULL: the fixed shift; else the shifts of z_x's rows (log2 units)
+  const float* shift_y;    // likewise for z_y
   int x_is_query;          // ROWS: 1 when X holds the queries
   const float* crow;       // [slots][n][nx]
   int crow_slots;
@@ -166,7 +183,7 @@ struct ScaleGradParams {
   int kind;
   int64_t na, nmin;
   int n_prefix;
-  float scale, bias;
+  Scalars sc;
   float weight[kMaxPrefix];
   const float* csum;       // [na]
   const float* rowsig;     // SigLIP: [slots][n][na]
@@ -176,5 +193,19 @@ struct ScaleGradParams {
   float* d_bias;           // device scalar or NULL
 };
 cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream);
+
+// The shifts of the max-shifted path from a kFwdMax forward: u[k][i] = max over the row
+// slots, v[k][j] = max over the column partials of every row block (CLIP; NULL otherwise).
+struct MaxReduceParams {
+  int n_prefix;
+  int64_t na, nb;
+  const float* rowmax;     // [slots_a][n][na]
+  int slots_a;
+  const float* colmax;     // [blocks][n][nb] or NULL
+  int blocks;
+  float* u;                // [n][na]
+  float* v;                // [n][nb] or NULL
+};
+cudaError_t launch_max_reduce(const MaxReduceParams& p, cudaStream_t stream);
 
 }  // namespace ufc

@@ -56,7 +56,7 @@ struct Plan {
   size_t fixed = 0;                  // bytes of everything but the weight array
   // offsets
   size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
-      o_terms_b, o_loss, o_at, o_bt, o_csum, o_sig, o_w, total;
+      o_terms_b, o_loss, o_at, o_bt, o_csum, o_sig, o_sh_a, o_sh_b, o_w, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -118,6 +118,10 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.o_bt = take(grads ? sizeof(uint16_t) * D * P.ldb : 0);
   P.o_csum = take(grads ? f * Na : 0);  // per-row sums of the row scalars (logit-scale gradient)
   P.o_sig = take(grads && kind == KIND_SIGLIP ? f * n * Na * 4 * P.wgt.splits : 0);  // sigmoid sums (bias)
+  // the max-shifted path's row and column shifts (taken for every call: the scale that
+  // picks the path may live on the device)
+  P.o_sh_a = take(kind != KIND_SIGLIP ? f * n * Na : 0);
+  P.o_sh_b = take(kind == KIND_CLIP ? f * n * Nb : 0);
   P.fixed = o;
   P.o_w = o;
   P.chunk = 0;
@@ -273,13 +277,14 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
                                    const float* prefix_weights, float* loss_per_prefix, float* row_terms,
                                    float* col_terms, float* dA, float* dB, void* workspace, size_t workspace_bytes,
                                    int* device_status, void* stream_handle) {
-  return uf_contrastive_fwd_bwd_ex(A, B, Na, Nb, D, prefixes, n_prefix, kind, logit_scale, bias, prefix_weights,
-                                   loss_per_prefix, row_terms, col_terms, dA, dB, nullptr, nullptr, workspace,
-                                   workspace_bytes, device_status, stream_handle);
+  return uf_contrastive_fwd_bwd_ex(A, B, Na, Nb, D, prefixes, n_prefix, kind, logit_scale, bias, nullptr, nullptr,
+                                   prefix_weights, loss_per_prefix, row_terms, col_terms, dA, dB, nullptr, nullptr,
+                                   workspace, workspace_bytes, device_status, stream_handle);
 }
 
 uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
                                       const int* prefixes, int n_prefix, int kind, float logit_scale, float bias,
+                                      const float* logit_scale_dev, const float* bias_dev,
                                       const float* prefix_weights, float* loss_per_prefix, float* row_terms,
                                       float* col_terms, float* dA, float* dB, float* d_logit_scale, float* d_bias,
                                       void* workspace, size_t workspace_bytes, int* device_status,
@@ -290,13 +295,17 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
   const bool grads = dA != nullptr;
   if ((d_logit_scale || d_bias) && !grads) return UF_INVALID_ARGUMENT;  // they come out of the backward
   if ((d_logit_scale && !aligned(d_logit_scale, 4)) || (d_bias && !aligned(d_bias, 4))) return UF_INVALID_ARGUMENT;
+  if ((logit_scale_dev && !aligned(logit_scale_dev, 4)) || (bias_dev && !aligned(bias_dev, 4)))
+    return UF_INVALID_ARGUMENT;
   Plan P;
   if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, grads, workspace_bytes, P)) return UF_INVALID_ARGUMENT;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(workspace, 256) || !aligned(loss_per_prefix, 4))
     return UF_INVALID_ARGUMENT;
   if (grads && (!aligned(dA, 16) || !aligned(dB, 16))) return UF_INVALID_ARGUMENT;
   if ((row_terms && !aligned(row_terms, 4)) || (col_terms && !aligned(col_terms, 4))) return UF_INVALID_ARGUMENT;
-  if (!std::isfinite(logit_scale) || !std::isfinite(bias)) return UF_INVALID_ARGUMENT;
+  // host scalars are checked here; ones on the device by the first kernel (*device_status)
+  if ((!logit_scale_dev && !std::isfinite(logit_scale)) || (!bias_dev && !std::isfinite(bias)))
+    return UF_INVALID_ARGUMENT;
   float w[kMaxPrefix];
   for (int k = 0; k < kMaxPrefix; ++k) w[k] = 0.f;
   for (int k = 0; k < n_prefix; ++k) {
@@ -304,12 +313,17 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     if (!std::isfinite(w[k])) return UF_INVALID_ARGUMENT;
   }
   if (kind == KIND_SIGLIP) {
-    if (std::fabs(logit_scale) + std::fabs(bias) > 80.f) return UF_UNSUPPORTED;
-    if (d_logit_scale && logit_scale == 0.f) return UF_UNSUPPORTED;  // taken as (sum W cos) / t
-  } else {
+    if (!logit_scale_dev && !bias_dev && std::fabs(logit_scale) + std::fabs(bias) > kMaxSiglipRange)
+      return UF_UNSUPPORTED;
+    if (d_logit_scale && !logit_scale_dev && logit_scale == 0.f) return UF_UNSUPPORTED;  // taken as (sum W cos) / t
+  } else if (!logit_scale_dev) {
     if (!(logit_scale > 0.f)) return UF_INVALID_ARGUMENT;
-    if (logit_scale > 40.f) return UF_UNSUPPORTED;
+    if (logit_scale > kMaxLogitScale) return UF_UNSUPPORTED;
   }
+  // CLIP/ROWS statistics with the fixed shift tau while tau <= 40 is known on the host;
+  // the max-shifted path otherwise
+  const bool shifted = kind != KIND_SIGLIP && (logit_scale_dev != nullptr || logit_scale > kFixedShiftMaxScale);
+  const Scalars sc{logit_scale, bias, logit_scale_dev, bias_dev};
   if (workspace_bytes < P.total) return UF_WORKSPACE_TOO_SMALL;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
@@ -322,8 +336,9 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
   const uint16_t* A16 = static_cast<const uint16_t*>(A);
   const uint16_t* B16 = static_cast<const uint16_t*>(B);
   const int n = n_prefix;
-  const float log2e = 1.4426950408889634f;
   const bool siglip = kind == KIND_SIGLIP;
+  float* shift_a = shifted ? F(P.o_sh_a) : nullptr;
+  float* shift_b = shifted && kind == KIND_CLIP ? F(P.o_sh_b) : nullptr;
 
   // ---- tensor maps
   // [128 x 64] boxes for the owner rows, [256 x 64] for the walked rows, [64 dims x 64] for
@@ -351,6 +366,9 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
 
   // ---- 1. inverse norms, positives' cosines, transposed copies
   PrepParams pp{};
+  pp.kind = kind;
+  pp.sc = sc;
+  pp.status = device_status;
   pp.A = A16;
   pp.B = B16;
   pp.na = Na;
@@ -386,8 +404,9 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     sp.prefix_end[k] = prefixes[k];
     sp.weight[k] = w[k];
   }
-  sp.tau_or_t = logit_scale;
-  sp.bias = bias;
+  sp.sc = sc;
+  sp.shift_a = shift_a;
+  sp.shift_b = shift_b;
   sp.rinv_a = F(P.o_rinv_a);
   sp.rinv_b = F(P.o_rinv_b);
   sp.pos_cos = F(P.o_pos);
@@ -400,7 +419,8 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
   sp.loss = loss_per_prefix;
 
   // ---- 2. forward statistics (all kinds without gradients; CLIP/ROWS with them): one pass
-  // over the grid gives every row sum and, for CLIP, every column sum
+  // over the grid gives every row sum and, for CLIP, every column sum (the max-shifted path
+  // runs a max pass first for the shifts)
   if (!siglip || !grads) {
     FwdParams fp{};
     fp.nx = Na;
@@ -409,17 +429,40 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     for (int k = 0; k < n; ++k) fp.prefix_end[k] = prefixes[k];
     fp.n_col_tiles = static_cast<int>(P.ftiles);
     fp.tiles_per_split = P.fwd_a.tiles_per_split;
-    fp.L = logit_scale * log2e;
-    fp.b2 = bias * log2e;
+    fp.sc = sc;
     fp.rinv_x = F(P.o_rinv_a);
     fp.rinv_y = F(P.o_rinv_b);
     fp.rowacc = F(P.o_acc_a);
     fp.colacc = kind == KIND_CLIP ? F(P.o_acc_b) : nullptr;
     fp.status = device_status;
+    const dim3 fgrid(static_cast<unsigned>(cdiv(Na, kTileRows)), P.fwd_a.splits, 1);
+    if (shifted) {
+      fp.mode = kFwdMax;
+      {
+        ProfScope ps(UF_KERNEL_FWD_TILE, 1, stream);
+        UF_CHECK(launch_fwd(kind, tmA, tmBf, fp, fgrid, stream));
+      }
+      MaxReduceParams mp{};
+      mp.n_prefix = n;
+      mp.na = Na;
+      mp.nb = Nb;
+      mp.rowmax = fp.rowacc;
+      mp.slots_a = 4 * P.fwd_a.splits;
+      mp.colmax = fp.colacc;
+      mp.blocks = static_cast<int>(P.rb_a);
+      mp.u = shift_a;
+      mp.v = shift_b;
+      {
+        ProfScope ps(UF_KERNEL_STATS, 1, stream);
+        UF_CHECK(launch_max_reduce(mp, stream));
+      }
+      fp.mode = kFwdShifted;
+      fp.shift_x = shift_a;
+      fp.shift_y = shift_b;
+    }
     {
       ProfScope ps(UF_KERNEL_FWD_TILE, 1, stream);
-      UF_CHECK(launch_fwd(kind, tmA, tmBf, fp, dim3(static_cast<unsigned>(cdiv(Na, kTileRows)), P.fwd_a.splits, 1),
-                          stream));
+      UF_CHECK(launch_fwd(kind, tmA, tmBf, fp, fgrid, stream));
     }
     sp.rowacc_a = fp.rowacc;
     sp.slots_a = 4 * P.fwd_a.splits;
@@ -456,13 +499,14 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     for (int k = 0; k < n; ++k) wp.prefix_end[k] = prefixes[k];
     wp.n_col_tiles = static_cast<int>(cdiv(Nb, kWgtCols));
     wp.tiles_per_split = P.wgt.tiles_per_split;
-    wp.L = logit_scale * log2e;
-    wp.b2 = bias * log2e;
+    wp.sc = sc;
+    wp.shifted = shifted ? 1 : 0;
     wp.rinv_x = F(P.o_rinv_a);
     wp.rinv_y = F(P.o_rinv_b);
     wp.alpha_x = siglip ? nullptr : F(P.o_fa);
     wp.beta_y = (kind == KIND_CLIP) ? F(P.o_fb) : nullptr;
-    for (int k = 0; k < n; ++k) wp.m_scale[k] = static_cast<float>(w[k] * logit_scale / static_cast<double>(Na));
+    for (int k = 0; k < n; ++k)  // SigLIP: w_k / N (the kernel multiplies by t); shifted: w_k
+      wp.m_scale[k] = shifted ? w[k] : static_cast<float>(w[k] / static_cast<double>(Na));
     wp.w_rows_per_prefix = P.chunk;
     wp.rowacc = siglip ? F(P.o_acc_a) : nullptr;  // the SigLIP loss sums
     wp.rowsig = (siglip && d_bias) ? F(P.o_sig) : nullptr;  // and, for the bias gradient, the sigmoid sums
@@ -527,8 +571,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
       q.prefix_end[k] = prefixes[k];
       q.weight[k] = w[k];
     }
-    q.tau_or_t = logit_scale;
-    q.bias = bias;
+    q.sc = sc;
     q.X = xa ? A16 : B16;
     q.Y = xa ? B16 : A16;
     q.rinv_x = F(xa ? P.o_rinv_a : P.o_rinv_b);
@@ -536,10 +579,14 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     q.pos_cos = F(P.o_pos);
     q.z_x = F(xa ? P.o_zr : P.o_zc);
     q.z_y = F(xa ? P.o_zc : P.o_zr);
+    q.shift_x = xa ? shift_a : shift_b;
+    q.shift_y = xa ? shift_b : shift_a;
     if (kind == KIND_ROWS) {
       q.x_is_query = xa ? 1 : 0;
       q.z_x = F(P.o_zr);
       q.z_y = F(P.o_zr);
+      q.shift_x = shift_a;
+      q.shift_y = shift_a;
     }
     q.crow = F(xa ? P.o_crow_a : P.o_crow_b);
     q.crow_slots = P.slices;
@@ -557,8 +604,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     g.na = Na;
     g.nmin = P.nmin;
     g.n_prefix = n;
-    g.scale = logit_scale;
-    g.bias = bias;
+    g.sc = sc;
     for (int k = 0; k < n; ++k) g.weight[k] = w[k];
     g.csum = d_logit_scale ? F(P.o_csum) : nullptr;
     g.rowsig = (siglip && d_bias) ? F(P.o_sig) : nullptr;

@@ -5,6 +5,10 @@
 //     m^k_ij = rho_i sigma_j dL/dcos^k_ij
 // (CLIP/ROWS: e^{s_ij - tau} rho_i sigma_j (alpha_i + beta_j) with the softmax
 // normalisers folded into alpha, beta; SigLIP: sigma(x_ij) rho_i sigma_j w_k t / N).
+// On the max-shifted path (large or device-held tau) the row and column probabilities
+// take their own shifts, m = w_k (sigma_j 2^(x + a_i) + 2^(x + log2 rho_i + b_j)), with
+// a_i = log2(rho_i alpha_i / w_k) - u_i and b_j = log2(sigma_j beta_j / w_k) - v_j from the
+// statistics (two exponentials per cell instead of one).
 // This kernel recomputes the scores tile by tile exactly like the forward pass (128 x 256
 // tcgen05 tiles, the K walk band by band into a cumulative TMEM accumulator, two
 // accumulators so the MMA of one tile overlaps the epilogue of the other) and writes m^k
@@ -135,6 +139,42 @@ __device__ __forceinline__ uint4 cells8(const float* dot, uint32_t c1, uint32_t 
   return make_uint4(packed[0], packed[1], packed[2], packed[3]);
 }
 
+// The max-shifted variant of cells8 (CLIP/ROWS): R1 = L rho_i, A = a_i, Bl = log2 rho_i,
+// wk = w_k; c2 holds b_j (CLIP).  Masks as in cells8.
+template <int KIND, bool CHECK>
+__device__ __forceinline__ uint4 cells8_shifted(const float* dot, uint32_t c1, uint32_t c2, float R1, float A, float Bl,
+                                                float wk, int col0, int ncols, int dcol, bool row_ok) {
+  const float4 s1a = ld_shared_v4f(c1), s1b = ld_shared_v4f(c1 + 16);
+  const float s1v[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
+  float s2v[8];
+  if constexpr (KIND == KIND_CLIP) {
+    const float4 s2a = ld_shared_v4f(c2), s2b = ld_shared_v4f(c2 + 16);
+    s2v[0] = s2a.x; s2v[1] = s2a.y; s2v[2] = s2a.z; s2v[3] = s2a.w;
+    s2v[4] = s2b.x; s2v[5] = s2b.y; s2v[6] = s2b.z; s2v[7] = s2b.w;
+  }
+  uint32_t packed[4];
+  const float2 r1 = make_float2(R1, R1), ra = make_float2(A, A), rb = make_float2(Bl, Bl), w2 = make_float2(wk, wk);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float2 s1 = make_float2(s1v[j], s1v[j + 1]);
+    const float2 x = mul2(mul2(r1, s1), make_float2(dot[j], dot[j + 1]));
+    const float2 t1 = add2(x, ra);
+    float2 m = mul2(s1, make_float2(ex2_approx(t1.x), ex2_approx(t1.y)));
+    if constexpr (KIND == KIND_CLIP) {
+      const float2 t2 = add2(add2(x, make_float2(s2v[j], s2v[j + 1])), rb);
+      m = add2(m, make_float2(ex2_approx(t2.x), ex2_approx(t2.y)));
+    }
+    m = mul2(m, w2);
+    if constexpr (CHECK) {
+      const int col = col0 + j;
+      if (!(row_ok && col < ncols && col != dcol)) m.x = 0.f;
+      if (!(row_ok && col + 1 < ncols && col + 1 != dcol)) m.y = 0.f;
+    }
+    packed[j / 2] = pack_bf16x2(m.x, m.y);
+  }
+  return make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
 // Tiles in pairs (t even in accumulator 0, t + 1 in accumulator 1), band by band,
 // alternating within a pair.  Step s -> (tile, band); producer, MMA and epilogue all walk it.
 struct Schedule {
@@ -150,7 +190,7 @@ struct Schedule {
   }
 };
 
-template <int KIND>
+template <int KIND, bool SHIFTED>
 __global__ void __launch_bounds__(kThreads, 1)
     wgt_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                const __grid_constant__ CUtensorMap tm_w, const WgtParams p) {
@@ -304,6 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_alpha = (row_ok && p.alpha_x) ? p.alpha_x[static_cast<int64_t>(k) * p.nx + gi] : 0.f;
     };
     if (T > 0) load_row(0);
+    const float L = p.sc.t() * 1.4426950408889634f;
+    const float b2 = p.sc.b() * 1.4426950408889634f;
+    const float t_sc = p.sc.t();
     const int64_t slot_off = static_cast<int64_t>(split * 4 + cq) * n * p.nx + gi;
     const float siglip_loss = (KIND == KIND_SIGLIP && p.rowacc) ? 1.f : 0.f;
     const int64_t wrow = static_cast<int64_t>(il0) + q * 32;  // this warp's first row in the weight array
@@ -329,13 +372,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kMaxPrefix; ++kk)
             if (kk == k) ms = p.m_scale[kk];
-          R2 = rho * ms;  // rho_i w_k t / N
+          R2 = rho * ms * t_sc;  // rho_i w_k t / N
           R3 = siglip_loss;
+        } else if constexpr (SHIFTED) {
+          R2 = n_alpha;          // a_i
+          R3 = lg2_approx(rho);  // log2 rho_i
         } else {
-          R2 = n_alpha;   // rho_i alpha_i
+          R2 = n_alpha;          // rho_i alpha_i
           R3 = rho;
         }
-        const float R1 = p.L * rho;
+        float wk = 0.f;
+        if constexpr (SHIFTED) {
+#pragma unroll
+          for (int kk = 0; kk < kMaxPrefix; ++kk)
+            if (kk == k) wk = p.m_scale[kk];
+        }
+        const float R1 = L * rho;
         load_row(b + 1 < n ? b + 1 : 0);
         for (int u = 0; u < width; ++u) {
           const int t = tp + u;
@@ -366,17 +418,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) bulk_wait_read0();
           __syncwarp();
           float2 al = make_float2(0.f, 0.f);
-          if (check) {
+          if constexpr (SHIFTED) {
+            if (check) {
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                st_shared_v4(stage_row + ((ch ^ swz) << 4),
+                             cells8_shifted<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, wk,
+                                                        cq * 64 + ch * 8, ncols, diag_col, row_ok));
+            } else {
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                st_shared_v4(stage_row + ((ch ^ swz) << 4),
+                             cells8_shifted<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, wk, 0,
+                                                         0, 0, true));
+            }
+          } else if (check) {
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
               st_shared_v4(stage_row + ((ch ^ swz) << 4),
-                           cells8<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, p.L, p.b2,
+                           cells8<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, L, b2,
                                               cq * 64 + ch * 8, ncols, diag_col, row_ok, al));
           } else {
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
               st_shared_v4(stage_row + ((ch ^ swz) << 4),
-                           cells8<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, p.L, p.b2, 0, 0,
+                           cells8<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, L, b2, 0, 0,
                                                0, true, al));
           }
           fence_proxy_async_smem();
@@ -414,28 +480,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int KIND>
+template <int KIND, bool SHIFTED>
 static cudaError_t setup_one() {
-  return cudaFuncSetAttribute(wgt_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  return cudaFuncSetAttribute(wgt_kernel<KIND, SHIFTED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 }  // namespace wgt
 
 cudaError_t wgt_kernel_setup() {
   cudaError_t e;
-  if ((e = wgt::setup_one<KIND_CLIP>()) != cudaSuccess) return e;
-  if ((e = wgt::setup_one<KIND_SIGLIP>()) != cudaSuccess) return e;
-  return wgt::setup_one<KIND_ROWS>();
+  if ((e = wgt::setup_one<KIND_CLIP, false>()) != cudaSuccess) return e;
+  if ((e = wgt::setup_one<KIND_CLIP, true>()) != cudaSuccess) return e;
+  if ((e = wgt::setup_one<KIND_SIGLIP, false>()) != cudaSuccess) return e;
+  if ((e = wgt::setup_one<KIND_ROWS, false>()) != cudaSuccess) return e;
+  return wgt::setup_one<KIND_ROWS, true>();
 }
 
 cudaError_t launch_wgt(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const CUtensorMap& tm_w,
                        const WgtParams& p, dim3 grid, cudaStream_t stream) {
-  if (kind == KIND_CLIP)
-    wgt::wgt_kernel<KIND_CLIP><<<grid, wgt::kThreads, wgt::smem_bytes, stream>>>(tm_x, tm_y, tm_w, p);
-  else if (kind == KIND_SIGLIP)
-    wgt::wgt_kernel<KIND_SIGLIP><<<grid, wgt::kThreads, wgt::smem_bytes, stream>>>(tm_x, tm_y, tm_w, p);
-  else
-    wgt::wgt_kernel<KIND_ROWS><<<grid, wgt::kThreads, wgt::smem_bytes, stream>>>(tm_x, tm_y, tm_w, p);
+  using wgt::wgt_kernel;
+  constexpr int T = wgt::kThreads, S = wgt::smem_bytes;
+  if (kind == KIND_SIGLIP && p.shifted) return cudaErrorInvalidValue;
+  if (kind == KIND_CLIP) {
+    if (p.shifted) wgt_kernel<KIND_CLIP, true><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
+    else wgt_kernel<KIND_CLIP, false><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
+  } else if (kind == KIND_SIGLIP) {
+    wgt_kernel<KIND_SIGLIP, false><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
+  } else {
+    if (p.shifted) wgt_kernel<KIND_ROWS, true><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
+    else wgt_kernel<KIND_ROWS, false><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
+  }
   return cudaGetLastError();
 }
 

@@ -47,11 +47,13 @@ extern "C" {
 #endif
 
 /* Status codes.  UF_DEVICE_TIMEOUT is only ever written to *device_status by a kernel
- * whose bounded wait ran out; the host-side call itself never returns it. */
+ * whose bounded wait ran out; the host-side call itself never returns it.  A kernel also
+ * writes UF_INVALID_ARGUMENT there when a logit scale or bias that it reads from device
+ * memory (uf_contrastive_fwd_bwd_ex) is out of range. */
 typedef enum uf_status {
   UF_OK = 0,
   UF_INVALID_ARGUMENT = 1,    /* null pointer, bad size, misaligned pointer, bad prefix ladder */
-  UF_UNSUPPORTED = 2,         /* valid request this build does not implement (e.g. scale > 40) */
+  UF_UNSUPPORTED = 2,         /* valid request this build does not implement (e.g. scale > 256) */
   UF_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < uf_contrastive_workspace_min(...) */
   UF_CUDA_ERROR = 4,          /* a CUDA runtime call or kernel launch failed */
   UF_DEVICE_TIMEOUT = 5       /* a kernel gave up a bounded wait (read from *device_status) */
@@ -104,9 +106,11 @@ UF_API size_t uf_contrastive_workspace_min(int64_t Na, int64_t Nb, int D, const 
  *   prefixes        host, n_prefix strictly increasing multiples of 64, last <= D.
  *   n_prefix        1..8.
  *   kind            a uf_loss_kind_t.
- *   logit_scale     CLIP/ROWS: tau in s = tau * cos, 0 < tau <= 40 (the forward uses the
- *                   fixed shift s - tau, exact while e^{-2 tau} is a normal float; larger
- *                   tau returns UF_UNSUPPORTED).  SigLIP: t in x = t cos + b, |t| + |b| <= 80.
+ *   logit_scale     CLIP/ROWS: tau in s = tau * cos, 0 < tau <= 256 (larger tau returns
+ *                   UF_UNSUPPORTED).  Up to tau = 40 the softmax sums use the fixed shift
+ *                   s - tau (every term stays a normal float); above it they take each
+ *                   row's and column's largest logit as its shift, found by one more pass
+ *                   over the scores.  SigLIP: t in x = t cos + b, |t| + |b| <= 80.
  *   bias            SigLIP b; ignored otherwise.
  *   prefix_weights  host, n_prefix weights w_p of the gradient, or NULL for all 1.
  *   loss_per_prefix device fp32 [n_prefix]: the unweighted L_p.
@@ -134,10 +138,18 @@ UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t 
                                    size_t workspace_bytes, int* device_status, void* stream);
 
 /*
- * uf_contrastive_fwd_bwd that also differentiates the weighted loss sum_p w_p L_p with
- * respect to its two scalar parameters, which training learns (blog post "Scaling-Up
- * Contrastive Learning over NVLink Multicast", section "One Set or Two": SigLIP's learned
- * temperature t and bias b; CLIP's logit scale likewise):
+ * uf_contrastive_fwd_bwd for a loss whose two scalar parameters are learned (blog post
+ * "Scaling-Up Contrastive Learning over NVLink Multicast", section "One Set or Two":
+ * SigLIP's learned temperature t and bias b; CLIP's logit scale likewise).  It can read
+ * them from device memory and differentiates the weighted loss sum_p w_p L_p in them:
+ *   logit_scale_dev device fp32 scalar or NULL.  When given, the kernels read the logit
+ *                   scale there when they run (logit_scale is ignored), so a CUDA graph
+ *                   captured once follows a scale that the optimizer updates in place.
+ *                   CLIP/ROWS then always take the max-shifted statistics (the host cannot
+ *                   pick the fixed shift for a value it does not see).  A value outside
+ *                   the range logit_scale allows makes the first kernel store
+ *                   UF_INVALID_ARGUMENT in *device_status; the outputs are then undefined.
+ *   bias_dev        device fp32 scalar or NULL: the same for bias (SigLIP).
  *   d_logit_scale   device fp32 scalar or NULL: dL/d(logit_scale) (tau for CLIP / ROWS,
  *                   t for SigLIP), computed as (1 / logit_scale) sum_ij dL/dcos_ij cos_ij
  *                   from the backward's row scalars; SigLIP with logit_scale == 0 returns
@@ -145,12 +157,14 @@ UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t 
  *   d_bias          device fp32 scalar or NULL: dL/db for SigLIP, from the per-row sums of
  *                   sigmoid(x_ij) over the negatives and the positives' sigmoid(-x_ii);
  *                   written 0 for CLIP and ROWS.
- * Both need the backward (dA and dB non-NULL), else UF_INVALID_ARGUMENT.  Every other
- * argument means what it means in uf_contrastive_fwd_bwd, which is this call with both NULL.
+ * d_logit_scale and d_bias need the backward (dA and dB non-NULL), else
+ * UF_INVALID_ARGUMENT.  Every other argument means what it means in
+ * uf_contrastive_fwd_bwd, which is this call with the four new pointers NULL.
  */
 UF_API uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
                                       const int* prefixes, int n_prefix, int kind, float logit_scale,
-                                      float bias, const float* prefix_weights, float* loss_per_prefix,
+                                      float bias, const float* logit_scale_dev, const float* bias_dev,
+                                      const float* prefix_weights, float* loss_per_prefix,
                                       float* row_terms, float* col_terms, float* dA, float* dB,
                                       float* d_logit_scale, float* d_bias, void* workspace,
                                       size_t workspace_bytes, int* device_status, void* stream);

@@ -112,7 +112,7 @@ def test_argument_errors_are_found_on_the_host(lib):
     assert _call(logit_scale=-1.0) == INV
     assert _call(logit_scale=float("nan")) == INV
     assert _call(prefix_weights=[1, 1, float("inf"), 1, 1]) == INV
-    assert _call(logit_scale=100.0) == UNS            # beyond the fixed-shift range
+    assert _call(logit_scale=300.0) == UNS            # beyond the largest supported scale (256)
     assert _call(kind=1, logit_scale=70.0, bias=-20.0) == UNS
     assert _call(workspace_bytes=1024) == WS
 
@@ -133,8 +133,8 @@ def test_missing_library_fails_loudly(tmp_path):
 
 def _call_ex(d_logit_scale=FAKE, d_bias=FAKE, **kw):
     args = dict(A=FAKE, B=FAKE, Na=256, Nb=256, D=1024, prefixes=LADDER, kind=0, logit_scale=1 / 0.07, bias=0.0,
-                prefix_weights=None, loss_per_prefix=FAKE, row_terms=None, col_terms=None, dA=FAKE, dB=FAKE,
-                d_logit_scale=d_logit_scale, d_bias=d_bias, workspace=FAKE, workspace_bytes=1 << 40,
+                logit_scale_dev=None, bias_dev=None, prefix_weights=None, loss_per_prefix=FAKE, row_terms=None,
+                col_terms=None, dA=FAKE, dB=FAKE, d_logit_scale=d_logit_scale, d_bias=d_bias, workspace=FAKE, workspace_bytes=1 << 40,
                 device_status=None, stream=None)
     args.update(kw)
     return binding.uf_contrastive_fwd_bwd_ex(**args)
@@ -150,7 +150,7 @@ def test_scale_gradient_argument_errors_are_found_on_the_host(lib):
     assert _call_ex(kind=1, logit_scale=0.0, bias=0.0, d_logit_scale=None) != UNS  # the bias alone is fine
     # the same checks as the plain entry point still apply
     assert _call_ex(Nb=255) == INV
-    assert _call_ex(logit_scale=100.0) == UNS
+    assert _call_ex(logit_scale=300.0) == UNS
     # the workspace needed is the same with or without the scalar gradients
     need = binding.uf_contrastive_workspace_min(256, 256, 1024, LADDER, 1, 1)
     assert _call_ex(kind=1, logit_scale=10.0, bias=-10.0, workspace_bytes=need - 256) == 3
@@ -163,3 +163,21 @@ def test_valid_scale_gradient_call_without_gpu_reports_cuda_error(lib):
         pytest.skip("a GPU is present")
     assert _call_ex() == 4
     assert _call_ex(kind=1, logit_scale=10.0, bias=-10.0) == 4
+
+
+def test_device_scalars_are_checked_on_the_host_only_for_alignment(lib):
+    INV, CUDA = 1, 4
+    assert _call_ex(logit_scale_dev=FAKE + 2) == INV
+    assert _call_ex(bias_dev=FAKE + 1) == INV
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # a host value that would be refused is ignored when the device holds the scalar: the
+    # call gets as far as the first CUDA call
+    assert _call_ex(logit_scale=float("nan"), logit_scale_dev=FAKE) == CUDA
+    assert _call_ex(logit_scale=1000.0, logit_scale_dev=FAKE) == CUDA
+    assert _call_ex(kind=1, logit_scale=70.0, bias=-20.0, bias_dev=FAKE) == CUDA
+    # large host scales take the max-shifted path instead of being refused
+    assert _call_ex(logit_scale=100.0) == CUDA
+    assert _call_ex(logit_scale=256.0) == CUDA
