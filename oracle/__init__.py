@@ -16,4 +16,5 @@ from .ref import (  # noqa: F401
     row_terms_sampled,
     grad_rows,
     scale_grads,
+    label_matrix,
 )

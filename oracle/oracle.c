@@ -17,8 +17,13 @@
  *            logits s = scale * cos, positives on the diagonal (blog, "One Set or
  *            Two": CLIP turns each row of cosines into a softmax over the batch);
  *     SIGLIP pairwise sigmoid: L = -(1/N) sum_i sum_j log sigmoid(z_ij (t cos + b)),
- *            z = +1 on the diagonal, -1 elsewhere (blog, "One Set or Two", the
- *            SigLIP equation);
+ *            N the rows of A, z = +1 for a positive pair and -1 for every negative
+ *            (blog, "One Set or Two", the SigLIP equation).  The positives are the
+ *            diagonal cells (i, i), i < Na, unless a label matrix names them (the
+ *            *_labels entry points: Z[i * Nb + j] != 0 marks (i, j) positive; a row may
+ *            have several positives or none).  Nb >= Na: the columns past Na are
+ *            extra negatives (the blog's "explicit hard negatives ... gathered as
+ *            extra band columns", section "Scaling-Up");
  *     ROWS   row-direction InfoNCE: L = mean_{i<Nq} CE(row i) over all Nk keys,
  *            the positive of query i being key i.
  *   Gradients are taken by the chain rule, prefix by prefix, and summed with the
@@ -76,10 +81,15 @@ static int check_args(int kind, int64_t Na, int64_t Nb, int D, const int* prefix
     if (prefixes[k] <= 0 || prefixes[k] > D) return -1;
     if (k && prefixes[k] <= prefixes[k - 1]) return -1;
   }
-  if ((kind == ORC_CLIP || kind == ORC_SIGLIP) && Na != Nb) return -1;
-  if (kind == ORC_ROWS && Nb < Na) return -1;
+  if (kind == ORC_CLIP && Na != Nb) return -1;
+  if ((kind == ORC_ROWS || kind == ORC_SIGLIP) && Nb < Na) return -1;
   if (kind < 0 || kind > 2) return -1;
   return 0;
+}
+
+/* Is (i, j) a positive pair?  The label matrix when there is one, else the diagonal. */
+static int positive(const unsigned char* Z, int64_t Nb, int64_t i, int64_t j) {
+  return Z ? Z[i * Nb + j] != 0 : i == j;
 }
 
 /*
@@ -93,10 +103,12 @@ static int check_args(int kind, int64_t Na, int64_t Nb, int D, const int* prefix
  *                      ROWS: 0
  * Returns 0, or -1 on bad arguments, -2 when out of memory.
  */
-int orc_fwd_bwd_f64(int kind, const double* A, const double* B, int64_t Na, int64_t Nb, int D,
-                    const int* prefixes, int n, double scale, double bias, const double* weights,
-                    double* loss, double* dA, double* dB, double* row_terms, double* col_terms) {
+static int fwd_bwd(int kind, const double* A, const double* B, int64_t Na, int64_t Nb, int D,
+                   const int* prefixes, int n, double scale, double bias, const double* weights,
+                   const unsigned char* Z, double* loss, double* dA, double* dB, double* row_terms,
+                   double* col_terms) {
   if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
+  if (Z && kind != ORC_SIGLIP) return -1;
   double* C = (double*)malloc((size_t)Na * Nb * sizeof(double));  /* cosines */
   double* G = (double*)malloc((size_t)Na * Nb * sizeof(double));  /* dL/dcos */
   double* ra = (double*)malloc((size_t)Na * sizeof(double));
@@ -194,13 +206,14 @@ int orc_fwd_bwd_f64(int kind, const double* A, const double* B, int64_t Na, int6
       for (int64_t i = 0; i < Na; ++i)
         for (int64_t j = 0; j < Nb; ++j) {
           double x = t * C[i * Nb + j] + b;
-          double z = (i == j) ? 1.0 : -1.0;
+          const int pos = positive(Z, Nb, i, j);
+          double z = pos ? 1.0 : -1.0;
           double l = softplus(-z * x); /* -log sigmoid(z x) */
           L += l;
           if (row_terms) row_terms[(int64_t)k * Na + i] += l;
           if (col_terms) col_terms[(int64_t)k * Nb + j] += l;
           /* d/dx softplus(-z x) = -z sigmoid(-z x) = sigmoid(x) - [z == +1] */
-          G[i * Nb + j] = t * (sigmoid(x) - (i == j ? 1.0 : 0.0)) / N;
+          G[i * Nb + j] = t * (sigmoid(x) - (pos ? 1.0 : 0.0)) / N;
         }
       L /= N;
     }
@@ -236,19 +249,53 @@ int orc_fwd_bwd_f64(int kind, const double* A, const double* B, int64_t Na, int6
   return 0;
 }
 
+int orc_fwd_bwd_f64(int kind, const double* A, const double* B, int64_t Na, int64_t Nb, int D,
+                    const int* prefixes, int n, double scale, double bias, const double* weights,
+                    double* loss, double* dA, double* dB, double* row_terms, double* col_terms) {
+  return fwd_bwd(kind, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, NULL, loss, dA, dB, row_terms,
+                 col_terms);
+}
+
+/* SIGLIP with the positives named by the label matrix Z (Na x Nb bytes, nonzero = positive). */
+int orc_fwd_bwd_labels_f64(const double* A, const double* B, int64_t Na, int64_t Nb, int D,
+                           const int* prefixes, int n, double scale, double bias, const double* weights,
+                           const unsigned char* Z, double* loss, double* dA, double* dB, double* row_terms,
+                           double* col_terms) {
+  if (!Z) return -1;
+  return fwd_bwd(ORC_SIGLIP, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, Z, loss, dA, dB, row_terms,
+                 col_terms);
+}
+
 /* The same on bf16 inputs (the form every test and the library consume): widen, then compute. */
-int orc_fwd_bwd(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
-                const int* prefixes, int n, double scale, double bias, const double* weights,
-                double* loss, double* dA, double* dB, double* row_terms, double* col_terms) {
+static int fwd_bwd_bf16(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
+                        const int* prefixes, int n, double scale, double bias, const double* weights,
+                        const unsigned char* Z, double* loss, double* dA, double* dB, double* row_terms,
+                        double* col_terms) {
   if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
   double* A = widen_matrix(A16, Na, D);
   double* B = widen_matrix(B16, Nb, D);
-  int rc = (A && B) ? orc_fwd_bwd_f64(kind, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, loss,
-                                      dA, dB, row_terms, col_terms)
+  int rc = (A && B) ? fwd_bwd(kind, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, Z, loss, dA, dB,
+                              row_terms, col_terms)
                     : -2;
   free(A);
   free(B);
   return rc;
+}
+
+int orc_fwd_bwd(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
+                const int* prefixes, int n, double scale, double bias, const double* weights,
+                double* loss, double* dA, double* dB, double* row_terms, double* col_terms) {
+  return fwd_bwd_bf16(kind, A16, B16, Na, Nb, D, prefixes, n, scale, bias, weights, NULL, loss, dA, dB,
+                      row_terms, col_terms);
+}
+
+int orc_fwd_bwd_labels(const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
+                       const int* prefixes, int n, double scale, double bias, const double* weights,
+                       const unsigned char* Z, double* loss, double* dA, double* dB, double* row_terms,
+                       double* col_terms) {
+  if (!Z) return -1;
+  return fwd_bwd_bf16(ORC_SIGLIP, A16, B16, Na, Nb, D, prefixes, n, scale, bias, weights, Z, loss, dA, dB,
+                      row_terms, col_terms);
 }
 
 /*
@@ -259,14 +306,15 @@ int orc_fwd_bwd(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, 
  *          Prow / Pcol the softmax of tau * cos over the row / the column;
  *   ROWS   dL_k/dtau = (1/Nq) sum_i (sum_j Prow_ij cos_ij - cos_ii);
  *   SIGLIP with x = t cos + b and d/dx softplus(-z x) = sigmoid(x) - [z = +1]:
- *          dL_k/dt = (1/N) sum_ij (sigmoid(x_ij) - [i = j]) cos_ij,
- *          dL_k/db = (1/N) sum_ij (sigmoid(x_ij) - [i = j]);  dbias = 0 for CLIP / ROWS.
+ *          dL_k/dt = (1/N) sum_ij (sigmoid(x_ij) - [(i, j) positive]) cos_ij,
+ *          dL_k/db = (1/N) sum_ij (sigmoid(x_ij) - [(i, j) positive]);  dbias = 0 for CLIP / ROWS.
  * Returns 0, or -1 on bad arguments, -2 when out of memory.
  */
-int orc_scale_grads_f64(int kind, const double* A, const double* B, int64_t Na, int64_t Nb, int D,
-                        const int* prefixes, int n, double scale, double bias, const double* weights,
-                        double* dscale, double* dbias) {
+static int scale_grads(int kind, const double* A, const double* B, int64_t Na, int64_t Nb, int D,
+                       const int* prefixes, int n, double scale, double bias, const double* weights,
+                       const unsigned char* Z, double* dscale, double* dbias) {
   if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
+  if (Z && kind != ORC_SIGLIP) return -1;
   double* C = (double*)malloc((size_t)Na * Nb * sizeof(double));
   double* ra = (double*)malloc((size_t)Na * sizeof(double));
   double* rb = (double*)malloc((size_t)Nb * sizeof(double));
@@ -321,7 +369,7 @@ int orc_scale_grads_f64(int kind, const double* A, const double* B, int64_t Na, 
       const double t = scale, N = (double)Na;
       for (int64_t i = 0; i < Na; ++i)
         for (int64_t j = 0; j < Nb; ++j) {
-          const double g = sigmoid(t * C[i * Nb + j] + bias) - (i == j ? 1.0 : 0.0);
+          const double g = sigmoid(t * C[i * Nb + j] + bias) - (positive(Z, Nb, i, j) ? 1.0 : 0.0);
           gk += g * C[i * Nb + j];
           bk += g;
         }
@@ -337,17 +385,43 @@ int orc_scale_grads_f64(int kind, const double* A, const double* B, int64_t Na, 
   return 0;
 }
 
-int orc_scale_grads(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
-                    const int* prefixes, int n, double scale, double bias, const double* weights,
-                    double* dscale, double* dbias) {
+int orc_scale_grads_f64(int kind, const double* A, const double* B, int64_t Na, int64_t Nb, int D,
+                        const int* prefixes, int n, double scale, double bias, const double* weights,
+                        double* dscale, double* dbias) {
+  return scale_grads(kind, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, NULL, dscale, dbias);
+}
+
+int orc_scale_grads_labels_f64(const double* A, const double* B, int64_t Na, int64_t Nb, int D,
+                               const int* prefixes, int n, double scale, double bias, const double* weights,
+                               const unsigned char* Z, double* dscale, double* dbias) {
+  if (!Z) return -1;
+  return scale_grads(ORC_SIGLIP, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, Z, dscale, dbias);
+}
+
+static int scale_grads_bf16(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
+                            const int* prefixes, int n, double scale, double bias, const double* weights,
+                            const unsigned char* Z, double* dscale, double* dbias) {
   if (check_args(kind, Na, Nb, D, prefixes, n)) return -1;
   double* A = widen_matrix(A16, Na, D);
   double* B = widen_matrix(B16, Nb, D);
-  int rc = (A && B) ? orc_scale_grads_f64(kind, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, dscale, dbias)
+  int rc = (A && B) ? scale_grads(kind, A, B, Na, Nb, D, prefixes, n, scale, bias, weights, Z, dscale, dbias)
                     : -2;
   free(A);
   free(B);
   return rc;
+}
+
+int orc_scale_grads(int kind, const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
+                    const int* prefixes, int n, double scale, double bias, const double* weights,
+                    double* dscale, double* dbias) {
+  return scale_grads_bf16(kind, A16, B16, Na, Nb, D, prefixes, n, scale, bias, weights, NULL, dscale, dbias);
+}
+
+int orc_scale_grads_labels(const uint16_t* A16, const uint16_t* B16, int64_t Na, int64_t Nb, int D,
+                           const int* prefixes, int n, double scale, double bias, const double* weights,
+                           const unsigned char* Z, double* dscale, double* dbias) {
+  if (!Z) return -1;
+  return scale_grads_bf16(ORC_SIGLIP, A16, B16, Na, Nb, D, prefixes, n, scale, bias, weights, Z, dscale, dbias);
 }
 
 /*

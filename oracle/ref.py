@@ -49,8 +49,16 @@ def _bind(path):
     lib.orc_scale_grads.argtypes = [ctypes.c_int, P, P, i64, i64, ctypes.c_int, P, ctypes.c_int,
                                     ctypes.c_double, ctypes.c_double, P, P, P]
     lib.orc_scale_grads_f64.argtypes = lib.orc_scale_grads.argtypes
+    # SigLIP with a label matrix: the same arguments without the kind, the labels after the weights
+    lib.orc_fwd_bwd_labels.argtypes = [P, P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_double,
+                                       ctypes.c_double, P, P, P, P, P, P, P]
+    lib.orc_fwd_bwd_labels_f64.argtypes = lib.orc_fwd_bwd_labels.argtypes
+    lib.orc_scale_grads_labels.argtypes = [P, P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_double,
+                                           ctypes.c_double, P, P, P, P]
+    lib.orc_scale_grads_labels_f64.argtypes = lib.orc_scale_grads_labels.argtypes
     for f in (lib.orc_fwd_bwd, lib.orc_fwd_bwd_f64, lib.orc_row_stats, lib.orc_grad_rows, lib.orc_scale_grads,
-              lib.orc_scale_grads_f64):
+              lib.orc_scale_grads_f64, lib.orc_fwd_bwd_labels, lib.orc_fwd_bwd_labels_f64,
+              lib.orc_scale_grads_labels, lib.orc_scale_grads_labels_f64):
         f.restype = ctypes.c_int
     return lib
 
@@ -89,19 +97,45 @@ def _prefix_array(prefixes):
     return np.ascontiguousarray(np.asarray(prefixes, dtype=np.int32))
 
 
-def fwd_bwd(kind, A, B, prefixes, scale, bias=0.0, weights=None, grads=True):
+def label_matrix(labels, Na, Nb):
+    """Dense Na x Nb uint8 label matrix (1 = positive pair) from a boolean matrix or from
+    CSR positive lists ``(offsets, ids)`` (row i's positives are ids[offsets[i]:offsets[i+1]])."""
+    if isinstance(labels, tuple):
+        offsets, ids = (np.asarray(x, np.int64) for x in labels)
+        if offsets.shape != (Na + 1,) or offsets[0] != 0 or np.any(np.diff(offsets) < 0):
+            raise ValueError("bad CSR offsets")
+        if ids.size != offsets[-1] or (ids.size and (ids.min() < 0 or ids.max() >= Nb)):
+            raise ValueError("bad CSR ids")
+        Z = np.zeros((Na, Nb), np.uint8)
+        rows = np.repeat(np.arange(Na), np.diff(offsets))
+        Z[rows, ids] = 1
+        return Z
+    Z = np.ascontiguousarray(np.asarray(labels) != 0, dtype=np.uint8)
+    if Z.shape != (Na, Nb):
+        raise ValueError("label matrix must be Na x Nb")
+    return Z
+
+
+def fwd_bwd(kind, A, B, prefixes, scale, bias=0.0, weights=None, grads=True, labels=None):
     """Full float64 forward and backward.
 
     A and B are bf16 bit patterns (uint16), or float64 arrays (used by the
-    finite-difference pins, which need continuous inputs).
+    finite-difference pins, which need continuous inputs).  ``labels`` (SigLIP only): the
+    positive pairs, as for ``label_matrix``; by default the diagonal cells (i, i), i < Na.
     Returns dict(loss=[n], dA=(Na,D), dB=(Nb,D), row_terms=(n,Na), col_terms=(n,Nb)).
     """
     A, B = np.ascontiguousarray(A), np.ascontiguousarray(B)
-    if A.dtype == np.float64 and B.dtype == np.float64:
-        fn = _load().orc_fwd_bwd_f64
-    else:
+    f64 = A.dtype == np.float64 and B.dtype == np.float64
+    if not f64:
         A, B = _bits(A), _bits(B)
-        fn = _load().orc_fwd_bwd
+    if labels is not None:
+        if kind != "siglip":
+            raise ValueError("label matrices are defined for SigLIP only")
+        Z = label_matrix(labels, A.shape[0], B.shape[0])
+        lab = _load().orc_fwd_bwd_labels_f64 if f64 else _load().orc_fwd_bwd_labels
+        fn = lambda _k, *a: lab(*a[:10], _ptr(Z), *a[10:])  # noqa: E731
+    else:
+        fn = _load().orc_fwd_bwd_f64 if f64 else _load().orc_fwd_bwd
     Na, D = A.shape
     Nb = B.shape[0]
     pre = _prefix_array(prefixes)
@@ -157,16 +191,22 @@ def grad_rows(kind, x_is_a, X, Y, prefixes, scale, bias, rows, lse_x=None, lse_y
     return out
 
 
-def scale_grads(kind, A, B, prefixes, scale, bias=0.0, weights=None):
+def scale_grads(kind, A, B, prefixes, scale, bias=0.0, weights=None, labels=None):
     """(dL/dscale, dL/dbias) of sum_k w_k L_k, from the loss definitions; see oracle.c.
 
-    A and B are bf16 bit patterns (uint16) or float64 arrays."""
+    A and B are bf16 bit patterns (uint16) or float64 arrays; ``labels`` as in fwd_bwd."""
     A, B = np.ascontiguousarray(A), np.ascontiguousarray(B)
-    if A.dtype == np.float64 and B.dtype == np.float64:
-        fn = _load().orc_scale_grads_f64
-    else:
+    f64 = A.dtype == np.float64 and B.dtype == np.float64
+    if not f64:
         A, B = _bits(A), _bits(B)
-        fn = _load().orc_scale_grads
+    if labels is not None:
+        if kind != "siglip":
+            raise ValueError("label matrices are defined for SigLIP only")
+        Z = label_matrix(labels, A.shape[0], B.shape[0])
+        lab = _load().orc_scale_grads_labels_f64 if f64 else _load().orc_scale_grads_labels
+        fn = lambda _k, *a: lab(*a[:10], _ptr(Z), *a[10:])  # noqa: E731
+    else:
+        fn = _load().orc_scale_grads_f64 if f64 else _load().orc_scale_grads
     pre = _prefix_array(prefixes)
     w = None if weights is None else np.ascontiguousarray(np.asarray(weights, np.float64))
     ds = np.zeros(1)

@@ -61,6 +61,7 @@ CASES = [
     ("siglip", 10, 10, 128, (32, 64, 128), 10.0, -10.0),
     ("rows", 6, 15, 128, (64, 128), 1 / 0.05, 0.0),
     ("clip", 9, 9, 128, (128,), 3.0, 0.0),
+    ("siglip", 6, 10, 128, (64, 128), 4.0, -2.0),   # columns past Na: extra negatives only
 ]
 
 
@@ -376,11 +377,98 @@ def test_generators_are_seeded_and_chunk_invariant():
 # The test copies oracle.c, plants one mistake by text substitution, compiles the copy
 # into a temporary library and checks that the pins above reject it.
 
+# ---- SigLIP with a label matrix (several positives per row, extra negative columns)
+
+def torch_siglip_labels(A, B, prefixes, t, b, weights, Z):
+    """Per-prefix losses, dA, dB, d/dt and d/db of sum_k w_k L_k by torch autograd (float64),
+    z = +1 where the label matrix Z is set, -1 elsewhere."""
+    At = torch.tensor(A, dtype=torch.float64, requires_grad=True)
+    Bt = torch.tensor(B, dtype=torch.float64, requires_grad=True)
+    tt = torch.tensor(t, dtype=torch.float64, requires_grad=True)
+    bt = torch.tensor(b, dtype=torch.float64, requires_grad=True)
+    z = 2.0 * torch.tensor(Z, dtype=torch.float64) - 1.0
+    losses, total = [], 0.0
+    for p, w in zip(prefixes, weights):
+        cos = F.normalize(At[:, :p], dim=1, eps=1e-30) @ F.normalize(Bt[:, :p], dim=1, eps=1e-30).T
+        L = -F.logsigmoid(z * (tt * cos + bt)).sum() / At.shape[0]
+        losses.append(L.item())
+        total = total + w * L
+    total.backward()
+    return np.array(losses), At.grad.numpy(), Bt.grad.numpy(), tt.grad.item(), bt.grad.item()
+
+
+def _labels(Na, Nb, seed):
+    """Random CSR positives: up to three per row (one row has none), ids increasing."""
+    rng = np.random.default_rng(seed)
+    offsets, ids = [0], []
+    for i in range(Na):
+        k = 0 if i == 1 else int(rng.integers(1, 4))
+        ids += sorted(rng.choice(Nb, size=k, replace=False).tolist())
+        offsets.append(len(ids))
+    return np.array(offsets), np.array(ids)
+
+
+def test_labels_match_torch_autograd():
+    rng = np.random.default_rng(23)
+    Na, Nb, D, pre = 7, 11, 128, (32, 64, 128)
+    a = rng.standard_normal((Na, D))
+    b = rng.standard_normal((Nb, D))
+    b[:Na] += a
+    A, B = _bits(a), _bits(b)
+    csr = _labels(Na, Nb, 5)
+    Z = oracle.label_matrix(csr, Na, Nb)
+    w = rng.uniform(0.5, 2.0, len(pre))
+    t, bias = 4.0, -2.0
+    got = oracle.fwd_bwd("siglip", A, B, pre, t, bias, w, labels=csr)
+    ref = torch_siglip_labels(_wide(A), _wide(B), pre, t, bias, w, Z)
+    np.testing.assert_allclose(got["loss"], ref[0], rtol=1e-12)
+    np.testing.assert_allclose(got["dA"], ref[1], rtol=1e-9, atol=1e-13)
+    np.testing.assert_allclose(got["dB"], ref[2], rtol=1e-9, atol=1e-13)
+    ds, db = oracle.scale_grads("siglip", A, B, pre, t, bias, w, labels=csr)
+    np.testing.assert_allclose([ds, db], ref[3:], rtol=1e-10, atol=1e-13)
+    # the dense matrix and the CSR lists name the same pairs
+    np.testing.assert_array_equal(oracle.fwd_bwd("siglip", A, B, pre, t, bias, w, labels=Z)["dA"], got["dA"])
+
+
+def test_diagonal_labels_equal_the_default_positives():
+    A, B = _random_pair(9, 128, 24)
+    Z = np.eye(9, dtype=np.uint8)
+    r0 = oracle.fwd_bwd("siglip", A, B, (64, 128), 10.0, -10.0)
+    r1 = oracle.fwd_bwd("siglip", A, B, (64, 128), 10.0, -10.0, labels=Z)
+    for k in r0:
+        np.testing.assert_array_equal(r0[k], r1[k])
+
+
+def test_labels_one_hot_closed_form():
+    """One-hot rows: cos_ij = [i == j], so every cell's logit is t + b (diagonal) or b, and
+    the loss counts positive / negative cells of each kind."""
+    Na, Nb, D, t, b = 5, 9, 64, 6.0, -1.5
+    E = np.eye(Nb, D)
+    A, B = _bits(E[:Na]), _bits(E)
+    csr = _labels(Na, Nb, 8)
+    Z = oracle.label_matrix(csr, Na, Nb).astype(bool)
+    sp = lambda y: np.log1p(np.exp(y))  # noqa: E731
+    diag = np.zeros((Na, Nb), bool)
+    diag[np.arange(Na), np.arange(Na)] = True
+    n_pd, n_po = (Z & diag).sum(), (Z & ~diag).sum()
+    n_nd, n_no = (~Z & diag).sum(), (~Z & ~diag).sum()
+    L = (n_pd * sp(-(t + b)) + n_nd * sp(t + b) + n_po * sp(-b) + n_no * sp(b)) / Na
+    got = oracle.fwd_bwd("siglip", A, B, (32, 64), t, b, labels=csr)
+    np.testing.assert_allclose(got["loss"], [L, L], rtol=1e-13)
+    # d/db: every cell's sigmoid minus one per positive
+    sig = lambda y: 1.0 / (1.0 + np.exp(-y))  # noqa: E731
+    dbias = 2 * (Na * sig(t + b) + (Na * Nb - Na) * sig(b) - Z.sum()) / Na
+    assert abs(oracle.scale_grads("siglip", A, B, (32, 64), t, b, labels=csr)[1] - dbias) < 1e-13
+
+
 MUTATIONS = {
     "dropped_projection_term": (
         "out[d] += g * (B[j * D + d] * rb[j] - c * A[i * D + d] * ra[i]) * ra[i];",
         "out[d] += g * (B[j * D + d] * rb[j]) * ra[i];"),
-    "siglip_label_sign": ("double z = (i == j) ? 1.0 : -1.0;", "double z = (i == j) ? -1.0 : 1.0;"),
+    "siglip_label_sign": ("double z = pos ? 1.0 : -1.0;", "double z = pos ? -1.0 : 1.0;"),
+    "labels_ignored": ("return Z ? Z[i * Nb + j] != 0 : i == j;", "return i == j;"),
+    "labels_row_shifted": ("return Z ? Z[i * Nb + j] != 0 : i == j;",
+                           "return Z ? Z[((i + 1) % (Nb < 2 ? 1 : 2)) * Nb + j] != 0 : i == j;"),
     "column_lse_transposed": (
         "for (int64_t i = 0; i < Na; ++i) s += exp(tau * C[i * Nb + j] - m);",
         "for (int64_t i = 0; i < Na; ++i) s += exp(tau * C[j * Nb + i] - m);"),
@@ -391,8 +479,9 @@ MUTATIONS = {
                       "out[d] += g * (A[i * D + d] * ra[i] - c * B[j * D + d] * rb[j]) * ra[i];"),
     "dscale_column_half_dropped": ("gk = 0.5 * (rows / (double)Na + cols / (double)Nb);",
                                    "gk = 0.5 * (rows / (double)Na);"),
-    "dscale_positive_sign": ("const double g = sigmoid(t * C[i * Nb + j] + bias) - (i == j ? 1.0 : 0.0);",
-                             "const double g = sigmoid(t * C[i * Nb + j] + bias) + (i == j ? 1.0 : 0.0);"),
+    "dscale_positive_sign": (
+        "const double g = sigmoid(t * C[i * Nb + j] + bias) - (positive(Z, Nb, i, j) ? 1.0 : 0.0);",
+        "const double g = sigmoid(t * C[i * Nb + j] + bias) + (positive(Z, Nb, i, j) ? 1.0 : 0.0);"),
 }
 
 
@@ -405,6 +494,7 @@ def _pins_pass():
         test_one_hot_orthogonal_closed_forms,
         lambda: test_scale_grads_match_autograd(*CASES[0]),
         lambda: test_scale_grads_match_autograd(*CASES[1]),
+        test_labels_match_torch_autograd,
     ]
     for c in checks:
         try:
