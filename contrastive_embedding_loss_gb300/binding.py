@@ -59,7 +59,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                            P, P]
     lib.uf_contrastive_fwd_bwd.restype = I32
     lib.uf_contrastive_fwd_bwd_ex.argtypes = [P, P, I64, I64, I32, P, I32, I32, F32, F32, P, P, P, P, P, P, P, P, P,
-                                              P, P, SZ, P, P]
+                                              P, P, P, P, SZ, P, P]
     lib.uf_contrastive_fwd_bwd_ex.restype = I32
     lib.uf_contrastive_profile.argtypes = [I32]
     lib.uf_contrastive_profile.restype = I32
@@ -116,16 +116,18 @@ def uf_contrastive_fwd_bwd(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, p
 
 
 def uf_contrastive_fwd_bwd_ex(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias, logit_scale_dev, bias_dev,
-                              prefix_weights, loss_per_prefix, row_terms, col_terms, dA, dB, d_logit_scale, d_bias,
-                              workspace, workspace_bytes, device_status, stream) -> int:
-    """Raw call with the scalars optionally on the device (``*_dev``) and their gradients
-    (``d_logit_scale``, ``d_bias``): device fp32 scalar addresses or None."""
+                              pos_offsets, pos_ids, prefix_weights, loss_per_prefix, row_terms, col_terms, dA, dB,
+                              d_logit_scale, d_bias, workspace, workspace_bytes, device_status, stream) -> int:
+    """Raw call with the scalars optionally on the device (``*_dev``), SigLIP positives as
+    device CSR lists (``pos_offsets`` int64, ``pos_ids`` int32) and the scalars' gradients
+    (``d_logit_scale``, ``d_bias``): device addresses or None."""
     pre = _int_array(list(prefixes))
     w = None if prefix_weights is None else (ctypes.c_float * len(prefix_weights))(*prefix_weights)
     return int(load().uf_contrastive_fwd_bwd_ex(A, B, int(Na), int(Nb), int(D), pre, len(prefixes), int(kind),
-                                                float(logit_scale), float(bias), logit_scale_dev, bias_dev, w,
-                                                loss_per_prefix, row_terms, col_terms, dA, dB, d_logit_scale, d_bias,
-                                                workspace, int(workspace_bytes), device_status, stream))
+                                                float(logit_scale), float(bias), logit_scale_dev, bias_dev,
+                                                pos_offsets, pos_ids, w, loss_per_prefix, row_terms, col_terms, dA,
+                                                dB, d_logit_scale, d_bias, workspace, int(workspace_bytes),
+                                                device_status, stream))
 
 
 KERNEL_GROUPS = ("prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd", "gemm")
@@ -151,9 +153,20 @@ def uf_contrastive_profile_read(group: int):
 
 # ---- torch convenience ------------------------------------------------------------
 
+_EMPTY_IDS = {}
+
+
+def _empty_ids(dev):
+    """A valid device address for an ids array with no entries (a labelled batch without positives)."""
+    import torch
+
+    if dev not in _EMPTY_IDS:
+        _EMPTY_IDS[dev] = torch.zeros(1, dtype=torch.int32, device=dev)
+    return _EMPTY_IDS[dev].data_ptr()
+
 def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), logit_scale=1 / 0.07, bias=0.0,
                         prefix_weights=None, grads=True, terms=False, workspace=None, device_status=None,
-                        stream=None, scale_grads=False):
+                        stream=None, scale_grads=False, labels=None):
     """Run the loss on bf16 CUDA tensors A (Na x D) and B (Nb x D).
 
     Returns a dict with ``loss`` (n_prefix fp32), ``dA``/``dB`` (fp32, when grads) and
@@ -161,7 +174,9 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
     fp32 tensors ``d_logit_scale`` and ``d_bias`` (the weighted loss's derivatives in
     the logit scale and the SigLIP bias; needs grads).  ``logit_scale`` and ``bias`` may
     be floats or one-element fp32 CUDA tensors; a tensor is read by the kernels when they
-    run (graph capture of a learned scale).  ``workspace`` may be a preallocated uint8
+    run (graph capture of a learned scale).  ``labels`` (SigLIP): the positive pairs as CSR
+    lists ``(offsets, ids)`` (int64 [Na + 1] and int32 CUDA tensors, or host arrays, which
+    are copied to the device) in place of the diagonal.  ``workspace`` may be a preallocated uint8
     CUDA tensor of at least ``uf_contrastive_workspace_min`` bytes (its size sets how many
     rows of backward weights the library keeps at once); by default one of the
     recommended ``uf_contrastive_workspace_size`` bytes is allocated.
@@ -204,9 +219,15 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
 
     ls_host, ls_dev = scalar(logit_scale)
     b_host, b_dev = scalar(bias)
+    offs = ids = None
+    if labels is not None:
+        offs, ids = labels
+        offs = torch.as_tensor(offs, dtype=torch.int64, device=dev).contiguous()
+        ids = torch.as_tensor(ids, dtype=torch.int32, device=dev).contiguous()
     with torch.cuda.device(dev):
         st = uf_contrastive_fwd_bwd_ex(A.data_ptr(), B.data_ptr(), Na, Nb, D, prefixes, k, ls_host, b_host, ls_dev,
-                                       b_dev, prefix_weights, out["loss"].data_ptr(), ptr(out.get("row_terms")),
+                                       b_dev, ptr(offs), ptr(ids) if ids is not None and ids.numel() else
+                                       (None if ids is None else _empty_ids(dev)), prefix_weights, out["loss"].data_ptr(), ptr(out.get("row_terms")),
                                        ptr(out.get("col_terms")), ptr(out.get("dA")), ptr(out.get("dB")),
                                        ptr(out.get("d_logit_scale")), ptr(out.get("d_bias")), workspace.data_ptr(),
                                        workspace.numel(), ptr(device_status), s.cuda_stream)

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
     const float* acc = side_a ? p.rowacc_a : p.rowacc_b;
     const int slots = side_a ? p.slots_a : p.slots_b;
     const double w = p.weight[k];
-    const bool has_pos = i < nmin;
+    const bool has_pos = p.diag_pos && i < nmin;
     const double cos_ii = has_pos ? static_cast<double>(p.pos_cos[k * nmin + i]) : 0.0;
     if (p.kind == KIND_SIGLIP) {
       if (!side_a) {
@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
       const double s = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
       // (log2 units)
       const double x_ii = tau * cos_ii + bias;
-      p.terms_a[ee] = static_cast<float>(s * 0.6931471805599453 + (has_pos ? softplus_d(-x_ii) : 0.0));
+      const double lab = p.pos_term ? static_cast<double>(p.pos_term[ee]) : 0.0;  // -sum of the positives' x
+      p.terms_a[ee] = static_cast<float>(s * 0.6931471805599453 + (has_pos ? softplus_d(-x_ii) : 0.0) + lab);
       continue;
     }
     if (p.kind == KIND_ROWS && !side_a) {
@@ -387,7 +388,9 @@ __global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams 
         double neg = 0.0;  // sum over the negatives of row i of sigmoid(x_ij), fixed slot order
         for (int sl = 0; sl < p.sig_slots; ++sl) neg += p.rowsig[(static_cast<int64_t>(sl) * n + k) * p.na + i];
         double pos = 0.0;  // the positive's share: sigmoid(x_ii) - 1 = -sigmoid(-x_ii)
-        if (i < p.nmin) {
+        if (p.lcount) {    // labelled positives were summed as negatives: -1 for each
+          pos = -static_cast<double>(p.lcount[i]);
+        } else if (i < p.nmin) {
           const double x = static_cast<double>(scale) * p.pos_cos[k * p.nmin + i] + bias;
           pos = -1.0 / (1.0 + exp(x));
         }
@@ -450,6 +453,93 @@ cudaError_t launch_max_reduce(const MaxReduceParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------ labels
+// SigLIP with explicit positives (see LabelParams).  The dense passes score every cell as
+// a negative; a positive cell differs by the label only: its loss is softplus(-x) =
+// softplus(x) - x and its gradient in x is sigmoid(x) - 1 = -sigmoid(-x).  So the loss takes
+// -x per positive (terms mode) and the positive cells' weights are rewritten with their
+// exact value before the gradient GEMMs read them (patch mode).
+__global__ void __launch_bounds__(256) labels_kernel(const LabelParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int n = p.n_prefix;
+  const bool patch = p.W != nullptr;
+  const int64_t first = patch ? p.row0 : 0, last = patch ? p.row0 + p.rows : p.na;
+  const float t = p.sc.t(), bias = p.sc.b();
+  const int pn = p.prefix_end[n - 1];
+  const int64_t total = p.offsets[p.na];  // entries of ids (the caller's promise): no read goes past it
+  for (int64_t i = first + warp_id; i < last; i += n_warps) {
+    const int64_t lo = p.offsets[i];
+    int64_t hi = p.offsets[i + 1];
+    bool bad = lo < 0 || hi < lo || hi > total;
+    if (hi > total) hi = total;
+    float xs[kMaxPrefix];
+#pragma unroll
+    for (int k = 0; k < kMaxPrefix; ++k) xs[k] = 0.f;
+    int count = 0;
+    const uint4* ra = reinterpret_cast<const uint4*>(p.A + i * p.d);
+    int prev = -1;
+    for (int64_t q = bad ? hi : lo; q < hi; ++q) {
+      const int j = p.ids[q];
+      if (j < 0 || j >= p.nb || j <= prev) {  // out of range, repeated or out of order: skipped
+        bad = true;
+        continue;
+      }
+      prev = j;
+      ++count;
+      const uint4* rb = reinterpret_cast<const uint4*>(p.B + static_cast<int64_t>(j) * p.d);
+      float dab[kMaxPrefix];
+#pragma unroll
+      for (int k = 0; k < kMaxPrefix; ++k) dab[k] = 0.f;
+      for (int ch = lane; ch * 8 < pn; ch += 32) {
+        const int b = band_of(ch * 8, p.prefix_end, n);
+        const uint4 va = __ldg(ra + ch), vb = __ldg(rb + ch);
+        const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+        float sd = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sd = fmaf(bf16_lo(wa[u]), bf16_lo(wb[u]), fmaf(bf16_hi(wa[u]), bf16_hi(wb[u]), sd));
+#pragma unroll
+        for (int k = 0; k < kMaxPrefix; ++k)
+          if (k == b) dab[k] += sd;
+      }
+      float cum = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMaxPrefix; ++k) {
+        if (k >= n) break;
+        cum += warp_sum(dab[k]);  // the prefix-k dot product, on every lane
+        const float rho = p.rinv_a[k * p.na + i], sig = p.rinv_b[k * p.nb + j];
+        const float x = t * (cum * rho * sig) + bias;
+        if (!patch) {
+          xs[k] += x;
+        } else if (lane == 0) {
+          const float m = -(1.f / (1.f + expf(x))) * rho * sig *
+                          static_cast<float>(p.weight[k] * t / static_cast<double>(p.na));
+          const __nv_bfloat16 h = __float2bfloat16_rn(m);
+          p.W[(static_cast<int64_t>(k) * p.w_rows_per_prefix + (i - p.row0)) * p.ldw + j] =
+              *reinterpret_cast<const uint16_t*>(&h);
+        }
+      }
+    }
+    if (lane == 0) {
+      if (bad && p.status) atomicExch(p.status, kStatusBadScalar);
+      if (!patch) {
+        for (int k = 0; k < n; ++k) p.pos_term[k * p.na + i] = -xs[k];
+        p.lcount[i] = static_cast<float>(count);
+      }
+    }
+  }
+}
+
+cudaError_t launch_labels(const LabelParams& p, cudaStream_t stream) {
+  const int64_t rows = p.W ? p.rows : p.na;
+  int64_t blocks = (rows * 32 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  labels_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream) {
   scale_grad_kernel<<<1, 1024, 0, stream>>>(p);
   return cudaGetLastError();
@@ -472,6 +562,7 @@ cudaError_t aux_kernels_setup() {
   if ((e = cudaFuncGetAttributes(&fa, finalize_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, scale_grad_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, max_reduce_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, labels_kernel)) != cudaSuccess) return e;
   return cudaFuncGetAttributes(&fa, norm_bwd_kernel);
 }
 

@@ -27,6 +27,8 @@
 // those maxima, so the largest term of every sum is 1 whatever the scale.
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -68,6 +70,7 @@ struct Params {
   const float* rinv_y;  // [n][ny]
   const float* shift_x; // kFwdShifted: [n][nx]
   const float* shift_y; // kFwdShifted, CLIP: [n][ny]
+  int no_diag;          // the diagonal cells are not masked (SigLIP with a label matrix)
   float* rowacc;        // [split * 4 + quarter][n][nx]
   float* colacc;        // [row block][n][ny] (CLIP) or NULL
   int* status;
@@ -428,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float R1 = rowf[k * kTileRows + r];
         const int64_t left = p.ny - j0;
         const int ncols = left < kCols ? static_cast<int>(left) : kCols;
-        const int dcol = static_cast<int>(i0 - j0) + r;  // tile column of this row's positive, if any
+        // tile column of this row's positive, if any (none when a label matrix names them)
+        const int dcol = p.no_diag ? INT_MIN : static_cast<int>(i0 - j0) + r;
         // masks are only evaluated in the few tiles that need them (padding columns, the
         // positives' diagonal, padding rows); every other tile takes the unmasked path
         const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
@@ -519,6 +523,7 @@ cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
   p.rinv_y = q.rinv_y;
   p.shift_x = q.shift_x;
   p.shift_y = q.shift_y;
+  p.no_diag = q.no_diag;
   p.rowacc = q.rowacc;
   p.colacc = q.colacc;
   p.status = q.status;

@@ -31,6 +31,7 @@ struct FwdParams {
   const float* rinv_y;
   const float* shift_x;     // kFwdShifted: u [n][nx]
   const float* shift_y;     // kFwdShifted, CLIP: v [n][ny]
+  int no_diag;              // SigLIP with a label matrix: the diagonal is not special (every cell a negative)
   float* rowacc;            // [split * 4 + column quarter][n][nx]
   float* colacc;            // [row block][n][ny] (CLIP only)
   int* status;
@@ -60,6 +61,7 @@ struct WgtParams {
   const float* rinv_y;            // [n][ny]
   const float* beta_y;            // [n][ny] sigma_j beta_j (CLIP) or NULL; shifted: log2(sigma_j beta_j / w_k) - v_j
   float m_scale[kMaxPrefix];      // SigLIP: w_k / N (times t in the kernel); shifted CLIP/ROWS: w_k
+  int no_diag;                    // SigLIP with a label matrix: weights for every cell as a negative
   int64_t w_rows_per_prefix;      // rows between prefixes in the weight array (multiple of 128)
   float* rowacc;                  // SigLIP: [split * 4 + quarter][n][nx] loss sums (log2 units), or NULL
   float* rowsig;                  // SigLIP, with rowacc: the same slots, sums of sigmoid(x_ij) over the
@@ -134,6 +136,8 @@ struct StatsParams {
   const float* pos_cos;
   const float* shift_a;    // NULL: the fixed shift tau; else the rows' shifts u [n][na] (log2 units)
   const float* shift_b;    // CLIP, with shift_a: the columns' shifts v [n][nb]
+  int diag_pos;            // 1: the diagonal cells (i, i), i < min(na, nb), are the positives
+  const float* pos_term;   // SigLIP with a label matrix: [n][na] the positives' share of the row terms, or NULL
   const float* rowacc_a;   // [slots_a][n][na]
   int slots_a;
   const float* rowacc_b;   // [slots_b][n][nb] (CLIP)
@@ -188,6 +192,7 @@ struct ScaleGradParams {
   const float* csum;       // [na]
   const float* rowsig;     // SigLIP: [slots][n][na]
   int sig_slots;
+  const float* lcount;     // SigLIP with a label matrix: [na] positives per row (else the diagonal)
   const float* pos_cos;    // [n][nmin]
   float* d_scale;          // device scalar or NULL
   float* d_bias;           // device scalar or NULL
@@ -207,5 +212,35 @@ struct MaxReduceParams {
   float* v;                // [n][nb] or NULL
 };
 cudaError_t launch_max_reduce(const MaxReduceParams& p, cudaStream_t stream);
+
+// SigLIP with a label matrix given as CSR positive lists (offsets [na + 1], ids), one warp
+// per row of A.  Every positive (i, j) gets its cosines recomputed per prefix (fp32 dot of
+// the bf16 rows) and x = t cos + b.  Entries that break the format (a row whose offsets
+// decrease, an id outside [0, nb) or not above the row's previous id) are skipped and
+// set *status = kStatusBadScalar.
+//   terms mode (W == NULL): pos_term[k][i] = -sum_j x^k_ij (the loss of a positive cell is
+//                the negative cell's minus x), lcount[i] = valid positives of row i
+//   patch mode (W != NULL): for rows [row0, row0 + rows) write the exact weight of every
+//                positive cell, bf16(-sigmoid(-x) rho sigma w_k t / N), over the negative-cell
+//                weight the weight pass stored at W[(k * w_rows_per_prefix + i - row0) * ldw + j]
+struct LabelParams {
+  const int64_t* offsets;
+  const int* ids;
+  const uint16_t* A;
+  const uint16_t* B;
+  int64_t na, nb;
+  int d, n_prefix;
+  int prefix_end[kMaxPrefix];
+  Scalars sc;
+  float weight[kMaxPrefix];
+  const float* rinv_a;
+  const float* rinv_b;
+  float* pos_term;
+  float* lcount;
+  uint16_t* W;
+  int64_t row0, rows, w_rows_per_prefix, ldw;
+  int* status;
+};
+cudaError_t launch_labels(const LabelParams& p, cudaStream_t stream);
 
 }  // namespace ufc

@@ -56,7 +56,7 @@ struct Plan {
   size_t fixed = 0;                  // bytes of everything but the weight array
   // offsets
   size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
-      o_terms_b, o_loss, o_at, o_bt, o_csum, o_sig, o_sh_a, o_sh_b, o_w, total;
+      o_terms_b, o_loss, o_at, o_bt, o_csum, o_sig, o_sh_a, o_sh_b, o_lab, o_lcount, o_w, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -67,8 +67,9 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
                Plan& P) {
   if (Na < 1 || Nb < 1 || D < 64 || D > 4096 || D % 64 != 0 || n < 1 || n > kMaxPrefix || !prefixes) return false;
   if (kind != KIND_CLIP && kind != KIND_SIGLIP && kind != KIND_ROWS) return false;
-  if ((kind == KIND_CLIP || kind == KIND_SIGLIP) && Na != Nb) return false;
-  if (kind == KIND_ROWS && Nb < Na) return false;
+  if (kind == KIND_CLIP && Na != Nb) return false;
+  // ROWS and SigLIP: the columns past Na are extra negatives (explicit hard negatives)
+  if ((kind == KIND_ROWS || kind == KIND_SIGLIP) && Nb < Na) return false;
   if (Na > (int64_t(1) << 31) || Nb > (int64_t(1) << 31)) return false;
   for (int k = 0; k < n; ++k) {
     if (prefixes[k] <= 0 || prefixes[k] % 64 != 0 || prefixes[k] > D) return false;
@@ -122,6 +123,9 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   // picks the path may live on the device)
   P.o_sh_a = take(kind != KIND_SIGLIP ? f * n * Na : 0);
   P.o_sh_b = take(kind == KIND_CLIP ? f * n * Nb : 0);
+  // SigLIP with a label matrix: the positives' share of the row terms, positives per row
+  P.o_lab = take(kind == KIND_SIGLIP ? f * n * Na : 0);
+  P.o_lcount = take(kind == KIND_SIGLIP ? f * Na : 0);
   P.fixed = o;
   P.o_w = o;
   P.chunk = 0;
@@ -278,13 +282,14 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
                                    float* col_terms, float* dA, float* dB, void* workspace, size_t workspace_bytes,
                                    int* device_status, void* stream_handle) {
   return uf_contrastive_fwd_bwd_ex(A, B, Na, Nb, D, prefixes, n_prefix, kind, logit_scale, bias, nullptr, nullptr,
-                                   prefix_weights, loss_per_prefix, row_terms, col_terms, dA, dB, nullptr, nullptr,
+                                   nullptr, nullptr, prefix_weights, loss_per_prefix, row_terms, col_terms, dA, dB, nullptr, nullptr,
                                    workspace, workspace_bytes, device_status, stream_handle);
 }
 
 uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
                                       const int* prefixes, int n_prefix, int kind, float logit_scale, float bias,
                                       const float* logit_scale_dev, const float* bias_dev,
+                                      const int64_t* pos_offsets, const int* pos_ids,
                                       const float* prefix_weights, float* loss_per_prefix, float* row_terms,
                                       float* col_terms, float* dA, float* dB, float* d_logit_scale, float* d_bias,
                                       void* workspace, size_t workspace_bytes, int* device_status,
@@ -297,6 +302,10 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
   if ((d_logit_scale && !aligned(d_logit_scale, 4)) || (d_bias && !aligned(d_bias, 4))) return UF_INVALID_ARGUMENT;
   if ((logit_scale_dev && !aligned(logit_scale_dev, 4)) || (bias_dev && !aligned(bias_dev, 4)))
     return UF_INVALID_ARGUMENT;
+  const bool labels = pos_offsets != nullptr;
+  if ((pos_offsets == nullptr) != (pos_ids == nullptr)) return UF_INVALID_ARGUMENT;
+  if (labels && (!aligned(pos_offsets, 8) || !aligned(pos_ids, 4))) return UF_INVALID_ARGUMENT;
+  if (labels && kind != KIND_SIGLIP) return UF_UNSUPPORTED;  // the pages define labelled positives for SigLIP
   Plan P;
   if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, grads, workspace_bytes, P)) return UF_INVALID_ARGUMENT;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(workspace, 256) || !aligned(loss_per_prefix, 4))
@@ -393,6 +402,32 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     UF_CHECK(launch_transpose(B16, Bt, Nb, D, P.ldb, stream));
   }
 
+  // SigLIP with a label matrix: the positives' loss terms and counts (the dense passes score
+  // every cell as a negative)
+  LabelParams lp{};
+  if (labels) {
+    lp.offsets = pos_offsets;
+    lp.ids = pos_ids;
+    lp.A = A16;
+    lp.B = B16;
+    lp.na = Na;
+    lp.nb = Nb;
+    lp.d = D;
+    lp.n_prefix = n;
+    for (int k = 0; k < n; ++k) {
+      lp.prefix_end[k] = prefixes[k];
+      lp.weight[k] = w[k];
+    }
+    lp.sc = sc;
+    lp.rinv_a = F(P.o_rinv_a);
+    lp.rinv_b = F(P.o_rinv_b);
+    lp.pos_term = F(P.o_lab);
+    lp.lcount = F(P.o_lcount);
+    lp.status = device_status;
+    ProfScope ps(UF_KERNEL_PREP, 1, stream);
+    UF_CHECK(launch_labels(lp, stream));
+  }
+
   float* terms_a = row_terms ? row_terms : F(P.o_terms_a);
   float* terms_b = col_terms ? col_terms : F(P.o_terms_b);
   StatsParams sp{};
@@ -407,6 +442,8 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
   sp.sc = sc;
   sp.shift_a = shift_a;
   sp.shift_b = shift_b;
+  sp.diag_pos = labels ? 0 : 1;
+  sp.pos_term = labels ? F(P.o_lab) : nullptr;
   sp.rinv_a = F(P.o_rinv_a);
   sp.rinv_b = F(P.o_rinv_b);
   sp.pos_cos = F(P.o_pos);
@@ -430,6 +467,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     fp.n_col_tiles = static_cast<int>(P.ftiles);
     fp.tiles_per_split = P.fwd_a.tiles_per_split;
     fp.sc = sc;
+    fp.no_diag = labels ? 1 : 0;
     fp.rinv_x = F(P.o_rinv_a);
     fp.rinv_y = F(P.o_rinv_b);
     fp.rowacc = F(P.o_acc_a);
@@ -501,6 +539,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     wp.tiles_per_split = P.wgt.tiles_per_split;
     wp.sc = sc;
     wp.shifted = shifted ? 1 : 0;
+    wp.no_diag = labels ? 1 : 0;
     wp.rinv_x = F(P.o_rinv_a);
     wp.rinv_y = F(P.o_rinv_b);
     wp.alpha_x = siglip ? nullptr : F(P.o_fa);
@@ -539,6 +578,16 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
         UF_CHECK(launch_wgt(kind, tmA, tmBf, tmWs, wp, dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), P.wgt.splits),
                             stream));
       }
+      if (labels) {  // the labelled positives' exact weights over the negative-cell ones
+        LabelParams pq = lp;
+        pq.W = W;
+        pq.row0 = r0;
+        pq.rows = rows;
+        pq.w_rows_per_prefix = P.chunk;
+        pq.ldw = P.ldw;
+        ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
+        UF_CHECK(launch_labels(pq, stream));
+      }
       ProfScope ps(UF_KERNEL_GEMM, 2, stream);
       ga.m_rows = rows;
       ga.row0 = r0;
@@ -563,7 +612,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     q.kind = kind;
     q.nx = xa ? Na : Nb;
     q.ny = xa ? Nb : Na;
-    q.nmin = P.nmin;
+    q.nmin = labels ? 0 : P.nmin;  // labelled positives went through the GEMMs with their exact weights
     q.n_total = Na;
     q.d = D;
     q.n_prefix = n;
@@ -609,6 +658,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     g.csum = d_logit_scale ? F(P.o_csum) : nullptr;
     g.rowsig = (siglip && d_bias) ? F(P.o_sig) : nullptr;
     g.sig_slots = 4 * P.wgt.splits;
+    g.lcount = labels ? F(P.o_lcount) : nullptr;
     g.pos_cos = F(P.o_pos);
     g.d_scale = d_logit_scale;
     g.d_bias = d_bias;

@@ -21,6 +21,8 @@
 // and one 64-column quarter of the tile).
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -410,7 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ncols = left < kCols ? static_cast<int>(left) : kCols;
           const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
           const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (il0 + kTileRows > p.rows);
-          const int diag_col = static_cast<int>(dtile) + r;  // tile column of this row's positive
+          // tile column of this row's positive (none when a label matrix names the positives:
+          // every cell is then written as a negative and the positives are patched afterwards)
+          const int diag_col = p.no_diag ? INT_MIN : static_cast<int>(dtile) + r;
           const uint32_t cf = colf_s + (t & 3) * kColfBytes + cq * 64 * 4;
           const uint32_t c1 = cf + (k * 2 + 0) * kCols * 4;
           const uint32_t c2 = cf + (k * 2 + 1) * kCols * 4;

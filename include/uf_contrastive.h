@@ -102,7 +102,9 @@ UF_API size_t uf_contrastive_workspace_min(int64_t Na, int64_t Nb, int D, const 
  *
  *   A, B            device, bf16, row-major Na x D and Nb x D, 16-byte aligned.
  *   Na, Nb, D       rows and width.  D is a multiple of 64 and <= 4096; Na, Nb >= 1.
- *                   CLIP and SigLIP need Na == Nb; ROWS needs Nb >= Na.
+ *                   CLIP needs Na == Nb; ROWS and SigLIP need Nb >= Na: row i < Na of A is
+ *                   paired with row i of B, and the rows of B past Na are extra negatives
+ *                   (explicit hard negatives) for every row of A.
  *   prefixes        host, n_prefix strictly increasing multiples of 64, last <= D.
  *   n_prefix        1..8.
  *   kind            a uf_loss_kind_t.
@@ -150,6 +152,17 @@ UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t 
  *                   the range logit_scale allows makes the first kernel store
  *                   UF_INVALID_ARGUMENT in *device_status; the outputs are then undefined.
  *   bias_dev        device fp32 scalar or NULL: the same for bias (SigLIP).
+ *   pos_offsets,    SigLIP only (else UF_UNSUPPORTED): the positive pairs as CSR lists on the
+ *   pos_ids         device, in place of the diagonal (blog, section "Scaling-Up": each entry
+ *                   can carry several positives and explicit hard negatives).  Row i of A
+ *                   has the positives B[pos_ids[q]] for pos_offsets[i] <= q < pos_offsets[i+1];
+ *                   every other cell is a negative (z = -1).  pos_offsets: int64 [Na + 1],
+ *                   8-byte aligned, pos_offsets[0] = 0, nondecreasing; pos_ids: int32, each
+ *                   row's ids strictly increasing in [0, Nb).  A row may have no positive.
+ *                   Entries that break these rules are skipped and make the kernels store
+ *                   UF_INVALID_ARGUMENT in *device_status (the ids array must still hold
+ *                   pos_offsets[Na] entries).  Both NULL: the diagonal (i, i), i < Na.
+ *                   The row terms then hold sum_j softplus(-z_ij x_ij) for the labels.
  *   d_logit_scale   device fp32 scalar or NULL: dL/d(logit_scale) (tau for CLIP / ROWS,
  *                   t for SigLIP), computed as (1 / logit_scale) sum_ij dL/dcos_ij cos_ij
  *                   from the backward's row scalars; SigLIP with logit_scale == 0 returns
@@ -159,11 +172,12 @@ UF_API uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t 
  *                   written 0 for CLIP and ROWS.
  * d_logit_scale and d_bias need the backward (dA and dB non-NULL), else
  * UF_INVALID_ARGUMENT.  Every other argument means what it means in
- * uf_contrastive_fwd_bwd, which is this call with the four new pointers NULL.
+ * uf_contrastive_fwd_bwd, which is this call with the six new pointers NULL.
  */
 UF_API uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
                                       const int* prefixes, int n_prefix, int kind, float logit_scale,
                                       float bias, const float* logit_scale_dev, const float* bias_dev,
+                                      const int64_t* pos_offsets, const int* pos_ids,
                                       const float* prefix_weights, float* loss_per_prefix,
                                       float* row_terms, float* col_terms, float* dA, float* dB,
                                       float* d_logit_scale, float* d_bias, void* workspace,

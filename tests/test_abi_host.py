@@ -51,6 +51,8 @@ def test_workspace_size(lib):
     # invalid requests size to 0
     assert ws(256, 255, 1024, LADDER, 0, 1) == 0      # CLIP needs Na == Nb
     assert ws(256, 100, 1024, LADDER, 2, 1) == 0      # ROWS needs Nb >= Na
+    assert ws(256, 100, 1024, LADDER, 1, 1) == 0      # so does SigLIP
+    assert ws(256, 700, 1024, LADDER, 1, 1) > 0       # SigLIP with extra negative columns
     assert ws(256, 256, 1000, LADDER, 0, 1) == 0      # D not a multiple of 64
     assert ws(256, 256, 1024, (64, 100), 0, 1) == 0   # prefix not a multiple of 64
     assert ws(256, 256, 1024, (128, 64), 0, 1) == 0   # not increasing
@@ -133,7 +135,8 @@ def test_missing_library_fails_loudly(tmp_path):
 
 def _call_ex(d_logit_scale=FAKE, d_bias=FAKE, **kw):
     args = dict(A=FAKE, B=FAKE, Na=256, Nb=256, D=1024, prefixes=LADDER, kind=0, logit_scale=1 / 0.07, bias=0.0,
-                logit_scale_dev=None, bias_dev=None, prefix_weights=None, loss_per_prefix=FAKE, row_terms=None,
+                logit_scale_dev=None, bias_dev=None, pos_offsets=None, pos_ids=None, prefix_weights=None,
+                loss_per_prefix=FAKE, row_terms=None,
                 col_terms=None, dA=FAKE, dB=FAKE, d_logit_scale=d_logit_scale, d_bias=d_bias, workspace=FAKE, workspace_bytes=1 << 40,
                 device_status=None, stream=None)
     args.update(kw)
@@ -181,3 +184,21 @@ def test_device_scalars_are_checked_on_the_host_only_for_alignment(lib):
     # large host scales take the max-shifted path instead of being refused
     assert _call_ex(logit_scale=100.0) == CUDA
     assert _call_ex(logit_scale=256.0) == CUDA
+
+
+def test_label_arguments_are_checked_on_the_host(lib):
+    INV, UNS, CUDA = 1, 2, 4
+    sig = dict(kind=1, logit_scale=10.0, bias=-10.0)
+    assert _call_ex(pos_offsets=FAKE, pos_ids=FAKE) == UNS          # CLIP: no labelled positives
+    assert _call_ex(kind=2, logit_scale=20.0, pos_offsets=FAKE, pos_ids=FAKE) == UNS
+    assert _call_ex(pos_offsets=FAKE, **sig) == INV                  # offsets and ids go together
+    assert _call_ex(pos_ids=FAKE, **sig) == INV
+    assert _call_ex(pos_offsets=FAKE + 4, pos_ids=FAKE, **sig) == INV  # int64 offsets: 8-byte aligned
+    assert _call_ex(pos_offsets=FAKE, pos_ids=FAKE + 2, **sig) == INV
+    assert _call_ex(Nb=200, **sig) == INV                            # SigLIP needs Nb >= Na
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call_ex(pos_offsets=FAKE, pos_ids=FAKE, **sig) == CUDA
+    assert _call_ex(Nb=700, **sig) == CUDA                           # extra negative columns
