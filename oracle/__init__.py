@@ -17,4 +17,5 @@ from .ref import (  # noqa: F401
     grad_rows,
     scale_grads,
     label_matrix,
+    oneset,
 )

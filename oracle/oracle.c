@@ -299,6 +299,96 @@ int orc_fwd_bwd_labels(const uint16_t* A16, const uint16_t* B16, int64_t Na, int
 }
 
 /*
+ * One-set SigLIP (blog, section "One Set or Two": the loss scores one set against itself,
+ * with the same labels for mirrored cells; an image and its caption are two rows of the
+ * set marked as a positive pair).  For the N x D set X and the N x N label matrix Z
+ * (symmetric; the diagonal is ignored):
+ *   L_k = -(1/N) sum_i sum_{j != i} log sigmoid(z_ij (t cos_ij + b)),
+ * cos_ij between x_i[:p] and x_j[:p].  Every cell depends on both of its rows, so
+ *   dX_i += w G_ij (xhat_j - cos_ij xhat_i) / |x_i|   (x_i as the first argument)
+ *   dX_j += w G_ij (xhat_i - cos_ij xhat_j) / |x_j|   (x_j as the second),
+ * G_ij = dL/dcos_ij = t (sigmoid(x_ij) - [z_ij = +1]) / N.  Also dL/dt = sum_ij G_ij cos_ij / t
+ * written as (1/N) sum (sigmoid - [z = +1]) cos, and dL/db = (1/N) sum (sigmoid - [z = +1]).
+ * row_terms[k][i] = sum_{j != i} softplus(-z_ij x_ij).  dX, row_terms, dscale, dbias may be NULL.
+ */
+int orc_oneset_f64(const double* X, int64_t N, int D, const int* prefixes, int n, double t, double b,
+                   const double* weights, const unsigned char* Z, double* loss, double* dX, double* row_terms,
+                   double* dscale, double* dbias) {
+  if (check_args(ORC_SIGLIP, N, N, D, prefixes, n) || !Z) return -1;
+  double* C = (double*)malloc((size_t)N * N * sizeof(double));
+  double* G = (double*)malloc((size_t)N * N * sizeof(double));
+  double* r = (double*)malloc((size_t)N * sizeof(double));
+  if (!C || !G || !r) {
+    free(C); free(G); free(r);
+    return -2;
+  }
+  if (dX) memset(dX, 0, (size_t)N * D * sizeof(double));
+  double ds = 0, db = 0;
+  for (int k = 0; k < n; ++k) {
+    const int p = prefixes[k];
+    const double w = weights ? weights[k] : 1.0;
+    for (int64_t i = 0; i < N; ++i) r[i] = inv_norm(X + i * D, p);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t i = 0; i < N; ++i)
+      for (int64_t j = 0; j < N; ++j) {
+        double dot = 0;
+        for (int d = 0; d < p; ++d) dot += X[i * D + d] * X[j * D + d];
+        C[i * N + j] = dot * r[i] * r[j];
+      }
+    double L = 0, gk = 0, bk = 0;
+    for (int64_t i = 0; i < N; ++i) {
+      double row = 0;
+      for (int64_t j = 0; j < N; ++j) {
+        if (j == i) { /* a row is not paired with itself */
+          G[i * N + j] = 0;
+          continue;
+        }
+        const double x = t * C[i * N + j] + b;
+        const int pos = Z[i * N + j] != 0;
+        const double zij = pos ? 1.0 : -1.0;  /* the label z_ij */
+        row += softplus(-zij * x);
+        const double g = sigmoid(x) - (pos ? 1.0 : 0.0);
+        G[i * N + j] = t * g / (double)N;
+        gk += g * C[i * N + j];
+        bk += g;
+      }
+      L += row;
+      if (row_terms) row_terms[(int64_t)k * N + i] = row;
+    }
+    loss[k] = L / (double)N;
+    ds += w * gk / (double)N;
+    db += w * bk / (double)N;
+    if (dX) {
+#pragma omp parallel for schedule(dynamic, 4)
+      for (int64_t i = 0; i < N; ++i) {
+        double* out = dX + i * D;
+        for (int64_t j = 0; j < N; ++j) {
+          /* cell (i, j) through its first argument, and cell (j, i) through its second */
+          const double g1 = w * G[i * N + j], g2 = w * G[j * N + i], c = C[i * N + j];
+          if (g1 == 0.0 && g2 == 0.0) continue;
+          for (int d = 0; d < p; ++d)
+            out[d] += (g1 + g2) * (X[j * D + d] * r[j] - c * X[i * D + d] * r[i]) * r[i];
+        }
+      }
+    }
+  }
+  if (dscale) *dscale = ds;
+  if (dbias) *dbias = db;
+  free(C); free(G); free(r);
+  return 0;
+}
+
+int orc_oneset(const uint16_t* X16, int64_t N, int D, const int* prefixes, int n, double t, double b,
+               const double* weights, const unsigned char* Z, double* loss, double* dX, double* row_terms,
+               double* dscale, double* dbias) {
+  if (check_args(ORC_SIGLIP, N, N, D, prefixes, n) || !Z) return -1;
+  double* X = widen_matrix(X16, N, D);
+  int rc = X ? orc_oneset_f64(X, N, D, prefixes, n, t, b, weights, Z, loss, dX, row_terms, dscale, dbias) : -2;
+  free(X);
+  return rc;
+}
+
+/*
  * Derivatives of the weighted total sum_k weights[k] * L_k with respect to the logit scale
  * and (SIGLIP) the bias, taken directly from the loss definitions on float64 inputs:
  *   CLIP   dL_k/dtau = 1/2 [ (1/N) sum_i (sum_j Prow_ij cos_ij - cos_ii)

@@ -56,9 +56,12 @@ def _bind(path):
     lib.orc_scale_grads_labels.argtypes = [P, P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_double, P, P, P, P]
     lib.orc_scale_grads_labels_f64.argtypes = lib.orc_scale_grads_labels.argtypes
+    lib.orc_oneset.argtypes = [P, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_double, ctypes.c_double, P, P, P, P,
+                               P, P, P]
+    lib.orc_oneset_f64.argtypes = lib.orc_oneset.argtypes
     for f in (lib.orc_fwd_bwd, lib.orc_fwd_bwd_f64, lib.orc_row_stats, lib.orc_grad_rows, lib.orc_scale_grads,
               lib.orc_scale_grads_f64, lib.orc_fwd_bwd_labels, lib.orc_fwd_bwd_labels_f64,
-              lib.orc_scale_grads_labels, lib.orc_scale_grads_labels_f64):
+              lib.orc_scale_grads_labels, lib.orc_scale_grads_labels_f64, lib.orc_oneset, lib.orc_oneset_f64):
         f.restype = ctypes.c_int
     return lib
 
@@ -216,3 +219,29 @@ def scale_grads(kind, A, B, prefixes, scale, bias=0.0, weights=None, labels=None
     if rc:
         raise ValueError(f"oracle scale_grads failed ({rc})")
     return float(ds[0]), float(db[0])
+
+
+def oneset(X, prefixes, t, b, labels, weights=None, grads=True):
+    """One-set SigLIP of the set X against itself (see oracle.c): dict(loss=[n], dX=(N, D),
+    row_terms=(n, N), dscale, dbias).  X: bf16 bit patterns or float64; labels as for
+    ``label_matrix`` (symmetric; the diagonal is ignored)."""
+    X = np.ascontiguousarray(X)
+    f64 = X.dtype == np.float64
+    if not f64:
+        X = _bits(X)
+    N, D = X.shape
+    Z = label_matrix(labels, N, N)
+    pre = _prefix_array(prefixes)
+    n = pre.size
+    w = None if weights is None else np.ascontiguousarray(np.asarray(weights, np.float64))
+    loss = np.zeros(n)
+    dX = np.zeros((N, D)) if grads else None
+    rt = np.zeros((n, N))
+    ds = np.zeros(1)
+    db = np.zeros(1)
+    fn = _load().orc_oneset_f64 if f64 else _load().orc_oneset
+    rc = fn(_ptr(X), N, D, _ptr(pre), n, float(t), float(b), _ptr(w), _ptr(Z), _ptr(loss), _ptr(dX), _ptr(rt),
+            _ptr(ds), _ptr(db))
+    if rc:
+        raise ValueError(f"oracle oneset failed ({rc})")
+    return dict(loss=loss, dX=dX, row_terms=rt, dscale=float(ds[0]), dbias=float(db[0]))

@@ -461,11 +461,112 @@ def test_labels_one_hot_closed_form():
     assert abs(oracle.scale_grads("siglip", A, B, (32, 64), t, b, labels=csr)[1] - dbias) < 1e-13
 
 
+# ---- the one-set loss (one set scored against itself, mirrored cells share labels)
+
+def _sym_labels(N, seed):
+    """Seeded symmetric positives between distinct rows: a few pairs and one triple."""
+    rng = np.random.default_rng(seed)
+    Z = np.zeros((N, N), np.uint8)
+    perm = rng.permutation(N)
+    for u in range(0, N - 1, 3):
+        i, j = perm[u], perm[u + 1]
+        Z[i, j] = Z[j, i] = 1
+    i, j, k = perm[:3]
+    Z[i, k] = Z[k, i] = 1
+    return Z
+
+
+def torch_oneset(X, prefixes, t, b, weights, Z):
+    Xt = torch.tensor(X, dtype=torch.float64, requires_grad=True)
+    tt = torch.tensor(t, dtype=torch.float64, requires_grad=True)
+    bt = torch.tensor(b, dtype=torch.float64, requires_grad=True)
+    N = Xt.shape[0]
+    z = 2.0 * torch.tensor(Z, dtype=torch.float64) - 1.0
+    off = 1.0 - torch.eye(N, dtype=torch.float64)
+    losses, total = [], 0.0
+    for p, w in zip(prefixes, weights):
+        xn = F.normalize(Xt[:, :p], dim=1, eps=1e-30)
+        L = -(F.logsigmoid(z * (tt * (xn @ xn.T) + bt)) * off).sum() / N
+        losses.append(L.item())
+        total = total + w * L
+    total.backward()
+    return np.array(losses), Xt.grad.numpy(), tt.grad.item(), bt.grad.item()
+
+
+def test_oneset_matches_torch_autograd():
+    rng = np.random.default_rng(31)
+    N, D, pre = 9, 128, (32, 64, 128)
+    X = _bits(rng.standard_normal((N, D)))
+    Z = _sym_labels(N, 3)
+    w = rng.uniform(0.5, 2.0, len(pre))
+    t, b = 5.0, -2.5
+    got = oracle.oneset(X, pre, t, b, Z, w)
+    L, gX, gt, gb = torch_oneset(_wide(X), pre, t, b, w, Z)
+    np.testing.assert_allclose(got["loss"], L, rtol=1e-12)
+    np.testing.assert_allclose(got["dX"], gX, rtol=1e-9, atol=1e-13)
+    np.testing.assert_allclose([got["dscale"], got["dbias"]], [gt, gb], rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(got["row_terms"].mean(axis=1), got["loss"], rtol=1e-13)
+
+
+def test_oneset_is_the_two_set_loss_of_the_set_with_itself():
+    """Both roles of every row: dX = dA + dB of the two-set loss at A = B = X, whose diagonal
+    cells (cosine 1, no gradient) hold the only difference in the loss."""
+    rng = np.random.default_rng(32)
+    N, pre, t, b = 8, (64, 128), 4.0, -1.0
+    X = _bits(rng.standard_normal((N, 128)))
+    Z = _sym_labels(N, 4)
+    one = oracle.oneset(X, pre, t, b, Z)
+    two = oracle.fwd_bwd("siglip", X, X, pre, t, b, labels=Z)
+    sp = lambda y: np.log1p(np.exp(y))  # noqa: E731
+    diag = sp(t + b) * N / N  # every self-cell is a negative (Z has an empty diagonal) with x = t + b
+    np.testing.assert_allclose(one["loss"], two["loss"] - diag, rtol=1e-12)
+    np.testing.assert_allclose(one["dX"], two["dA"] + two["dB"], rtol=1e-9, atol=1e-13)
+
+
+def test_oneset_identical_rows_closed_form():
+    N, t, b = 6, 3.0, -1.0
+    X = _bits(np.tile(np.random.default_rng(5).standard_normal(128), (N, 1)))
+    Z = _sym_labels(N, 6)
+    sp = lambda y: np.log1p(np.exp(y))  # noqa: E731
+    pos = Z.sum(axis=1)
+    L = np.sum(pos * sp(-(t + b)) + (N - 1 - pos) * sp(t + b)) / N
+    got = oracle.oneset(X, (64, 128), t, b, Z)
+    np.testing.assert_allclose(got["loss"], [L, L], rtol=1e-13)
+    assert np.abs(got["dX"]).max() < 1e-12
+
+
+def test_oneset_finite_differences():
+    rng = np.random.default_rng(33)
+    N, D, pre = 5, 16, (8, 16)
+    X = rng.standard_normal((N, D))
+    Z = _sym_labels(N, 7)
+    w = np.array([0.6, 1.4])
+    t, b = 2.0, -0.5
+    got = oracle.oneset(X, pre, t, b, Z, w)
+
+    def f(X_=X, t_=t, b_=b):
+        return float(np.dot(w, oracle.oneset(X_, pre, t_, b_, Z, w, grads=False)["loss"]))
+
+    h = 1e-6
+    for (i, d) in ((0, 3), (2, 9), (4, 15)):
+        Xp, Xm = X.copy(), X.copy()
+        Xp[i, d] += h
+        Xm[i, d] -= h
+        np.testing.assert_allclose(got["dX"][i, d], (f(Xp) - f(Xm)) / (2 * h), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(got["dscale"], (f(t_=t + h) - f(t_=t - h)) / (2 * h), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(got["dbias"], (f(b_=b + h) - f(b_=b - h)) / (2 * h), rtol=1e-6, atol=1e-9)
+
+
 MUTATIONS = {
     "dropped_projection_term": (
         "out[d] += g * (B[j * D + d] * rb[j] - c * A[i * D + d] * ra[i]) * ra[i];",
         "out[d] += g * (B[j * D + d] * rb[j]) * ra[i];"),
     "siglip_label_sign": ("double z = pos ? 1.0 : -1.0;", "double z = pos ? -1.0 : 1.0;"),
+    "oneset_second_argument_dropped": (
+        "out[d] += (g1 + g2) * (X[j * D + d] * r[j] - c * X[i * D + d] * r[i]) * r[i];",
+        "out[d] += (g1) * (X[j * D + d] * r[j] - c * X[i * D + d] * r[i]) * r[i];"),
+    "oneset_self_cell_counted": ("if (j == i) { /* a row is not paired with itself */",
+                                 "if (j == i && 0) { /* a row is not paired with itself */"),
     "labels_ignored": ("return Z ? Z[i * Nb + j] != 0 : i == j;", "return i == j;"),
     "labels_row_shifted": ("return Z ? Z[i * Nb + j] != 0 : i == j;",
                            "return Z ? Z[((i + 1) % (Nb < 2 ? 1 : 2)) * Nb + j] != 0 : i == j;"),
@@ -495,6 +596,7 @@ def _pins_pass():
         lambda: test_scale_grads_match_autograd(*CASES[0]),
         lambda: test_scale_grads_match_autograd(*CASES[1]),
         test_labels_match_torch_autograd,
+        test_oneset_matches_torch_autograd,
     ]
     for c in checks:
         try:
