@@ -61,6 +61,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.uf_contrastive_fwd_bwd_ex.argtypes = [P, P, I64, I64, I32, P, I32, I32, F32, F32, P, P, P, P, P, P, P, P, P,
                                               P, P, P, P, SZ, P, P]
     lib.uf_contrastive_fwd_bwd_ex.restype = I32
+    lib.uf_contrastive_oneset_fwd_bwd.argtypes = [P, I64, I32, P, I32, F32, F32, P, P, P, P, P, P, P, P, P, P, P, SZ,
+                                                  P, P]
+    lib.uf_contrastive_oneset_fwd_bwd.restype = I32
     lib.uf_contrastive_profile.argtypes = [I32]
     lib.uf_contrastive_profile.restype = I32
     lib.uf_contrastive_profile_read.argtypes = [I32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64),
@@ -128,6 +131,18 @@ def uf_contrastive_fwd_bwd_ex(A, B, Na, Nb, D, prefixes, kind, logit_scale, bias
                                                 pos_offsets, pos_ids, w, loss_per_prefix, row_terms, col_terms, dA,
                                                 dB, d_logit_scale, d_bias, workspace, int(workspace_bytes),
                                                 device_status, stream))
+
+
+def uf_contrastive_oneset_fwd_bwd(X, N, D, prefixes, logit_scale, bias, logit_scale_dev, bias_dev, pos_offsets,
+                                  pos_ids, prefix_weights, loss_per_prefix, row_terms, dX, d_logit_scale, d_bias,
+                                  workspace, workspace_bytes, device_status, stream) -> int:
+    """Raw call of the one-set loss: every pointer argument is an int device address or None."""
+    pre = _int_array(list(prefixes))
+    w = None if prefix_weights is None else (ctypes.c_float * len(prefix_weights))(*prefix_weights)
+    return int(load().uf_contrastive_oneset_fwd_bwd(X, int(N), int(D), pre, len(prefixes), float(logit_scale),
+                                                    float(bias), logit_scale_dev, bias_dev, pos_offsets, pos_ids, w,
+                                                    loss_per_prefix, row_terms, dX, d_logit_scale, d_bias, workspace,
+                                                    int(workspace_bytes), device_status, stream))
 
 
 KERNEL_GROUPS = ("prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd", "gemm")
@@ -233,6 +248,62 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
                                        workspace.numel(), ptr(device_status), s.cuda_stream)
     if st != UF_OK:
         raise UfError(st, "uf_contrastive_fwd_bwd")
+    return out
+
+
+def oneset_fwd_bwd(X, labels, prefixes=(64, 128, 256, 512, 1024), logit_scale=10.0, bias=-10.0,
+                   prefix_weights=None, grads=True, terms=False, workspace=None, device_status=None, stream=None,
+                   scale_grads=False):
+    """One-set SigLIP of the bf16 CUDA tensor X (N x D) against itself.  ``labels``: the
+    symmetric positive pairs as CSR lists ``(offsets, ids)`` (device tensors or host arrays).
+    Returns a dict with ``loss``, ``dX`` (when grads), ``row_terms`` (when terms) and, with
+    ``scale_grads``, ``d_logit_scale`` / ``d_bias``.  Scalars may be one-element fp32 CUDA
+    tensors, as in ``contrastive_fwd_bwd``."""
+    import torch
+
+    if X.dtype != torch.bfloat16 or not X.is_cuda:
+        raise TypeError("X must be a bf16 CUDA tensor")
+    X = X.contiguous()
+    N, D = X.shape
+    dev = X.device
+    n = len(prefixes)
+    k = KINDS["siglip"]
+    if workspace is None:
+        need = uf_contrastive_workspace_size(N, N, D, prefixes, k, grads)
+        if need == 0:
+            raise UfError(1, "uf_contrastive_workspace_size")
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = {"loss": torch.empty(n, dtype=torch.float32, device=dev)}
+    if grads:
+        out["dX"] = torch.empty((N, D), dtype=torch.float32, device=dev)
+    if terms:
+        out["row_terms"] = torch.empty((n, N), dtype=torch.float32, device=dev)
+    if scale_grads:
+        out["d_logit_scale"] = torch.empty(1, dtype=torch.float32, device=dev)
+        out["d_bias"] = torch.empty(1, dtype=torch.float32, device=dev)
+    offs, ids = labels
+    offs = torch.as_tensor(offs, dtype=torch.int64, device=dev).contiguous()
+    ids = torch.as_tensor(ids, dtype=torch.int32, device=dev).contiguous()
+    ids_ptr = ids.data_ptr() if ids.numel() else _empty_ids(dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+
+    def scalar(v):
+        if isinstance(v, torch.Tensor):
+            return 0.0, v.data_ptr()
+        return float(v), None
+
+    ls_host, ls_dev = scalar(logit_scale)
+    b_host, b_dev = scalar(bias)
+    with torch.cuda.device(dev):
+        st = uf_contrastive_oneset_fwd_bwd(X.data_ptr(), N, D, prefixes, ls_host, b_host, ls_dev, b_dev,
+                                           offs.data_ptr(), ids_ptr, prefix_weights, out["loss"].data_ptr(),
+                                           ptr(out.get("row_terms")), ptr(out.get("dX")),
+                                           ptr(out.get("d_logit_scale")), ptr(out.get("d_bias")),
+                                           workspace.data_ptr(), workspace.numel(), ptr(device_status),
+                                           s.cuda_stream)
+    if st != UF_OK:
+        raise UfError(st, "uf_contrastive_oneset_fwd_bwd")
     return out
 
 

@@ -363,10 +363,11 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
           y[2] = bf16_lo(yv.y);
           y[3] = bf16_hi(yv.y);
         }
-        o.x = g[0] - r_c * x[0] + q_c * y[0];
-        o.y = g[1] - r_c * x[1] + q_c * y[1];
-        o.z = g[2] - r_c * x[2] + q_c * y[2];
-        o.w = g[3] - r_c * x[3] + q_c * y[3];
+        const float s = p.double_out ? 2.f : 1.f;
+        o.x = s * (g[0] - r_c * x[0] + q_c * y[0]);
+        o.y = s * (g[1] - r_c * x[1] + q_c * y[1]);
+        o.z = s * (g[2] - r_c * x[2] + q_c * y[2]);
+        o.w = s * (g[3] - r_c * x[3] + q_c * y[3]);
       }
       *reinterpret_cast<float4*>(out + c4) = o;
     }
@@ -459,6 +460,20 @@ cudaError_t launch_max_reduce(const MaxReduceParams& p, cudaStream_t stream) {
 // softplus(x) - x and its gradient in x is sigmoid(x) - 1 = -sigmoid(-x).  So the loss takes
 // -x per positive (terms mode) and the positive cells' weights are rewritten with their
 // exact value before the gradient GEMMs read them (patch mode).
+// Is i among row j's positives?  (binary search of its increasing ids, within bounds)
+__device__ __forceinline__ bool has_mirror(const LabelParams& p, int j, int i, int64_t total) {
+  int64_t lo = p.offsets[j], hi = p.offsets[j + 1];
+  if (lo < 0 || hi > total || hi < lo) return false;
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    const int v = p.ids[mid];
+    if (v == i) return true;
+    if (v < i) lo = mid + 1;
+    else hi = mid;
+  }
+  return false;
+}
+
 __global__ void __launch_bounds__(256) labels_kernel(const LabelParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -484,6 +499,10 @@ __global__ void __launch_bounds__(256) labels_kernel(const LabelParams p) {
       const int j = p.ids[q];
       if (j < 0 || j >= p.nb || j <= prev) {  // out of range, repeated or out of order: skipped
         bad = true;
+        continue;
+      }
+      if (p.oneset && (j == i || !has_mirror(p, j, static_cast<int>(i), total))) {
+        bad = true;  // one set: no self-pairs, and mirrored cells share their label
         continue;
       }
       prev = j;

@@ -176,6 +176,7 @@ struct NormBwdParams {
   int g_splits;
   float* dX;               // [nx][d]
   float* csum;             // NULL or [nx]: sum over prefixes of the full row scalar C_k (logit-scale gradient)
+  int double_out;          // one-set loss: write 2 dX (the row's gradient through both roles of every cell)
 };
 cudaError_t launch_norm_bwd(const NormBwdParams& p, cudaStream_t stream);
 
@@ -239,6 +240,7 @@ struct LabelParams {
   float* lcount;
   uint16_t* W;
   int64_t row0, rows, w_rows_per_prefix, ldw;
+  int oneset;              // one-set loss: a self-pair (j == i) or a pair whose mirror is missing is malformed
   int* status;
 };
 cudaError_t launch_labels(const LabelParams& p, cudaStream_t stream);

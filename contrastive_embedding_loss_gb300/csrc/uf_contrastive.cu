@@ -286,14 +286,19 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
                                    workspace, workspace_bytes, device_status, stream_handle);
 }
 
-uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
-                                      const int* prefixes, int n_prefix, int kind, float logit_scale, float bias,
-                                      const float* logit_scale_dev, const float* bias_dev,
-                                      const int64_t* pos_offsets, const int* pos_ids,
-                                      const float* prefix_weights, float* loss_per_prefix, float* row_terms,
-                                      float* col_terms, float* dA, float* dB, float* d_logit_scale, float* d_bias,
-                                      void* workspace, size_t workspace_bytes, int* device_status,
-                                      void* stream_handle) {
+}  // extern "C"
+
+namespace {
+
+// The two-set loss of A against B, or (oneset) the one-set loss of the set A = B against
+// itself: self-cells masked, labels required, dA = dX receives both roles of every cell
+// (twice the A-side gradient, the weights being symmetric), no B-side GEMM.
+uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D, const int* prefixes,
+                     int n_prefix, int kind, float logit_scale, float bias, const float* logit_scale_dev,
+                     const float* bias_dev, const int64_t* pos_offsets, const int* pos_ids,
+                     const float* prefix_weights, float* loss_per_prefix, float* row_terms, float* col_terms,
+                     float* dA, float* dB, float* d_logit_scale, float* d_bias, void* workspace,
+                     size_t workspace_bytes, int* device_status, void* stream_handle, bool oneset) {
   // ---- argument checks (nothing is enqueued on failure)
   if (!A || !B || !loss_per_prefix || !workspace) return UF_INVALID_ARGUMENT;
   if ((dA == nullptr) != (dB == nullptr)) return UF_INVALID_ARGUMENT;
@@ -394,7 +399,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     UF_CHECK(launch_prep(pp, stream));
   }
   if (grads) {
-    {
+    if (!oneset) {  // (one set: A^T is B^T)
       ProfScope ps(UF_KERNEL_TRANSPOSE, 1, stream);
       UF_CHECK(launch_transpose(A16, At, Na, D, P.lda, stream));
     }
@@ -423,6 +428,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     lp.rinv_b = F(P.o_rinv_b);
     lp.pos_term = F(P.o_lab);
     lp.lcount = F(P.o_lcount);
+    lp.oneset = oneset ? 1 : 0;
     lp.status = device_status;
     ProfScope ps(UF_KERNEL_PREP, 1, stream);
     UF_CHECK(launch_labels(lp, stream));
@@ -467,7 +473,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     fp.n_col_tiles = static_cast<int>(P.ftiles);
     fp.tiles_per_split = P.fwd_a.tiles_per_split;
     fp.sc = sc;
-    fp.no_diag = labels ? 1 : 0;
+    fp.no_diag = labels && !oneset ? 1 : 0;  // one set: the diagonal cells are the self-cells, masked
     fp.rinv_x = F(P.o_rinv_a);
     fp.rinv_y = F(P.o_rinv_b);
     fp.rowacc = F(P.o_acc_a);
@@ -539,7 +545,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     wp.tiles_per_split = P.wgt.tiles_per_split;
     wp.sc = sc;
     wp.shifted = shifted ? 1 : 0;
-    wp.no_diag = labels ? 1 : 0;
+    wp.no_diag = labels && !oneset ? 1 : 0;
     wp.rinv_x = F(P.o_rinv_a);
     wp.rinv_y = F(P.o_rinv_b);
     wp.alpha_x = siglip ? nullptr : F(P.o_fa);
@@ -592,10 +598,12 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
       ga.m_rows = rows;
       ga.row0 = r0;
       UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
-      gb.kdim = rows;
-      gb.b_col0 = r0;
-      gb.accumulate = r0 > 0;
-      UF_CHECK(launch_gemm(tmWm, tmAt, tmAt128, gb, true, stream));
+      if (!oneset) {
+        gb.kdim = rows;
+        gb.b_col0 = r0;
+        gb.accumulate = r0 > 0;
+        UF_CHECK(launch_gemm(tmWm, tmAt, tmAt128, gb, true, stream));
+      }
     }
     if (siglip) {
       sp.rowacc_a = F(P.o_acc_a);
@@ -606,7 +614,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
   }
 
   // ---- 4. projection term and diagonal correction
-  for (int side = 0; side < 2; ++side) {
+  for (int side = 0; side < (oneset ? 1 : 2); ++side) {
     const bool xa = side == 0;
     NormBwdParams q{};
     q.kind = kind;
@@ -642,6 +650,7 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
     q.csum = (xa && d_logit_scale) ? F(P.o_csum) : nullptr;
     q.G = xa ? dA : dB;
     q.g_splits = 1;
+    q.double_out = oneset ? 1 : 0;
     q.dX = xa ? dA : dB;
     ProfScope ps(UF_KERNEL_NORM_BWD, 1, stream);
     UF_CHECK(launch_norm_bwd(q, stream));
@@ -668,6 +677,35 @@ uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, 
   if (col_terms && kind != KIND_CLIP) UF_CHECK(cudaMemsetAsync(col_terms, 0, sizeof(float) * n * Nb, stream));
 #undef UF_CHECK
   return UF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64_t Na, int64_t Nb, int D,
+                                      const int* prefixes, int n_prefix, int kind, float logit_scale, float bias,
+                                      const float* logit_scale_dev, const float* bias_dev,
+                                      const int64_t* pos_offsets, const int* pos_ids,
+                                      const float* prefix_weights, float* loss_per_prefix, float* row_terms,
+                                      float* col_terms, float* dA, float* dB, float* d_logit_scale, float* d_bias,
+                                      void* workspace, size_t workspace_bytes, int* device_status,
+                                      void* stream_handle) {
+  return run_loss(A, B, Na, Nb, D, prefixes, n_prefix, kind, logit_scale, bias, logit_scale_dev, bias_dev,
+                  pos_offsets, pos_ids, prefix_weights, loss_per_prefix, row_terms, col_terms, dA, dB, d_logit_scale,
+                  d_bias, workspace, workspace_bytes, device_status, stream_handle, false);
+}
+
+uf_status_t uf_contrastive_oneset_fwd_bwd(const void* X, int64_t N, int D, const int* prefixes, int n_prefix,
+                                          float logit_scale, float bias, const float* logit_scale_dev,
+                                          const float* bias_dev, const int64_t* pos_offsets, const int* pos_ids,
+                                          const float* prefix_weights, float* loss_per_prefix, float* row_terms,
+                                          float* dX, float* d_logit_scale, float* d_bias, void* workspace,
+                                          size_t workspace_bytes, int* device_status, void* stream_handle) {
+  if (!pos_offsets || !pos_ids) return UF_INVALID_ARGUMENT;  // a one-set batch names its pairs
+  return run_loss(X, X, N, N, D, prefixes, n_prefix, KIND_SIGLIP, logit_scale, bias, logit_scale_dev, bias_dev,
+                  pos_offsets, pos_ids, prefix_weights, loss_per_prefix, row_terms, nullptr, dX, dX, d_logit_scale,
+                  d_bias, workspace, workspace_bytes, device_status, stream_handle, true);
 }
 
 uf_status_t uf_contrastive_profile(int enable) {

@@ -184,6 +184,37 @@ UF_API uf_status_t uf_contrastive_fwd_bwd_ex(const void* A, const void* B, int64
                                       size_t workspace_bytes, int* device_status, void* stream);
 
 /*
+ * One-set SigLIP: the set X scored against itself (blog post "Scaling-Up Contrastive
+ * Learning over NVLink Multicast", section "One Set or Two": one set, the same labels and
+ * weights for mirrored cells, so the owner of a row differentiates both of its cells; an
+ * image and its caption are two rows of the set marked as a positive pair):
+ *   L_p = -(1/N) sum_i sum_{j != i} log sigmoid(z_ij (t cos_ij + b)),
+ * cos_ij between rows i and j of X on the prefix, z_ij = +1 for the listed pairs, -1 else.
+ *   X               device bf16 N x D, 16-byte aligned.
+ *   pos_offsets,    required: the positive pairs as device CSR lists (format as in
+ *   pos_ids         uf_contrastive_fwd_bwd_ex).  They must be symmetric (j listed in row i
+ *                   exactly when i is listed in row j) and name no self-pair; entries that
+ *                   break this are skipped and reported as UF_INVALID_ARGUMENT in
+ *                   *device_status.
+ *   row_terms       device fp32 [n_prefix][N] or NULL: sum_{j != i} softplus(-z_ij x_ij).
+ *   dX              device fp32 N x D or NULL (forward only): the gradient of
+ *                   sum_p w_p L_p through both cells of every pair.
+ *   workspace       at least uf_contrastive_workspace_min(N, N, D, prefixes, n_prefix,
+ *                   UF_LOSS_SIGLIP, dX != NULL) bytes (uf_contrastive_workspace_size
+ *                   recommended), 256-byte aligned.
+ * Every other argument as in uf_contrastive_fwd_bwd_ex.  The symmetric weights make the
+ * gradient one contraction: the B side of the two-set backward is skipped.
+ */
+UF_API uf_status_t uf_contrastive_oneset_fwd_bwd(const void* X, int64_t N, int D, const int* prefixes,
+                                          int n_prefix, float logit_scale, float bias,
+                                          const float* logit_scale_dev, const float* bias_dev,
+                                          const int64_t* pos_offsets, const int* pos_ids,
+                                          const float* prefix_weights, float* loss_per_prefix,
+                                          float* row_terms, float* dX, float* d_logit_scale, float* d_bias,
+                                          void* workspace, size_t workspace_bytes, int* device_status,
+                                          void* stream);
+
+/*
  * uf_contrastive_fwd_bwd without a workspace argument, for callers that cannot allocate
  * device memory: hosts that reserve all of their memory at start-up and forbid
  * allocation afterwards, plugins whose host application owns every device buffer, or

@@ -202,3 +202,26 @@ def test_label_arguments_are_checked_on_the_host(lib):
         pytest.skip("a GPU is present")
     assert _call_ex(pos_offsets=FAKE, pos_ids=FAKE, **sig) == CUDA
     assert _call_ex(Nb=700, **sig) == CUDA                           # extra negative columns
+
+
+def test_oneset_arguments_are_checked_on_the_host(lib):
+    INV, UNS, CUDA = 1, 2, 4
+    args = dict(X=FAKE, N=256, D=1024, prefixes=LADDER, logit_scale=10.0, bias=-10.0, logit_scale_dev=None,
+                bias_dev=None, pos_offsets=FAKE, pos_ids=FAKE, prefix_weights=None, loss_per_prefix=FAKE,
+                row_terms=None, dX=FAKE, d_logit_scale=None, d_bias=None, workspace=FAKE, workspace_bytes=1 << 40,
+                device_status=None, stream=None)
+    call = lambda **kw: binding.uf_contrastive_oneset_fwd_bwd(**{**args, **kw})  # noqa: E731
+    assert call(pos_offsets=None) == INV           # a one-set batch names its pairs
+    assert call(pos_ids=None) == INV
+    assert call(X=None) == INV
+    assert call(X=FAKE + 2) == INV
+    assert call(logit_scale=70.0, bias=-20.0) == UNS
+    assert call(d_logit_scale=FAKE, dX=None) == INV  # the scalar gradients come out of the backward
+    need = binding.uf_contrastive_workspace_min(256, 256, 1024, LADDER, 1, 1)
+    assert call(workspace_bytes=need - 256) == 3
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call() == CUDA
+    assert call(dX=None) == CUDA
