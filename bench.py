@@ -149,10 +149,14 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def csrc_digest():
+# the dominant kernel's own sources: its counters stand until one of these changes
+GEMM_SOURCES = ("gemm_kernel.cu", "ptx.cuh", "common.cuh")
+
+
+def kernel_digest(files=GEMM_SOURCES):
     h = hashlib.sha1()
     d = os.path.join(ROOT, "contrastive_embedding_loss_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in files:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -167,7 +171,7 @@ def ncu_traffic(workload):
             rec = json.load(f).get(workload)
     except Exception:
         return None
-    if not rec or rec.get("csrc_digest") != csrc_digest():
+    if not rec or rec.get("kernel_digest") != kernel_digest():
         return None
     return rec.get("dram_bytes_per_launch")
 
