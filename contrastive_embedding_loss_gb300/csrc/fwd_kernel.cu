@@ -220,6 +220,126 @@ __device__ __forceinline__ float fwd_cells_shifted(const float (&v)[64], const f
   return rs.x + rs.y;
 }
 
+// Reduce-scatter of NV values over the 2^STAGES lanes that differ in lane bits M0, M0/2, ...:
+// each stage keeps half of the values (the upper half where the lane bit is set) and adds
+// (MAX: takes the maximum of) the partner's other half, so lane bits (M0, M0/2, ...) select,
+// from the most significant, which NV / 2^STAGES values a lane ends with in v[0..].
+template <bool MAX, int NV, int M0, int STAGES>
+__device__ __forceinline__ void reduce_scatter_bits(float (&v)[NV], int lane) {
+#pragma unroll
+  for (int st = 0; st < STAGES; ++st) {
+    const int m = M0 >> st, h = NV >> (st + 1);
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float lo = v[i], hi = v[i + h];
+      const float send = upper ? lo : hi;
+      const float keep = upper ? hi : lo;
+      const float got = __shfl_xor_sync(0xffffffffu, send, m);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+}
+
+// The column-summing (CLIP) epilogue on the 16x256b TMEM layout: v[0..31] and v[32..63] are
+// the warp's rows 0-15 and 16-31 (of its 32-row quadrant q), 64 columns; lane l = 4 g + c
+// holds rows {g, g + 8} of each half and columns 8 r + 2 c + {0, 1}, r = 0..7 (register
+// 4 r + 2 s + b of a half: row g + 8 s, column 8 r + 2 c + b).  A column's 32 cells then sit
+// 4 to a lane on 8 lanes, so the column sums are in-thread adds and a 3-stage scatter over 8
+// lanes (instead of 31 exchanges per 32 columns on the 32x32b layout), and a row's 16 cells
+// per lane meet over 4 lanes.  MODE as in the kernel; rf, ru: this prefix's row factors
+// L rho and (kFwdShifted) row shifts for the tile's 128 rows; cf, vs: the quarter's column
+// factors sigma and (kFwdShifted) column shifts.  Returns the row value of the lane's own row
+// (32 q + 16 (c >> 1) + g + 8 (c & 1)); the warp's 32-row column partials go to cp[0..63].
+template <int MODE, bool CHECK>
+__device__ __forceinline__ void fwd_cells16_half(const float (&v)[32], int h, const float* cf, const float* vs,
+                                                 const float* rf, const float* ru, float L, int q, int lane,
+                                                 int col_base, int ncols, int dtile, int rows_left, float2 (&rs)[4],
+                                                 float2 (&cs)[8]) {
+  const int g = lane >> 2, c4 = lane & 3;
+  float R1[2], U[2];
+#pragma unroll
+  for (int sub = 0; sub < 2; ++sub) {
+    const int row = q * 32 + 16 * h + g + 8 * sub;
+    R1[sub] = rf[row];
+    U[sub] = MODE == kFwdShifted ? ru[row] : 0.f;
+  }
+  const float2 nl = make_float2(-L, -L);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int c = 8 * r + 2 * c4;  // column within the quarter
+    const float2 sg = *reinterpret_cast<const float2*>(cf + c);
+    float2 nv = make_float2(0.f, 0.f);
+    if constexpr (MODE == kFwdShifted) {
+      const float2 vv = *reinterpret_cast<const float2*>(vs + c);
+      nv = make_float2(-vv.x, -vv.y);
+    }
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+      const int idx = 2 * h + sub;
+      const float2 d = make_float2(v[r * 4 + 2 * sub], v[r * 4 + 2 * sub + 1]);
+      const float2 r1s = mul2(make_float2(R1[sub], R1[sub]), sg);
+      bool ok0 = true, ok1 = true;
+      if constexpr (CHECK) {
+        const int row = q * 32 + 16 * h + g + 8 * sub;
+        const int col = col_base + c, dcol = dtile + row;
+        const bool rok = row < rows_left;
+        ok0 = rok && col < ncols;
+        ok1 = rok && col + 1 < ncols;
+        if constexpr (MODE != kFwdMax) {  // the max includes the positive; the sums leave it out
+          ok0 = ok0 && col != dcol;
+          ok1 = ok1 && col + 1 != dcol;
+        }
+      }
+      if constexpr (MODE == kFwdMax) {
+        float2 x = mul2(r1s, d);  // the same two roundings as the shifted pass
+        if (!ok0) x.x = -INFINITY;
+        if (!ok1) x.y = -INFINITY;
+        rs[idx] = make_float2(fmaxf(rs[idx].x, x.x), fmaxf(rs[idx].y, x.y));
+        cs[r] = make_float2(fmaxf(cs[r].x, x.x), fmaxf(cs[r].y, x.y));
+      } else if constexpr (MODE == kFwdShifted) {
+        const float2 x = mul2(r1s, d);
+        const float2 xr = add2(x, make_float2(-U[sub], -U[sub]));
+        const float2 xc = add2(x, nv);
+        float2 er = make_float2(ex2_approx(xr.x), ex2_approx(xr.y));
+        float2 ec = make_float2(ex2_approx(xc.x), ex2_approx(xc.y));
+        if (!ok0) er.x = ec.x = 0.f;
+        if (!ok1) er.y = ec.y = 0.f;
+        rs[idx] = add2(rs[idx], er);
+        cs[r] = add2(cs[r], ec);
+      } else {
+        const float2 x = fma2(r1s, d, nl);
+        float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (!ok0) e.x = 0.f;
+        if (!ok1) e.y = 0.f;
+        rs[idx] = add2(rs[idx], e);
+        cs[r] = add2(cs[r], e);
+      }
+    }
+  }
+}
+
+// After both halves: the row values meet over the 4 lanes of a row group (lane bits 1, 0) and
+// the column values over the 8 lanes that share c4 (lane bits 4, 3, 2), leaving the lane the
+// columns 8 g + 2 c4 + {0, 1}, written to cp.  Returns the lane's own row value.
+template <int MODE>
+__device__ __forceinline__ float fwd_cells16_reduce(const float2 (&rs)[4], const float2 (&cs)[8], int lane,
+                                                    float* cp) {
+  const int g = lane >> 2, c4 = lane & 3;
+  float rv[4], cv[16];
+#pragma unroll
+  for (int idx = 0; idx < 4; ++idx) rv[idx] = MODE == kFwdMax ? fmaxf(rs[idx].x, rs[idx].y) : rs[idx].x + rs[idx].y;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    cv[2 * r] = cs[r].x;
+    cv[2 * r + 1] = cs[r].y;
+  }
+  reduce_scatter_bits<MODE == kFwdMax, 4, 2, 2>(rv, lane);
+  reduce_scatter_bits<MODE == kFwdMax, 16, 16, 3>(cv, lane);
+  *reinterpret_cast<float2*>(cp + 8 * g + 2 * c4) = make_float2(cv[0], cv[1]);
+  return rv[0];
+}
+
 // The order in which tiles and bands are fed to the MMA: tiles in pairs (t even in
 // accumulator 0, t + 1 in accumulator 1), band by band, alternating within a pair.
 // Step index s -> (tile, band); the producer, the MMA issuer and the epilogue all walk it.
@@ -367,6 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;
     const int64_t gi = i0 + r;
     const bool row_ok = gi < p.nx;
+    // the row whose sums this lane keeps: its own (32x32b layout), or with the column sums on
+    // the 16x256b layout the one fwd_cells16 leaves it
+    const int r_own = COLS ? q * 32 + 16 * ((lane & 3) >> 1) + (lane >> 2) + 8 * (lane & 1) : r;
+    const int64_t gi_own = i0 + r_own;
+    const bool own_ok = gi_own < p.nx;
     const int etid = threadIdx.x - kEpiWarp0 * 32;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     constexpr int CF = kMaxPrefix * kCols;  // floats per column-factor buffer
@@ -421,11 +546,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         tc_fence_after();
-        float v[64];
-        tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, v);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[a]);
+        float v[COLS ? 32 : 64];  // COLS: one 16-row half at a time (fewer live registers)
+        if constexpr (COLS)
+          tmem_ld16x256_x8(tmem + lane_addr + a * kCols + cq * 64, reinterpret_cast<float(&)[32]>(v));
+        else
+          tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, reinterpret_cast<float(&)[64]>(v));
+        if constexpr (!COLS) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+        }
+        float2 rs16[4], cs16[8];  // COLS: the row and column accumulators of fwd_cells16_half
+        if constexpr (COLS) {
+          constexpr float kInit = MODE == kFwdMax ? -INFINITY : 0.f;
+#pragma unroll
+          for (int idx = 0; idx < 4; ++idx) rs16[idx] = make_float2(kInit, kInit);
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) cs16[rr] = make_float2(kInit, kInit);
+        }
 
         const float* cf = colf + (t & 3) * CF + k * kCols + cq * 64;
         const float R1 = rowf[k * kTileRows + r];
@@ -439,7 +577,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (i0 + kTileRows > p.nx);
         float* cp = cpart + (((snap & 1) * 4 + cq) * 4 + q) * 64;
         float rs;
-        if constexpr (MODE == kFwdMax) {
+        if constexpr (COLS) {
+          const float* vs = colsh + (t & 3) * CF + k * kCols + cq * 64;
+          float L;
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(L) : "r"(scal_s));
+          const int dt = p.no_diag ? INT_MIN / 2 : static_cast<int>(dtile);
+          const int rows_left = p.nx - i0 < kTileRows ? static_cast<int>(p.nx - i0) : kTileRows;
+          const float* rf = rowf + k * kTileRows;
+          const float* ru = rowsh + k * kTileRows;
+          float (&v32)[32] = reinterpret_cast<float(&)[32]>(v);
+          for (int h = 0; h < 2; ++h) {
+            if (h == 1) {  // the second 16-row half; then the accumulator is free for the MMA
+              tmem_ld16x256_x8(tmem + lane_addr + (16u << 16) + a * kCols + cq * 64, v32);
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[a]);
+            }
+            if (check)
+              fwd_cells16_half<MODE, true>(v32, h, cf, vs, rf, ru, L, q, lane, cq * 64, ncols, dt, rows_left, rs16,
+                                           cs16);
+            else
+              fwd_cells16_half<MODE, false>(v32, h, cf, vs, rf, ru, L, q, lane, cq * 64, ncols, dt, rows_left, rs16,
+                                            cs16);
+          }
+          rs = fwd_cells16_reduce<MODE>(rs16, cs16, lane, cp);
+        } else if constexpr (MODE == kFwdMax) {
           rs = check ? fwd_cells_max<COLS, true>(v, cf, R1, cq * 64, ncols, row_ok, lane, cp)
                      : fwd_cells_max<COLS, false>(v, cf, R1, cq * 64, ncols, row_ok, lane, cp);
         } else if constexpr (MODE == kFwdShifted) {
@@ -476,9 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++snap;
     }
     cp_async_wait<0>();
-    if (row_ok && ok) {
+    if (own_ok && ok) {
       const int slot = split * 4 + cq;
-      for (int k = 0; k < n; ++k) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi] = acc_row[k];
+      for (int k = 0; k < n; ++k) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi_own] = acc_row[k];
     }
   }
 
