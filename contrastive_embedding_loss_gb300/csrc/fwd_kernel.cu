@@ -640,7 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait<0>();
     if (own_ok && ok) {
       const int slot = split * 4 + cq;
-      for (int k = 0; k < n; ++k) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi_own] = acc_row[k];
+      if constexpr (COLS) {
+#pragma unroll  // (a constant index keeps acc_row in registers, which the 16x256b epilogue has room for)
+        for (int k = 0; k < kMaxPrefix; ++k)
+          if (k < n) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi_own] = acc_row[k];
+      } else {
+        for (int k = 0; k < n; ++k) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi_own] = acc_row[k];
+      }
     }
   }
 
