@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float acc_row[kMaxPrefix];
 #pragma unroll
     for (int k = 0; k < kMaxPrefix; ++k) acc_row[k] = MODE == kFwdMax ? -INFINITY : 0.f;
-    uint32_t uses[2] = {0, 0};
+    uint32_t uses0 = 0, uses1 = 0;  // uses of each accumulator (scalars: a runtime index would put them in local memory)
     uint32_t snap = 0;  // snapshots processed (selects the column-partial buffer)
     bool ok = true;
     for (int s = 0; s < sched.steps(); ++s) {
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int a = t & 1;
       const int k = b;
       const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
-      if (ok && !wait_bounded(&acc_full[a], uses[a] & 1, abort_flag)) {
+      if (ok && !wait_bounded(&acc_full[a], (a ? uses1 : uses0) & 1, abort_flag)) {
         fail(p, abort_flag);
         ok = false;
       }
@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kMaxPrefix; ++kk)
           if (kk == k) acc_row[kk] = MODE == kFwdMax ? fmaxf(acc_row[kk], rs) : acc_row[kk] + rs;
       }
-      ++uses[a];
+      if (a) ++uses1; else ++uses0;
       if constexpr (COLS) {
         // combine the four row quadrants of this column quarter; one warp writes the partial
         named_bar_sync(2 + cq, 128);
