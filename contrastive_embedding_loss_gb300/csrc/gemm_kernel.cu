@@ -71,11 +71,11 @@ __device__ __forceinline__ int prefix_end_of(const GemmParams& p, int k) {
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
+// One CTA of the contraction; vblock is its index in the contraction's own grid.
 // AMN: the weights are the MN-major A operand (B side: rows of G are columns of m^k).
 template <bool AMN>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_yt,
-                const __grid_constant__ CUtensorMap tm_yt128, const GemmParams p) {
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtensorMap& tm_yt,
+                                          const CUtensorMap& tm_yt128, const GemmParams& p, uint32_t vblock) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem + off_a;
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int kk = 0; kk < kMaxPrefix; ++kk)
     if (kk < p.n_prefix) n_slices = (p.prefix_end[kk] + kN - 1) / kN;
   const int64_t pairs = (p.m_rows + 2 * kTileRows - 1) / (2 * kTileRows);
-  const int64_t cta = blockIdx.x >> 1;                 // [group][pair][slice in group]
+  const int64_t cta = vblock >> 1;                     // [group][pair][slice in group]
   const int64_t per_group = pairs * 2;
   const int grp = static_cast<int>(cta / per_group);
   const int64_t rem = cta % per_group;
@@ -317,8 +317,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool AMN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_yt,
+                const __grid_constant__ CUtensorMap tm_yt128, const GemmParams p) {
+  gemm_body<AMN>(tm_w, tm_yt, tm_yt128, p, blockIdx.x);
+}
+
+// Both contractions of a weight chunk in one grid: the dA CTAs (K-major weights) first, then
+// the dB ones (MN-major), so the second fills the first's last wave instead of waiting for
+// it (split: the dA grid's size, even, so no CTA pair straddles the two).
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel_both(const __grid_constant__ CUtensorMap tk_w, const __grid_constant__ CUtensorMap tk_yt,
+                     const __grid_constant__ CUtensorMap tk_yt128, const GemmParams pk,
+                     const __grid_constant__ CUtensorMap tn_w, const __grid_constant__ CUtensorMap tn_yt,
+                     const __grid_constant__ CUtensorMap tn_yt128, const GemmParams pn, const unsigned split) {
+  if (blockIdx.x < split)
+    gemm_body<false>(tk_w, tk_yt, tk_yt128, pk, blockIdx.x);
+  else
+    gemm_body<true>(tn_w, tn_yt, tn_yt128, pn, blockIdx.x - split);
+}
+
+template <bool AMN>
 static cudaError_t setup_one() {
   return cudaFuncSetAttribute(gemm_kernel<AMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+// CTAs of one contraction: [slice pair][row-block pair][slice in the pair][rank]
+unsigned grid_of(const GemmParams& p) {
+  const int pn = p.prefix_end[p.n_prefix - 1];
+  const int64_t blocks = (p.m_rows + kTileRows - 1) / kTileRows;
+  const int64_t n_slices = (pn + kN - 1) / kN;
+  const int64_t groups = (n_slices + 1) / 2;
+  return static_cast<unsigned>(groups * ((blocks + 1) / 2) * 2 * 2);
 }
 
 }  // namespace gemm
@@ -326,17 +356,36 @@ static cudaError_t setup_one() {
 cudaError_t gemm_kernel_setup() {
   cudaError_t e;
   if ((e = gemm::setup_one<false>()) != cudaSuccess) return e;
-  return gemm::setup_one<true>();
+  if ((e = gemm::setup_one<true>()) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm::gemm_kernel_both, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::smem_bytes);
+}
+
+double gemm_grid_pairs(const GemmParams& p) { return 0.5 * gemm::grid_of(p); }
+
+cudaError_t launch_gemm_both(const CUtensorMap& tk_w, const CUtensorMap& tk_yt, const CUtensorMap& tk_yt128,
+                             const GemmParams& pk, const CUtensorMap& tn_w, const CUtensorMap& tn_yt,
+                             const CUtensorMap& tn_yt128, const GemmParams& pn, cudaStream_t stream) {
+  const unsigned split = gemm::grid_of(pk);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(split + gemm::grid_of(pn));
+  cfg.blockDim = dim3(gemm::kThreads);
+  cfg.dynamicSmemBytes = gemm::smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel_both, tk_w, tk_yt, tk_yt128, pk, tn_w, tn_yt, tn_yt128, pn,
+                            split);
 }
 
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const CUtensorMap& tm_yt128,
                         const GemmParams& p, bool weights_mn, cudaStream_t stream) {
-  const int pn = p.prefix_end[p.n_prefix - 1];
-  const int64_t blocks = (p.m_rows + kTileRows - 1) / kTileRows;
   cudaLaunchConfig_t cfg = {};
-  const int64_t n_slices = (pn + gemm::kN - 1) / gemm::kN;
-  const int64_t groups = (n_slices + 1) / 2;
-  cfg.gridDim = dim3(static_cast<unsigned>(groups * ((blocks + 1) / 2) * 2 * 2));
+  cfg.gridDim = dim3(gemm::grid_of(p));
   cfg.blockDim = dim3(gemm::kThreads);
   cfg.dynamicSmemBytes = gemm::smem_bytes;
   cfg.stream = stream;

@@ -102,6 +102,15 @@ constexpr int kGemmBBox = 32;   // rows per TMA box of the GEMMs' B operand (Y^T
 cudaError_t gemm_kernel_setup();
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const CUtensorMap& tm_yt128,
                         const GemmParams& p, bool weights_mn, cudaStream_t stream);
+// CTA pairs of one contraction's grid, and the dA grid size (in waves of CTA pairs) below which
+// both contractions go in one grid.
+double gemm_grid_pairs(const GemmParams& p);
+constexpr double kGemmMergeWaves = 4.0;
+// Both contractions of one weight chunk (dA with K-major weights, dB with MN-major ones) as one
+// grid, so the dB CTAs fill the dA contraction's last wave.
+cudaError_t launch_gemm_both(const CUtensorMap& tk_w, const CUtensorMap& tk_yt, const CUtensorMap& tk_yt128,
+                             const GemmParams& pk, const CUtensorMap& tn_w, const CUtensorMap& tn_yt,
+                             const CUtensorMap& tn_yt128, const GemmParams& pn, cudaStream_t stream);
 
 // Per-row inverse norms of every prefix for A and B, plus the positives' cosines
 // cos_ii for i < min(Na, Nb).  Layouts [n][rows].

@@ -176,6 +176,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 std::mutex g_init_mu;
 uint64_t g_init_mask = 0;  // devices already set up (device ordinal < 64)
+int g_sm_count[64];        // their SM counts
 
 // ---- optional per-kernel timing (uf_contrastive_profile)
 struct ProfRecord {
@@ -257,6 +258,8 @@ uf_status_t uf_contrastive_init(int device) {
              aux_kernels_setup() != cudaSuccess || !get_encode()) {
     st = UF_CUDA_ERROR;
   }
+  if (st == UF_OK && cudaDeviceGetAttribute(&g_sm_count[device], cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    st = UF_CUDA_ERROR;
   cudaSetDevice(prev);
   if (st == UF_OK) g_init_mask |= uint64_t(1) << device;
   return st;
@@ -594,15 +597,26 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
         ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
         UF_CHECK(launch_labels(pq, stream));
       }
-      ProfScope ps(UF_KERNEL_GEMM, 2, stream);
       ga.m_rows = rows;
       ga.row0 = r0;
-      UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
-      if (!oneset) {
+      // A dA contraction of few waves (few rows: ROWS's queries, small batches) leaves SMs idle
+      // in its last wave, which one grid with the dB contraction fills (ROWS 8192 x 262144:
+      // GEMMs 14.0 -> 12.2 ms).  A long one runs alone: the two read the weights in different
+      // orders, and mixed they share L2 worse (CLIP N = 65536: 23.7 -> 24.6 ms merged).
+      const bool merge = !oneset && gemm_grid_pairs(ga) / (0.5 * g_sm_count[dev]) < kGemmMergeWaves;
+      ProfScope ps(UF_KERNEL_GEMM, oneset || merge ? 1 : 2, stream);
+      if (oneset) {  // (the B side of the one-set loss is the A side's mirror)
+        UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
+      } else {
         gb.kdim = rows;
         gb.b_col0 = r0;
         gb.accumulate = r0 > 0;
-        UF_CHECK(launch_gemm(tmWm, tmAt, tmAt128, gb, true, stream));
+        if (merge) {
+          UF_CHECK(launch_gemm_both(tmWk, tmBt, tmBt128, ga, tmWm, tmAt, tmAt128, gb, stream));
+        } else {
+          UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
+          UF_CHECK(launch_gemm(tmWm, tmAt, tmAt128, gb, true, stream));
+        }
       }
     }
     if (siglip) {
