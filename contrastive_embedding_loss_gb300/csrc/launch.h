@@ -45,8 +45,9 @@ cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
 // [prefix][row][column] array (row stride in elements fixed by tm_w), plus (SigLIP) the
 // row loss sums.  One launch covers rows
 // [row0, row0 + rows) of X; grid = (ceil(rows / 128), splits of the 256-column tiles).
-// tm_x: [128 x 64] boxes of X; tm_y: [256 x 64] boxes of Y; tm_w: [32 x 64] boxes of the
-// weight array viewed as [n * w_rows_per_prefix rows][ny columns].
+// tm_x: [128 x 64] boxes of X; tm_y: [128 x 64] boxes of Y (each CTA of a pair stages half of
+// the 256-row tile); tm_w: [32 x 64] boxes of the weight array viewed as
+// [n * w_rows_per_prefix rows][ny columns].  Launched as CTA pairs (clusters of 2 along x).
 struct WgtParams {
   int64_t nx, ny;                 // full sizes of X and Y
   int64_t row0, rows;             // this launch's rows of X

@@ -584,7 +584,7 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
       wp.rows = rows;
       {
         ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-        UF_CHECK(launch_wgt(kind, tmA, tmBf, tmWs, wp, dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), P.wgt.splits),
+        UF_CHECK(launch_wgt(kind, tmA, tmB, tmWs, wp, dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), P.wgt.splits),
                             stream));
       }
       if (labels) {  // the labelled positives' exact weights over the negative-cell ones

@@ -19,6 +19,13 @@
 //
 // Warps (576 threads): 0 TMA, 1 MMA, 2..17 epilogue (warp w reads TMEM lanes 32 (w % 4)..
 // and one 64-column quarter of the tile).
+//
+// Pairs.  Two CTAs (a cluster of 2 along the row blocks) compute their two 128-row blocks'
+// score tiles together as one M = 256, N = 256 `tcgen05.mma.cta_group::2`: each CTA stages
+// its own 128 rows of X and half (128 rows) of the Y tile, so a CTA's operand traffic per
+// tile is two thirds of what a lone 128 x 256 tile needs (16 + 16 KB a K step instead of
+// 16 + 32 KB) and three stages fit where two did.  The leader (rank 0) issues the MMAs and
+// its barriers count both CTAs' copies; each CTA's epilogue reads its own TMEM.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -34,9 +41,9 @@ constexpr int kThreads = 576;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kNS = 2;                              // operand stages
-constexpr int kXBytes = kTileRows * kChunk * 2;     // 16 KB
-constexpr int kYBytes = kCols * kChunk * 2;         // 32 KB
+constexpr int kNS = 3;                              // operand stages
+constexpr int kXBytes = kTileRows * kChunk * 2;     // 16 KB: this CTA's 128 rows of X
+constexpr int kYBytes = (kCols / 2) * kChunk * 2;   // 16 KB: this CTA's half of the Y tile
 constexpr int kStageRows = 32;                      // one warp's rows of a weight block
 constexpr int kStageBytes = kStageRows * kChunk * 2;  // 4 KB: [32 rows x 64 columns] bf16, 128-byte swizzle
 constexpr int kColfBytes = kMaxPrefix * 2 * kCols * 4;  // [prefix][sigma, sigma*beta][256 columns]
@@ -210,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_misc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
   const int64_t il0 = static_cast<int64_t>(blockIdx.x) * kTileRows;  // first row within this launch
   const int64_t i0 = p.row0 + il0;                                    // first row of X
   const int split = blockIdx.y;
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], kEpiWarps);
+      mbar_init(&acc_empty[a], 2 * kEpiWarps);  // the epilogue warps of both CTAs (leader's copy)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -237,16 +245,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_w);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, 512);  // the same columns in both SMs of the pair
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (T > 0 && warp == 0 && lane == 0) {
     // ------------------------------------------------------------- operand producer
+    // Both CTAs copy their parts into their own shared memory; completion is counted on the
+    // leader's barrier, which the leader arms for the bytes of both.
     uint32_t it = 0;
     bool ok = true;
     for (int s = 0; s < sched.steps() && ok; ++s) {
@@ -261,18 +271,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&s_full[st], kXBytes + kYBytes);
-        tma_load_2d(sx + st * kXBytes, &tm_x, &s_full[st], c * kChunk, static_cast<int>(i0));
-        tma_load_2d(sy + st * kYBytes, &tm_y, &s_full[st], c * kChunk, j0);
+        const uint32_t bar = mapa_shared(smem_u32(&s_full[st]), 0);
+        if (rank == 0) mbar_arrive_expect_tx(&s_full[st], 2 * (kXBytes + kYBytes));
+        tma_load_2d_pair(sx + st * kXBytes, &tm_x, bar, c * kChunk, static_cast<int>(i0));
+        tma_load_2d_pair(sy + st * kYBytes, &tm_y, bar, c * kChunk, j0 + static_cast<int>(rank) * (kCols / 2));
       }
     }
-    for (uint32_t k = 0; k < kNS && k < it; ++k) {  // let the last copies land
-      const uint32_t q = it - 1 - k;
-      mbar_wait(&s_full[q % kNS], (q / kNS) & 1, kWaitLimitNs);
+    if (rank == 0) {
+      for (uint32_t k = 0; k < kNS && k < it; ++k) {  // let the last copies land
+        const uint32_t q = it - 1 - k;
+        mbar_wait(&s_full[q % kNS], (q / kNS) & 1, kWaitLimitNs);
+      }
+    } else {
+      // the follower's copies are counted on the leader's barriers: wait until the MMAs that
+      // read them (hence the copies) are done, i.e. the last stages are released
+      for (uint32_t k = 0; k < kNS && k < it; ++k) {
+        const uint32_t q = it - 1 - k;
+        mbar_wait(&s_empty[q % kNS], (q / kNS) & 1, kWaitLimitNs);
+      }
     }
-  } else if (T > 0 && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------- MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(kTileRows, kCols);
+  } else if (T > 0 && warp == 1 && lane == 0 && rank == 0) {
+    // ------------------------------------------------------------- MMA issuer (leader)
+    const uint32_t idesc = idesc_bf16_f32(2 * kTileRows, kCols);
     uint32_t it = 0;
     uint32_t uses[2] = {0, 0};
     bool ok = true;
@@ -299,15 +319,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ax = smem_u32(sx + st * kXBytes), ay = smem_u32(sy + st * kYBytes);
 #pragma unroll
         for (int kk = 0; kk < kChunk / 16; ++kk)  // bands accumulate: only a tile's first step starts fresh
-          umma_bf16(d, sdesc_kmajor_sw128(ax + kk * 32), sdesc_kmajor_sw128(ay + kk * 32), idesc,
-                    (c != 0 || kk != 0) ? 1u : 0u);
-        umma_commit(&s_empty[st]);
+          umma_bf16_pair(d, sdesc_kmajor_sw128(ax + kk * 32), sdesc_kmajor_sw128(ay + kk * 32), idesc,
+                         (c != 0 || kk != 0) ? 1u : 0u);
+        umma_commit_pair(&s_empty[st]);  // releases the stage in both CTAs
       }
-      if (ok) umma_commit(&acc_full[a]);
+      if (ok) umma_commit_pair(&acc_full[a]);
       ++uses[a];
     }
-    umma_commit(drain);
+    umma_commit_pair(drain);
     mbar_wait(drain, 0, kWaitLimitNs);
+  } else if (T > 0 && warp == 1 && lane == 0) {
+    mbar_wait(drain, 0, kWaitLimitNs);  // the follower: the pair's last MMAs are done
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;                       // TMEM lane quadrant (rows 32q..32q+31)
@@ -405,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, v);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[a]);
+          if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&acc_empty[a]), 0));  // the leader's copy
 
           const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
           const int64_t left = p.ny - j0;
@@ -451,7 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && j0 + cq * 64 < p.ny) {  // a quarter wholly past the last column stores nothing
+          // a quarter wholly past the last column stores nothing, nor does the second CTA of
+          // a pair that lies wholly past the launch's rows (its rows are not in the chunk)
+          if (lane == 0 && il0 < p.rows && j0 + cq * 64 < p.ny) {
             // the weights are written once here and read back by the GEMMs much later: keep
             // them from evicting the score operands, which every CTA re-reads
             tma_store_2d_hint(&tm_w, stage, static_cast<int>(j0 + cq * 64),
@@ -477,10 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // no MMA, copy or remote arrive of the pair is still in flight
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -503,18 +527,25 @@ cudaError_t wgt_kernel_setup() {
 cudaError_t launch_wgt(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_y, const CUtensorMap& tm_w,
                        const WgtParams& p, dim3 grid, cudaStream_t stream) {
   using wgt::wgt_kernel;
-  constexpr int T = wgt::kThreads, S = wgt::smem_bytes;
   if (kind == KIND_SIGLIP && p.shifted) return cudaErrorInvalidValue;
-  if (kind == KIND_CLIP) {
-    if (p.shifted) wgt_kernel<KIND_CLIP, true><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
-    else wgt_kernel<KIND_CLIP, false><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
-  } else if (kind == KIND_SIGLIP) {
-    wgt_kernel<KIND_SIGLIP, false><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
-  } else {
-    if (p.shifted) wgt_kernel<KIND_ROWS, true><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
-    else wgt_kernel<KIND_ROWS, false><<<grid, T, S, stream>>>(tm_x, tm_y, tm_w, p);
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((grid.x + 1) / 2 * 2, grid.y, 1);  // CTA pairs along the row blocks
+  cfg.blockDim = dim3(wgt::kThreads);
+  cfg.dynamicSmemBytes = wgt::smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (kind == KIND_CLIP)
+    return p.shifted ? cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_CLIP, true>, tm_x, tm_y, tm_w, p)
+                     : cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_CLIP, false>, tm_x, tm_y, tm_w, p);
+  if (kind == KIND_SIGLIP) return cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_SIGLIP, false>, tm_x, tm_y, tm_w, p);
+  return p.shifted ? cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_ROWS, true>, tm_x, tm_y, tm_w, p)
+                   : cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_ROWS, false>, tm_x, tm_y, tm_w, p);
 }
 
 }  // namespace ufc
