@@ -5,17 +5,19 @@
 //     B side:  G[j, d] = sum_k [d < p_k] sum_i m^k[i, j] A[i, d]      (weights MN-major)
 //
 // (prefix-expanded: prefix k contributes to its first p_k dimensions).  Two CTAs on two SMs
-// form a pair (a cluster of 2, cta_group::2): together they own 256 rows of G (128 each)
-// and one 256-dimension slice [d0, d0 + 256).  For each prefix reaching the slice, from the
-// widest down, they stream 64-long K chunks of m^k (A operand: each CTA its own 128 rows)
-// and of the other side's transposed embeddings restricted to the slice (B operand, K-major,
-// N = min(p_k, d0 + 256) - d0 rows, each CTA holding half of them); the leader CTA issues
-// 256 x N x 16 MMAs that read both halves, so each SM loads half of the B operand a
-// single-SM 128-row tile would need.  Accumulators: two per CTA in TMEM (256 columns each),
-// alternating between prefixes, so the epilogue of prefix k (add G^k into G in global
-// memory; r^k = x_row . G^k_row, the projection scalar of the norm backward, as this
-// slice's partial) overlaps the MMAs of prefix k - 1.  The weights come from HBM and the
-// other operand mostly from L2: each has its own TMA ring and producer.
+// form a pair (a cluster of 2, cta_group::2): together they own 256 rows of G (128 each) and
+// two adjacent 256-dimension slices, one 256-column TMEM accumulator each.  For each prefix
+// reaching the slices, from the widest down, they stream 64-long K chunks of m^k (A operand:
+// each CTA its own 128 rows, staged once for both slices) and of the other side's transposed
+// embeddings restricted to each slice (B operand, K-major, N = the prefix's width within the
+// slice, each CTA holding half of the rows); the leader CTA issues one 256 x N x 16 MMA per
+// slice.  The prefixes accumulate into the same accumulators, so after prefix k they hold
+// sum_{k' >= k} G^k'; the epilogue reads each such snapshot for the projection scalars of the
+// norm backward (r^k = x_row . G^k_row, this slice's part, is the difference of x . snapshot
+// between prefix k and the one before it, taken over prefix k's width) and writes G once, at
+// the end.  Two slices per pair halve the re-reads of each weight tile that one slice per pair
+// had (the widest prefixes reach every slice).  The weights come from HBM and the other
+// operand mostly from L2: each has its own TMA ring and producer.
 //
 // Warps (224 threads per CTA): lane 0 of warp 0 loads the weights, lane 0 of warp 6 the
 // other operand, lane 0 of warp 1 (leader CTA only) issues the MMAs, warps 2..5 are the
@@ -28,10 +30,11 @@ namespace gemm {
 
 constexpr int kThreads = 224;
 constexpr int kN = 256;                          // gradient slice width = TMEM columns per accumulator
-constexpr int kNA = 7;                           // weight stages
-constexpr int kNB = 6;                           // stages of the other operand
+constexpr int kNA = 5;                           // weight stages
+constexpr int kNB = 4;                           // stages of the other operand
 constexpr int kABytes = kTileRows * kChunk * 2;  // 16 KB: this CTA's 128 rows of G x 64 of K
-constexpr int kBBytes = kN / 2 * kChunk * 2;     // 16 KB: this CTA's half of up to 256 dims x 64 of K
+constexpr int kBHalf = kN / 2 * kChunk * 2;      // 16 KB: this CTA's half of up to 256 dims x 64 of K
+constexpr int kBBytes = 2 * kBHalf;              // both slices of the CTA
 constexpr int kBox = kGemmBBox;                  // rows per B-operand TMA box
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
@@ -91,29 +94,30 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
-  // Grid: [slice pair][row-block pair][slice in the pair][rank].  Slices 2s and 2s + 1 of a
-  // row block run side by side and start on the same weights (the widest prefixes reach
-  // both), which they share through L2; the heavy first pair (every prefix reaches slice 0)
-  // runs first, which keeps the tail of the launch short.
+  // Grid: [slice group][row-block pair][rank].  A CTA pair owns 256 rows of G and the two
+  // adjacent 256-dimension slices s0 = 2 grp and s1 = 2 grp + 1 (one 256-column TMEM
+  // accumulator each), so every weight tile is staged once for both.  The heavy first group
+  // (every prefix reaches slice 0) runs first, which keeps the tail of the launch short.
   int n_slices = 0;
 #pragma unroll
   for (int kk = 0; kk < kMaxPrefix; ++kk)
     if (kk < p.n_prefix) n_slices = (p.prefix_end[kk] + kN - 1) / kN;
   const int64_t pairs = (p.m_rows + 2 * kTileRows - 1) / (2 * kTileRows);
-  const int64_t cta = vblock >> 1;                     // [group][pair][slice in group]
-  const int64_t per_group = pairs * 2;
-  const int grp = static_cast<int>(cta / per_group);
-  const int64_t rem = cta % per_group;
-  const int64_t pair_i = rem / 2;
-  const int slice = grp * 2 + static_cast<int>(rem % 2);
+  const int64_t cta = vblock >> 1;
+  const int grp = static_cast<int>(cta / pairs);
+  const int64_t pair_i = cta % pairs;
   const int64_t m0 = (pair_i * 2 + rank) * kTileRows;  // first row of G in this launch
-  const int d0 = slice * kN;
+  const int d0 = grp * 2 * kN;                          // first dimension of slice s0
   const int n = p.n_prefix;
-  const bool idle = slice >= n_slices;  // an odd slice count leaves the last group half empty
-  int k_first = idle ? n : 0;  // prefixes k_first .. n-1 reach this slice
+  int k_first = 0;  // prefixes k_first .. n-1 reach slice s0 (and so this CTA)
 #pragma unroll
   for (int k = 0; k < kMaxPrefix; ++k)
-    if (!idle && k < n && p.prefix_end[k] <= d0) k_first = k + 1;
+    if (k < n && p.prefix_end[k] <= d0) k_first = k + 1;
+  // prefix k's width within slice s (0: it does not reach the slice)
+  auto width = [&](int k, int sl) {
+    const int w = prefix_end_of(p, k) - (d0 + sl * kN);
+    return w < 0 ? 0 : (w > kN ? kN : w);
+  };
   const int nkc = static_cast<int>((p.kdim + kChunk - 1) / kChunk);  // K chunks per prefix
 
   if (threadIdx.x == 0) {
@@ -125,10 +129,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 8);  // the four epilogue warps of each CTA of the pair (leader's copy)
-    }
+    mbar_init(&acc_full[0], 1);
+    mbar_init(&acc_empty[0], 8);  // the four epilogue warps of each CTA of the pair (leader's copy)
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_w);
@@ -145,9 +147,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
 
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ------------------------------------------------------------- TMA producers
-    // warp 0: the weights (A operand); warp 6: the other side's transposed rows (B operand).
-    // Both CTAs load their own parts into their own shared memory; completion is counted on
-    // the leader's barrier, which the leader arms for the bytes of both.
+    // warp 0: the weights (A operand); warp 6: the other side's transposed rows (B operand)
+    // for both slices.  Both CTAs load their own parts into their own shared memory;
+    // completion is counted on the leader's barrier, which the leader arms for both.
     const bool wa = warp == 0;
     const int ns = wa ? kNA : kNB;
     uint64_t* fullb = wa ? a_full : b_full;
@@ -155,8 +157,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
     uint32_t it = 0;
     bool ok = true;
     for (int k = n - 1; k >= k_first && ok; --k) {
-      const int nk = min(prefix_end_of(p, k), d0 + kN) - d0;
-      const int half = nk / 2;  // B rows held by each CTA
+      const int h0 = width(k, 0) / 2, h1 = width(k, 1) / 2;  // B rows of each slice held by each CTA
       const int64_t wrow = static_cast<int64_t>(k) * p.w_rows_per_prefix;
       for (int c = 0; c < nkc; ++c, ++it) {
         const uint32_t st = it % ns, ph = (it / ns) & 1;
@@ -166,7 +167,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
           break;
         }
         const uint32_t bar = mapa_shared(smem_u32(&fullb[st]), 0);
-        if (rank == 0) mbar_arrive_expect_tx(&fullb[st], 2 * (wa ? kABytes : half * kChunk * 2));
+        if (rank == 0) mbar_arrive_expect_tx(&fullb[st], 2 * (wa ? kABytes : (h0 + h1) * kChunk * 2));
         if (wa) {
           if constexpr (AMN) {
             // [64 K rows x 64 M columns] twice: M blocks 0..63 and 64..127 of this CTA's rows
@@ -177,15 +178,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
             tma_load_2d_pair(sa + st * kABytes, &tm_w, bar, c * kChunk, static_cast<int>(wrow + m0));
           }
         } else {
-          // one 128-row box when the half is full (one TMA instruction: the producer's issue
-          // rate limits this loop), else 32-row boxes
-          if (half == kN / 2)
-            tma_load_2d_pair(sb + st * kBBytes, &tm_yt128, bar, static_cast<int>(p.b_col0 + c * kChunk),
-                             d0 + static_cast<int>(rank) * half);
-          else
-            for (int r0 = 0; r0 < half; r0 += kBox)
-              tma_load_2d_pair(sb + st * kBBytes + r0 * kChunk * 2, &tm_yt, bar,
-                               static_cast<int>(p.b_col0 + c * kChunk), d0 + static_cast<int>(rank) * half + r0);
+          for (int sl = 0; sl < 2; ++sl) {
+            const int half = sl ? h1 : h0;
+            const int dim0 = d0 + sl * kN + static_cast<int>(rank) * half;
+            uint8_t* dst = sb + st * kBBytes + sl * kBHalf;
+            // one 128-row box when the half is full (one TMA instruction: the producer's
+            // issue rate limits this loop), else 32-row boxes
+            if (half == kN / 2)
+              tma_load_2d_pair(dst, &tm_yt128, bar, static_cast<int>(p.b_col0 + c * kChunk), dim0);
+            else
+              for (int r0 = 0; r0 < half; r0 += kBox)
+                tma_load_2d_pair(dst + r0 * kChunk * 2, &tm_yt, bar, static_cast<int>(p.b_col0 + c * kChunk),
+                                 dim0 + r0);
+          }
         }
       }
     }
@@ -204,21 +209,23 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------------- MMA issuer (leader)
+    // The prefixes accumulate, widest first, into one accumulator per slice: after prefix k
+    // it holds sum_{k' >= k} G^k' (prefix k' writes its first width(k', s) columns).
     uint32_t it = 0, pi = 0;
     bool ok = true;
     for (int k = n - 1; k >= k_first && ok; --k, ++pi) {
-      const int nk = min(prefix_end_of(p, k), d0 + kN) - d0;
-      const uint32_t a = pi & 1;
-      // the epilogue must have read this accumulator's previous prefix
-      if (pi >= 2 && !wait_bounded(&acc_empty[a], ((pi - 2) >> 1) & 1, abort_flag)) {
+      const int w0 = width(k, 0), w1 = width(k, 1);
+      // the epilogue must have read the previous prefix's snapshot before this one adds to it
+      if (pi >= 1 && !wait_bounded(&acc_empty[0], (pi - 1) & 1, abort_flag)) {
         fail(p, abort_flag);
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t d = tmem + a * kN;
-      const uint32_t idesc = AMN ? idesc_bf16_f32_amn(2 * kTileRows, static_cast<uint32_t>(nk))
-                                 : idesc_bf16_f32(2 * kTileRows, static_cast<uint32_t>(nk));
+      const uint32_t id0 = AMN ? idesc_bf16_f32_amn(2 * kTileRows, static_cast<uint32_t>(w0))
+                               : idesc_bf16_f32(2 * kTileRows, static_cast<uint32_t>(w0));
+      const uint32_t id1 = AMN ? idesc_bf16_f32_amn(2 * kTileRows, static_cast<uint32_t>(w1))
+                               : idesc_bf16_f32(2 * kTileRows, static_cast<uint32_t>(w1));
       for (int c = 0; c < nkc; ++c, ++it) {
         const uint32_t sta = it % kNA, pha = (it / kNA) & 1;
         const uint32_t stb = it % kNB, phb = (it / kNB) & 1;
@@ -234,77 +241,114 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
           // K = 16 per MMA: MN-major A advances 16 K rows (two 1024-byte atoms), K-major 32 bytes
           const uint64_t adesc = AMN ? sdesc_mnmajor_sw128(as + kk * 2048, kABytes / 2, 1024)
                                      : sdesc_kmajor_sw128(as + kk * 32);
-          umma_bf16_pair(d, adesc, sdesc_kmajor_sw128(bs + kk * 32), idesc, (c != 0 || kk != 0) ? 1u : 0u);
+          const uint32_t acc = (pi != 0 || c != 0 || kk != 0) ? 1u : 0u;  // the widest prefix starts fresh
+          umma_bf16_pair(tmem, adesc, sdesc_kmajor_sw128(bs + kk * 32), id0, acc);
+          if (w1 > 0) umma_bf16_pair(tmem + kN, adesc, sdesc_kmajor_sw128(bs + kBHalf + kk * 32), id1, acc);
         }
-        umma_commit_pair(&a_empty[sta]);  // releases the stage in both CTAs
+        umma_commit_pair(&a_empty[sta]);  // releases the stages in both CTAs
         umma_commit_pair(&b_empty[stb]);
       }
-      if (ok) umma_commit_pair(&acc_full[a]);
+      if (ok) umma_commit_pair(&acc_full[0]);
     }
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------- epilogue
+    // After each prefix k: d_s(c) = x . S_k over the first c columns of slice s at every
+    // 64-column boundary c; r^k (this slice's part) = d_s(w_k) - (the previous snapshot's
+    // d_s(w_k)), as S_k - S_{k+1} = G^k over the first w_k columns.  After the last prefix,
+    // the accumulators are G: written once (added over weight chunks when accumulating).
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const int64_t gl = m0 + r;              // row within this launch
     const int64_t g = p.row0 + gl;          // row of G / X / crow
     const bool row_ok = gl < p.m_rows;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    float* grow = p.G + g * p.d + d0;
-    const uint16_t* xrow = p.X + g * p.d + d0;
-    // prefixes that do not reach this slice contribute nothing to its slot
-    if (row_ok && !p.accumulate && !idle)
-      for (int k = 0; k < k_first; ++k) p.crow[(static_cast<int64_t>(slice) * n + k) * p.crow_rows + g] = 0.f;
+    const int wmax[2] = {width(n - 1, 0), width(n - 1, 1)};  // columns of each slice with data
+    // prefixes that do not reach a slice contribute nothing to its slot
+    if (row_ok && !p.accumulate)
+      for (int sl = 0; sl < 2; ++sl)
+        if (2 * grp + sl < n_slices)
+          for (int k = 0; k < n; ++k)
+            if (width(k, sl) == 0) p.crow[(static_cast<int64_t>(2 * grp + sl) * n + k) * p.crow_rows + g] = 0.f;
+    float prevd[2][kN / 64], curd[2][kN / 64];
+#pragma unroll
+    for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+      for (int b = 0; b < kN / 64; ++b) prevd[sl][b] = 0.f;
     uint32_t pi = 0;
     bool ok = true;
     for (int k = n - 1; k >= k_first; --k, ++pi) {
       if (!ok) continue;
-      const int nk = min(prefix_end_of(p, k), d0 + kN) - d0;
-      const uint32_t a = pi & 1;
-      if (!wait_bounded(&acc_full[a], (pi >> 1) & 1, abort_flag)) {
+      if (!wait_bounded(&acc_full[0], pi & 1, abort_flag)) {
         fail(p, abort_flag);
         ok = false;
         continue;
       }
       tc_fence_after();
-      const bool first = pi == 0 && !p.accumulate;  // the widest prefix writes G, the others add
-      float rk = 0.f;
-      for (int c = 0; c < nk; c += 32) {
-        float v[32];
-        tmem_ld32(tmem + lane_addr + a * kN + c, v);
-        if (row_ok) {
+      const bool last = k == k_first;
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + c + j);
-            rk = fmaf(bf16_lo(xv.x), v[j + 0], rk);
-            rk = fmaf(bf16_hi(xv.x), v[j + 1], rk);
-            rk = fmaf(bf16_lo(xv.y), v[j + 2], rk);
-            rk = fmaf(bf16_hi(xv.y), v[j + 3], rk);
-            rk = fmaf(bf16_lo(xv.z), v[j + 4], rk);
-            rk = fmaf(bf16_hi(xv.z), v[j + 5], rk);
-            rk = fmaf(bf16_lo(xv.w), v[j + 6], rk);
-            rk = fmaf(bf16_hi(xv.w), v[j + 7], rk);
-          }
+      for (int sl = 0; sl < 2; ++sl) {
+        float run = 0.f;
+        float* grow = p.G + g * p.d + d0 + sl * kN;
+        const uint16_t* xrow = p.X + g * p.d + d0 + sl * kN;
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-            if (!first) {
-              const float4 prev = *reinterpret_cast<const float4*>(grow + c + j);
-              o.x += prev.x;
-              o.y += prev.y;
-              o.z += prev.z;
-              o.w += prev.w;
+        for (int b = 0; b < kN / 64; ++b) curd[sl][b] = 0.f;
+        for (int c = 0; c < wmax[sl]; c += 32) {
+          float v[32];
+          tmem_ld32(tmem + lane_addr + sl * kN + c, v);
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(xrow + c + j);
+              run = fmaf(bf16_lo(xv.x), v[j + 0], run);
+              run = fmaf(bf16_hi(xv.x), v[j + 1], run);
+              run = fmaf(bf16_lo(xv.y), v[j + 2], run);
+              run = fmaf(bf16_hi(xv.y), v[j + 3], run);
+              run = fmaf(bf16_lo(xv.z), v[j + 4], run);
+              run = fmaf(bf16_hi(xv.z), v[j + 5], run);
+              run = fmaf(bf16_lo(xv.w), v[j + 6], run);
+              run = fmaf(bf16_hi(xv.w), v[j + 7], run);
             }
-            *reinterpret_cast<float4*>(grow + c + j) = o;
+            if (last) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4) {
+                float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                if (p.accumulate) {
+                  const float4 prev = *reinterpret_cast<const float4*>(grow + c + j);
+                  o.x += prev.x;
+                  o.y += prev.y;
+                  o.z += prev.z;
+                  o.w += prev.w;
+                }
+                *reinterpret_cast<float4*>(grow + c + j) = o;
+              }
+            }
           }
+#pragma unroll
+          for (int b = 0; b < kN / 64; ++b)
+            if (c + 32 == 64 * (b + 1)) curd[sl][b] = run;
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&acc_empty[a]), 0));
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&acc_empty[0]), 0));
       if (row_ok) {
-        float* pc = p.crow + (static_cast<int64_t>(slice) * n + k) * p.crow_rows + g;
-        *pc = p.accumulate ? *pc + rk : rk;
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl) {
+          const int w = width(k, sl);
+          if (w > 0) {
+            float rk = 0.f;
+#pragma unroll
+            for (int b = 0; b < kN / 64; ++b)
+              if (w == 64 * (b + 1)) rk = curd[sl][b] - prevd[sl][b];
+            float* pc = p.crow + (static_cast<int64_t>(2 * grp + sl) * n + k) * p.crow_rows + g;
+            *pc = p.accumulate ? *pc + rk : rk;
+          }
+        }
       }
+#pragma unroll
+      for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+        for (int b = 0; b < kN / 64; ++b) prevd[sl][b] = curd[sl][b];
     }
   }
 
@@ -342,13 +386,13 @@ static cudaError_t setup_one() {
   return cudaFuncSetAttribute(gemm_kernel<AMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-// CTAs of one contraction: [slice pair][row-block pair][slice in the pair][rank]
+// CTAs of one contraction: [slice group (two slices)][row-block pair][rank]
 unsigned grid_of(const GemmParams& p) {
   const int pn = p.prefix_end[p.n_prefix - 1];
   const int64_t blocks = (p.m_rows + kTileRows - 1) / kTileRows;
   const int64_t n_slices = (pn + kN - 1) / kN;
   const int64_t groups = (n_slices + 1) / 2;
-  return static_cast<unsigned>(groups * ((blocks + 1) / 2) * 2 * 2);
+  return static_cast<unsigned>(groups * ((blocks + 1) / 2) * 2);
 }
 
 }  // namespace gemm
