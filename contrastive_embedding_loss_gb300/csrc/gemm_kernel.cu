@@ -276,8 +276,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
       for (int b = 0; b < kN / 64; ++b) prevd[sl][b] = 0.f;
     uint32_t pi = 0;
     bool ok = true;
+    // x rows are read in 32-column chunks, each fetched one chunk ahead (the first before the
+    // snapshot is ready): the MMA waits for this read, so it must not wait on L2 per chunk
+    auto load_x = [&](int sl, int c, uint4 (&xv)[4]) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.X + g * p.d + d0 + sl * kN + c);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) xv[u] = row_ok ? src[u] : make_uint4(0, 0, 0, 0);
+    };
     for (int k = n - 1; k >= k_first; --k, ++pi) {
       if (!ok) continue;
+      uint4 xcur[4], xnext[4];
+      load_x(0, 0, xcur);
       if (!wait_bounded(&acc_full[0], pi & 1, abort_flag)) {
         fail(p, abort_flag);
         ok = false;
@@ -289,16 +298,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
       for (int sl = 0; sl < 2; ++sl) {
         float run = 0.f;
         float* grow = p.G + g * p.d + d0 + sl * kN;
-        const uint16_t* xrow = p.X + g * p.d + d0 + sl * kN;
 #pragma unroll
         for (int b = 0; b < kN / 64; ++b) curd[sl][b] = 0.f;
         for (int c = 0; c < wmax[sl]; c += 32) {
+          // the next chunk: this slice's, else the next slice's first
+          if (c + 32 < wmax[sl]) load_x(sl, c + 32, xnext);
+          else if (sl == 0 && wmax[1] > 0) load_x(1, 0, xnext);
           float v[32];
           tmem_ld32(tmem + lane_addr + sl * kN + c, v);
           if (row_ok) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              const uint4 xv = *reinterpret_cast<const uint4*>(xrow + c + j);
+            for (int u = 0; u < 4; ++u) {
+              const uint4 xv = xcur[u];
+              const int j = 8 * u;
               run = fmaf(bf16_lo(xv.x), v[j + 0], run);
               run = fmaf(bf16_hi(xv.x), v[j + 1], run);
               run = fmaf(bf16_lo(xv.y), v[j + 2], run);
@@ -326,6 +338,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
 #pragma unroll
           for (int b = 0; b < kN / 64; ++b)
             if (c + 32 == 64 * (b + 1)) curd[sl][b] = run;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) xcur[u] = xnext[u];
         }
       }
       tc_fence_before();
