@@ -120,6 +120,30 @@ def test_clip_n65536_sampled_and_properties(ctx):
         assert err <= 1e-2 * g2.abs().max().item(), what
 
 
+def test_clip_n65536_in_two_large_chunks(ctx):
+    """A workspace that holds 40960 rows of weights cuts the backward into two chunks.  The
+    first chunk's dA grid is more than four waves of CTA pairs, so its two contractions run
+    as separate launches, and the second chunk's dB contraction adds into the first's: the
+    chunked result matches the one-chunk result (dA exactly: each row of dA comes from one
+    chunk over every column; dB up to the fp32 rounding of adding two chunks)."""
+    kind, A16, B16, s, b = synth.workload("clip_n65536_hardneg")
+    N, D = A16.shape
+    k = ctx.KINDS[kind]
+    wmin = ctx.uf_contrastive_workspace_min(N, N, D, LADDER, k, True)  # one 128-row chunk
+    ws = torch.empty(wmin + len(LADDER) * (40960 - 128) * N * 2, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    A, B = dev(A16), dev(B16)
+    two = ctx.contrastive_fwd_bwd(A, B, kind, LADDER, s, b, grads=True, workspace=ws, device_status=status)
+    del ws
+    one = ctx.contrastive_fwd_bwd(A, B, kind, LADDER, s, b, grads=True, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(two["loss"], one["loss"])
+    assert torch.equal(two["dA"], one["dA"])
+    err = (two["dB"] - one["dB"]).abs().max().item()
+    assert err <= 1e-4 * one["dB"].abs().max().item(), err
+
+
 def test_rows_q8192_k262144_sampled(ctx):
     kind, Q16, K16, s, b = synth.workload("rows_q8192_k262144")
     out = run(ctx, kind, Q16, K16, s, b)
