@@ -77,6 +77,12 @@ SMALL = [
     ("rows", 1, 300, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 19),       # one query
     ("clip", 192, 192, 1024, LADDER, 40.0, 0.0, 3.0, 21),         # the largest supported tau
     ("clip", 260, 260, 640, (64, 320, 640), 5.0, 0.0, 1.0, 22),   # an odd number of 256-dimension slices
+    # the limits of the API: one 64-wide band, eight prefixes, D up to 4096 (sixteen slices)
+    ("clip", 300, 300, 64, (64,), 1 / 0.07, 0.0, 1.0, 23),
+    ("clip", 260, 260, 512, (64, 128, 192, 256, 320, 384, 448, 512), 1 / 0.07, 0.0, 1.0, 24),
+    ("siglip", 200, 200, 2048, (64, 128, 256, 512, 1024, 2048), 10.0, -10.0, 0.7, 25),
+    ("rows", 130, 400, 4096, (64, 256, 1024, 4096), 1 / 0.05, 0.0, 0.8, 26),
+    ("clip", 256, 256, 4096, (64, 128, 256, 512, 1024, 2048, 4096), 1 / 0.07, 0.0, 1.0, 27),
 ]
 
 
