@@ -120,6 +120,25 @@ def test_clip_n65536_sampled_and_properties(ctx):
         assert err <= 1e-2 * g2.abs().max().item(), what
 
 
+def test_clip_n65536_at_the_clip_clamp_sampled(ctx):
+    """tau = 100 (CLIP's clamp) at the full size: the max-shifted statistics (a max pass, the
+    shifts of 65536 rows and columns over 512 row blocks, shifted sums, two exponentials in the
+    weight pass).  Noise 6 puts the positives' cosine near 0.16, where the fixed shift would lose
+    every sum to fp32 underflow; the loss stays O(1)."""
+    kind, s, b = "clip", 100.0, 0.0
+    A16, B16 = synth.paired(65536, 1024, 6.0, 31)
+    out = run(ctx, kind, A16, B16, s, b)
+    check_loss_is_mean_of_terms(out, kind)
+    rows = sample(A16.shape[0], 256, 6)
+    check_terms(out["row_terms"][:, rows].double().cpu().numpy(),
+                oracle.row_terms_sampled(kind, A16, B16, LADDER, s, b, rows), "row terms")
+    cols = sample(B16.shape[0], 256, 7)
+    check_terms(out["col_terms"][:, cols].double().cpu().numpy(),
+                oracle.row_terms_sampled(kind, B16, A16, LADDER, s, b, cols), "col terms")
+    check_euler(A16, out["dA"], "dA")
+    check_euler(B16, out["dB"], "dB")
+
+
 def test_clip_n65536_in_two_large_chunks(ctx):
     """A workspace that holds 40960 rows of weights cuts the backward into two chunks.  The
     first chunk's dA grid is more than four waves of CTA pairs, so its two contractions run
