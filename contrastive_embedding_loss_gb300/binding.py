@@ -64,6 +64,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.uf_contrastive_oneset_fwd_bwd.argtypes = [P, I64, I32, P, I32, F32, F32, P, P, P, P, P, P, P, P, P, P, P, SZ,
                                                   P, P]
     lib.uf_contrastive_oneset_fwd_bwd.restype = I32
+    lib.uf_contrastive_selftest_wait.argtypes = [P, I32, P]
+    lib.uf_contrastive_selftest_wait.restype = I32
     lib.uf_contrastive_profile.argtypes = [I32]
     lib.uf_contrastive_profile.restype = I32
     lib.uf_contrastive_profile_read.argtypes = [I32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64),
@@ -143,6 +145,12 @@ def uf_contrastive_oneset_fwd_bwd(X, N, D, prefixes, logit_scale, bias, logit_sc
                                                     float(bias), logit_scale_dev, bias_dev, pos_offsets, pos_ids, w,
                                                     loss_per_prefix, row_terms, dX, d_logit_scale, d_bias, workspace,
                                                     int(workspace_bytes), device_status, stream))
+
+
+def uf_contrastive_selftest_wait(device_status, limit_ms, stream) -> int:
+    """Raw call: one kernel whose bounded wait runs out stores UF_DEVICE_TIMEOUT at the int
+    device address device_status (a check of the kernels' failure path)."""
+    return int(load().uf_contrastive_selftest_wait(device_status, int(limit_ms), stream))
 
 
 KERNEL_GROUPS = ("prep", "transpose", "fwd_tile", "stats", "bwd_tile", "norm_bwd", "gemm")

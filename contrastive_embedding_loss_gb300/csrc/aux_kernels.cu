@@ -11,6 +11,7 @@
 #include <cmath>
 
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace ufc {
 
@@ -559,6 +560,29 @@ cudaError_t launch_labels(const LabelParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------ wait self-test
+// The bounded wait of the pipeline kernels, on a barrier that nothing completes: one thread
+// gives up after limit_ns and reports as they do (UF_DEVICE_TIMEOUT in *status), and the
+// kernel ends, leaving the context usable.
+__global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    if (!mbar_wait_abortable(&bar, 0, &abort_flag, limit_ns)) {
+      abort_flag = 1;
+      atomicExch(status, kStatusTimeout);
+    }
+  }
+}
+
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream) {
   scale_grad_kernel<<<1, 1024, 0, stream>>>(p);
   return cudaGetLastError();
@@ -582,6 +606,7 @@ cudaError_t aux_kernels_setup() {
   if ((e = cudaFuncGetAttributes(&fa, scale_grad_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, max_reduce_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, labels_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, wait_selftest_kernel)) != cudaSuccess) return e;
   return cudaFuncGetAttributes(&fa, norm_bwd_kernel);
 }
 

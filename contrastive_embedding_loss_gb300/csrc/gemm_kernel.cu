@@ -47,15 +47,7 @@ constexpr int smem_bytes = off_misc + 16 + 1024;
 static_assert(smem_bytes <= 232448, "gemm shared memory");
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-  }
+  return mbar_wait_abortable(bar, parity, abort_flag, kWaitLimitNs);
 }
 
 __device__ __forceinline__ void fail(const GemmParams& p, volatile int* abort_flag) {

@@ -255,4 +255,7 @@ struct LabelParams {
 };
 cudaError_t launch_labels(const LabelParams& p, cudaStream_t stream);
 
+// One thread waits, with the pipeline kernels' bounded wait, on a barrier nothing completes.
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
+
 }  // namespace ufc

@@ -722,6 +722,17 @@ uf_status_t uf_contrastive_oneset_fwd_bwd(const void* X, int64_t N, int D, const
                   d_bias, workspace, workspace_bytes, device_status, stream_handle, true);
 }
 
+uf_status_t uf_contrastive_selftest_wait(int* device_status, int limit_ms, void* stream_handle) {
+  if (!device_status || !aligned(device_status, 4) || limit_ms < 1 || limit_ms > 10000) return UF_INVALID_ARGUMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UF_CUDA_ERROR;
+  if (uf_contrastive_init(dev) != UF_OK) return UF_CUDA_ERROR;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  if (launch_wait_selftest(device_status, static_cast<uint64_t>(limit_ms) * 1000000ull, stream) != cudaSuccess)
+    return UF_CUDA_ERROR;
+  return UF_OK;
+}
+
 uf_status_t uf_contrastive_profile(int enable) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (enable) {

@@ -245,6 +245,17 @@ UF_API uf_status_t uf_contrastive_fwd_bwd_static(const void* A, const void* B, i
                                                   int* device_status, void* stream);
 
 /*
+ * Self-test of the failure path: every pipeline kernel waits on its barriers with a bound
+ * (4 s) and, when one runs out, stores UF_DEVICE_TIMEOUT in *device_status and ends, so the
+ * CUDA context stays usable.  This enqueues one kernel that takes the same bounded wait on a
+ * barrier that nothing completes, with a limit of limit_ms (1..10000) milliseconds: after it,
+ * *device_status (a device int, 4-byte aligned) holds UF_DEVICE_TIMEOUT.  Nothing faults,
+ * traps or hangs.  Returns UF_INVALID_ARGUMENT for a NULL or misaligned status or a limit out
+ * of range, UF_CUDA_ERROR when the launch fails.
+ */
+UF_API uf_status_t uf_contrastive_selftest_wait(int* device_status, int limit_ms, void* stream);
+
+/*
  * Optional per-kernel timing, for benchmarks and profiling (not part of the loss).
  * While enabled, every uf_contrastive_fwd_bwd records a pair of CUDA events on its
  * stream around each group of internal kernel launches and keeps the pairs in a host

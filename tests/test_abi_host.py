@@ -225,3 +225,16 @@ def test_oneset_arguments_are_checked_on_the_host(lib):
         pytest.skip("a GPU is present")
     assert call() == CUDA
     assert call(dX=None) == CUDA
+
+
+def test_wait_selftest_arguments(lib):
+    INV, CUDA = 1, 4
+    assert binding.uf_contrastive_selftest_wait(None, 100, None) == INV
+    assert binding.uf_contrastive_selftest_wait(FAKE + 2, 100, None) == INV
+    assert binding.uf_contrastive_selftest_wait(FAKE, 0, None) == INV
+    assert binding.uf_contrastive_selftest_wait(FAKE, 10001, None) == INV
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert binding.uf_contrastive_selftest_wait(FAKE, 100, None) == CUDA
