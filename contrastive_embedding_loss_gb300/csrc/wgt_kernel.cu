@@ -415,12 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
           }
           tc_fence_after();
-          float v[64];
-          tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, v);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&acc_empty[a]), 0));  // the leader's copy
-
+          // this warp's 64 columns as two 32-column halves, the second read once the first is
+          // processed (32 fewer live registers: the SigLIP and max-shifted epilogues no longer
+          // spill); the accumulator is released after the second read
+          float v0[32], v1[32];
+          const uint32_t ta = tmem + lane_addr + a * kCols + cq * 64;
+          tmem_ld32(ta, v0);
           const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
           const int64_t left = p.ny - j0;
           const int ncols = left < kCols ? static_cast<int>(left) : kCols;
@@ -436,33 +436,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) bulk_wait_read0();
           __syncwarp();
           float2 al = make_float2(0.f, 0.f);
-          if constexpr (SHIFTED) {
-            if (check) {
+          // four 8-column chunks of one half (vh: its 32 values; chb: its first chunk); the mask
+          // test is hoisted out of the unrolled loops
+          auto chunks = [&](const float* vh, int chb) {
+            const uint32_t dst = stage_row, f1 = c1 + chb * 32, f2 = c2 + chb * 32;
+            const int col0 = cq * 64 + chb * 8;
+            if constexpr (SHIFTED) {
+              if (check) {
 #pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                st_shared_v4(stage_row + ((ch ^ swz) << 4),
-                             cells8_shifted<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, wk,
-                                                        cq * 64 + ch * 8, ncols, diag_col, row_ok));
+                for (int cc = 0; cc < 4; ++cc)
+                  st_shared_v4(dst + (((chb + cc) ^ swz) << 4),
+                               cells8_shifted<KIND, true>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, wk,
+                                                          col0 + cc * 8, ncols, diag_col, row_ok));
+              } else {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                  st_shared_v4(dst + (((chb + cc) ^ swz) << 4),
+                               cells8_shifted<KIND, false>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, wk, 0,
+                                                           0, 0, true));
+              }
+            } else if (check) {
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                st_shared_v4(dst + (((chb + cc) ^ swz) << 4),
+                             cells8<KIND, true>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, L, b2,
+                                                col0 + cc * 8, ncols, diag_col, row_ok, al));
             } else {
 #pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                st_shared_v4(stage_row + ((ch ^ swz) << 4),
-                             cells8_shifted<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, wk, 0,
-                                                         0, 0, true));
+              for (int cc = 0; cc < 4; ++cc)
+                st_shared_v4(dst + (((chb + cc) ^ swz) << 4),
+                             cells8<KIND, false>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, L, b2, 0, 0, 0,
+                                                 true, al));
             }
-          } else if (check) {
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              st_shared_v4(stage_row + ((ch ^ swz) << 4),
-                           cells8<KIND, true>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, L, b2,
-                                              cq * 64 + ch * 8, ncols, diag_col, row_ok, al));
-          } else {
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              st_shared_v4(stage_row + ((ch ^ swz) << 4),
-                           cells8<KIND, false>(v + ch * 8, c1 + ch * 32, c2 + ch * 32, R1, R2, R3, L, b2, 0, 0,
-                                               0, true, al));
-          }
+          };
+          chunks(v0, 0);
+          tmem_ld32(ta + 32, v1);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&acc_empty[a]), 0));  // the leader's copy
+          chunks(v1, 4);
           fence_proxy_async_smem();
           __syncwarp();
           // a quarter wholly past the last column stores nothing, nor does the second CTA of
