@@ -13,11 +13,13 @@
 // band while the epilogue reads this one's.
 //
 // Epilogue.  16 warps: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows) and one
-// quarter (64 columns) of the tile.  Column sums: each warp reduces its 32 rows per
-// column by a shuffle reduce-scatter (lane l ends with column l of each 32-column group),
-// the four row-quadrant warps of a column quarter combine through shared memory, and one
-// of them writes the 128-row partial of every column to global memory (one slot per row
-// block; a reduction kernel adds the slots in a fixed order).
+// quarter (64 columns) of the tile, half of it at a time.  Row-only sums (ROWS, SigLIP) use
+// the 32x32b layout: a lane holds one row, read as two 32-column groups.  With column sums
+// (CLIP) the 16x256b layout puts a column's 32 cells 4 to a lane on 8 lanes (two 16-row
+// halves), so the column sums are in-thread adds and a 3-stage scatter over 8 lanes; the
+// four row-quadrant warps of a column quarter combine through shared memory, and one of them
+// writes the 128-row partial of every column to global memory (one slot per row block; a
+// reduction kernel adds the slots in a fixed order).
 //
 // Shifts.  The default sums 2^(x - L) with x = tau log2(e) cos and the fixed shift L =
 // tau log2(e): |cos| <= 1 keeps every term in [2^-2L, 1], normal fp32 while tau <= 40.
@@ -85,131 +87,80 @@ __device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag) 
   if (p.status) atomicExch(p.status, kStatusTimeout);
 }
 
-// Sum (or MAX: maximum) of 32 values over the warp's 32 lanes, scattered: lane l returns
-// the sum of v[l].  (fp32 throughout: the summands span e^-2tau .. 1, beyond what fp16
-// pairs could carry.)
-template <bool MAX = false>
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < m; ++i) {
-      const float lo = v[i], hi = v[i + m];
-      const float send = upper ? lo : hi;
-      const float keep = upper ? hi : lo;
-      const float got = __shfl_xor_sync(0xffffffffu, send, m);
-      v[i] = MAX ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  return v[0];
-}
+// The row-only epilogues (ROWS, SigLIP) on the 32x32b TMEM layout: a lane holds one row and
+// the warp's 64 columns of it arrive as two 32-column groups.  Each function takes group g
+// (v: its 32 values; columns g*32 .. g*32+31 of the warp's quarter) and adds to rs, two
+// interleaved row accumulators.  CHECK evaluates the masks (padding columns and rows, the
+// positive's diagonal cell).
 
-// One snapshot of this thread's 64 cells: the row sum is returned, and (COLS) the
-// warp's 32-row column partials of the 64 columns go to cp[0..63].  CHECK evaluates the
-// masks (padding columns and rows, the positive's diagonal cell).
-template <int KIND, bool COLS, bool CHECK>
-__device__ __forceinline__ float fwd_cells(const float (&v)[64], const float* cf, float R1, float L, float b2,
-                                           int col_base, int ncols, int dcol, bool row_ok, int lane, float* cp) {
-  float2 rs = make_float2(0.f, 0.f);  // two interleaved row sums
+// Sums of 2^(R1 sigma_j dot - L) (CLIP/ROWS) or softplus(x) in log2 units (SigLIP).
+template <int KIND, bool CHECK>
+__device__ __forceinline__ void fwd_cells(const float (&v)[32], int g, const float* cf, float R1, float L, float b2,
+                                          int col_base, int ncols, int dcol, bool row_ok, float2& rs) {
   const float2 r1 = make_float2(R1, R1), nl = make_float2(-L, -L);
 #pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    float e[32];
+  for (int j = 0; j < 32; j += 2) {
+    const int c = g * 32 + j;
+    float2 val;
+    if constexpr (KIND == KIND_SIGLIP) {
+      float w[2];
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const int c = g * 32 + j;
-      float2 val;
-      if constexpr (KIND == KIND_SIGLIP) {
-        float w[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float x2 = fmaf(R1 * cf[c + u], v[c + u], b2);
-          w[u] = fmaxf(x2, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(x2)));
-        }
-        val = make_float2(w[0], w[1]);
-      } else {
-        // two cells per packed instruction: 2^(R1 sigma_j dot - L)
-        const float2 x = fma2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[c], v[c + 1]), nl);
-        val = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      for (int u = 0; u < 2; ++u) {
+        const float x2 = fmaf(R1 * cf[c + u], v[j + u], b2);
+        w[u] = fmaxf(x2, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(x2)));
       }
-      if constexpr (CHECK) {
-        const int col = col_base + c;
-        if (!(row_ok && col < ncols && col != dcol)) val.x = 0.f;
-        if (!(row_ok && col + 1 < ncols && col + 1 != dcol)) val.y = 0.f;
-      }
-      e[j] = val.x;
-      e[j + 1] = val.y;
-      rs = add2(rs, val);
+      val = make_float2(w[0], w[1]);
+    } else {
+      // two cells per packed instruction
+      const float2 x = fma2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[j], v[j + 1]), nl);
+      val = make_float2(ex2_approx(x.x), ex2_approx(x.y));
     }
-    if constexpr (COLS) cp[g * 32 + lane] = reduce_scatter32(e, lane);  // column col_base + g*32 + lane
+    if constexpr (CHECK) {
+      const int col = col_base + c;
+      if (!(row_ok && col < ncols && col != dcol)) val.x = 0.f;
+      if (!(row_ok && col + 1 < ncols && col + 1 != dcol)) val.y = 0.f;
+    }
+    rs = add2(rs, val);
   }
-  return rs.x + rs.y;
 }
 
-// kFwdMax: the row maximum of x = R1 sigma_j dot over this thread's 64 cells is returned,
-// the warp's 32-row column maxima go to cp (COLS).  Only padding is masked (to -inf).
-template <bool COLS, bool CHECK>
-__device__ __forceinline__ float fwd_cells_max(const float (&v)[64], const float* cf, float R1, int col_base,
-                                               int ncols, bool row_ok, int lane, float* cp) {
-  float2 rm = make_float2(-INFINITY, -INFINITY);
+// kFwdMax: the running maxima of x = R1 sigma_j dot.  Only padding is masked (to -inf).
+template <bool CHECK>
+__device__ __forceinline__ void fwd_cells_max(const float (&v)[32], int g, const float* cf, float R1, int col_base,
+                                              int ncols, bool row_ok, float2& rm) {
   const float2 r1 = make_float2(R1, R1);
 #pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    float x[32];
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const int c = g * 32 + j;
-      // the same two roundings as fwd_cells_shifted, so that x - u_i <= 0 holds exactly there
-      float2 val = mul2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[c], v[c + 1]));
-      if constexpr (CHECK) {
-        const int col = col_base + c;
-        if (!(row_ok && col < ncols)) val.x = -INFINITY;
-        if (!(row_ok && col + 1 < ncols)) val.y = -INFINITY;
-      }
-      x[j] = val.x;
-      x[j + 1] = val.y;
-      rm = make_float2(fmaxf(rm.x, val.x), fmaxf(rm.y, val.y));
+  for (int j = 0; j < 32; j += 2) {
+    const int c = g * 32 + j;
+    // the same two roundings as fwd_cells_shifted, so that x - u_i <= 0 holds exactly there
+    float2 val = mul2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[j], v[j + 1]));
+    if constexpr (CHECK) {
+      const int col = col_base + c;
+      if (!(row_ok && col < ncols)) val.x = -INFINITY;
+      if (!(row_ok && col + 1 < ncols)) val.y = -INFINITY;
     }
-    if constexpr (COLS) cp[g * 32 + lane] = reduce_scatter32<true>(x, lane);
+    rm = make_float2(fmaxf(rm.x, val.x), fmaxf(rm.y, val.y));
   }
-  return fmaxf(rm.x, rm.y);
 }
 
-// kFwdShifted: the row sum of 2^(x - U) is returned (U the row's shift), and (COLS) the
-// warp's column partials of 2^(x - vs[c]) go to cp.  Masks as in fwd_cells.
-template <bool COLS, bool CHECK>
-__device__ __forceinline__ float fwd_cells_shifted(const float (&v)[64], const float* cf, const float* vs, float R1,
-                                                   float U, int col_base, int ncols, int dcol, bool row_ok, int lane,
-                                                   float* cp) {
-  float2 rs = make_float2(0.f, 0.f);
+// kFwdShifted: sums of 2^(x - U), U the row's shift.  Masks as in fwd_cells.
+template <bool CHECK>
+__device__ __forceinline__ void fwd_cells_shifted(const float (&v)[32], int g, const float* cf, float R1, float U,
+                                                  int col_base, int ncols, int dcol, bool row_ok, float2& rs) {
   const float2 r1 = make_float2(R1, R1), nu = make_float2(-U, -U);
 #pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    float e[32];
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const int c = g * 32 + j;
-      const float2 x = mul2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[c], v[c + 1]));
-      const float2 xr = add2(x, nu);
-      float2 er = make_float2(ex2_approx(xr.x), ex2_approx(xr.y));
-      float2 ec = make_float2(0.f, 0.f);
-      if constexpr (COLS) {
-        const float2 xc = add2(x, make_float2(-vs[c], -vs[c + 1]));
-        ec = make_float2(ex2_approx(xc.x), ex2_approx(xc.y));
-      }
-      if constexpr (CHECK) {
-        const int col = col_base + c;
-        if (!(row_ok && col < ncols && col != dcol)) er.x = ec.x = 0.f;
-        if (!(row_ok && col + 1 < ncols && col + 1 != dcol)) er.y = ec.y = 0.f;
-      }
-      e[j] = ec.x;
-      e[j + 1] = ec.y;
-      rs = add2(rs, er);
+  for (int j = 0; j < 32; j += 2) {
+    const int c = g * 32 + j;
+    const float2 x = mul2(mul2(r1, make_float2(cf[c], cf[c + 1])), make_float2(v[j], v[j + 1]));
+    const float2 xr = add2(x, nu);
+    float2 er = make_float2(ex2_approx(xr.x), ex2_approx(xr.y));
+    if constexpr (CHECK) {
+      const int col = col_base + c;
+      if (!(row_ok && col < ncols && col != dcol)) er.x = 0.f;
+      if (!(row_ok && col + 1 < ncols && col + 1 != dcol)) er.y = 0.f;
     }
-    if constexpr (COLS) cp[g * 32 + lane] = reduce_scatter32(e, lane);
+    rs = add2(rs, er);
   }
-  return rs.x + rs.y;
 }
 
 // Reduce-scatter of NV values over the 2^STAGES lanes that differ in lane bits M0, M0/2, ...:
@@ -538,16 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         tc_fence_after();
-        float v[COLS ? 32 : 64];  // COLS: one 16-row half at a time (fewer live registers)
+        // one half of the warp's 64 x 32 cells at a time (fewer live registers): COLS, 16 rows
+        // on the 16x256b layout; otherwise 32 columns on the 32x32b layout
+        float v[32];
         if constexpr (COLS)
-          tmem_ld16x256_x8(tmem + lane_addr + a * kCols + cq * 64, reinterpret_cast<float(&)[32]>(v));
+          tmem_ld16x256_x8(tmem + lane_addr + a * kCols + cq * 64, v);
         else
-          tmem_ld64(tmem + lane_addr + a * kCols + cq * 64, reinterpret_cast<float(&)[64]>(v));
-        if constexpr (!COLS) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[a]);
-        }
+          tmem_ld32(tmem + lane_addr + a * kCols + cq * 64, v);
         float2 rs16[4], cs16[8];  // COLS: the row and column accumulators of fwd_cells16_half
         if constexpr (COLS) {
           constexpr float kInit = MODE == kFwdMax ? -INFINITY : 0.f;
@@ -567,9 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // positives' diagonal, padding rows); every other tile takes the unmasked path
         const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
         const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (i0 + kTileRows > p.nx);
-        float* cp = cpart + (((snap & 1) * 4 + cq) * 4 + q) * 64;
         float rs;
         if constexpr (COLS) {
+          float* cp = cpart + (((snap & 1) * 4 + cq) * 4 + q) * 64;
           const float* vs = colsh + (t & 3) * CF + k * kCols + cq * 64;
           float L;
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(L) : "r"(scal_s));
@@ -577,35 +525,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int rows_left = p.nx - i0 < kTileRows ? static_cast<int>(p.nx - i0) : kTileRows;
           const float* rf = rowf + k * kTileRows;
           const float* ru = rowsh + k * kTileRows;
-          float (&v32)[32] = reinterpret_cast<float(&)[32]>(v);
           for (int h = 0; h < 2; ++h) {
             if (h == 1) {  // the second 16-row half; then the accumulator is free for the MMA
-              tmem_ld16x256_x8(tmem + lane_addr + (16u << 16) + a * kCols + cq * 64, v32);
+              tmem_ld16x256_x8(tmem + lane_addr + (16u << 16) + a * kCols + cq * 64, v);
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&acc_empty[a]);
             }
             if (check)
-              fwd_cells16_half<MODE, true>(v32, h, cf, vs, rf, ru, L, q, lane, cq * 64, ncols, dt, rows_left, rs16,
+              fwd_cells16_half<MODE, true>(v, h, cf, vs, rf, ru, L, q, lane, cq * 64, ncols, dt, rows_left, rs16,
                                            cs16);
             else
-              fwd_cells16_half<MODE, false>(v32, h, cf, vs, rf, ru, L, q, lane, cq * 64, ncols, dt, rows_left, rs16,
+              fwd_cells16_half<MODE, false>(v, h, cf, vs, rf, ru, L, q, lane, cq * 64, ncols, dt, rows_left, rs16,
                                             cs16);
           }
           rs = fwd_cells16_reduce<MODE>(rs16, cs16, lane, cp);
-        } else if constexpr (MODE == kFwdMax) {
-          rs = check ? fwd_cells_max<COLS, true>(v, cf, R1, cq * 64, ncols, row_ok, lane, cp)
-                     : fwd_cells_max<COLS, false>(v, cf, R1, cq * 64, ncols, row_ok, lane, cp);
-        } else if constexpr (MODE == kFwdShifted) {
-          const float* vs = colsh + (t & 3) * CF + k * kCols + cq * 64;
-          const float U = rowsh[k * kTileRows + r];
-          rs = check ? fwd_cells_shifted<COLS, true>(v, cf, vs, R1, U, cq * 64, ncols, dcol, row_ok, lane, cp)
-                     : fwd_cells_shifted<COLS, false>(v, cf, vs, R1, U, cq * 64, ncols, dcol, row_ok, lane, cp);
         } else {
-          float L, b2;  // (a 32-bit shared address keeps the epilogue within its 96 registers)
-          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(L), "=f"(b2) : "r"(scal_s));
-          rs = check ? fwd_cells<KIND, COLS, true>(v, cf, R1, L, b2, cq * 64, ncols, dcol, row_ok, lane, cp)
-                     : fwd_cells<KIND, COLS, false>(v, cf, R1, L, b2, cq * 64, ncols, dcol, row_ok, lane, cp);
+          float L = 0.f, b2 = 0.f, U = 0.f;
+          if constexpr (MODE == kFwdShifted) {
+            U = rowsh[k * kTileRows + r];
+          } else if constexpr (MODE == kFwdSum) {
+            // (a 32-bit shared address keeps the epilogue within its 96 registers)
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(L), "=f"(b2) : "r"(scal_s));
+          }
+          constexpr float kInit = MODE == kFwdMax ? -INFINITY : 0.f;
+          float2 acc = make_float2(kInit, kInit);
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            if (g == 1) {  // the second 32 columns; then the accumulator is free for the MMA
+              tmem_ld32(tmem + lane_addr + a * kCols + cq * 64 + 32, v);
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[a]);
+            }
+            if constexpr (MODE == kFwdMax) {
+              if (check) fwd_cells_max<true>(v, g, cf, R1, cq * 64, ncols, row_ok, acc);
+              else fwd_cells_max<false>(v, g, cf, R1, cq * 64, ncols, row_ok, acc);
+            } else if constexpr (MODE == kFwdShifted) {
+              if (check) fwd_cells_shifted<true>(v, g, cf, R1, U, cq * 64, ncols, dcol, row_ok, acc);
+              else fwd_cells_shifted<false>(v, g, cf, R1, U, cq * 64, ncols, dcol, row_ok, acc);
+            } else {
+              if (check) fwd_cells<KIND, true>(v, g, cf, R1, L, b2, cq * 64, ncols, dcol, row_ok, acc);
+              else fwd_cells<KIND, false>(v, g, cf, R1, L, b2, cq * 64, ncols, dcol, row_ok, acc);
+            }
+          }
+          rs = MODE == kFwdMax ? fmaxf(acc.x, acc.y) : acc.x + acc.y;
         }
 #pragma unroll
         for (int kk = 0; kk < kMaxPrefix; ++kk)
@@ -632,13 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait<0>();
     if (own_ok && ok) {
       const int slot = split * 4 + cq;
-      if constexpr (COLS) {
-#pragma unroll  // (a constant index keeps acc_row in registers, which the 16x256b epilogue has room for)
-        for (int k = 0; k < kMaxPrefix; ++k)
-          if (k < n) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi_own] = acc_row[k];
-      } else {
-        for (int k = 0; k < n; ++k) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi_own] = acc_row[k];
-      }
+#pragma unroll  // (a constant index keeps acc_row in registers)
+      for (int k = 0; k < kMaxPrefix; ++k)
+        if (k < n) p.rowacc[(static_cast<int64_t>(slot) * n + k) * p.nx + gi_own] = acc_row[k];
     }
   }
 
