@@ -105,22 +105,38 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
 }
 
 // ------------------------------------------------------------------------------ transpose
+// 64 x 64 tiles through shared memory, 16-byte global accesses both ways: a thread loads 8
+// consecutive columns of one row of X and stores 8 consecutive rows of one column (a row of
+// X^T).  The tile is kept as [column][row] in 8-row chunks whose order within a column is
+// XOR-swizzled with the column's 8-column group, so the scalar stores of a warp (one chunk of
+// 8 columns per 8 threads) and its 16-byte loads hit distinct banks.
 __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restrict__ X, uint16_t* __restrict__ Xt,
                                                         int64_t rows, int d, int64_t ld) {
-  __shared__ uint16_t tile[64][66];
+  __shared__ __align__(16) uint16_t tile[64][64];
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 64;
   const int c0 = blockIdx.y * 64;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
-  for (int y = ty; y < 64; y += 4) {
+  const int sub = threadIdx.x & 7;  // which 8-element chunk a thread moves
+  const int lr = threadIdx.x >> 3;  // 0..31
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int y = lr + 32 * h;  // row within the tile
     const int64_t r = r0 + y;
-    tile[y][tx] = (r < rows) ? X[r * d + c0 + tx] : uint16_t(0);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    // rows past the end load zeros: the grid spans ld = rows rounded up to 64, so the
+    // padding columns of X^T, which the gradient GEMM reads with zero weights, hold no NaNs
+    if (r < rows) v = *reinterpret_cast<const uint4*>(X + r * d + c0 + sub * 8);
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+    const int phys = (((y >> 3) ^ sub) << 3) | (y & 7);  // columns sub*8 + k all lie in group `sub`
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tile[sub * 8 + k][phys] = e[k];
   }
   __syncthreads();
-  // the grid spans ld = rows rounded up to 64, so the padding columns get the zeros
-  // loaded above: the gradient GEMM reads them (with zero weights) and must not meet NaNs
-  for (int y = ty; y < 64; y += 4) {
-    const int64_t r = r0 + tx;
-    Xt[static_cast<int64_t>(c0 + y) * ld + r] = tile[tx][y];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int x = lr + 32 * h;  // column within the tile: a row of X^T
+    const int phys = sub ^ ((x >> 3) & 7);
+    const uint4 v = *reinterpret_cast<const uint4*>(&tile[x][phys * 8]);
+    *reinterpret_cast<uint4*>(Xt + static_cast<int64_t>(c0 + x) * ld + r0 + sub * 8) = v;
   }
 }
 
