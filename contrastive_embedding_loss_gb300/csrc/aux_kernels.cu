@@ -32,10 +32,13 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------------------------ prep
-// One warp per item r < max(Na, Nb): rows A_r and B_r together while r < Nmin (so the
-// positive pair's dot products come from the same registers), otherwise the one row.
+// Eight lanes per item, four items per warp; item r < max(Na, Nb) covers rows A_r and B_r
+// together while r < Nmin (so the positive pair's dot products come from the same
+// registers), otherwise the one row.  A lane reads every eighth 16-byte chunk of the row,
+// four chunks in flight, and the eight lanes of an item meet in a 3-stage shuffle reduce.
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;  // the lane within its item's group of eight
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_items = p.na > p.nb ? p.na : p.nb;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -47,45 +50,66 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
                                           : (t > 0.f && t <= kMaxLogitScale);
     if (!ok) atomicExch(p.status, kStatusBadScalar);
   }
-  for (int64_t r = warp_id; r < n_items; r += n_warps) {
+  const int pn = p.prefix_end[n - 1];
+  const int n_chunks = pn / 8;  // 16-byte chunks of a row up to the last prefix end
+  for (int64_t r0 = warp_id * 4; r0 < n_items; r0 += n_warps * 4) {  // uniform over the warp
+    const int64_t r = r0 + (lane >> 3);
     const bool has_a = r < p.na, has_b = r < p.nb, pair = r < p.nmin;
     float ssa[kMaxPrefix], ssb[kMaxPrefix], dab[kMaxPrefix];
 #pragma unroll
     for (int k = 0; k < kMaxPrefix; ++k) ssa[k] = ssb[k] = dab[k] = 0.f;
-    const uint4* ra = reinterpret_cast<const uint4*>(p.A + r * p.d);
-    const uint4* rb = reinterpret_cast<const uint4*>(p.B + r * p.d);
-    const int pn = p.prefix_end[n - 1];
-    for (int ch = lane; ch * 8 < pn; ch += 32) {
-      const int b = band_of(ch * 8, p.prefix_end, n);
-      uint4 va = make_uint4(0, 0, 0, 0), vb = make_uint4(0, 0, 0, 0);
-      if (has_a) va = __ldg(ra + ch);
-      if (has_b) vb = __ldg(rb + ch);
-      const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
-      float sa = 0.f, sb = 0.f, sd = 0.f;
+    const uint4* ra = reinterpret_cast<const uint4*>(p.A + (has_a ? r : 0) * p.d);
+    const uint4* rb = reinterpret_cast<const uint4*>(p.B + (has_b ? r : 0) * p.d);
+    for (int ch0 = sub; ch0 < n_chunks; ch0 += 32) {
+      uint4 va[4], vb[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float a0 = bf16_lo(wa[q]), a1 = bf16_hi(wa[q]);
-        const float b0 = bf16_lo(wb[q]), b1 = bf16_hi(wb[q]);
-        sa = fmaf(a0, a0, fmaf(a1, a1, sa));
-        sb = fmaf(b0, b0, fmaf(b1, b1, sb));
-        sd = fmaf(a0, b0, fmaf(a1, b1, sd));
+      for (int u = 0; u < 4; ++u) {  // the loads first: four chunks of each row in flight
+        const int ch = ch0 + 8 * u;
+        va[u] = make_uint4(0u, 0u, 0u, 0u);
+        vb[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (ch < n_chunks) {
+          if (has_a) va[u] = __ldg(ra + ch);
+          if (has_b) vb[u] = __ldg(rb + ch);
+        }
       }
 #pragma unroll
-      for (int k = 0; k < kMaxPrefix; ++k)
-        if (k == b) {
-          ssa[k] += sa;
-          ssb[k] += sb;
-          dab[k] += sd;
+      for (int u = 0; u < 4; ++u) {
+        const int ch = ch0 + 8 * u;
+        const int b = band_of(ch * 8, p.prefix_end, n);  // == n past the end: adds nowhere
+        const uint32_t wa[4] = {va[u].x, va[u].y, va[u].z, va[u].w}, wb[4] = {vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+        float sa = 0.f, sb = 0.f, sd = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float a0 = bf16_lo(wa[q]), a1 = bf16_hi(wa[q]);
+          const float b0 = bf16_lo(wb[q]), b1 = bf16_hi(wb[q]);
+          sa = fmaf(a0, a0, fmaf(a1, a1, sa));
+          sb = fmaf(b0, b0, fmaf(b1, b1, sb));
+          sd = fmaf(a0, b0, fmaf(a1, b1, sd));
         }
+#pragma unroll
+        for (int k = 0; k < kMaxPrefix; ++k)
+          if (k == b) {
+            ssa[k] += sa;
+            ssb[k] += sb;
+            dab[k] += sd;
+          }
+      }
     }
     float ca = 0.f, cb = 0.f, cd = 0.f;
 #pragma unroll
     for (int k = 0; k < kMaxPrefix; ++k) {
       if (k >= n) break;
-      ca += warp_sum(ssa[k]);
-      cb += warp_sum(ssb[k]);
-      cd += warp_sum(dab[k]);
-      if (lane == 0) {
+      float va = ssa[k], vb = ssb[k], vd = dab[k];
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {  // the eight lanes of this item
+        va += __shfl_xor_sync(0xffffffffu, va, o);
+        vb += __shfl_xor_sync(0xffffffffu, vb, o);
+        vd += __shfl_xor_sync(0xffffffffu, vd, o);
+      }
+      ca += va;
+      cb += vb;
+      cd += vd;
+      if (sub == 0) {
         const float rA = 1.f / fmaxf(sqrtf(ca), 1e-30f);
         const float rB = 1.f / fmaxf(sqrtf(cb), 1e-30f);
         if (has_a) p.rinv_a[k * p.na + r] = rA;
@@ -98,7 +122,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
   const int64_t items = p.na > p.nb ? p.na : p.nb;
-  int64_t blocks = (items * 32 + 255) / 256;
+  int64_t blocks = (items * 8 + 255) / 256;  // eight lanes per item
   if (blocks > 152 * 16) blocks = 152 * 16;
   prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
