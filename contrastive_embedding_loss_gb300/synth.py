@@ -31,6 +31,7 @@ __all__ = [
     "paired",
     "paired_hard",
     "queries_keys",
+    "prefix_ladder",
     "workload",
     "WORKLOADS",
 ]
@@ -75,6 +76,19 @@ def paired(N: int, D: int, noise: float, seed: int):
         A[r0:r1] = round_to_bf16_bits(a)
         B[r0:r1] = round_to_bf16_bits(b)
     return A, B
+
+
+def prefix_ladder(N: int, D: int = 1024):
+    """The prefix-ladder batch as bf16 bits (N <= 64 rows, D > 64): row i is one-hot at
+    dimension i within [0, 64), then 0.125 in every dimension of [64, D).  Every entry is
+    exact in bf16, and every off-diagonal cosine at a prefix p is the same number, so the
+    losses have closed forms (tests/golden/make_closed_forms.py)."""
+    if not 1 <= N <= 64 or D <= 64:
+        raise ValueError("the prefix ladder needs 1 <= N <= 64 and D > 64")
+    x = np.zeros((N, D))
+    x[np.arange(N), np.arange(N)] = 1.0
+    x[:, 64:] = 0.125
+    return round_to_bf16_bits(x)
 
 
 def paired_hard(N: int, D: int, noise: float, dup_frac: float, dup_noise: float, seed: int):
