@@ -238,3 +238,49 @@ def test_wait_selftest_arguments(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert binding.uf_contrastive_selftest_wait(FAKE, 100, None) == CUDA
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "uf_contrastive.h"
+
+int main(void) {
+  const int ladder[5] = {64, 128, 256, 512, 1024};
+  size_t ws = uf_contrastive_workspace_size(256, 256, 1024, ladder, 5, UF_LOSS_CLIP_SYMMETRIC, 1);
+  size_t wmin = uf_contrastive_workspace_min(256, 256, 1024, ladder, 5, UF_LOSS_CLIP_SYMMETRIC, 1);
+  size_t bad = uf_contrastive_workspace_size(256, 255, 1024, ladder, 5, UF_LOSS_CLIP_SYMMETRIC, 1);
+  float loss[5];
+  uf_status_t st = uf_contrastive_fwd_bwd(NULL, NULL, 256, 256, 1024, ladder, 5, UF_LOSS_CLIP_SYMMETRIC,
+                                          14.0f, 0.0f, NULL, loss, NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL);
+  printf("%d %s %zu %zu %zu %d %s\n", uf_contrastive_version(), uf_status_name(UF_DEVICE_TIMEOUT), ws, wmin, bad,
+         (int)st, uf_status_name(st));
+  return 0;
+}
+"""
+
+
+def test_header_compiles_and_links_as_plain_c(lib, tmp_path):
+    """The boundary is plain C99: the header compiles with gcc -std=c99 -Wall -Werror, a C
+    program links against the library and calls the entry points that need no GPU."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    so = binding.library_path()
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                           os.path.join(root, "include"), str(src), "-o", str(exe), so,
+                           "-Wl,-rpath," + os.path.dirname(so)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    version, timeout_name, ws, wmin, bad, st, st_name = out.stdout.split()
+    assert int(version) == binding.uf_contrastive_version()
+    assert timeout_name == "device-timeout"
+    assert int(ws) == binding.uf_contrastive_workspace_size(256, 256, 1024, (64, 128, 256, 512, 1024), 0, True)
+    assert 0 < int(wmin) <= int(ws) and int(bad) == 0  # CLIP needs Na == Nb
+    assert int(st) == 1 and st_name == "invalid-argument"  # NULL inputs are refused on the host
