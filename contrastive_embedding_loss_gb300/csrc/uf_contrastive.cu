@@ -293,6 +293,46 @@ uf_status_t uf_contrastive_fwd_bwd(const void* A, const void* B, int64_t Na, int
 
 namespace {
 
+// Every buffer a call writes (the outputs, *device_status and the workspace) must overlap no
+// other such buffer and no input: a kernel writing an output over an input that a later kernel
+// reads, or over another output, would return garbage.  The inputs may overlap one another
+// (A == B is a valid request).  pos_ids is checked by its first element (its length is only
+// known on the device).
+bool disjoint_buffers(const void* A, const void* B, int64_t Na, int64_t Nb, int D, int n, const float* scale_dev,
+                      const float* bias_dev, const int64_t* pos_offsets, const int* pos_ids, const float* loss,
+                      const float* row_terms, const float* col_terms, const float* dA, const float* dB,
+                      const float* d_scale, const float* d_bias, const void* workspace, size_t workspace_bytes,
+                      const int* status) {
+  struct Range {
+    uintptr_t lo, hi;  // [lo, hi); empty for a NULL pointer
+  };
+  auto range = [](const void* p, uint64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Range{a, p ? a + static_cast<uintptr_t>(bytes) : a};
+  };
+  const uint64_t f = sizeof(float), d = static_cast<uint64_t>(D), un = static_cast<uint64_t>(n);
+  const uint64_t na = static_cast<uint64_t>(Na), nb = static_cast<uint64_t>(Nb);
+  const Range written[] = {
+      range(loss, f * un),          range(row_terms, f * un * na), range(col_terms, f * un * nb),
+      range(dA, f * na * d),        range(dB, f * nb * d),         range(d_scale, f),
+      range(d_bias, f),             range(status, sizeof(int)),    range(workspace, workspace_bytes),
+  };
+  const Range read[] = {
+      range(A, 2 * na * d),  range(B, 2 * nb * d),
+      range(scale_dev, f),   range(bias_dev, f),
+      range(pos_offsets, sizeof(int64_t) * (na + 1)), range(pos_ids, sizeof(int)),
+  };
+  auto overlap = [](const Range& x, const Range& y) { return x.lo < x.hi && y.lo < y.hi && x.lo < y.hi && y.lo < x.hi; };
+  const int nw = static_cast<int>(sizeof(written) / sizeof(written[0]));
+  for (int i = 0; i < nw; ++i) {
+    for (int j = i + 1; j < nw; ++j)
+      if (overlap(written[i], written[j])) return false;
+    for (const Range& r : read)
+      if (overlap(written[i], r)) return false;
+  }
+  return true;
+}
+
 // The two-set loss of A against B, or (oneset) the one-set loss of the set A = B against
 // itself: self-cells masked, labels required, dA = dX receives both roles of every cell
 // (twice the A-side gradient, the weights being symmetric), no B-side GEMM.
@@ -320,6 +360,10 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     return UF_INVALID_ARGUMENT;
   if (grads && (!aligned(dA, 16) || !aligned(dB, 16))) return UF_INVALID_ARGUMENT;
   if ((row_terms && !aligned(row_terms, 4)) || (col_terms && !aligned(col_terms, 4))) return UF_INVALID_ARGUMENT;
+  if (!disjoint_buffers(A, B, Na, Nb, D, n_prefix, logit_scale_dev, bias_dev, pos_offsets, pos_ids, loss_per_prefix,
+                        row_terms, col_terms, dA, oneset ? nullptr : dB, d_logit_scale, d_bias, workspace,
+                        workspace_bytes, device_status))
+    return UF_INVALID_ARGUMENT;
   // host scalars are checked here; ones on the device by the first kernel (*device_status)
   if ((!logit_scale_dev && !std::isfinite(logit_scale)) || (!bias_dev && !std::isfinite(bias)))
     return UF_INVALID_ARGUMENT;

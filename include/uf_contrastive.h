@@ -29,6 +29,12 @@
  * caller's stream and returns without synchronising, so it can be captured in a CUDA
  * graph.  Calls on different streams are independent as long as each has its own
  * workspace and outputs.
+ *
+ * Buffers.  No buffer a call writes may overlap another such buffer or any input.  The written
+ * buffers are the loss, the terms, the gradients, the scalar gradients, *device_status and the
+ * workspace; the inputs are A, B, the device-held scalars and the label lists.  A call that
+ * breaks this returns UF_INVALID_ARGUMENT and enqueues nothing.  The inputs may overlap one
+ * another (A == B is a valid request).
  */
 #ifndef UF_CONTRASTIVE_H_
 #define UF_CONTRASTIVE_H_

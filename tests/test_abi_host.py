@@ -81,33 +81,40 @@ def test_workspace_size(lib):
     assert ws(big, big, 1024, LADDER, 0, 1) - ws(big, big, 1024, LADDER, 0, 0) < (48 << 30) + (1 << 30)
 
 
-FAKE = 1 << 20  # a 256-byte aligned fake device address; these calls return before any CUDA call
+# Fake device addresses for calls that return before any CUDA call: 256-byte aligned, one
+# 4 GiB slot per argument so that no two buffers overlap (the library refuses overlapping
+# written buffers); the workspace sits above every slot, so its 1 TiB reaches none of them.
+F = {name: (i + 1) * (4 << 30) for i, name in enumerate(
+    ["A", "B", "loss", "row_terms", "col_terms", "dA", "dB", "d_scale", "d_bias", "scale_dev", "bias_dev",
+     "pos_offsets", "pos_ids", "status", "X"])}
+WS = 1 << 44
+FAKE = F["status"]  # any single aligned address
 
 
 def _call(**kw):
-    args = dict(A=FAKE, B=FAKE, Na=256, Nb=256, D=1024, prefixes=LADDER, kind=0, logit_scale=1 / 0.07, bias=0.0,
-                prefix_weights=None, loss_per_prefix=FAKE, row_terms=None, col_terms=None, dA=FAKE, dB=FAKE,
-                workspace=FAKE, workspace_bytes=1 << 40, device_status=None, stream=None)
+    args = dict(A=F["A"], B=F["B"], Na=256, Nb=256, D=1024, prefixes=LADDER, kind=0, logit_scale=1 / 0.07,
+                bias=0.0, prefix_weights=None, loss_per_prefix=F["loss"], row_terms=None, col_terms=None,
+                dA=F["dA"], dB=F["dB"], workspace=WS, workspace_bytes=1 << 40, device_status=None, stream=None)
     args.update(kw)
     return binding.uf_contrastive_fwd_bwd(**args)
 
 
 def test_workspace_below_the_minimum_is_rejected_on_the_host(lib):
-    WS = 3
+    SMALL = 3
     need = binding.uf_contrastive_workspace_min(256, 256, 1024, LADDER, 0, 1)
-    assert _call(workspace_bytes=need - 256) == WS
-    assert _call(workspace_bytes=0) == WS
+    assert _call(workspace_bytes=need - 256) == SMALL
+    assert _call(workspace_bytes=0) == SMALL
 
 
 def test_argument_errors_are_found_on_the_host(lib):
-    INV, UNS, WS = 1, 2, 3
+    INV, UNS, SMALL = 1, 2, 3
     assert _call(A=None) == INV
     assert _call(loss_per_prefix=None) == INV
     assert _call(workspace=None) == INV
     assert _call(dB=None) == INV                      # dA and dB go together
-    assert _call(A=FAKE + 2) == INV                   # misaligned
-    assert _call(workspace=FAKE + 16) == INV          # workspace must be 256-byte aligned
-    assert _call(dA=FAKE + 4) == INV
+    assert _call(A=F["A"] + 2) == INV                 # misaligned
+    assert _call(workspace=WS + 16) == INV            # workspace must be 256-byte aligned
+    assert _call(dA=F["dA"] + 4) == INV
     assert _call(Nb=255) == INV
     assert _call(prefixes=(64, 64)) == INV
     assert _call(kind=3) == INV
@@ -116,7 +123,7 @@ def test_argument_errors_are_found_on_the_host(lib):
     assert _call(prefix_weights=[1, 1, float("inf"), 1, 1]) == INV
     assert _call(logit_scale=300.0) == UNS            # beyond the largest supported scale (256)
     assert _call(kind=1, logit_scale=70.0, bias=-20.0) == UNS
-    assert _call(workspace_bytes=1024) == WS
+    assert _call(workspace_bytes=1024) == SMALL
 
 
 def test_valid_call_without_gpu_reports_cuda_error(lib):
@@ -133,11 +140,11 @@ def test_missing_library_fails_loudly(tmp_path):
         binding.load(str(tmp_path / "nope.so"))
 
 
-def _call_ex(d_logit_scale=FAKE, d_bias=FAKE, **kw):
-    args = dict(A=FAKE, B=FAKE, Na=256, Nb=256, D=1024, prefixes=LADDER, kind=0, logit_scale=1 / 0.07, bias=0.0,
-                logit_scale_dev=None, bias_dev=None, pos_offsets=None, pos_ids=None, prefix_weights=None,
-                loss_per_prefix=FAKE, row_terms=None,
-                col_terms=None, dA=FAKE, dB=FAKE, d_logit_scale=d_logit_scale, d_bias=d_bias, workspace=FAKE, workspace_bytes=1 << 40,
+def _call_ex(d_logit_scale=F["d_scale"], d_bias=F["d_bias"], **kw):
+    args = dict(A=F["A"], B=F["B"], Na=256, Nb=256, D=1024, prefixes=LADDER, kind=0, logit_scale=1 / 0.07,
+                bias=0.0, logit_scale_dev=None, bias_dev=None, pos_offsets=None, pos_ids=None, prefix_weights=None,
+                loss_per_prefix=F["loss"], row_terms=None, col_terms=None, dA=F["dA"], dB=F["dB"],
+                d_logit_scale=d_logit_scale, d_bias=d_bias, workspace=WS, workspace_bytes=1 << 40,
                 device_status=None, stream=None)
     args.update(kw)
     return binding.uf_contrastive_fwd_bwd_ex(**args)
@@ -147,8 +154,8 @@ def test_scale_gradient_argument_errors_are_found_on_the_host(lib):
     INV, UNS = 1, 2
     assert _call_ex(dA=None, dB=None) == INV                    # they come out of the backward
     assert _call_ex(d_bias=None, dA=None, dB=None) == INV
-    assert _call_ex(d_logit_scale=FAKE + 2) == INV              # fp32 scalars: 4-byte aligned
-    assert _call_ex(d_bias=FAKE + 1) == INV
+    assert _call_ex(d_logit_scale=F["d_scale"] + 2) == INV              # fp32 scalars: 4-byte aligned
+    assert _call_ex(d_bias=F["d_bias"] + 1) == INV
     assert _call_ex(kind=1, logit_scale=0.0, bias=0.0) == UNS   # SigLIP t = 0: dL/dt is not (sum W cos) / t
     assert _call_ex(kind=1, logit_scale=0.0, bias=0.0, d_logit_scale=None) != UNS  # the bias alone is fine
     # the same checks as the plain entry point still apply
@@ -170,17 +177,17 @@ def test_valid_scale_gradient_call_without_gpu_reports_cuda_error(lib):
 
 def test_device_scalars_are_checked_on_the_host_only_for_alignment(lib):
     INV, CUDA = 1, 4
-    assert _call_ex(logit_scale_dev=FAKE + 2) == INV
-    assert _call_ex(bias_dev=FAKE + 1) == INV
+    assert _call_ex(logit_scale_dev=F["scale_dev"] + 2) == INV
+    assert _call_ex(bias_dev=F["bias_dev"] + 1) == INV
     import torch
 
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     # a host value that would be refused is ignored when the device holds the scalar: the
     # call gets as far as the first CUDA call
-    assert _call_ex(logit_scale=float("nan"), logit_scale_dev=FAKE) == CUDA
-    assert _call_ex(logit_scale=1000.0, logit_scale_dev=FAKE) == CUDA
-    assert _call_ex(kind=1, logit_scale=70.0, bias=-20.0, bias_dev=FAKE) == CUDA
+    assert _call_ex(logit_scale=float("nan"), logit_scale_dev=F["scale_dev"]) == CUDA
+    assert _call_ex(logit_scale=1000.0, logit_scale_dev=F["scale_dev"]) == CUDA
+    assert _call_ex(kind=1, logit_scale=70.0, bias=-20.0, bias_dev=F["bias_dev"]) == CUDA
     # large host scales take the max-shifted path instead of being refused
     assert _call_ex(logit_scale=100.0) == CUDA
     assert _call_ex(logit_scale=256.0) == CUDA
@@ -189,34 +196,34 @@ def test_device_scalars_are_checked_on_the_host_only_for_alignment(lib):
 def test_label_arguments_are_checked_on_the_host(lib):
     INV, UNS, CUDA = 1, 2, 4
     sig = dict(kind=1, logit_scale=10.0, bias=-10.0)
-    assert _call_ex(pos_offsets=FAKE, pos_ids=FAKE) == UNS          # CLIP: no labelled positives
-    assert _call_ex(kind=2, logit_scale=20.0, pos_offsets=FAKE, pos_ids=FAKE) == UNS
-    assert _call_ex(pos_offsets=FAKE, **sig) == INV                  # offsets and ids go together
-    assert _call_ex(pos_ids=FAKE, **sig) == INV
-    assert _call_ex(pos_offsets=FAKE + 4, pos_ids=FAKE, **sig) == INV  # int64 offsets: 8-byte aligned
-    assert _call_ex(pos_offsets=FAKE, pos_ids=FAKE + 2, **sig) == INV
+    assert _call_ex(pos_offsets=F["pos_offsets"], pos_ids=F["pos_ids"]) == UNS          # CLIP: no labelled positives
+    assert _call_ex(kind=2, logit_scale=20.0, pos_offsets=F["pos_offsets"], pos_ids=F["pos_ids"]) == UNS
+    assert _call_ex(pos_offsets=F["pos_offsets"], **sig) == INV                  # offsets and ids go together
+    assert _call_ex(pos_ids=F["pos_ids"], **sig) == INV
+    assert _call_ex(pos_offsets=F["pos_offsets"] + 4, pos_ids=F["pos_ids"], **sig) == INV  # int64 offsets: 8-byte aligned
+    assert _call_ex(pos_offsets=F["pos_offsets"], pos_ids=F["pos_ids"] + 2, **sig) == INV
     assert _call_ex(Nb=200, **sig) == INV                            # SigLIP needs Nb >= Na
     import torch
 
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    assert _call_ex(pos_offsets=FAKE, pos_ids=FAKE, **sig) == CUDA
+    assert _call_ex(pos_offsets=F["pos_offsets"], pos_ids=F["pos_ids"], **sig) == CUDA
     assert _call_ex(Nb=700, **sig) == CUDA                           # extra negative columns
 
 
 def test_oneset_arguments_are_checked_on_the_host(lib):
     INV, UNS, CUDA = 1, 2, 4
-    args = dict(X=FAKE, N=256, D=1024, prefixes=LADDER, logit_scale=10.0, bias=-10.0, logit_scale_dev=None,
-                bias_dev=None, pos_offsets=FAKE, pos_ids=FAKE, prefix_weights=None, loss_per_prefix=FAKE,
-                row_terms=None, dX=FAKE, d_logit_scale=None, d_bias=None, workspace=FAKE, workspace_bytes=1 << 40,
-                device_status=None, stream=None)
+    args = dict(X=F["X"], N=256, D=1024, prefixes=LADDER, logit_scale=10.0, bias=-10.0, logit_scale_dev=None,
+                bias_dev=None, pos_offsets=F["pos_offsets"], pos_ids=F["pos_ids"], prefix_weights=None,
+                loss_per_prefix=F["loss"], row_terms=None, dX=F["dA"], d_logit_scale=None, d_bias=None, workspace=WS,
+                workspace_bytes=1 << 40, device_status=None, stream=None)
     call = lambda **kw: binding.uf_contrastive_oneset_fwd_bwd(**{**args, **kw})  # noqa: E731
     assert call(pos_offsets=None) == INV           # a one-set batch names its pairs
     assert call(pos_ids=None) == INV
     assert call(X=None) == INV
-    assert call(X=FAKE + 2) == INV
+    assert call(X=F["X"] + 2) == INV
     assert call(logit_scale=70.0, bias=-20.0) == UNS
-    assert call(d_logit_scale=FAKE, dX=None) == INV  # the scalar gradients come out of the backward
+    assert call(d_logit_scale=F["d_scale"], dX=None) == INV  # the scalar gradients come out of the backward
     need = binding.uf_contrastive_workspace_min(256, 256, 1024, LADDER, 1, 1)
     assert call(workspace_bytes=need - 256) == 3
     import torch
@@ -284,3 +291,34 @@ def test_header_compiles_and_links_as_plain_c(lib, tmp_path):
     assert int(ws) == binding.uf_contrastive_workspace_size(256, 256, 1024, (64, 128, 256, 512, 1024), 0, True)
     assert 0 < int(wmin) <= int(ws) and int(bad) == 0  # CLIP needs Na == Nb
     assert int(st) == 1 and st_name == "invalid-argument"  # NULL inputs are refused on the host
+
+
+def test_overlapping_buffers_are_refused_on_the_host(lib):
+    INV, CUDA = 1, 4
+    n, Na, D = len(LADDER), 256, 1024
+    dA_end = F["dA"] + Na * D * 4
+    assert _call(dB=F["dA"] + 256) == INV                          # two outputs share bytes
+    assert _call(dA=F["A"]) == INV                                 # an output over an input
+    assert _call(dB=F["B"] + 4096) == INV
+    assert _call(loss_per_prefix=WS + 1024) == INV                 # an output inside the workspace
+    assert _call(device_status=F["dA"] + 64) == INV                # the status word inside an output
+    assert _call(workspace=F["dA"], workspace_bytes=1 << 30) == INV
+    assert _call(row_terms=F["row_terms"], col_terms=F["row_terms"] + n * Na * 4 - 4) == INV
+    assert _call_ex(d_bias=F["d_scale"]) == INV                    # the two scalar gradients
+    assert _call_ex(kind=1, logit_scale=10.0, bias=-10.0, pos_offsets=F["pos_offsets"], pos_ids=F["pos_ids"],
+                    loss_per_prefix=F["pos_offsets"] + 8 * Na) == INV  # the loss over the label offsets' last entry
+    assert _call_ex(logit_scale_dev=F["dA"] + 128) == INV          # a device scalar inside an output
+    oneset = dict(X=F["X"], N=Na, D=D, prefixes=LADDER, logit_scale=10.0, bias=-10.0, logit_scale_dev=None,
+                  bias_dev=None, pos_offsets=F["pos_offsets"], pos_ids=F["pos_ids"], prefix_weights=None,
+                  loss_per_prefix=F["loss"], row_terms=None, dX=F["X"], d_logit_scale=None, d_bias=None,
+                  workspace=WS, workspace_bytes=1 << 40, device_status=None, stream=None)
+    assert binding.uf_contrastive_oneset_fwd_bwd(**oneset) == INV  # dX over the set itself
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # what is allowed: inputs that overlap (A == B), and buffers that touch without sharing a byte
+    assert _call(B=F["A"]) == CUDA
+    assert _call(dB=dA_end) == CUDA
+    assert _call(loss_per_prefix=WS - n * 4) == CUDA
+    assert _call(device_status=dA_end + Na * D * 4) == CUDA  # free memory past the end of dA
