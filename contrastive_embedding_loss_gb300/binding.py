@@ -187,6 +187,24 @@ def _empty_ids(dev):
         _EMPTY_IDS[dev] = torch.zeros(1, dtype=torch.int32, device=dev)
     return _EMPTY_IDS[dev].data_ptr()
 
+def _check_buffers(dev, workspace, device_status):
+    """The caller's scratch and status word: a contiguous uint8 workspace and an int32 status
+    tensor, both on the inputs' device."""
+    import torch
+
+    if workspace is not None and (workspace.dtype != torch.uint8 or workspace.device != dev
+                                  or not workspace.is_contiguous()):
+        raise TypeError("workspace must be a contiguous uint8 tensor on the inputs' device")
+    if device_status is not None and (device_status.dtype != torch.int32 or device_status.device != dev
+                                      or device_status.numel() < 1):
+        raise TypeError("device_status must be an int32 tensor (one element) on the inputs' device")
+
+
+def _check_labels(offs, n_rows):
+    if offs.dim() != 1 or offs.numel() != n_rows + 1:
+        raise ValueError(f"label offsets must hold rows + 1 = {n_rows + 1} entries, not {offs.numel()}")
+
+
 def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), logit_scale=1 / 0.07, bias=0.0,
                         prefix_weights=None, grads=True, terms=False, workspace=None, device_status=None,
                         stream=None, scale_grads=False, labels=None):
@@ -206,8 +224,15 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
     """
     import torch
 
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D (rows x D)")
+    if A.shape[1] != B.shape[1]:
+        raise ValueError(f"A and B must have the same width D ({A.shape[1]} vs {B.shape[1]})")
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or not A.is_cuda or not B.is_cuda:
         raise TypeError("A and B must be bf16 CUDA tensors")
+    if A.device != B.device:
+        raise ValueError("A and B must be on the same device")
+    _check_buffers(A.device, workspace, device_status)
     A = A.contiguous()
     B = B.contiguous()
     Na, D = A.shape
@@ -235,8 +260,8 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
 
     def scalar(v):  # (host value, device pointer)
         if isinstance(v, torch.Tensor):
-            if v.dtype != torch.float32 or not v.is_cuda or v.numel() != 1:
-                raise TypeError("a device logit scale / bias must be a one-element fp32 CUDA tensor")
+            if v.dtype != torch.float32 or v.device != dev or v.numel() != 1:
+                raise TypeError("a device logit scale / bias must be a one-element fp32 tensor on A's device")
             return 0.0, v.data_ptr()
         return float(v), None
 
@@ -247,6 +272,7 @@ def contrastive_fwd_bwd(A, B, kind="clip", prefixes=(64, 128, 256, 512, 1024), l
         offs, ids = labels
         offs = torch.as_tensor(offs, dtype=torch.int64, device=dev).contiguous()
         ids = torch.as_tensor(ids, dtype=torch.int32, device=dev).contiguous()
+        _check_labels(offs, Na)
     with torch.cuda.device(dev):
         st = uf_contrastive_fwd_bwd_ex(A.data_ptr(), B.data_ptr(), Na, Nb, D, prefixes, k, ls_host, b_host, ls_dev,
                                        b_dev, ptr(offs), ptr(ids) if ids is not None and ids.numel() else
@@ -269,8 +295,11 @@ def oneset_fwd_bwd(X, labels, prefixes=(64, 128, 256, 512, 1024), logit_scale=10
     tensors, as in ``contrastive_fwd_bwd``."""
     import torch
 
+    if X.dim() != 2:
+        raise ValueError("X must be 2-D (rows x D)")
     if X.dtype != torch.bfloat16 or not X.is_cuda:
         raise TypeError("X must be a bf16 CUDA tensor")
+    _check_buffers(X.device, workspace, device_status)
     X = X.contiguous()
     N, D = X.shape
     dev = X.device
@@ -292,12 +321,15 @@ def oneset_fwd_bwd(X, labels, prefixes=(64, 128, 256, 512, 1024), logit_scale=10
     offs, ids = labels
     offs = torch.as_tensor(offs, dtype=torch.int64, device=dev).contiguous()
     ids = torch.as_tensor(ids, dtype=torch.int32, device=dev).contiguous()
+    _check_labels(offs, N)
     ids_ptr = ids.data_ptr() if ids.numel() else _empty_ids(dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
 
     def scalar(v):
         if isinstance(v, torch.Tensor):
+            if v.dtype != torch.float32 or v.device != dev or v.numel() != 1:
+                raise TypeError("a device logit scale / bias must be a one-element fp32 tensor on X's device")
             return 0.0, v.data_ptr()
         return float(v), None
 

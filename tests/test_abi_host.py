@@ -322,3 +322,21 @@ def test_overlapping_buffers_are_refused_on_the_host(lib):
     assert _call(dB=dA_end) == CUDA
     assert _call(loss_per_prefix=WS - n * 4) == CUDA
     assert _call(device_status=dA_end + Na * D * 4) == CUDA  # free memory past the end of dA
+
+
+def test_binding_checks_shapes_before_anything_else(lib):
+    """The binding refuses malformed tensors itself: the C ABI takes D from one matrix and
+    would read the other with that row length."""
+    import torch
+
+    A = torch.zeros(4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="same width"):
+        binding.contrastive_fwd_bwd(A, torch.zeros(4, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="2-D"):
+        binding.contrastive_fwd_bwd(A[0], A)
+    with pytest.raises(ValueError, match="2-D"):
+        binding.oneset_fwd_bwd(A[0], (np.zeros(5, np.int64), np.zeros(0, np.int32)))
+    with pytest.raises(TypeError, match="CUDA"):
+        binding.contrastive_fwd_bwd(A, A)  # host tensors: no CPU path
+    with pytest.raises(TypeError, match="CUDA"):
+        binding.oneset_fwd_bwd(A, (np.zeros(5, np.int64), np.zeros(0, np.int32)))
