@@ -60,6 +60,32 @@ def test_oracle_matches_the_closed_forms(case):
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=floor)
 
 
+def closed_form_grad_cases():
+    """[(kind, rows, cols, scale, bias, [(i, d, dA[i, d])])] from the gradient fixture."""
+    groups = {}
+    with open(os.path.join(GOLDEN, "closed_forms_prefix_ladder_grads.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            kind, na, nb, sc, bias, i, d, v = line.split()
+            groups.setdefault((kind, int(na), int(nb), float(sc), float(bias)), []).append((int(i), int(d), float(v)))
+    return [(*key, pts) for key, pts in groups.items()]
+
+
+GRAD_CASES = closed_form_grad_cases()
+GRAD_IDS = [f"{c[0]}-{c[1]}x{c[2]}-s{c[3]:g}" for c in GRAD_CASES]
+
+
+@pytest.mark.parametrize("case", GRAD_CASES, ids=GRAD_IDS)
+def test_oracle_matches_the_closed_form_gradients(case):
+    kind, na, nb, sc, bias, pts = case
+    A, B = ladder_inputs(na, nb)
+    dA = oracle.fwd_bwd(kind, A, B, LADDER, sc, bias)["dA"]
+    scale = np.abs(dA).max()
+    for i, d, want in pts:
+        np.testing.assert_allclose(dA[i, d], want, rtol=1e-10, atol=1e-12 * scale, err_msg=f"dA[{i},{d}]")
+
+
 def test_oracle_reproduces_its_stored_outputs():
     with open(os.path.join(GOLDEN, "oracle_small.json")) as f:
         fx = json.load(f)
@@ -139,4 +165,37 @@ def test_closed_forms_catch_planted_mistakes(name, tmp_path):
 
     with oracle.ref.use_library(str(so)):
         assert not all_pass(), f"planted mistake {name} was not caught by the closed forms"
+    assert all_pass()
+
+
+GRAD_MUTATIONS = {
+    "dropped_projection_term": (
+        "out[d] += g * (B[j * D + d] * rb[j] - c * A[i * D + d] * ra[i]) * ra[i];",
+        "out[d] += g * (B[j * D + d] * rb[j]) * ra[i];"),
+    "prefix_norm_uses_full_width": LOSS_MUTATIONS["prefix_norm_uses_full_width"],
+}
+
+
+@pytest.mark.parametrize("name", sorted(GRAD_MUTATIONS))
+def test_closed_form_gradients_catch_planted_mistakes(name, tmp_path):
+    import subprocess
+
+    old, new = GRAD_MUTATIONS[name]
+    src = open(oracle.ref._SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path = tmp_path / "oracle_mut.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / "liboracle_mut.so"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", str(path), "-o", str(so), "-lm"])
+
+    def all_pass():
+        for case in GRAD_CASES:
+            try:
+                test_oracle_matches_the_closed_form_gradients(case)
+            except AssertionError:
+                return False
+        return True
+
+    with oracle.ref.use_library(str(so)):
+        assert not all_pass(), f"planted mistake {name} was not caught by the closed-form gradients"
     assert all_pass()
