@@ -71,6 +71,12 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] == 0
+    assert d["unit"] == d["e2e"]["unit"] == d["cpu_baseline"]["unit"] == "pairs/s"
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["config"]["workload"] == "clip_n256"
 
