@@ -62,12 +62,33 @@ def executed_flops(kind, Na, Nb, D, prefixes=None):
 
 
 def group_flops(group, kind, Na, Nb, D, prefixes):
-    """Algorithmic tensor flops of one kernel group per step (None: not a tensor kernel)."""
+    """Algorithmic tensor flops of one kernel group per step (None: not a tensor kernel): the
+    method's own work.  A score pass is 2 Na Nb p_n (the prefixes nest, so one K sweep serves
+    all of them); each gradient contraction is 2 Na Nb p_n as well (every output dimension d
+    receives the running sum of the weights of the prefixes that reach d, so it is contracted
+    once)."""
     pre = list(prefixes)
     if group in ("fwd_tile", "bwd_tile"):
-        return 2.0 * Na * Nb * pre[-1]  # one score pass over every prefix (cumulative bands)
+        return 2.0 * Na * Nb * pre[-1]
     if group == "gemm":
-        return 2 * 2.0 * Na * Nb * sum(pre)  # dA and dB contractions, prefix-expanded
+        return 2 * 2.0 * Na * Nb * pre[-1]  # the dA and the dB contraction
+    return None
+
+
+def group_flops_executed(group, kind, Na, Nb, D, prefixes):
+    """Tensor flops the library's kernels of one group actually issue per step."""
+    pre = list(prefixes)
+    if group == "gemm":
+        return 2 * 2.0 * Na * Nb * sum(pre)  # prefix-expanded: prefix k contributes its p_k dimensions
+    return group_flops(group, kind, Na, Nb, D, prefixes)
+
+
+def group_bytes(group, kind, Na, Nb, D, prefixes):
+    """Algorithmic HBM bytes of one kernel group per step: what the method must move for it
+    at the least (the two gradient contractions: each writes its fp32 gradient once and reads
+    the other side's bf16 embeddings once; the weights never need to leave the chip)."""
+    if group == "gemm":
+        return 4.0 * (Na + Nb) * D + 2.0 * (Na + Nb) * D
     return None
 
 
@@ -358,12 +379,22 @@ def main():
     alg_step = group_flops(dom, kind, Na, Nb, D, LADDER)
     roof = None
     if alg_step is not None:
-        alg_launch = alg_step * args.steps / max(dom_launches, 1)
+        per_launch = args.steps / max(dom_launches, 1)
+        alg_launch = alg_step * per_launch
+        exe_launch = group_flops_executed(dom, kind, Na, Nb, D, LADDER) * per_launch
         achieved = alg_launch / (per_launch_ms / 1e3) / 1e12
+        traffic = ncu_traffic(args.workload)
+        alg_bytes = group_bytes(dom, kind, Na, Nb, D, LADDER)
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved / peak_tf, "traffic": ncu_traffic(args.workload),
+                "frac": achieved / peak_tf, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
-                "algorithmic_flops_per_launch": alg_launch, "launches_per_step": dom_launches / args.steps,
+                "algorithmic_flops_per_launch": alg_launch,
+                "executed_flops_per_launch": exe_launch,
+                "executed_tflops": exe_launch / (per_launch_ms / 1e3) / 1e12,
+                "algorithmic_bytes_per_launch": None if alg_bytes is None else alg_bytes * per_launch,
+                "traffic_over_algorithmic": (None if traffic is None or alg_bytes is None
+                                             else traffic / (alg_bytes * per_launch)),
+                "launches_per_step": dom_launches / args.steps,
                 "ms_per_launch": per_launch_ms, "share_of_step": dom_ms / ms_local}
     cflops = credited_flops(kind, Na, Nb, D)
     line = {
@@ -382,7 +413,10 @@ def main():
         "e2e": {"value": e2e_value, "unit": "pairs/s", "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
                 "d2h_bytes_per_step": int(loss_h.numel() * 4), "ms_per_step": ms_e2e / args.steps,
                 "copies": f"pinned host -> device, split over {COPY_SPLIT} streams, double-buffered: step i + 1's "
-                          f"inputs copied during step i (every copy inside the timed region)"},
+                          f"inputs copied during step i (every copy inside the timed region)",
+                "results": "the per-prefix loss is copied to pinned host memory every step; dA and dB "
+                           f"({2 * (Na + Nb) * D} bytes of fp32) stay on the device, where the training step "
+                           "that consumes them runs"},
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:

@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
   const int64_t items = p.na > p.nb ? p.na : p.nb;
   int64_t blocks = (items * 8 + 255) / 256;  // eight lanes per item
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > int64_t(16) * current_sm_count()) blocks = int64_t(16) * current_sm_count();
   prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(1024) finalize_kernel(const StatsParams p) {
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(p.n_prefix) * (p.na + p.nb);
   int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks > int64_t(8) * current_sm_count()) blocks = int64_t(8) * current_sm_count();
   stats_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(256) max_reduce_kernel(const MaxReduceParams p
 cudaError_t launch_max_reduce(const MaxReduceParams& p, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(p.n_prefix) * (p.na + (p.v ? p.nb : 0));
   int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks > int64_t(8) * current_sm_count()) blocks = int64_t(8) * current_sm_count();
   max_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(256) labels_kernel(const LabelParams p) {
 cudaError_t launch_labels(const LabelParams& p, cudaStream_t stream) {
   const int64_t rows = p.W ? p.rows : p.na;
   int64_t blocks = (rows * 32 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > int64_t(16) * current_sm_count()) blocks = int64_t(16) * current_sm_count();
   if (blocks < 1) blocks = 1;
   labels_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
@@ -630,7 +630,7 @@ cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream) {
 
 cudaError_t launch_norm_bwd(const NormBwdParams& p, cudaStream_t stream) {
   int64_t blocks = (p.nx * 32 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > int64_t(16) * current_sm_count()) blocks = int64_t(16) * current_sm_count();
   norm_bwd_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }

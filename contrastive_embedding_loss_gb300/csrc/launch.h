@@ -8,6 +8,9 @@
 
 namespace ufc {
 
+// SM count of the current device (grid caps of the grid-stride kernels).
+int current_sm_count();
+
 // Load every auxiliary kernel now (aux_kernels.cu).
 cudaError_t aux_kernels_setup();
 

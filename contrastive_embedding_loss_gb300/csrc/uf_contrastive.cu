@@ -17,7 +17,11 @@ using namespace ufc;
 
 namespace {
 
-constexpr int kTargetCtas = 600;  // about four waves of one CTA per SM on a 152-SM GB300
+// CTAs the forward and weight passes aim for when they split the columns of short row ranges.
+// A constant (about four waves of one CTA per SM on a 152-SM GB300), not the device's SM
+// count: the split sets the size of the per-split partial-sum arrays, and the workspace size
+// must be a function of the problem alone (it is queried before any device is chosen).
+constexpr int kTargetCtas = 600;
 
 struct Split {
   int splits = 1;
@@ -225,6 +229,19 @@ struct ProfScope {
 };
 
 }  // namespace
+
+namespace ufc {
+// SM count of the current device (read at uf_contrastive_init; queried here if the device was
+// never initialised, e.g. by a launcher called from a test harness).
+int current_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) return g_sm_count[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+  return n;
+}
+}  // namespace ufc
 
 extern "C" {
 

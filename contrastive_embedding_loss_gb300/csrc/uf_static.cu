@@ -10,6 +10,7 @@
 // until the process exits.  The entry point allocates nothing: it looks up the array's
 // device address, checks that the call fits, and runs the ordinary entry point with the
 // array as its workspace.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -23,16 +24,49 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_workspace[UF_STATIC_WORKSPACE_BYTES];
 
 std::mutex g_static_mu;
-void* g_static_ptr[64] = {};  // per-device address of g_static_workspace, looked up once
+void* g_static_ptr[64] = {};              // per-device address of g_static_workspace
+unsigned long long g_static_ctx[64] = {};  // id of the context that address belongs to
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the current context (the driver never reuses one within a process), or 0.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 // Device address of the array on `device` (which must be current); nullptr on failure.
+// The address is looked up at a device's first call and again whenever the device's
+// context has changed since (after cudaDeviceReset the module, and the array with it, is
+// loaded afresh at another address).
 void* static_workspace(int device) {
-  std::lock_guard<std::mutex> lock(g_static_mu);
   if (device < 0 || device >= 64) return nullptr;
-  if (!g_static_ptr[device]) {
+  unsigned long long ctx = current_context_id();  // 0 while no context is current on this thread
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[device] || ctx == 0 || g_static_ctx[device] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) return nullptr;
+    if (ctx == 0) ctx = current_context_id();  // the lookup made the primary context current
     g_static_ptr[device] = p;
+    g_static_ctx[device] = ctx;
   }
   return g_static_ptr[device];
 }

@@ -20,7 +20,11 @@
  *                           of query i being key i (Nb >= Na).
  * The gradients returned are those of sum_p w_p L_p (w_p = 1 unless given).
  * Precision policy (UForm README, "Training is BF16"): operands bf16, products and
- * every accumulation fp32, gradients fp32.  The Na x Nb logits are never stored.
+ * every accumulation fp32, gradients fp32.  The forward never stores the Na x Nb logits.
+ * The backward does store Na x Nb data in the caller's workspace: for every prefix, the
+ * bf16 per-cell weights rho_i sigma_j dL/dcos_ij (for a chunk of A's rows at a time when
+ * the workspace is smaller than uf_contrastive_workspace_size), which tensor-core GEMMs
+ * then contract with the embeddings.
  *
  * Conventions (UForm Swift binding page, sections "Errors" and "Design": one C verb per
  * operation named <lib>_<noun>_<verb>, an enum status with a name function; section
@@ -232,11 +236,12 @@ UF_API uf_status_t uf_contrastive_oneset_fwd_bwd(const void* X, int64_t N, int D
  * passes inputs and outputs, with the same meaning and rules as uf_contrastive_fwd_bwd.
  *   - A request whose uf_contrastive_workspace_min() exceeds UF_STATIC_WORKSPACE_BYTES
  *     returns UF_WORKSPACE_TOO_SMALL before anything is enqueued (at D = 1024 with the
- *     five-prefix ladder, CLIP with gradients fits up to about N = 10240, SigLIP to a
- *     larger N); inside that bound the backward cuts A's rows into as many weight chunks
- *     as the array needs.
- *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *     five-prefix ladder and Na = Nb = N, with gradients: CLIP fits up to N = 12201,
+ *     SigLIP up to N = 14976); inside that bound the backward cuts A's rows into as many
+ *     weight chunks as the array needs.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current), and so does the first call after the device's context was replaced
+ *     (cudaDeviceReset); make such a call before any stream capture.
  *   - All calls on a device share the one array, and it keeps whatever the last call left
  *     there (nothing in it needs clearing: every element is written before it is read).
  *     Calls whose GPU work overlaps -- on different streams, or from different threads --

@@ -13,6 +13,7 @@ from .ref import (  # noqa: F401
     build,
     fwd_bwd,
     row_stats,
+    softmax_normalisers,
     row_terms_sampled,
     grad_rows,
     scale_grads,

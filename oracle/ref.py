@@ -171,6 +171,54 @@ def row_stats(kind, X, Y, prefixes, scale, bias, rows):
     return lse, pos
 
 
+def softmax_normalisers(kind, X, Y, prefixes, scale, row_chunk=None):
+    """Every row's softmax log-normaliser at every prefix, for large batches: (lse, pos) with
+    lse[k, i] = log sum_j exp(scale cos^k_ij) over all rows j of Y and pos[k, i] = scale cos^k_ii
+    (0 for i >= len(Y)).  These are the log-sum-exp terms of the InfoNCE losses (blog
+    "Scaling-Up Contrastive Learning over NVLink Multicast", section "One Set or Two": each
+    row of cosines becomes a softmax over the batch); ``grad_rows`` takes them as lse_x /
+    lse_y, and CLIP's column normalisers are this function with X and Y exchanged.
+
+    The same definition as ``row_stats`` (bf16 widened exactly to float64; each prefix
+    normalised on its own, inverse norm 1/max(|x[:p]|, 1e-30)), with one float64 library
+    matmul per prefix and row chunk as the dot-product step, in torch CPU ops (all host
+    cores) so that a batch of 65536 x 65536 takes minutes rather than the C loops' hour.
+    CLIP and ROWS only (SigLIP has no normaliser)."""
+    import torch
+
+    if kind not in ("clip", "rows"):
+        raise ValueError("softmax normalisers exist for clip and rows only")
+    X, Y = _bits(X), _bits(Y)
+    pre = [int(p) for p in prefixes]
+    Xd = torch.from_numpy(_widen(X))
+    Yd = torch.from_numpy(_widen(Y))
+    Nx, Ny = Xd.shape[0], Yd.shape[0]
+    if row_chunk is None:
+        row_chunk = max(64, min(Nx, (1 << 27) // Ny))  # about 1 GiB of float64 scores per chunk
+    lse = np.zeros((len(pre), Nx))
+    pos = np.zeros((len(pre), Nx))
+    for k, p in enumerate(pre):
+        xn = Xd[:, :p] / Xd[:, :p].norm(dim=1, keepdim=True).clamp_min(1e-30)
+        yn = Yd[:, :p] / Yd[:, :p].norm(dim=1, keepdim=True).clamp_min(1e-30)
+        for r0 in range(0, Nx, row_chunk):
+            s = xn[r0:r0 + row_chunk] @ yn.T
+            s.mul_(float(scale))
+            m = min(r0 + s.shape[0], Ny) - r0
+            if m > 0:
+                idx = torch.arange(m)
+                pos[k, r0:r0 + m] = s[idx, r0 + idx].numpy()
+            # log-sum-exp with the shift |scale| (|cos| <= 1 bounds every logit by it, and
+            # e^(-2 |scale|) is far inside float64's range for every accepted scale)
+            sh = abs(float(scale))
+            lse[k, r0:r0 + s.shape[0]] = (s.sub_(sh).exp_().sum(dim=1).log_() + sh).numpy()
+    return lse, pos
+
+
+def _widen(bits):
+    """bf16 bit patterns -> float64, exactly."""
+    return (np.ascontiguousarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def row_terms_sampled(kind, X, Y, prefixes, scale, bias, rows):
     """Per-row loss terms (shape (n, len(rows))), computed one row at a time."""
     lse, pos = row_stats(kind, X, Y, prefixes, scale, bias, rows)

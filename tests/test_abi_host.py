@@ -340,3 +340,31 @@ def test_binding_checks_shapes_before_anything_else(lib):
         binding.contrastive_fwd_bwd(A, A)  # host tensors: no CPU path
     with pytest.raises(TypeError, match="CUDA"):
         binding.oneset_fwd_bwd(A, (np.zeros(5, np.int64), np.zeros(0, np.int32)))
+
+
+def _largest_n_in_static_array(kind, limit):
+    lo, hi = 1, 1 << 20
+    while lo < hi:
+        m = (lo + hi + 1) // 2
+        need = binding.uf_contrastive_workspace_min(m, m, 1024, LADDER, kind, 1)
+        if need and need <= limit:
+            lo = m
+        else:
+            hi = m - 1
+    return lo
+
+
+def test_static_entry_bounds_match_its_documentation(lib):
+    """The header states the largest N that the no-allocation entry point's fixed scratch array
+    takes (D = 1024, five prefixes, Na = Nb = N, with gradients); those figures come from
+    uf_contrastive_workspace_min, and this pins them."""
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                            "uf_contrastive.h")).read()
+    limit = int(re.search(r"#define UF_STATIC_WORKSPACE_BYTES \((\d+)u << 20\)", hdr).group(1)) << 20
+    m = re.search(r"CLIP fits up to N = (\d+),\s*\*\s*SigLIP up to N = (\d+)", hdr)
+    assert m, "the header no longer states the bounds"
+    assert _largest_n_in_static_array(0, limit) == int(m.group(1))
+    assert _largest_n_in_static_array(1, limit) == int(m.group(2))
+    # one row more does not fit, and the entry point refuses it on the host
+    n = int(m.group(1)) + 1
+    assert binding.uf_contrastive_workspace_min(n, n, 1024, LADDER, 0, 1) > limit

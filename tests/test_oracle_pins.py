@@ -323,6 +323,35 @@ def test_sampled_row_functions_match_full(kind):
     np.testing.assert_allclose(gB, full["dB"][rows_b], rtol=1e-10, atol=1e-15)
 
 
+@pytest.mark.parametrize("kind", ["clip", "rows"])
+def test_softmax_normalisers_match_the_row_loops_and_feed_full_gradients(kind):
+    """The large-batch normalisers (one float64 matmul per prefix and row chunk) equal the C
+    oracle's row loops; fed to grad_rows as lse_x / lse_y they give the full backward's rows."""
+    Na, Nb = 70, (150 if kind == "rows" else 70)
+    A, _ = _random_pair(Na, 128, 23)
+    B, _ = _random_pair(Nb, 128, 24)
+    B[:Na] = _bits(_wide(A) + 0.5 * _wide(B[:Na]))
+    pre = (64, 128)
+    s = 1 / 0.07
+    lse_a, pos_a = oracle.softmax_normalisers(kind, A, B, pre, s, row_chunk=33)
+    la, pa = oracle.row_stats(kind, A, B, pre, s, 0.0, np.arange(Na))
+    np.testing.assert_allclose(lse_a, la.T, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(pos_a, pa.T, rtol=1e-13, atol=1e-13)
+    lse_b, _ = oracle.softmax_normalisers(kind, B, A, pre, s, row_chunk=64)
+    full = oracle.fwd_bwd(kind, A, B, pre, s, 0.0)
+    rows = np.array([0, 33, Na - 1])
+    gA = oracle.grad_rows(kind, True, A, B, pre, s, 0.0, rows, lse_a, lse_b)
+    np.testing.assert_allclose(gA, full["dA"][rows], rtol=1e-10, atol=1e-15)
+    cols = np.array([2, Na - 1, Nb - 1])
+    gB = oracle.grad_rows(kind, False, B, A, pre, s, 0.0, cols, lse_b, lse_a)
+    np.testing.assert_allclose(gB, full["dB"][cols], rtol=1e-10, atol=1e-15)
+    # identical rows: every logit equals the scale, so lse = scale + ln N (the closed form)
+    X = np.repeat(A[:1], 40, axis=0)
+    lse, pos = oracle.softmax_normalisers(kind, X, X, pre, s)
+    np.testing.assert_allclose(lse, s + math.log(40), rtol=1e-14)
+    np.testing.assert_allclose(pos, s, rtol=1e-14)
+
+
 def test_zero_norm_prefix_reading():
     """A row whose prefix is all zero scores cosine 0 there (inverse norm floored at 1e30)."""
     A, B = _random_pair(6, 128, 30)

@@ -1,11 +1,13 @@
 """Parity at the full benchmark sizes, in the launch configuration the benchmark times.
 
-Where the oracle can compute an output one row at a time, it does so on seeded samples
-(per-row loss terms of 512 rows / columns, SigLIP and row-InfoNCE gradient rows, whose
-normalisers are row-local).  Outputs that need every normaliser of the batch at once
-(CLIP gradients at N = 65536) are checked through properties that hold at any size:
-the per-row Euler identity sum_d x_d dL/dx_d = 0 of a scale-invariant loss, the mean of
-the row terms equalling the loss, and A <-> B swap symmetry.
+The oracle computes outputs one row at a time on seeded samples: per-row loss terms of 512
+rows and columns, and 512 gradient rows of each side.  A gradient row of an InfoNCE loss
+needs the softmax normalisers of every row (and for CLIP every column) of the batch; the
+oracle's large-batch normaliser routine (float64 matmuls on the host cores) supplies them,
+and the C oracle's row loops check it again on the sampled rows.  At N = 65536 the dA and
+dB contractions run as two separate launches, as in the benchmark.  Properties that hold at
+any size are checked as well: the per-row Euler identity sum_d x_d dL/dx_d = 0 of a
+scale-invariant loss, the mean of the row terms equalling the loss, A <-> B swap symmetry.
 """
 import numpy as np
 import pytest
@@ -104,11 +106,20 @@ def test_clip_n65536_sampled_and_properties(ctx):
     out = run(ctx, kind, A16, B16, s, b)
     check_loss_is_mean_of_terms(out, kind)
     rows = sample(A16.shape[0], 512, 3)
-    check_terms(out["row_terms"][:, rows].double().cpu().numpy(),
-                oracle.row_terms_sampled(kind, A16, B16, LADDER, s, b, rows), "row terms")
+    lse_r, pos_r = oracle.row_stats(kind, A16, B16, LADDER, s, b, rows)
+    check_terms(out["row_terms"][:, rows].double().cpu().numpy(), (lse_r - pos_r).T, "row terms")
     cols = sample(B16.shape[0], 512, 4)
-    check_terms(out["col_terms"][:, cols].double().cpu().numpy(),
-                oracle.row_terms_sampled(kind, B16, A16, LADDER, s, b, cols), "col terms")
+    lse_c, pos_c = oracle.row_stats(kind, B16, A16, LADDER, s, b, cols)
+    check_terms(out["col_terms"][:, cols].double().cpu().numpy(), (lse_c - pos_c).T, "col terms")
+    # gradient rows of both sides against the oracle, from every row's and column's normaliser
+    lse_a, _ = oracle.softmax_normalisers(kind, A16, B16, LADDER, s)
+    lse_b, _ = oracle.softmax_normalisers(kind, B16, A16, LADDER, s)
+    np.testing.assert_allclose(lse_a[:, rows], lse_r.T, rtol=1e-12)  # the two oracle routes agree
+    np.testing.assert_allclose(lse_b[:, cols], lse_c.T, rtol=1e-12)
+    gA = oracle.grad_rows(kind, True, A16, B16, LADDER, s, b, rows, lse_x=lse_a, lse_y=lse_b)
+    check_grad_rows(out["dA"][rows].double().cpu().numpy(), gA, "dA rows")
+    gB = oracle.grad_rows(kind, False, B16, A16, LADDER, s, b, cols, lse_x=lse_b, lse_y=lse_a)
+    check_grad_rows(out["dB"][cols].double().cpu().numpy(), gB, "dB rows")
     check_euler(A16, out["dA"], "dA")
     check_euler(B16, out["dB"], "dB")
     assert torch.all(out["dA"][:, LADDER[-1]:] == 0) if A16.shape[1] > LADDER[-1] else True
@@ -165,16 +176,21 @@ def test_clip_n65536_in_two_large_chunks(ctx):
 
 def test_rows_q8192_k262144_sampled(ctx):
     kind, Q16, K16, s, b = synth.workload("rows_q8192_k262144")
+    Nq, Nk = Q16.shape[0], K16.shape[0]
     out = run(ctx, kind, Q16, K16, s, b)
     check_loss_is_mean_of_terms(out, kind)
     assert torch.all(out["col_terms"] == 0)
-    rows = sample(Q16.shape[0], 128, 5)
+    rows = sample(Nq, 512, 5)
     lse, pos = oracle.row_stats(kind, Q16, K16, LADDER, s, b, rows)
     check_terms(out["row_terms"][:, rows].double().cpu().numpy(), (lse - pos).T, "query terms")
-    grows = rows[:64]
-    lse_full = np.zeros((len(LADDER), Q16.shape[0]))
-    lse_full[:, grows] = lse[:64].T
-    gQ = oracle.grad_rows(kind, True, Q16, K16, LADDER, s, b, grows, lse_x=lse_full)
-    check_grad_rows(out["dA"][grows].double().cpu().numpy(), gQ, "query gradient rows")
+    # every query's normaliser: the keys' gradient rows sum over all queries
+    lse_q, _ = oracle.softmax_normalisers(kind, Q16, K16, LADDER, s)
+    np.testing.assert_allclose(lse_q[:, rows], lse.T, rtol=1e-12)  # the two oracle routes agree
+    gQ = oracle.grad_rows(kind, True, Q16, K16, LADDER, s, b, rows, lse_x=lse_q)
+    check_grad_rows(out["dA"][rows].double().cpu().numpy(), gQ, "query gradient rows")
+    # 512 key rows: half among the positives' keys (< Nq), half among the negatives only
+    keys = np.concatenate([sample(Nq, 256, 8), Nq + sample(Nk - Nq, 256, 9)])
+    gK = oracle.grad_rows(kind, False, K16, Q16, LADDER, s, b, keys, lse_y=lse_q)
+    check_grad_rows(out["dB"][keys].double().cpu().numpy(), gK, "key gradient rows")
     check_euler(Q16, out["dA"], "dA")
     check_euler(K16, out["dB"], "dB")
