@@ -289,13 +289,21 @@ __device__ __forceinline__ float fwd_cells16_reduce(const float2 (&rs)[4], const
 struct Schedule {
   int T, n;
   __device__ int steps() const { return T * n; }
-  __device__ void at(int s, int& t, int& b) const {
-    const int pair = s / (2 * n);
-    const int rem = s - pair * 2 * n;
-    const int tp = 2 * pair;
-    const int width = (tp + 1 < T) ? 2 : 1;  // the last pair may hold one tile
-    b = rem / width;
-    t = tp + rem % width;
+};
+// Walks the schedule one step at a time without divisions (every epilogue thread keeps one).
+struct SchedIter {
+  int T, n;
+  int tp = 0, b = 0, u = 0;  // first tile of the pair, band, tile within the pair
+  int width = 0;             // tiles in this pair (the last pair may hold one)
+  __device__ SchedIter(int T_, int n_) : T(T_), n(n_), width(T_ > 1 ? 2 : 1) {}
+  __device__ int t() const { return tp + u; }
+  __device__ void next() {
+    if (++u < width) return;
+    u = 0;
+    if (++b < n) return;
+    b = 0;
+    tp += 2;
+    width = (tp + 1 < T) ? 2 : 1;
   }
 };
 
@@ -364,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- operand producer
     uint32_t it = 0;
     bool ok = true;
-    for (int s = 0; s < sched.steps() && ok; ++s) {
-      int t, b;
-      sched.at(s, t, b);
+    SchedIter si(T, n);
+    for (int s = 0; s < sched.steps() && ok; ++s, si.next()) {
+      const int t = si.t(), b = si.b;
       const int j0 = (t_begin + t) * kCols;
       const int c0 = b == 0 ? 0 : pend[b - 1] / kChunk, c1 = pend[b] / kChunk;
       for (int c = c0; c < c1; ++c, ++it) {
@@ -391,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;
     uint32_t uses[2] = {0, 0};
     bool ok = true;
-    for (int s = 0; s < sched.steps() && ok; ++s) {
-      int t, b;
-      sched.at(s, t, b);
+    SchedIter si(T, n);
+    for (int s = 0; s < sched.steps() && ok; ++s, si.next()) {
+      const int t = si.t(), b = si.b;
       const int a = t & 1;
       if (uses[a] > 0 && !wait_bounded(&acc_empty[a], (uses[a] - 1) & 1, abort_flag)) {
         fail(p, abort_flag);
@@ -469,9 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t uses0 = 0, uses1 = 0;  // uses of each accumulator (scalars: a runtime index would put them in local memory)
     uint32_t snap = 0;  // snapshots processed (selects the column-partial buffer)
     bool ok = true;
-    for (int s = 0; s < sched.steps(); ++s) {
-      int t, b;
-      sched.at(s, t, b);
+    SchedIter si(T, n);
+    for (int s = 0; s < sched.steps(); ++s, si.next()) {
+      const int t = si.t(), b = si.b;
       if ((t & 1) == 0 && b == 0) {
         // a tile pair begins (every warp reaches this point at the same step)
         named_bar_sync(1, kEpiThreads);          // all are done with the previous pair
