@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-workspace", action="store_true",
+                    help="run with uf_contrastive_workspace_min bytes (the backward in 128-row weight chunks)")
     return ap.parse_args()
 
 
@@ -278,7 +280,8 @@ def main():
     to_t = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)  # noqa: E731
     A_h, B_h = to_t(A16).pin_memory(), to_t(B16).pin_memory()
     A_d, B_d = A_h.to(dev), B_h.to(dev)
-    ws_bytes = binding.uf_contrastive_workspace_size(Na, Nb, D, LADDER, k, True)
+    ws_bytes = (binding.uf_contrastive_workspace_min if args.min_workspace else binding.uf_contrastive_workspace_size)(
+        Na, Nb, D, LADDER, k, True)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     loss = torch.empty(n, dtype=torch.float32, device=dev)
     dA = torch.empty((Na, D), dtype=torch.float32, device=dev)
@@ -319,6 +322,39 @@ def main():
     ms_step = ms / args.steps
     units = pairs_of(None, A16)
     value = units * world * args.steps / (ms / 1e3)
+
+    # ---- the same step captured once in a CUDA graph and replayed (the call only enqueues work
+    # on the caller's stream, so a training loop can capture it): what launch latency costs
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                gs = torch.cuda.current_stream(dev)
+                st = binding.uf_contrastive_fwd_bwd(A_d.data_ptr(), B_d.data_ptr(), Na, Nb, D, LADDER, k, scale, bias,
+                                                    None, loss.data_ptr(), None, None, dA.data_ptr(), dB.data_ptr(),
+                                                    ws.data_ptr(), ws_bytes, status.data_ptr(), gs.cuda_stream)
+                if st != binding.UF_OK:
+                    raise binding.UfError(st, "uf_contrastive_fwd_bwd (captured)")
+        stream.wait_stream(side)
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms_graph = barrier_max(ev0.elapsed_time(ev1), world)
+        graph = {"value": units * world * args.steps / (ms_graph / 1e3), "unit": "pairs/s",
+                 "ms_per_step": ms_graph / args.steps,
+                 "how": "one uf_contrastive_fwd_bwd captured in a CUDA graph, replayed every step"}
+        del g
+    except Exception as exc:  # capture is reported, not required
+        graph = {"error": str(exc)[:200]}
+    assert int(status.item()) == 0, "a kernel reported a timeout"
 
     # ---- end to end through the public API with host buffers: H2D inputs, D2H loss, every step.
     # A training loop's loader copies the next batch while the current one computes, so the
@@ -403,7 +439,8 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "kind": kind, "Na": int(Na), "Nb": int(Nb), "D": int(D),
                    "prefixes": list(LADDER), "logit_scale": scale, "bias": bias,
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+                   "workspace_bytes": int(ws_bytes)},
         "tflops_credited": cflops / (ms_step / 1e3) / 1e12,
         "tflops_executed": executed_flops(kind, Na, Nb, D, LADDER) / (ms_step / 1e3) / 1e12,
         "frac_credited_of_bf16_peak": cflops / (ms_step / 1e3) / 1e12 / peak_tf,
@@ -417,6 +454,7 @@ def main():
                 "results": "the per-prefix loss is copied to pinned host memory every step; dA and dB "
                            f"({2 * (Na + Nb) * D} bytes of fp32) stay on the device, where the training step "
                            "that consumes them runs"},
+        "graph": graph,
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:

@@ -639,13 +639,18 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     gb.X = B16;
     gb.crow = F(P.o_crow_b);
     gb.crow_rows = Nb;
+    // The column split of one chunk's weight pass: the whole problem's for SigLIP (its row slots
+    // of loss sums are sized by it); for CLIP and ROWS, which keep no per-split state, one sized
+    // for the chunk's own row blocks, so a small chunk still fills the GPU.
+    const Split wsplit = siglip ? P.wgt : plan_split(cdiv(P.chunk, kTileRows), 1, cdiv(Nb, kWgtCols));
+    wp.tiles_per_split = wsplit.tiles_per_split;
     for (int64_t r0 = 0; r0 < Na; r0 += P.chunk) {
       const int64_t rows = Na - r0 < P.chunk ? Na - r0 : P.chunk;
       wp.row0 = r0;
       wp.rows = rows;
       {
         ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-        UF_CHECK(launch_wgt(kind, tmA, tmB, tmWs, wp, dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), P.wgt.splits),
+        UF_CHECK(launch_wgt(kind, tmA, tmB, tmWs, wp, dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), wsplit.splits),
                             stream));
       }
       if (labels) {  // the labelled positives' exact weights over the negative-cell ones
