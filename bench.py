@@ -40,7 +40,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-workspace", action="store_true",
-                    help="run with uf_contrastive_workspace_min bytes (the backward in 128-row weight chunks)")
+                    help="run with uf_contrastive_workspace_min bytes (the backward in its smallest weight chunks)")
+    ap.add_argument("--weights-gib", type=float, default=None,
+                    help="run with uf_contrastive_workspace_min bytes plus this many GiB for the weight chunks")
     return ap.parse_args()
 
 
@@ -280,8 +282,10 @@ def main():
     to_t = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)  # noqa: E731
     A_h, B_h = to_t(A16).pin_memory(), to_t(B16).pin_memory()
     A_d, B_d = A_h.to(dev), B_h.to(dev)
-    ws_bytes = (binding.uf_contrastive_workspace_min if args.min_workspace else binding.uf_contrastive_workspace_size)(
-        Na, Nb, D, LADDER, k, True)
+    ws_bytes = binding.uf_contrastive_workspace_size(Na, Nb, D, LADDER, k, True)
+    if args.min_workspace or args.weights_gib is not None:
+        extra = int((args.weights_gib or 0.0) * (1 << 30)) // 256 * 256
+        ws_bytes = min(ws_bytes, binding.uf_contrastive_workspace_min(Na, Nb, D, LADDER, k, True) + extra)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     loss = torch.empty(n, dtype=torch.float32, device=dev)
     dA = torch.empty((Na, D), dtype=torch.float32, device=dev)

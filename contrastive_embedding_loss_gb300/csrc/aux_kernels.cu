@@ -572,11 +572,11 @@ __global__ void __launch_bounds__(256) labels_kernel(const LabelParams p) {
         const float x = t * (cum * rho * sig) + bias;
         if (!patch) {
           xs[k] += x;
-        } else if (lane == 0) {
+        } else if (lane == 0 && j >= p.col0 && j < p.col0 + p.cols) {  // (this launch's columns)
           const float m = -(1.f / (1.f + expf(x))) * rho * sig *
                           static_cast<float>(p.weight[k] * t / static_cast<double>(p.na));
           const __nv_bfloat16 h = __float2bfloat16_rn(m);
-          p.W[(static_cast<int64_t>(k) * p.w_rows_per_prefix + (i - p.row0)) * p.ldw + j] =
+          p.W[(static_cast<int64_t>(k) * p.w_rows_per_prefix + (i - p.row0)) * p.ldw + (j - p.col0)] =
               *reinterpret_cast<const uint16_t*>(&h);
         }
       }

@@ -46,17 +46,20 @@ cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
 
 // Backward weights (wgt_kernel.cu): m^k_ij = rho_i sigma_j dL/dcos^k_ij as bf16 into a
 // [prefix][row][column] array (row stride in elements fixed by tm_w), plus (SigLIP) the
-// row loss sums.  One launch covers rows
-// [row0, row0 + rows) of X; grid = (ceil(rows / 128), splits of the 256-column tiles).
+// row loss sums.  One launch covers rows [row0, row0 + rows) of X against rows
+// [col0, col0 + cols) of Y; grid = (ceil(rows / 128), splits of the 256-column tiles).
 // tm_x: [128 x 64] boxes of X; tm_y: [128 x 64] boxes of Y (each CTA of a pair stages half of
 // the 256-row tile); tm_w: [32 x 64] boxes of the weight array viewed as
 // [n * w_rows_per_prefix rows][ny columns].  Launched as CTA pairs (clusters of 2 along x).
 struct WgtParams {
   int64_t nx, ny;                 // full sizes of X and Y
   int64_t row0, rows;             // this launch's rows of X
+  int64_t col0, cols;             // this launch's rows of Y (columns of the weights; the array holds
+                                  // column col0 + c at its column c)
+  int add_rows;                   // SigLIP: add the row sums into rowacc / rowsig (a later column range)
+  int n_col_tiles;                // ceil(cols / 256)
   int n_prefix;
   int prefix_end[kMaxPrefix];
-  int n_col_tiles;                // ceil(ny / 256)
   int tiles_per_split;
   Scalars sc;
   int shifted;                    // CLIP/ROWS: the max-shifted statistics (alpha_x, beta_y in log2 form)
@@ -251,8 +254,9 @@ struct LabelParams {
   const float* rinv_b;
   float* pos_term;
   float* lcount;
-  uint16_t* W;
+  uint16_t* W;             // patch mode: the weights of rows [row0, row0 + rows), columns [col0, col0 + cols)
   int64_t row0, rows, w_rows_per_prefix, ldw;
+  int64_t col0, cols;
   int oneset;              // one-set loss: a self-pair (j == i) or a pair whose mirror is missing is malformed
   int* status;
 };

@@ -56,7 +56,8 @@ struct Plan {
   int slices = 0;                    // 256-dimension slices of the gradient GEMMs
   int64_t lda = 0, ldb = 0;          // padded leading dimensions of A^T and B^T
   int64_t ldw = 0;                   // row stride of the weight array (elements)
-  int64_t chunk = 0;                 // rows of X per weight chunk (multiple of 128)
+  int64_t chunk = 0;                 // rows of A per weight chunk (multiple of 128)
+  int64_t cchunk = 0;                // rows of B (weight columns) per weight chunk
   size_t fixed = 0;                  // bytes of everything but the weight array
   // offsets
   size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
@@ -66,7 +67,9 @@ struct Plan {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ws_limit: the workspace the caller provides (0: plan the default weight array).  The
-// weight array takes what is left after the fixed part, in chunks of 128 rows.
+// weight array takes what is left after the fixed part: every weight at once if it fits, else
+// chunks of (rows of A) x (rows of B), about square (multiples of 128 x 256), so that both
+// gradient contractions of a chunk stay wide.
 bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int kind, bool grads, size_t ws_limit,
                Plan& P) {
   if (Na < 1 || Nb < 1 || D < 64 || D > 4096 || D % 64 != 0 || n < 1 || n > kMaxPrefix || !prefixes) return false;
@@ -133,15 +136,38 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.fixed = o;
   P.o_w = o;
   P.chunk = 0;
+  P.cchunk = 0;
   if (grads) {
     const int64_t rows_max = cdiv(Na, kTileRows) * kTileRows;
-    const size_t row_bytes = sizeof(uint16_t) * static_cast<size_t>(n) * static_cast<size_t>(P.ldw);
+    const int64_t cols_max = cdiv(Nb, kWgtCols) * kWgtCols;
+    const size_t per = sizeof(uint16_t) * static_cast<size_t>(n);  // bytes per (row, column) cell
     const size_t budget = ws_limit ? (ws_limit > o ? ws_limit - o : 0) : kDefaultWeightBytes;
-    int64_t rows = static_cast<int64_t>(budget / row_bytes) / kTileRows * kTileRows;
-    if (rows > rows_max) rows = rows_max;
-    if (rows < kTileRows) rows = kTileRows;  // the minimum; a smaller workspace is rejected by the caller
-    P.chunk = rows;
-    o = align256(o + row_bytes * static_cast<size_t>(rows));
+    if (per * static_cast<size_t>(rows_max) * static_cast<size_t>(P.ldb) <= budget) {
+      P.chunk = rows_max;  // one chunk
+      P.cchunk = Nb;
+      P.ldw = P.ldb;
+    } else {
+      const double cells = static_cast<double>(budget / per);
+      int64_t R = static_cast<int64_t>(std::sqrt(cells)) / kTileRows * kTileRows;
+      if (R > rows_max) R = rows_max;
+      if (R < kTileRows) R = kTileRows;
+      int64_t C = static_cast<int64_t>(cells / static_cast<double>(R)) / kWgtCols * kWgtCols;
+      if (C > cols_max) C = cols_max;
+      if (C < kWgtCols) C = kWgtCols;  // the minimum chunk; a smaller workspace is rejected by the caller
+      if (C == cols_max) {  // every column in one chunk (rows as the 1-D layout): the rest buys rows
+        int64_t R2 = static_cast<int64_t>(cells / static_cast<double>(P.ldb)) / kTileRows * kTileRows;
+        if (R2 > rows_max) R2 = rows_max;
+        if (R2 < kTileRows) R2 = kTileRows;
+        P.chunk = R2;
+        P.cchunk = Nb;
+        P.ldw = P.ldb;
+      } else {
+        P.chunk = R;
+        P.cchunk = C;
+        P.ldw = C;
+      }
+    }
+    o = align256(o + per * static_cast<size_t>(P.chunk) * static_cast<size_t>(P.ldw));
   }
   P.total = o;
   return true;
@@ -597,16 +623,14 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     CUtensorMap tmWs, tmWk, tmWm, tmAt128, tmBt128;
     if (!encode_map(&tmAt128, At, D, Na, P.lda, 128) || !encode_map(&tmBt128, Bt, D, Nb, P.ldb, 128))
       return UF_CUDA_ERROR;
-    if (!encode_map(&tmWs, W, wrows, Nb, P.ldw, kWgtStoreRows) || !encode_map(&tmWk, W, wrows, Nb, P.ldw, kTileRows) ||
-        !encode_map(&tmWm, W, wrows, Nb, P.ldw, 64))
+    if (!encode_map(&tmWs, W, wrows, P.cchunk, P.ldw, kWgtStoreRows) ||
+        !encode_map(&tmWk, W, wrows, P.cchunk, P.ldw, kTileRows) || !encode_map(&tmWm, W, wrows, P.cchunk, P.ldw, 64))
       return UF_CUDA_ERROR;
     WgtParams wp{};
     wp.nx = Na;
     wp.ny = Nb;
     wp.n_prefix = n;
     for (int k = 0; k < n; ++k) wp.prefix_end[k] = prefixes[k];
-    wp.n_col_tiles = static_cast<int>(cdiv(Nb, kWgtCols));
-    wp.tiles_per_split = P.wgt.tiles_per_split;
     wp.sc = sc;
     wp.shifted = shifted ? 1 : 0;
     wp.no_diag = labels && !oneset ? 1 : 0;
@@ -628,13 +652,10 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
       for (int k = 0; k < n; ++k) g->prefix_end[k] = prefixes[k];
       g->status = device_status;
     }
-    ga.kdim = Nb;
     ga.G = dA;
     ga.X = A16;
     ga.crow = F(P.o_crow_a);
     ga.crow_rows = Na;
-    gb.m_rows = Nb;
-    gb.row0 = 0;
     gb.G = dB;
     gb.X = B16;
     gb.crow = F(P.o_crow_b);
@@ -642,46 +663,71 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     // The column split of one chunk's weight pass: the whole problem's for SigLIP (its row slots
     // of loss sums are sized by it); for CLIP and ROWS, which keep no per-split state, one sized
     // for the chunk's own row blocks, so a small chunk still fills the GPU.
-    const Split wsplit = siglip ? P.wgt : plan_split(cdiv(P.chunk, kTileRows), 1, cdiv(Nb, kWgtCols));
-    wp.tiles_per_split = wsplit.tiles_per_split;
+    const Split wsplit = siglip ? P.wgt : plan_split(cdiv(P.chunk, kTileRows), 1, cdiv(P.cchunk, kWgtCols));
+    // Chunks: rows [r0, r0 + rows) of A against rows [c0, c0 + cols) of B.  dA's rows add over
+    // the column chunks and dB's over the row chunks, each in a fixed order.  SigLIP's row loss
+    // sums then add over the column chunks too (from zero; each slot has one owner thread, which
+    // adds in program order).
+    const bool col_chunks = P.cchunk < Nb;
+    if (siglip && col_chunks) {
+      UF_CHECK(cudaMemsetAsync(F(P.o_acc_a), 0, sizeof(float) * n * Na * 4 * P.wgt.splits, stream));
+      if (wp.rowsig) UF_CHECK(cudaMemsetAsync(wp.rowsig, 0, sizeof(float) * n * Na * 4 * P.wgt.splits, stream));
+    }
     for (int64_t r0 = 0; r0 < Na; r0 += P.chunk) {
       const int64_t rows = Na - r0 < P.chunk ? Na - r0 : P.chunk;
-      wp.row0 = r0;
-      wp.rows = rows;
-      {
-        ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-        UF_CHECK(launch_wgt(kind, tmA, tmB, tmWs, wp, dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), wsplit.splits),
-                            stream));
-      }
-      if (labels) {  // the labelled positives' exact weights over the negative-cell ones
-        LabelParams pq = lp;
-        pq.W = W;
-        pq.row0 = r0;
-        pq.rows = rows;
-        pq.w_rows_per_prefix = P.chunk;
-        pq.ldw = P.ldw;
-        ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
-        UF_CHECK(launch_labels(pq, stream));
-      }
-      ga.m_rows = rows;
-      ga.row0 = r0;
-      // A dA contraction of few waves (few rows: ROWS's queries, small batches) leaves SMs idle
-      // in its last wave, which one grid with the dB contraction fills (ROWS 8192 x 262144:
-      // GEMMs 14.0 -> 12.2 ms).  A long one runs alone: the two read the weights in different
-      // orders, and mixed they share L2 worse (CLIP N = 65536: 23.7 -> 24.6 ms merged).
-      const bool merge = !oneset && gemm_grid_pairs(ga) / (0.5 * g_sm_count[dev]) < kGemmMergeWaves;
-      ProfScope ps(UF_KERNEL_GEMM, oneset || merge ? 1 : 2, stream);
-      if (oneset) {  // (the B side of the one-set loss is the A side's mirror)
-        UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
-      } else {
-        gb.kdim = rows;
-        gb.b_col0 = r0;
-        gb.accumulate = r0 > 0;
-        if (merge) {
-          UF_CHECK(launch_gemm_both(tmWk, tmBt, tmBt128, ga, tmWm, tmAt, tmAt128, gb, stream));
-        } else {
+      for (int64_t c0 = 0; c0 < Nb; c0 += P.cchunk) {
+        const int64_t cols = Nb - c0 < P.cchunk ? Nb - c0 : P.cchunk;
+        wp.row0 = r0;
+        wp.rows = rows;
+        wp.col0 = c0;
+        wp.cols = cols;
+        wp.add_rows = col_chunks ? 1 : 0;
+        wp.n_col_tiles = static_cast<int>(cdiv(cols, kWgtCols));
+        const Split cs = siglip ? P.wgt : wsplit;
+        wp.tiles_per_split = cs.tiles_per_split;
+        const int splits = static_cast<int>(cdiv(wp.n_col_tiles, cs.tiles_per_split));
+        {
+          ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
+          UF_CHECK(launch_wgt(kind, tmA, tmB, tmWs, wp, dim3(static_cast<unsigned>(cdiv(rows, kTileRows)), splits),
+                              stream));
+        }
+        if (labels) {  // the labelled positives' exact weights over the negative-cell ones
+          LabelParams pq = lp;
+          pq.W = W;
+          pq.row0 = r0;
+          pq.rows = rows;
+          pq.col0 = c0;
+          pq.cols = cols;
+          pq.w_rows_per_prefix = P.chunk;
+          pq.ldw = P.ldw;
+          ProfScope ps(UF_KERNEL_BWD_TILE, 1, stream);
+          UF_CHECK(launch_labels(pq, stream));
+        }
+        ga.m_rows = rows;
+        ga.row0 = r0;
+        ga.kdim = cols;
+        ga.b_col0 = c0;
+        ga.accumulate = c0 > 0;
+        // A dA contraction of few waves (few rows: ROWS's queries, small batches) leaves SMs idle
+        // in its last wave, which one grid with the dB contraction fills (ROWS 8192 x 262144:
+        // GEMMs 14.0 -> 12.2 ms).  A long one runs alone: the two read the weights in different
+        // orders, and mixed they share L2 worse (CLIP N = 65536: 23.7 -> 24.6 ms merged).
+        const bool merge = !oneset && gemm_grid_pairs(ga) / (0.5 * g_sm_count[dev]) < kGemmMergeWaves;
+        ProfScope ps(UF_KERNEL_GEMM, oneset || merge ? 1 : 2, stream);
+        if (oneset) {  // (the B side of the one-set loss is the A side's mirror)
           UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
-          UF_CHECK(launch_gemm(tmWm, tmAt, tmAt128, gb, true, stream));
+        } else {
+          gb.m_rows = cols;
+          gb.row0 = c0;
+          gb.kdim = rows;
+          gb.b_col0 = r0;
+          gb.accumulate = r0 > 0;
+          if (merge) {
+            UF_CHECK(launch_gemm_both(tmWk, tmBt, tmBt128, ga, tmWm, tmAt, tmAt128, gb, stream));
+          } else {
+            UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
+            UF_CHECK(launch_gemm(tmWm, tmAt, tmAt128, gb, true, stream));
+          }
         }
       }
     }

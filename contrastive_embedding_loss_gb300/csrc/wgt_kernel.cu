@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < sched.steps() && ok; ++s) {
       int t, b;
       sched.at(s, t, b);
-      const int j0 = (t_begin + t) * kCols;
+      const int j0 = static_cast<int>(p.col0) + (t_begin + t) * kCols;
       const int c0 = b == 0 ? 0 : pend[b - 1] / kChunk, c1 = pend[b] / kChunk;
       for (int c = c0; c < c1; ++c, ++it) {
         const uint32_t st = it % kNS, ph = (it / kNS) & 1;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // column factors of tile t live in buffer t & 3; a tile pair's factors are fetched by
     // cp.async while the previous pair is processed
     auto prefetch_colf = [&](int t) {
-      const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
+      const int64_t j0 = p.col0 + static_cast<int64_t>(t_begin + t) * kCols;
       const uint32_t dst = colf_s + (t & 3) * kColfBytes;
       for (int e = etid; e < n * 2 * kCols; e += kEpiThreads) {
         const int k = e / (2 * kCols), f = (e / kCols) & 1, c = e % kCols;
@@ -421,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v0[32], v1[32];
           const uint32_t ta = tmem + lane_addr + a * kCols + cq * 64;
           tmem_ld32(ta, v0);
-          const int64_t j0 = static_cast<int64_t>(t_begin + t) * kCols;
-          const int64_t left = p.ny - j0;
+          const int64_t j0 = p.col0 + static_cast<int64_t>(t_begin + t) * kCols;  // first column of Y
+          const int64_t left = p.col0 + p.cols - j0;  // columns of this launch left in the tile
           const int ncols = left < kCols ? static_cast<int>(left) : kCols;
           const int64_t dtile = i0 - j0;  // uniform over the CTA: does this tile hold any positive?
           const bool check = ncols < kCols || (dtile > -kTileRows && dtile < kCols) || (il0 + kTileRows > p.rows);
@@ -479,21 +479,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           // a quarter wholly past the last column stores nothing, nor does the second CTA of
           // a pair that lies wholly past the launch's rows (its rows are not in the chunk)
-          if (lane == 0 && il0 < p.rows && j0 + cq * 64 < p.ny) {
+          if (lane == 0 && il0 < p.rows && j0 + cq * 64 < p.col0 + p.cols) {
             // the weights are written once here and read back by the GEMMs much later: keep
             // them from evicting the score operands, which every CTA re-reads
-            tma_store_2d_hint(&tm_w, stage, static_cast<int>(j0 + cq * 64),
+            tma_store_2d_hint(&tm_w, stage, static_cast<int>(j0 - p.col0 + cq * 64),
                               static_cast<int>(static_cast<int64_t>(k) * p.w_rows_per_prefix + wrow),
                               l2_evict_first);
             bulk_commit();
           }
           if (KIND == KIND_SIGLIP && p.rowacc && row_ok) {
             float* pl = p.rowacc + slot_off + static_cast<int64_t>(k) * p.nx;
-            if (t == 0) *pl = al.x;
+            if (t == 0 && !p.add_rows) *pl = al.x;
             else atomicAdd(pl, al.x);
             if (p.rowsig) {
               float* ps = p.rowsig + slot_off + static_cast<int64_t>(k) * p.nx;
-              if (t == 0) *ps = al.y;
+              if (t == 0 && !p.add_rows) *ps = al.y;
               else atomicAdd(ps, al.y);
             }
           }

@@ -22,9 +22,9 @@
  * Precision policy (UForm README, "Training is BF16"): operands bf16, products and
  * every accumulation fp32, gradients fp32.  The forward never stores the Na x Nb logits.
  * The backward does store Na x Nb data in the caller's workspace: for every prefix, the
- * bf16 per-cell weights rho_i sigma_j dL/dcos_ij (for a chunk of A's rows at a time when
- * the workspace is smaller than uf_contrastive_workspace_size), which tensor-core GEMMs
- * then contract with the embeddings.
+ * bf16 per-cell weights rho_i sigma_j dL/dcos_ij (a chunk of A's rows by B's rows at a
+ * time when the workspace is smaller than uf_contrastive_workspace_size), which tensor-core
+ * GEMMs then contract with the embeddings.
  *
  * Conventions (UForm Swift binding page, sections "Errors" and "Design": one C verb per
  * operation named <lib>_<noun>_<verb>, an enum status with a name function; section
@@ -94,16 +94,18 @@ UF_API uf_status_t uf_contrastive_init(int device);
  * Recommended bytes of device scratch for uf_contrastive_fwd_bwd with these arguments (a
  * pure function of the arguments; 0 when they are invalid).  want_grads != 0 sizes the
  * workspace for the backward as well.  The backward keeps the bf16 weights of every
- * prefix for a chunk of A's rows in the workspace (n_prefix x rows x Nb x 2 bytes); the
- * recommended size holds all rows in one chunk unless that exceeds 48 GiB of weights, in
- * which case the rows are cut into equal chunks.  Any workspace of at least
- * uf_contrastive_workspace_min() bytes works: a smaller one only means more chunks.
+ * prefix for a chunk of rows of A by rows of B in the workspace (n_prefix x R x C x 2
+ * bytes); the recommended size holds every weight in one chunk unless that exceeds 48 GiB,
+ * in which case the weights are cut into about square chunks.  Any workspace of at least
+ * uf_contrastive_workspace_min() bytes works: a smaller one only means more chunks (dA then
+ * adds over the chunks of B's rows, dB over the chunks of A's rows, in a fixed order).
  */
 UF_API size_t uf_contrastive_workspace_size(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix,
                                      int kind, int want_grads);
 
-/* The smallest workspace that uf_contrastive_fwd_bwd accepts for these arguments (one
- * 128-row chunk of weights); 0 when they are invalid. */
+/* The smallest workspace that uf_contrastive_fwd_bwd accepts for these arguments (the
+ * smallest chunk of weights: 128 rows of A by 256 rows of B, or by all of B when it has no
+ * more); 0 when they are invalid. */
 UF_API size_t uf_contrastive_workspace_min(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix,
                                     int kind, int want_grads);
 
@@ -236,9 +238,9 @@ UF_API uf_status_t uf_contrastive_oneset_fwd_bwd(const void* X, int64_t N, int D
  * passes inputs and outputs, with the same meaning and rules as uf_contrastive_fwd_bwd.
  *   - A request whose uf_contrastive_workspace_min() exceeds UF_STATIC_WORKSPACE_BYTES
  *     returns UF_WORKSPACE_TOO_SMALL before anything is enqueued (at D = 1024 with the
- *     five-prefix ladder and Na = Nb = N, with gradients: CLIP fits up to N = 12201,
- *     SigLIP up to N = 14976); inside that bound the backward cuts A's rows into as many
- *     weight chunks as the array needs.
+ *     five-prefix ladder and Na = Nb = N, with gradients: CLIP fits up to N = 14009,
+ *     SigLIP up to N = 19648); inside that bound the backward cuts the weights into as many
+ *     chunks (rows of A by rows of B) as the array needs.
  *   - The first call on a device looks up the array's device address (with that device
  *     current), and so does the first call after the device's context was replaced
  *     (cudaDeviceReset); make such a call before any stream capture.

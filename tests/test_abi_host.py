@@ -69,7 +69,7 @@ def test_workspace_size(lib):
     # chunk (5 x 65536^2 x 2 bytes = 40 GiB) within the default 48 GiB weight budget
     full = 5 * 65536 * 65536 * 2
     assert full <= ws(65536, 65536, 1024, LADDER, 0, 1) - ws(65536, 65536, 1024, LADDER, 0, 0) < full + (2 << 30)
-    # the minimum holds one 128-row chunk of weights and never exceeds the recommendation
+    # the minimum holds the smallest chunk of weights (128 x 256) and never exceeds the recommendation
     wmin = binding.uf_contrastive_workspace_min
     for N in (1, 300, 4096, 65536):
         assert 0 < wmin(N, N, 1024, LADDER, 0, 1) <= ws(N, N, 1024, LADDER, 0, 1)
@@ -79,6 +79,12 @@ def test_workspace_size(lib):
     # larger batches are cut into row chunks: the weight array stays within its budget
     big = 262144
     assert ws(big, big, 1024, LADDER, 0, 1) - ws(big, big, 1024, LADDER, 0, 0) < (48 << 30) + (1 << 30)
+    # the smallest chunk of weights is 128 rows of A by 256 rows of B: what the backward adds to
+    # the minimum is that chunk and its O(N D) arrays (the transposed operands, 2 x D x N x 2
+    # bytes = 256 MiB here), not a full row of weights (5 x 128 x N x 2 bytes per chunk row)
+    per_weight_chunk = 5 * 128 * 256 * 2
+    extra = wmin(65536, 65536, 1024, LADDER, 0, 1) - wmin(65536, 65536, 1024, LADDER, 0, 0)
+    assert 2 * 1024 * 65536 * 2 + per_weight_chunk <= extra < 2 * 1024 * 65536 * 2 + per_weight_chunk + (32 << 20)
 
 
 # Fake device addresses for calls that return before any CUDA call: 256-byte aligned, one
