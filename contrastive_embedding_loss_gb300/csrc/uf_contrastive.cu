@@ -318,7 +318,7 @@ size_t uf_contrastive_workspace_size(int64_t Na, int64_t Nb, int D, const int* p
 size_t uf_contrastive_workspace_min(int64_t Na, int64_t Nb, int D, const int* prefixes, int n_prefix, int kind,
                                     int want_grads) {
   Plan P;
-  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, want_grads != 0, 1, P)) return 0;  // one 128-row chunk
+  if (!make_plan(Na, Nb, D, prefixes, n_prefix, kind, want_grads != 0, 1, P)) return 0;  // the smallest weight chunk
   return P.total;
 }
 

@@ -76,7 +76,7 @@ def test_workspace_size(lib):
     assert wmin(65536, 65536, 1024, LADDER, 0, 1) < (3 << 29)  # vs 40 GiB of weights for one chunk
     assert wmin(256, 255, 1024, LADDER, 0, 1) == 0
     assert wmin(4096, 4096, 1024, LADDER, 0, 0) == ws(4096, 4096, 1024, LADDER, 0, 0)  # no weights forward-only
-    # larger batches are cut into row chunks: the weight array stays within its budget
+    # larger batches are cut into chunks: the weight array stays within its budget
     big = 262144
     assert ws(big, big, 1024, LADDER, 0, 1) - ws(big, big, 1024, LADDER, 0, 0) < (48 << 30) + (1 << 30)
     # the smallest chunk of weights is 128 rows of A by 256 rows of B: what the backward adds to

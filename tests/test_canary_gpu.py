@@ -2,7 +2,7 @@
 allocation filled with a canary pattern, in front of it and behind it.  After the call, each
 canary region must be unchanged.  The buffers are the workspace, the loss, the row and column
 terms, dA and dB.  The cases are CLIP, SigLIP, ROWS and CLIP with the smallest workspace (the
-backward in row chunks), at ragged sizes."""
+backward in weight chunks), at ragged sizes."""
 import numpy as np
 import pytest
 

@@ -113,7 +113,7 @@ def test_parity_small(ctx, kind, Na, Nb, D, pre, scale, bias, noise, seed):
 
 CHUNKED = [
     # kind, Na, Nb, D, prefixes, scale, bias, noise, seed: the smallest workspace, so the
-    # backward weights are cut into 128-row chunks (the dB contraction adds over chunks)
+    # backward weights are cut into 128 x 256 chunks (dA adds over column chunks, dB over row chunks)
     ("clip", 640, 640, 1024, LADDER, 1 / 0.07, 0.0, 1.0, 51),
     ("siglip", 300, 300, 1024, LADDER, 10.0, -10.0, 0.7, 52),
     ("rows", 200, 700, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 53),

@@ -55,7 +55,7 @@ def _static_call(b, kind, A, B, scale, bias, grads):
 
 
 CASES = [
-    ("clip", 4096, 4096, 1 / 0.07, 0.0, True),    # the backward weights take several row chunks
+    ("clip", 4096, 4096, 1 / 0.07, 0.0, True),    # the backward weights take several chunks
     ("siglip", 700, 700, 10.0, -10.0, True),      # ragged tiles
     ("rows", 300, 9000, 1 / 0.05, 0.0, False),    # forward only
 ]
