@@ -111,6 +111,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
     return w < 0 ? 0 : (w > kN ? kN : w);
   };
   const int nkc = static_cast<int>((p.kdim + kChunk - 1) / kChunk);  // K chunks per prefix
+  // Order of the prefixes: the widest first (it writes every column of the slices, so it starts
+  // the accumulators afresh), then the narrower ones from a start that rotates with the pair.
+  // A narrow prefix reads as many weight bytes per K chunk as a wide one for a fraction of the
+  // MMA work, so the pairs of one wave should not all reach the narrow ones together.
+  const int n_rest = n - 1 - k_first;  // prefixes after the widest
+  const int rot = n_rest > 0 ? static_cast<int>(pair_i % n_rest) : 0;
+  auto prefix_at = [&](int step) {  // step 0: the widest; then n-2 .. k_first, rotated
+    if (step == 0) return n - 1;
+    int j = step - 1 + rot;
+    if (j >= n_rest) j -= n_rest;
+    return n - 2 - j;
+  };
+  const int n_steps = n - k_first;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNA; ++s) {
@@ -148,7 +161,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
     uint64_t* emptyb = wa ? a_empty : b_empty;
     uint32_t it = 0;
     bool ok = true;
-    for (int k = n - 1; k >= k_first && ok; --k) {
+    for (int step = 0; step < n_steps && ok; ++step) {
+      const int k = prefix_at(step);
       const int h0 = width(k, 0) / 2, h1 = width(k, 1) / 2;  // B rows of each slice held by each CTA
       const int64_t wrow = static_cast<int64_t>(k) * p.w_rows_per_prefix;
       for (int c = 0; c < nkc; ++c, ++it) {
@@ -205,7 +219,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
     // it holds sum_{k' >= k} G^k' (prefix k' writes its first width(k', s) columns).
     uint32_t it = 0, pi = 0;
     bool ok = true;
-    for (int k = n - 1; k >= k_first && ok; --k, ++pi) {
+    for (int step = 0; step < n_steps && ok; ++step, ++pi) {
+      const int k = prefix_at(step);
       const int w0 = width(k, 0), w1 = width(k, 1);
       // the epilogue must have read the previous prefix's snapshot before this one adds to it
       if (pi >= 1 && !wait_bounded(&acc_empty[0], (pi - 1) & 1, abort_flag)) {
@@ -275,7 +290,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
 #pragma unroll
       for (int u = 0; u < 4; ++u) xv[u] = row_ok ? src[u] : make_uint4(0, 0, 0, 0);
     };
-    for (int k = n - 1; k >= k_first; --k, ++pi) {
+    for (int step = 0; step < n_steps; ++step, ++pi) {
+      const int k = prefix_at(step);
       if (!ok) continue;
       uint4 xcur[4], xnext[4];
       load_x(0, 0, xcur);
@@ -285,7 +301,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
         continue;
       }
       tc_fence_after();
-      const bool last = k == k_first;
+      const bool last = step == n_steps - 1;
 #pragma unroll
       for (int sl = 0; sl < 2; ++sl) {
         float run = 0.f;
