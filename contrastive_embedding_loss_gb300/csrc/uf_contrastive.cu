@@ -17,28 +17,35 @@ using namespace ufc;
 
 namespace {
 
-// CTAs the forward and weight passes aim for when they split the columns of short row ranges.
-// A constant (about four waves of one CTA per SM on a 152-SM GB300), not the device's SM
-// count: the split sets the size of the per-split partial-sum arrays, and the workspace size
-// must be a function of the problem alone (it is queried before any device is chosen).
-constexpr int kTargetCtas = 600;
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// CTA slots of one wave for the forward and weight passes: both run one CTA per SM, and a
+// GB300 has 152 SMs.  A constant, not the device's SM count: the split sets the size of the
+// per-split partial-sum arrays, and the workspace size must be a function of the problem
+// alone (it is queried before any device is chosen).
+constexpr int64_t kWaveCtas = 152;
 
 struct Split {
   int splits = 1;
   int tiles_per_split = 1;
 };
 
-Split plan_split(int64_t row_blocks, int64_t slices, int64_t tiles) {
-  Split s;
-  int64_t want = (kTargetCtas + row_blocks * slices - 1) / (row_blocks * slices);
-  if (want < 1) want = 1;
-  if (want > tiles) want = tiles;
-  s.tiles_per_split = static_cast<int>((tiles + want - 1) / want);
-  s.splits = static_cast<int>((tiles + s.tiles_per_split - 1) / s.tiles_per_split);
-  return s;
+// The column split of a pass over row_blocks x tiles score tiles (one CTA per row block and
+// split).  s splits cost about waves(s) x (tiles per CTA + 1) tile times: a CTA's set-up and
+// its last tile's epilogue, which nothing overlaps, come to about one tile.  Takes the fewest
+// splits within 2 % of the cheapest (fewer partial sums to merge).
+Split plan_split(int64_t row_blocks, int64_t tiles) {
+  const int64_t s_max = tiles < 4 * kWaveCtas ? tiles : 4 * kWaveCtas;
+  auto cost = [&](int64_t s) { return cdiv(row_blocks * s, kWaveCtas) * (cdiv(tiles, s) + 1); };
+  int64_t best = cost(1);
+  for (int64_t s = 2; s <= s_max; ++s) best = cost(s) < best ? cost(s) : best;
+  int64_t s = 1;
+  while (s < s_max && cost(s) * 100 > best * 102) ++s;
+  Split r;
+  r.tiles_per_split = static_cast<int>(cdiv(tiles, s));
+  r.splits = static_cast<int>(cdiv(tiles, r.tiles_per_split));
+  return r;
 }
-
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Default size of the backward weight array (bf16 m^k of every prefix for a chunk of
 // rows): a GB300 has 288 GB of HBM, so the N = 65536 workloads keep every row in one chunk.
@@ -91,8 +98,8 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.grads = grads;
   P.rb_a = cdiv(Na, kTileRows);
   P.ftiles = cdiv(Nb, kFwdCols);
-  P.fwd_a = plan_split(P.rb_a, 1, P.ftiles);
-  P.wgt = plan_split(P.rb_a, 1, cdiv(Nb, kWgtCols));  // rows of A against 256-row tiles of B
+  P.fwd_a = plan_split(P.rb_a, P.ftiles);
+  P.wgt = plan_split(P.rb_a, cdiv(Nb, kWgtCols));  // rows of A against 256-row tiles of B
   P.slices = static_cast<int>(cdiv(prefixes[n - 1], 256));
   P.lda = cdiv(Na, 64) * 64;
   P.ldb = cdiv(Nb, 64) * 64;
@@ -663,7 +670,7 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     // The column split of one chunk's weight pass: the whole problem's for SigLIP (its row slots
     // of loss sums are sized by it); for CLIP and ROWS, which keep no per-split state, one sized
     // for the chunk's own row blocks, so a small chunk still fills the GPU.
-    const Split wsplit = siglip ? P.wgt : plan_split(cdiv(P.chunk, kTileRows), 1, cdiv(P.cchunk, kWgtCols));
+    const Split wsplit = siglip ? P.wgt : plan_split(cdiv(P.chunk, kTileRows), cdiv(P.cchunk, kWgtCols));
     // Chunks: rows [r0, r0 + rows) of A against rows [c0, c0 + cols) of B.  dA's rows add over
     // the column chunks and dB's over the row chunks, each in a fixed order.  SigLIP's row loss
     // sums then add over the column chunks too (from zero; each slot has one owner thread, which

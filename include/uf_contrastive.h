@@ -238,8 +238,8 @@ UF_API uf_status_t uf_contrastive_oneset_fwd_bwd(const void* X, int64_t N, int D
  * passes inputs and outputs, with the same meaning and rules as uf_contrastive_fwd_bwd.
  *   - A request whose uf_contrastive_workspace_min() exceeds UF_STATIC_WORKSPACE_BYTES
  *     returns UF_WORKSPACE_TOO_SMALL before anything is enqueued (at D = 1024 with the
- *     five-prefix ladder and Na = Nb = N, with gradients: CLIP fits up to N = 14009,
- *     SigLIP up to N = 19648); inside that bound the backward cuts the weights into as many
+ *     five-prefix ladder and Na = Nb = N, with gradients: CLIP fits up to N = 14223,
+ *     SigLIP up to N = 19456); inside that bound the backward cuts the weights into as many
  *     chunks (rows of A by rows of B) as the array needs.
  *   - The first call on a device looks up the array's device address (with that device
  *     current), and so does the first call after the device's context was replaced
