@@ -173,16 +173,17 @@ cudaError_t launch_transpose(const uint16_t* X, uint16_t* Xt, int64_t rows, int 
 // ------------------------------------------------------------------------------ stats
 // Elementwise over (prefix, row) of A and then of B.  The forward sums cover the
 // negatives only (Zneg, relative to the row's shift S: tau, or the row's largest logit on
-// the max-shifted path); the positive's share is handled here in float64:
+// the max-shifted path); the positive's share is handled here:
 //   CLIP/ROWS  term = -log P_ii = softplus(log Zneg + S - s_ii),  Z = Zneg + e^{s_ii - S}
 //   SigLIP     term = ln2 * (sum of negatives' softplus in log2 units) + softplus(-x_ii)
-__device__ __forceinline__ double softplus_d(double y) { return y > 0 ? y + log1p(exp(-y)) : log1p(exp(y)); }
+// In fp32: every input is an fp32 value and each result is a few roundings from it
+// (GB300's fp64 pipe would make this pass, not its memory traffic, the cost).
+__device__ __forceinline__ float softplus_f(float y) { return y > 0.f ? y + log1pf(expf(-y)) : log1pf(expf(y)); }
 
 // Sum of the slot partials acc[sl * stride] for sl < slots, in one fixed order: eight
 // interleaved fp32 accumulators (eight loads in flight per thread) combined pairwise.  The
-// partials are positive fp32 sums themselves, so fp32 keeps the total to a few ulps (GB300's
-// fp64 pipe is too slow for a 512-term sum per column).
-__device__ __forceinline__ double sum_slots(const float* acc, int slots, int64_t stride) {
+// partials are positive fp32 sums themselves, so fp32 keeps the total to a few ulps.
+__device__ __forceinline__ float sum_slots(const float* acc, int slots, int64_t stride) {
   float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int sl = 0;
   for (; sl + 8 <= slots; sl += 8) {
@@ -190,12 +191,14 @@ __device__ __forceinline__ double sum_slots(const float* acc, int slots, int64_t
     for (int u = 0; u < 8; ++u) s[u] += acc[static_cast<int64_t>(sl + u) * stride];
   }
   for (; sl < slots; ++sl) s[0] += acc[static_cast<int64_t>(sl) * stride];
-  return static_cast<double>(((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7])));
+  return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
 __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
+  constexpr float kLn2 = 0.693147180559945309f, kLog2e = 1.442695040888963407f;
   const int n = p.n_prefix;
-  const double tau = p.sc.t(), bias = p.sc.b();
+  const float tau = p.sc.t(), bias = p.sc.b();
+  const float N = static_cast<float>(p.na);
   const int64_t total_a = static_cast<int64_t>(n) * p.na;
   const int64_t total = total_a + static_cast<int64_t>(n) * p.nb;
   const int64_t nmin = p.na < p.nb ? p.na : p.nb;
@@ -208,19 +211,19 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
     const int64_t i = ee % nrows;
     const float* acc = side_a ? p.rowacc_a : p.rowacc_b;
     const int slots = side_a ? p.slots_a : p.slots_b;
-    const double w = p.weight[k];
+    const float w = p.weight[k];
     const bool has_pos = p.diag_pos && i < nmin;
-    const double cos_ii = has_pos ? static_cast<double>(p.pos_cos[k * nmin + i]) : 0.0;
+    const float cos_ii = has_pos ? p.pos_cos[k * nmin + i] : 0.f;
     if (p.kind == KIND_SIGLIP) {
       if (!side_a) {
         p.terms_b[ee] = 0.f;
         continue;
       }
-      const double s = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
+      const float s = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
       // (log2 units)
-      const double x_ii = tau * cos_ii + bias;
-      const double lab = p.pos_term ? static_cast<double>(p.pos_term[ee]) : 0.0;  // -sum of the positives' x
-      p.terms_a[ee] = static_cast<float>(s * 0.6931471805599453 + (has_pos ? softplus_d(-x_ii) : 0.0) + lab);
+      const float x_ii = fmaf(tau, cos_ii, bias);
+      const float lab = p.pos_term ? p.pos_term[ee] : 0.f;  // -sum of the positives' x
+      p.terms_a[ee] = s * kLn2 + (has_pos ? softplus_f(-x_ii) : 0.f) + lab;
       continue;
     }
     if (p.kind == KIND_ROWS && !side_a) {
@@ -228,34 +231,33 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
       continue;
     }
     // sum over negatives of exp(s_ij - S), S the shift of this row (column)
-    const double zneg = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
+    const float zneg = sum_slots(acc + static_cast<int64_t>(k) * nrows + i, slots, static_cast<int64_t>(n) * nrows);
     const float* shift = side_a ? p.shift_a : p.shift_b;
-    const double ush = shift ? static_cast<double>(shift[ee]) : tau * 1.4426950408889634;  // log2 units
-    const double S = shift ? ush * 0.6931471805599453 : tau;
-    const double s_ii = tau * cos_ii;
-    const double e_ii = has_pos ? exp(s_ii - S) : 0.0;
-    const double z = zneg + e_ii;
+    const float ush = shift ? shift[ee] : tau * kLog2e;  // log2 units
+    const float S = shift ? ush * kLn2 : tau;
+    const float s_ii = tau * cos_ii;
+    const float e_ii = has_pos ? expf(s_ii - S) : 0.f;
+    const float z = zneg + e_ii;
     // (zneg = 0 happens on the shifted path when the positive outweighs every negative
     // beyond fp32's range: log gives -inf and softplus(-inf) = 0, the exact limit)
-    const double term = has_pos ? softplus_d(log(zneg) + S - s_ii) : log(zneg) + S;
-    const double N = static_cast<double>(p.na);
-    const double rho = side_a ? p.rinv_a[k * p.na + i] : p.rinv_b[k * p.nb + i];
-    double f;
+    const float term = has_pos ? softplus_f(logf(zneg) + S - s_ii) : logf(zneg) + S;
+    const float rho = side_a ? p.rinv_a[k * p.na + i] : p.rinv_b[k * p.nb + i];
+    float f;
     if (shift) {  // log2(rho alpha / w) - u: the weight pass multiplies by w and takes 2^(x + f)
-      const double coef = (p.kind == KIND_CLIP) ? tau / (2.0 * N) : tau / N;
-      f = log2(rho * coef / z) - ush;
+      const float coef = (p.kind == KIND_CLIP) ? tau / (2.f * N) : tau / N;
+      f = log2f(rho * coef / z) - ush;
     } else {
-      const double coef = (p.kind == KIND_CLIP) ? w * tau / (2.0 * N) : w * tau / N;
+      const float coef = (p.kind == KIND_CLIP) ? w * tau / (2.f * N) : w * tau / N;
       f = rho * coef / z;
     }
     if (side_a) {
-      p.zr[ee] = static_cast<float>(zneg);
-      p.fa[ee] = static_cast<float>(f);
-      p.terms_a[ee] = static_cast<float>(term);
+      p.zr[ee] = zneg;
+      p.fa[ee] = f;
+      p.terms_a[ee] = term;
     } else {
-      p.zc[ee] = static_cast<float>(zneg);
-      p.fb[ee] = static_cast<float>(f);
-      p.terms_b[ee] = static_cast<float>(term);
+      p.zc[ee] = zneg;
+      p.fb[ee] = f;
+      p.terms_b[ee] = term;
     }
   }
 }
@@ -299,11 +301,10 @@ cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream) {
 // weight W_ii = W'_ii + w (the positive pair, in fp32), its full row scalar
 // C_k = sum_j W_ij cos_ij, and from them the band coefficients
 //   r_c = sum_{k>=c} rho_k^2 C_k,  q_c = sum_{k>=c} rho_k sigma_k W_ii,k.
-// Then the warp streams the row: dX[d] = sum_s G_s[d] - r_c X[d] + q_c Y[d].
-__global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
+// Then the warp streams the row: dX[d] = G[d] - r_c X[d] + q_c Y[d].
+// One side's rows: warp warp_id of n_warps takes rows warp_id, warp_id + n_warps, ...
+__device__ __forceinline__ void norm_bwd_body(const NormBwdParams& p, int64_t warp_id, int64_t n_warps) {
   const int lane = threadIdx.x & 31;
-  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int n = p.n_prefix;
   const int pn = p.prefix_end[n - 1];
   const float t_sc = p.sc.t(), b_sc = p.sc.b();
@@ -374,45 +375,64 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const NormBwdParams p) {
     }
     const uint16_t* xr = p.X + i * p.d;
     const uint16_t* yr = p.Y + (diag ? i : 0) * p.d;
+    const float* gr = p.G + i * p.d;
     float* out = p.dX + i * p.d;
-    for (int c4 = lane * 4; c4 < p.d; c4 += 128) {
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c4 < pn) {
-        const int b = band_of(c4, p.prefix_end, n);
-        float r_c = 0.f, q_c = 0.f;
+    const float s = p.double_out ? 2.f : 1.f;
+    // the row in pieces of 4 x 128 columns: every load of a piece is issued before its first
+    // use, so a row waits on memory once per piece, not once per 128 columns
+    constexpr int kU = 4;
+    for (int base = 0; base < p.d; base += 128 * kU) {
+      float4 gv[kU];
+      uint2 xv[kU], yv[kU];
 #pragma unroll
-        for (int k = 0; k < kMaxPrefix; ++k)
-          if (k == b) {
-            r_c = rc[k];
-            q_c = qc[k];
-          }
-        float g[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s = 0; s < p.g_splits; ++s) {
-          const float4 v = *reinterpret_cast<const float4*>(p.G + (static_cast<int64_t>(s) * p.nx + i) * p.d + c4);
-          g[0] += v.x;
-          g[1] += v.y;
-          g[2] += v.z;
-          g[3] += v.w;
+      for (int u = 0; u < kU; ++u) {
+        const int c4 = base + 128 * u + lane * 4;
+        gv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        xv[u] = yv[u] = make_uint2(0u, 0u);
+        if (c4 < pn) {
+          gv[u] = *reinterpret_cast<const float4*>(gr + c4);
+          xv[u] = *reinterpret_cast<const uint2*>(xr + c4);
+          if (diag) yv[u] = *reinterpret_cast<const uint2*>(yr + c4);
         }
-        const uint2 xv = *reinterpret_cast<const uint2*>(xr + c4);
-        const float x[4] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y)};
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-        if (diag) {
-          const uint2 yv = *reinterpret_cast<const uint2*>(yr + c4);
-          y[0] = bf16_lo(yv.x);
-          y[1] = bf16_hi(yv.x);
-          y[2] = bf16_lo(yv.y);
-          y[3] = bf16_hi(yv.y);
-        }
-        const float s = p.double_out ? 2.f : 1.f;
-        o.x = s * (g[0] - r_c * x[0] + q_c * y[0]);
-        o.y = s * (g[1] - r_c * x[1] + q_c * y[1]);
-        o.z = s * (g[2] - r_c * x[2] + q_c * y[2]);
-        o.w = s * (g[3] - r_c * x[3] + q_c * y[3]);
       }
-      *reinterpret_cast<float4*>(out + c4) = o;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c4 = base + 128 * u + lane * 4;
+        if (c4 >= p.d) continue;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c4 < pn) {
+          const int b = band_of(c4, p.prefix_end, n);
+          float r_c = 0.f, q_c = 0.f;
+#pragma unroll
+          for (int k = 0; k < kMaxPrefix; ++k)
+            if (k == b) {
+              r_c = rc[k];
+              q_c = qc[k];
+            }
+          o.x = s * (gv[u].x - r_c * bf16_lo(xv[u].x) + q_c * bf16_lo(yv[u].x));
+          o.y = s * (gv[u].y - r_c * bf16_hi(xv[u].x) + q_c * bf16_hi(yv[u].x));
+          o.z = s * (gv[u].z - r_c * bf16_lo(xv[u].y) + q_c * bf16_lo(yv[u].y));
+          o.w = s * (gv[u].w - r_c * bf16_hi(xv[u].y) + q_c * bf16_hi(yv[u].y));
+        }
+        *reinterpret_cast<float4*>(out + c4) = o;
+      }
     }
   }
+}
+
+// Both sides in one grid: blocks [0, split) take side a's rows, the rest side b's.
+__global__ void __launch_bounds__(256) norm_bwd_kernel(const __grid_constant__ NormBwdParams pa,
+                                                       const __grid_constant__ NormBwdParams pb,
+                                                       const unsigned split, const int sides) {
+  const bool first = blockIdx.x < split;
+  const unsigned blk = first ? blockIdx.x : blockIdx.x - split;
+  const unsigned nblk = first ? split : gridDim.x - split;
+  const int64_t warp_id = (static_cast<int64_t>(blk) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(nblk) * blockDim.x) >> 5;
+  if (first)
+    norm_bwd_body(pa, warp_id, n_warps);
+  else if (sides == 2)
+    norm_bwd_body(pb, warp_id, n_warps);
 }
 
 __global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams p) {
@@ -628,10 +648,19 @@ cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_norm_bwd(const NormBwdParams& p, cudaStream_t stream) {
-  int64_t blocks = (p.nx * 32 + 255) / 256;
-  if (blocks > int64_t(16) * current_sm_count()) blocks = int64_t(16) * current_sm_count();
-  norm_bwd_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+cudaError_t launch_norm_bwd(const NormBwdParams* sides, int n_sides, cudaStream_t stream) {
+  // blocks in proportion to each side's rows, at most 16 per SM in all
+  const int64_t cap = int64_t(16) * current_sm_count();
+  int64_t blocks[2] = {0, 0};
+  int64_t total = 0;
+  for (int s = 0; s < n_sides; ++s) total += (sides[s].nx * 32 + 255) / 256;
+  for (int s = 0; s < n_sides; ++s) {
+    const int64_t want = (sides[s].nx * 32 + 255) / 256;
+    blocks[s] = total > cap ? (want * cap + total - 1) / total : want;
+    if (blocks[s] < 1) blocks[s] = 1;
+  }
+  norm_bwd_kernel<<<static_cast<unsigned>(blocks[0] + blocks[1]), 256, 0, stream>>>(
+      sides[0], sides[n_sides - 1], static_cast<unsigned>(blocks[0]), n_sides);
   return cudaGetLastError();
 }
 

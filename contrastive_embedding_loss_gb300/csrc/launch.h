@@ -168,7 +168,7 @@ struct StatsParams {
 };
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream);
 
-// dX = sum_s G[s] - r_c * X + q_c * Y (diagonal rows), 0 past the last prefix.
+// dX = G - r_c * X + q_c * Y (diagonal rows), 0 past the last prefix.
 struct NormBwdParams {
   int kind;
   int64_t nx, ny, nmin, n_total;  // n_total: batch size used by the loss normaliser
@@ -188,13 +188,13 @@ struct NormBwdParams {
   int x_is_query;          // ROWS: 1 when X holds the queries
   const float* crow;       // [slots][n][nx]
   int crow_slots;
-  const float* G;          // [splits][nx][d]
-  int g_splits;
+  const float* G;          // [nx][d]
   float* dX;               // [nx][d]
   float* csum;             // NULL or [nx]: sum over prefixes of the full row scalar C_k (logit-scale gradient)
   int double_out;          // one-set loss: write 2 dX (the row's gradient through both roles of every cell)
 };
-cudaError_t launch_norm_bwd(const NormBwdParams& p, cudaStream_t stream);
+// sides: one or two (A's rows, then B's), run as one grid.
+cudaError_t launch_norm_bwd(const NormBwdParams* sides, int n_sides, cudaStream_t stream);
 
 // Gradients of the weighted loss in the logit scale and (SigLIP) the bias, from the row
 // scalars: d_scale = (1 / scale) sum_i csum[i]  (sum_ij W_ij cos_ij = scale dL/dscale), and

@@ -747,46 +747,49 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
   }
 
   // ---- 4. projection term and diagonal correction
-  for (int side = 0; side < (oneset ? 1 : 2); ++side) {
-    const bool xa = side == 0;
-    NormBwdParams q{};
-    q.kind = kind;
-    q.nx = xa ? Na : Nb;
-    q.ny = xa ? Nb : Na;
-    q.nmin = labels ? 0 : P.nmin;  // labelled positives went through the GEMMs with their exact weights
-    q.n_total = Na;
-    q.d = D;
-    q.n_prefix = n;
-    for (int k = 0; k < n; ++k) {
-      q.prefix_end[k] = prefixes[k];
-      q.weight[k] = w[k];
+  {
+    NormBwdParams qs[2] = {};
+    const int n_sides = oneset ? 1 : 2;
+    for (int side = 0; side < n_sides; ++side) {
+      const bool xa = side == 0;
+      NormBwdParams& q = qs[side];
+      q.kind = kind;
+      q.nx = xa ? Na : Nb;
+      q.ny = xa ? Nb : Na;
+      q.nmin = labels ? 0 : P.nmin;  // labelled positives went through the GEMMs with their exact weights
+      q.n_total = Na;
+      q.d = D;
+      q.n_prefix = n;
+      for (int k = 0; k < n; ++k) {
+        q.prefix_end[k] = prefixes[k];
+        q.weight[k] = w[k];
+      }
+      q.sc = sc;
+      q.X = xa ? A16 : B16;
+      q.Y = xa ? B16 : A16;
+      q.rinv_x = F(xa ? P.o_rinv_a : P.o_rinv_b);
+      q.rinv_y = F(xa ? P.o_rinv_b : P.o_rinv_a);
+      q.pos_cos = F(P.o_pos);
+      q.z_x = F(xa ? P.o_zr : P.o_zc);
+      q.z_y = F(xa ? P.o_zc : P.o_zr);
+      q.shift_x = xa ? shift_a : shift_b;
+      q.shift_y = xa ? shift_b : shift_a;
+      if (kind == KIND_ROWS) {
+        q.x_is_query = xa ? 1 : 0;
+        q.z_x = F(P.o_zr);
+        q.z_y = F(P.o_zr);
+        q.shift_x = shift_a;
+        q.shift_y = shift_a;
+      }
+      q.crow = F(xa ? P.o_crow_a : P.o_crow_b);
+      q.crow_slots = P.slices;
+      q.csum = (xa && d_logit_scale) ? F(P.o_csum) : nullptr;
+      q.G = xa ? dA : dB;
+      q.double_out = oneset ? 1 : 0;
+      q.dX = xa ? dA : dB;
     }
-    q.sc = sc;
-    q.X = xa ? A16 : B16;
-    q.Y = xa ? B16 : A16;
-    q.rinv_x = F(xa ? P.o_rinv_a : P.o_rinv_b);
-    q.rinv_y = F(xa ? P.o_rinv_b : P.o_rinv_a);
-    q.pos_cos = F(P.o_pos);
-    q.z_x = F(xa ? P.o_zr : P.o_zc);
-    q.z_y = F(xa ? P.o_zc : P.o_zr);
-    q.shift_x = xa ? shift_a : shift_b;
-    q.shift_y = xa ? shift_b : shift_a;
-    if (kind == KIND_ROWS) {
-      q.x_is_query = xa ? 1 : 0;
-      q.z_x = F(P.o_zr);
-      q.z_y = F(P.o_zr);
-      q.shift_x = shift_a;
-      q.shift_y = shift_a;
-    }
-    q.crow = F(xa ? P.o_crow_a : P.o_crow_b);
-    q.crow_slots = P.slices;
-    q.csum = (xa && d_logit_scale) ? F(P.o_csum) : nullptr;
-    q.G = xa ? dA : dB;
-    q.g_splits = 1;
-    q.double_out = oneset ? 1 : 0;
-    q.dX = xa ? dA : dB;
     ProfScope ps(UF_KERNEL_NORM_BWD, 1, stream);
-    UF_CHECK(launch_norm_bwd(q, stream));
+    UF_CHECK(launch_norm_bwd(qs, n_sides, stream));
   }
   // ---- 5. gradients in the logit scale and the bias
   if (d_logit_scale || d_bias) {
