@@ -1,8 +1,8 @@
 // aux_kernels.cu -- the HBM-streaming steps around the fused score kernel:
 //   prep      per-prefix inverse norms of every row and the positives' cosines
 //   transpose bf16 X (rows x d) -> X^T (d x rows), the K-major operand of the gradient MMA
-//   stats     fixed-shift row/column sums -> row terms, backward factors
-//   finalize  per-prefix loss (fp64, fixed reduction order)
+//   stats     fixed-shift row/column sums -> row terms, backward factors, and the per-prefix
+//             loss (fp64, fixed reduction order, by the last block to finish)
 //   norm_bwd  dX = G - r_c X + q_c Y: the cosine's projection term and the diagonal
 //             (positive-pair) correction, band by band.
 #include <cuda_bf16.h>
@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   const int64_t n_items = p.na > p.nb ? p.na : p.nb;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int n = p.n_prefix;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.stats_done = 0u;
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && (p.sc.scale_ptr || p.sc.bias_ptr)) {
     // scalars that only the device knows are range-checked here, where the host checks its own
     const float t = p.sc.t(), b = p.sc.b();
@@ -134,10 +135,16 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
 // X^T).  The tile is kept as [column][row] in 8-row chunks whose order within a column is
 // XOR-swizzled with the column's 8-column group, so the scalar stores of a warp (one chunk of
 // 8 columns per 8 threads) and its 16-byte loads hit distinct banks.
-__global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restrict__ X, uint16_t* __restrict__ Xt,
-                                                        int64_t rows, int d, int64_t ld) {
+// One launch for up to two matrices: blockIdx.z picks one (blocks past its rows return).
+__global__ void __launch_bounds__(256) transpose_kernel(const TransposeParams p) {
   __shared__ __align__(16) uint16_t tile[64][64];
+  const bool z = blockIdx.z != 0;  // (selects, not indexes: no copy of the parameters to local memory)
+  const uint16_t* __restrict__ X = z ? p.X[1] : p.X[0];
+  uint16_t* __restrict__ Xt = z ? p.Xt[1] : p.Xt[0];
+  const int64_t rows = z ? p.rows[1] : p.rows[0], ld = z ? p.ld[1] : p.ld[0];
+  const int d = p.d;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 64;
+  if (r0 >= ld) return;  // the other matrix has more rows
   const int c0 = blockIdx.y * 64;
   const int sub = threadIdx.x & 7;  // which 8-element chunk a thread moves
   const int lr = threadIdx.x >> 3;  // 0..31
@@ -164,9 +171,11 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restri
   }
 }
 
-cudaError_t launch_transpose(const uint16_t* X, uint16_t* Xt, int64_t rows, int d, int64_t ld, cudaStream_t stream) {
-  dim3 grid(static_cast<unsigned>((rows + 63) / 64), static_cast<unsigned>(d / 64));
-  transpose_kernel<<<grid, 256, 0, stream>>>(X, Xt, rows, d, ld);
+cudaError_t launch_transpose(const TransposeParams& p, cudaStream_t stream) {
+  int64_t ld_max = 0;
+  for (int z = 0; z < p.count; ++z) ld_max = p.ld[z] > ld_max ? p.ld[z] : ld_max;
+  dim3 grid(static_cast<unsigned>((ld_max + 63) / 64), static_cast<unsigned>(p.d / 64), static_cast<unsigned>(p.count));
+  transpose_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -194,8 +203,24 @@ __device__ __forceinline__ float sum_slots(const float* acc, int slots, int64_t 
   return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
-__global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
+// Each block also adds its terms per prefix in fp64 (a fixed order within the block) and
+// stores the sums in slot blockIdx.x of p.part; the last block to finish adds the slots in
+// block order into L_k.
+__global__ void __launch_bounds__(kStatsThreads) stats_kernel(const StatsParams p) {
   constexpr float kLn2 = 0.693147180559945309f, kLog2e = 1.442695040888963407f;
+  __shared__ double red[kStatsThreads / 32][kMaxPrefix];
+  __shared__ bool last_block;
+  // a thread's own terms in fp32 (the grid holds up to kStatsBlocks x 256 threads, so a thread
+  // adds about n (Na + Nb) / 311296 terms: four at N = 65536), the block and final sums in fp64
+  float tsum[kMaxPrefix];
+#pragma unroll
+  for (int k = 0; k < kMaxPrefix; ++k) tsum[k] = 0.f;
+  // adds t to tsum[k] (k is not a compile-time index)
+  auto add_term = [&](int k, float t) {
+#pragma unroll
+    for (int kk = 0; kk < kMaxPrefix; ++kk)
+      if (kk == k) tsum[kk] += t;
+  };
   const int n = p.n_prefix;
   const float tau = p.sc.t(), bias = p.sc.b();
   const float N = static_cast<float>(p.na);
@@ -223,7 +248,9 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
       // (log2 units)
       const float x_ii = fmaf(tau, cos_ii, bias);
       const float lab = p.pos_term ? p.pos_term[ee] : 0.f;  // -sum of the positives' x
-      p.terms_a[ee] = s * kLn2 + (has_pos ? softplus_f(-x_ii) : 0.f) + lab;
+      const float term = s * kLn2 + (has_pos ? softplus_f(-x_ii) : 0.f) + lab;
+      p.terms_a[ee] = term;
+      add_term(k, term);
       continue;
     }
     if (p.kind == KIND_ROWS && !side_a) {
@@ -259,40 +286,67 @@ __global__ void __launch_bounds__(256) stats_kernel(const StatsParams p) {
       p.fb[ee] = f;
       p.terms_b[ee] = term;
     }
+    add_term(k, term);
   }
-}
-
-// One block per prefix: L_k from the row (and column) terms, fp64, fixed order.
-__global__ void __launch_bounds__(1024) finalize_kernel(const StatsParams p) {
-  __shared__ double red[32];
-  const int k = blockIdx.x;
-  double s = 0.0;
-  for (int64_t i = threadIdx.x; i < p.na; i += blockDim.x) s += p.terms_a[k * p.na + i];
-  if (p.kind == KIND_CLIP)
-    for (int64_t j = threadIdx.x; j < p.nb; j += blockDim.x) s += p.terms_b[k * p.nb + j];
+  // the block's sums: warps, then the warp sums in warp order
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    double v = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0;
+  for (int k = 0; k < kMaxPrefix; ++k) {
+    if (k >= n) break;
+    double v = static_cast<double>(tsum[k]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (threadIdx.x == 0) {
-      const double denom = (p.kind == KIND_CLIP) ? 2.0 * p.na : static_cast<double>(p.na);
-      p.loss[k] = static_cast<float>(v / denom);
-    }
+    if (lane == 0) red[wid][k] = v;
   }
+  __syncthreads();
+  if (threadIdx.x < n) {
+    double v = 0.0;
+    for (int w = 0; w < kStatsThreads / 32; ++w) v += red[w][threadIdx.x];
+    p.part[static_cast<int64_t>(blockIdx.x) * kMaxPrefix + threadIdx.x] = v;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last_block = atomicAdd(p.done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last_block) return;
+  __threadfence();
+  // thread t adds slots t, t + 256, ... (every load issued up front), then the block adds the
+  // threads' sums as above: a fixed order for a given grid
+  double v[kMaxPrefix];
+#pragma unroll
+  for (int k = 0; k < kMaxPrefix; ++k) v[k] = 0.0;
+#pragma unroll
+  for (int r = 0; r < (kStatsBlocks + kStatsThreads - 1) / kStatsThreads; ++r) {
+    const unsigned b = threadIdx.x + r * kStatsThreads;
+    if (b < gridDim.x)
+#pragma unroll
+      for (int k = 0; k < kMaxPrefix; ++k)
+        if (k < n) v[k] += __ldcg(&p.part[static_cast<int64_t>(b) * kMaxPrefix + k]);
+  }
+  __syncthreads();  // (red is reused)
+#pragma unroll
+  for (int k = 0; k < kMaxPrefix; ++k) {
+    if (k >= n) break;
+    double x = v[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) red[wid][k] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < n) {
+    double x = 0.0;
+    for (int w = 0; w < kStatsThreads / 32; ++w) x += red[w][threadIdx.x];
+    const double denom = (p.kind == KIND_CLIP) ? 2.0 * p.na : static_cast<double>(p.na);
+    p.loss[threadIdx.x] = static_cast<float>(x / denom);
+  }
+  if (threadIdx.x == 0) *p.done = 0u;  // ready for the next launch
 }
 
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(p.n_prefix) * (p.na + p.nb);
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > int64_t(8) * current_sm_count()) blocks = int64_t(8) * current_sm_count();
-  stats_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  finalize_kernel<<<p.n_prefix, 1024, 0, stream>>>(p);
+  int64_t blocks = (total + kStatsThreads - 1) / kStatsThreads;
+  if (blocks > kStatsBlocks) blocks = kStatsBlocks;
+  stats_kernel<<<static_cast<unsigned>(blocks), kStatsThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -301,8 +355,10 @@ cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream) {
 // weight W_ii = W'_ii + w (the positive pair, in fp32), its full row scalar
 // C_k = sum_j W_ij cos_ij, and from them the band coefficients
 //   r_c = sum_{k>=c} rho_k^2 C_k,  q_c = sum_{k>=c} rho_k sigma_k W_ii,k.
-// Then the warp streams the row: dX[d] = G[d] - r_c X[d] + q_c Y[d].
+// Then the warp streams the row: dX[d] = G[d] (+ G2[d]) - r_c X[d] + q_c Y[d].
 // One side's rows: warp warp_id of n_warps takes rows warp_id, warp_id + n_warps, ...
+// HAS_G2: G2 (the split gradient contraction's second part) is added below dimension g2_ld.
+template <bool HAS_G2>
 __device__ __forceinline__ void norm_bwd_body(const NormBwdParams& p, int64_t warp_id, int64_t n_warps) {
   const int lane = threadIdx.x & 31;
   const int n = p.n_prefix;
@@ -382,15 +438,18 @@ __device__ __forceinline__ void norm_bwd_body(const NormBwdParams& p, int64_t wa
     // use, so a row waits on memory once per piece, not once per 128 columns
     constexpr int kU = 4;
     for (int base = 0; base < p.d; base += 128 * kU) {
-      float4 gv[kU];
+      float4 gv[kU], g2v[HAS_G2 ? kU : 1];
       uint2 xv[kU], yv[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int c4 = base + 128 * u + lane * 4;
         gv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         xv[u] = yv[u] = make_uint2(0u, 0u);
+        if constexpr (HAS_G2) g2v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c4 < pn) {
           gv[u] = *reinterpret_cast<const float4*>(gr + c4);
+          if constexpr (HAS_G2)
+            if (c4 < p.g2_ld) g2v[u] = *reinterpret_cast<const float4*>(p.G2 + i * p.g2_ld + c4);
           xv[u] = *reinterpret_cast<const uint2*>(xr + c4);
           if (diag) yv[u] = *reinterpret_cast<const uint2*>(yr + c4);
         }
@@ -400,6 +459,8 @@ __device__ __forceinline__ void norm_bwd_body(const NormBwdParams& p, int64_t wa
         const int c4 = base + 128 * u + lane * 4;
         if (c4 >= p.d) continue;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (HAS_G2)
+          gv[u] = make_float4(gv[u].x + g2v[u].x, gv[u].y + g2v[u].y, gv[u].z + g2v[u].z, gv[u].w + g2v[u].w);
         if (c4 < pn) {
           const int b = band_of(c4, p.prefix_end, n);
           float r_c = 0.f, q_c = 0.f;
@@ -421,6 +482,7 @@ __device__ __forceinline__ void norm_bwd_body(const NormBwdParams& p, int64_t wa
 }
 
 // Both sides in one grid: blocks [0, split) take side a's rows, the rest side b's.
+template <bool HAS_G2>
 __global__ void __launch_bounds__(256) norm_bwd_kernel(const __grid_constant__ NormBwdParams pa,
                                                        const __grid_constant__ NormBwdParams pb,
                                                        const unsigned split, const int sides) {
@@ -430,9 +492,9 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const __grid_constant__ N
   const int64_t warp_id = (static_cast<int64_t>(blk) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(nblk) * blockDim.x) >> 5;
   if (first)
-    norm_bwd_body(pa, warp_id, n_warps);
+    norm_bwd_body<HAS_G2>(pa, warp_id, n_warps);
   else if (sides == 2)
-    norm_bwd_body(pb, warp_id, n_warps);
+    norm_bwd_body<HAS_G2>(pb, warp_id, n_warps);
 }
 
 __global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams p) {
@@ -659,8 +721,13 @@ cudaError_t launch_norm_bwd(const NormBwdParams* sides, int n_sides, cudaStream_
     blocks[s] = total > cap ? (want * cap + total - 1) / total : want;
     if (blocks[s] < 1) blocks[s] = 1;
   }
-  norm_bwd_kernel<<<static_cast<unsigned>(blocks[0] + blocks[1]), 256, 0, stream>>>(
-      sides[0], sides[n_sides - 1], static_cast<unsigned>(blocks[0]), n_sides);
+  const unsigned grid = static_cast<unsigned>(blocks[0] + blocks[1]);
+  if (sides[0].G2)
+    norm_bwd_kernel<true><<<grid, 256, 0, stream>>>(sides[0], sides[n_sides - 1], static_cast<unsigned>(blocks[0]),
+                                                    n_sides);
+  else
+    norm_bwd_kernel<false><<<grid, 256, 0, stream>>>(sides[0], sides[n_sides - 1], static_cast<unsigned>(blocks[0]),
+                                                     n_sides);
   return cudaGetLastError();
 }
 
@@ -671,12 +738,12 @@ cudaError_t aux_kernels_setup() {
   if ((e = cudaFuncGetAttributes(&fa, prep_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, transpose_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, stats_kernel)) != cudaSuccess) return e;
-  if ((e = cudaFuncGetAttributes(&fa, finalize_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, scale_grad_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, max_reduce_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, labels_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, wait_selftest_kernel)) != cudaSuccess) return e;
-  return cudaFuncGetAttributes(&fa, norm_bwd_kernel);
+  if ((e = cudaFuncGetAttributes(&fa, norm_bwd_kernel<true>)) != cudaSuccess) return e;
+  return cudaFuncGetAttributes(&fa, norm_bwd_kernel<false>);
 }
 
 }  // namespace ufc

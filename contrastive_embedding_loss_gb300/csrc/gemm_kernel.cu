@@ -86,44 +86,59 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
-  // Grid: [slice group][row-block pair][rank].  A CTA pair owns 256 rows of G and the two
-  // adjacent 256-dimension slices s0 = 2 grp and s1 = 2 grp + 1 (one 256-column TMEM
-  // accumulator each), so every weight tile is staged once for both.  The heavy first group
-  // (every prefix reaches slice 0) runs first, which keeps the tail of the launch short.
+  // Grid: [unit type][row-block pair][rank].  A CTA pair owns 256 rows of G and the two
+  // adjacent 256-dimension slices s0 = 2 grp and s1 = 2 grp + 1 of its group (one 256-column
+  // TMEM accumulator each), so every weight tile is staged once for both.  A unit takes the
+  // prefixes from `top` down to the narrowest one reaching s0.  With p.split_rest, a group
+  // reached by two or more prefixes runs as two units: the widest prefix alone (into G) and
+  // the others (into G2, which the norm backward adds); those "rest" units come first in the
+  // launch, the heavier ones.  Otherwise one unit per group, the heavy first group first.
   int n_slices = 0;
 #pragma unroll
   for (int kk = 0; kk < kMaxPrefix; ++kk)
     if (kk < p.n_prefix) n_slices = (p.prefix_end[kk] + kN - 1) / kN;
+  const int n = p.n_prefix;
+  // groups 0 .. n_rest_groups - 1 are reached by two or more prefixes (the second widest's end
+  // lies past their first dimension)
+  const int n_rest_groups = (p.split_rest && n >= 2) ? (prefix_end_of(p, n - 2) + 2 * kN - 1) / (2 * kN) : 0;
   const int64_t pairs = (p.m_rows + 2 * kTileRows - 1) / (2 * kTileRows);
   const int64_t cta = vblock >> 1;
-  const int grp = static_cast<int>(cta / pairs);
+  const int type = static_cast<int>(cta / pairs);
+  const bool rest_unit = type < n_rest_groups;
+  const int grp = rest_unit ? type : type - n_rest_groups;
   const int64_t pair_i = cta % pairs;
   const int64_t m0 = (pair_i * 2 + rank) * kTileRows;  // first row of G in this launch
   const int d0 = grp * 2 * kN;                          // first dimension of slice s0
-  const int n = p.n_prefix;
-  int k_first = 0;  // prefixes k_first .. n-1 reach slice s0 (and so this CTA)
+  int k_first = 0;  // prefixes k_first .. n-1 reach slice s0
 #pragma unroll
   for (int k = 0; k < kMaxPrefix; ++k)
     if (k < n && p.prefix_end[k] <= d0) k_first = k + 1;
+  // this unit's prefixes: top, then top-1 .. k_first (none after top for a split group's
+  // widest-prefix unit)
+  const int top = rest_unit ? n - 2 : n - 1;
+  const bool split_group = grp < n_rest_groups;
+  const int n_steps = (!rest_unit && split_group) ? 1 : top + 1 - k_first;
+  float* const gout = rest_unit ? p.G2 : p.G;
+  const int64_t gld = rest_unit ? p.g2_ld : p.d;
   // prefix k's width within slice s (0: it does not reach the slice)
   auto width = [&](int k, int sl) {
     const int w = prefix_end_of(p, k) - (d0 + sl * kN);
     return w < 0 ? 0 : (w > kN ? kN : w);
   };
   const int nkc = static_cast<int>((p.kdim + kChunk - 1) / kChunk);  // K chunks per prefix
-  // Order of the prefixes: the widest first (it writes every column of the slices, so it starts
-  // the accumulators afresh), then the narrower ones from a start that rotates with the pair.
-  // A narrow prefix reads as many weight bytes per K chunk as a wide one for a fraction of the
-  // MMA work, so the pairs of one wave should not all reach the narrow ones together.
-  const int n_rest = n - 1 - k_first;  // prefixes after the widest
-  const int rot = n_rest > 0 ? static_cast<int>(pair_i % n_rest) : 0;
-  auto prefix_at = [&](int step) {  // step 0: the widest; then n-2 .. k_first, rotated
-    if (step == 0) return n - 1;
+  // Order of the prefixes: the unit's widest first (it writes every column the unit writes, so
+  // it starts the accumulators afresh), then the narrower ones from a start that rotates with
+  // the pair.  A narrow prefix reads as many weight bytes per K chunk as a wide one for a
+  // fraction of the MMA work, so the pairs of one wave should not all reach the narrow ones
+  // together.
+  const int n_after = n_steps - 1;  // prefixes after the unit's widest
+  const int rot = n_after > 0 ? static_cast<int>(pair_i % n_after) : 0;
+  auto prefix_at = [&](int step) {  // step 0: top; then top-1 .. k_first, rotated
+    if (step == 0) return top;
     int j = step - 1 + rot;
-    if (j >= n_rest) j -= n_rest;
-    return n - 2 - j;
+    if (j >= n_after) j -= n_after;
+    return top - 1 - j;
   };
-  const int n_steps = n - k_first;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNA; ++s) {
@@ -269,9 +284,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
     const int64_t g = p.row0 + gl;          // row of G / X / crow
     const bool row_ok = gl < p.m_rows;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    const int wmax[2] = {width(n - 1, 0), width(n - 1, 1)};  // columns of each slice with data
+    const int wmax[2] = {width(top, 0), width(top, 1)};  // columns of each slice with data
     // prefixes that do not reach a slice contribute nothing to its slot
-    if (row_ok && !p.accumulate)
+    if (row_ok && !p.accumulate && !rest_unit)
       for (int sl = 0; sl < 2; ++sl)
         if (2 * grp + sl < n_slices)
           for (int k = 0; k < n; ++k)
@@ -305,7 +320,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
 #pragma unroll
       for (int sl = 0; sl < 2; ++sl) {
         float run = 0.f;
-        float* grow = p.G + g * p.d + d0 + sl * kN;
+        float* grow = gout + g * gld + d0 + sl * kN;
 #pragma unroll
         for (int b = 0; b < kN / 64; ++b) curd[sl][b] = 0.f;
         for (int c = 0; c < wmax[sl]; c += 32) {
@@ -408,13 +423,17 @@ static cudaError_t setup_one() {
   return cudaFuncSetAttribute(gemm_kernel<AMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-// CTAs of one contraction: [slice group (two slices)][row-block pair][rank]
+// CTAs of one contraction: [unit type][row-block pair][rank]; the unit types are the slice
+// groups (two slices each) and, with split_rest, one more per group that two or more prefixes
+// reach (the same count as in gemm_body)
 unsigned grid_of(const GemmParams& p) {
-  const int pn = p.prefix_end[p.n_prefix - 1];
+  const int n = p.n_prefix;
+  const int pn = p.prefix_end[n - 1];
   const int64_t blocks = (p.m_rows + kTileRows - 1) / kTileRows;
   const int64_t n_slices = (pn + kN - 1) / kN;
   const int64_t groups = (n_slices + 1) / 2;
-  return static_cast<unsigned>(groups * ((blocks + 1) / 2) * 2);
+  const int64_t rest = (p.split_rest && n >= 2) ? (p.prefix_end[n - 2] + 2 * kN - 1) / (2 * kN) : 0;
+  return static_cast<unsigned>((groups + rest) * ((blocks + 1) / 2) * 2);
 }
 
 }  // namespace gemm

@@ -100,6 +100,9 @@ struct GemmParams {
   int prefix_end[kMaxPrefix];
   int accumulate;
   float* G;
+  int split_rest;                 // 1: the prefixes below the widest run as their own units, into G2
+  float* G2;                      // [m_rows][g2_ld] (split_rest): their part of G, dimensions < g2_ld
+  int64_t g2_ld;                  // the second-widest prefix's end
   const uint16_t* X;              // bf16 rows of the side G belongs to
   float* crow;                    // [slice][n][crow_rows]
   int64_t crow_rows;
@@ -133,11 +136,19 @@ struct PrepParams {
   float* rinv_a;
   float* rinv_b;
   float* pos_cos;
+  unsigned* stats_done;    // the statistics pass's block counter, zeroed here
 };
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
 
-// X (rows x d, bf16) -> Xt (d x ld, bf16): Xt[c][r] = X[r][c].
-cudaError_t launch_transpose(const uint16_t* X, uint16_t* Xt, int64_t rows, int d, int64_t ld, cudaStream_t stream);
+// X[z] (rows[z] x d, bf16) -> Xt[z] (d x ld[z], bf16): Xt[c][r] = X[r][c] for r < rows, 0 up to
+// ld (rows rounded up to 64), for z < count (one or two matrices, one launch).
+struct TransposeParams {
+  const uint16_t* X[2];
+  uint16_t* Xt[2];
+  int64_t rows[2], ld[2];
+  int d, count;
+};
+cudaError_t launch_transpose(const TransposeParams& p, cudaStream_t stream);
 
 // Loss statistics after the forward (CLIP / ROWS) or the A-side backward (SigLIP).
 struct StatsParams {
@@ -165,10 +176,17 @@ struct StatsParams {
   float* terms_a;          // [n][na]  row terms
   float* terms_b;          // [n][nb]  column terms (CLIP; 0 otherwise)
   float* loss;             // [n]
+  double* part;            // [kStatsBlocks][kMaxPrefix] per-block sums of the terms
+  unsigned* done;          // blocks finished; 0 before the launch (the prep pass zeroes it), 0 after
 };
+// The statistics pass: kStatsThreads threads a block, at most kStatsBlocks blocks (a constant,
+// so that the workspace does not depend on the device).
+constexpr int kStatsThreads = 256;
+constexpr int kStatsBlocks = 1216;
+static_assert(kStatsThreads / 32 >= kMaxPrefix, "the statistics pass sums one prefix per warp");
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream);
 
-// dX = G - r_c * X + q_c * Y (diagonal rows), 0 past the last prefix.
+// dX = G (+ G2) - r_c * X + q_c * Y (diagonal rows), 0 past the last prefix.
 struct NormBwdParams {
   int kind;
   int64_t nx, ny, nmin, n_total;  // n_total: batch size used by the loss normaliser
@@ -189,6 +207,8 @@ struct NormBwdParams {
   const float* crow;       // [slots][n][nx]
   int crow_slots;
   const float* G;          // [nx][d]
+  const float* G2;         // NULL, or [nx][g2_ld]: added to G below dimension g2_ld
+  int64_t g2_ld;
   float* dX;               // [nx][d]
   float* csum;             // NULL or [nx]: sum over prefixes of the full row scalar C_k (logit-scale gradient)
   int double_out;          // one-set loss: write 2 dX (the row's gradient through both roles of every cell)

@@ -65,10 +65,12 @@ struct Plan {
   int64_t ldw = 0;                   // row stride of the weight array (elements)
   int64_t chunk = 0;                 // rows of A per weight chunk (multiple of 128)
   int64_t cchunk = 0;                // rows of B (weight columns) per weight chunk
+  bool gsplit = false;               // gradient contractions split below the widest prefix
+  int64_t g2_ld = 0;                 // columns of their G2 arrays
   size_t fixed = 0;                  // bytes of everything but the weight array
   // offsets
   size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
-      o_terms_b, o_loss, o_at, o_bt, o_csum, o_sig, o_sh_a, o_sh_b, o_lab, o_lcount, o_w, total;
+      o_terms_b, o_spart, o_done, o_g2a, o_g2b, o_at, o_bt, o_csum, o_sig, o_sh_a, o_sh_b, o_lab, o_lcount, o_w, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -128,7 +130,8 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   P.o_crow_b = take(grads ? f * n * Nb * P.slices : 0);
   P.o_terms_a = take(f * n * Na);
   P.o_terms_b = take(f * n * Nb);
-  P.o_loss = take(f * kMaxPrefix);
+  P.o_spart = take(sizeof(double) * kMaxPrefix * kStatsBlocks);  // statistics pass: per-block loss sums
+  P.o_done = take(sizeof(unsigned));
   P.o_at = take(grads ? sizeof(uint16_t) * D * P.lda : 0);
   P.o_bt = take(grads ? sizeof(uint16_t) * D * P.ldb : 0);
   P.o_csum = take(grads ? f * Na : 0);  // per-row sums of the row scalars (logit-scale gradient)
@@ -140,6 +143,18 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
   // SigLIP with a label matrix: the positives' share of the row terms, positives per row
   P.o_lab = take(kind == KIND_SIGLIP ? f * n * Na : 0);
   P.o_lcount = take(kind == KIND_SIGLIP ? f * Na : 0);
+  // A gradient contraction of at most one wave of CTA pairs (both sides together) is bound by
+  // its heaviest unit, the slice group that every prefix reaches; there the prefixes below the
+  // widest run as units of their own, which write their part of G to G2 (CLIP N = 4096: GEMMs
+  // 0.234 -> 0.187 ms).  Larger grids balance over their waves without it.
+  P.g2_ld = n >= 2 ? prefixes[n - 2] : 0;
+  {
+    const int64_t groups = cdiv(cdiv(prefixes[n - 1], 256), 2);
+    const int64_t pairs = groups * (cdiv(Na, 2 * kTileRows) + cdiv(Nb, 2 * kTileRows));
+    P.gsplit = grads && n >= 2 && pairs <= kWaveCtas / 2;
+  }
+  P.o_g2a = take(P.gsplit ? f * Na * P.g2_ld : 0);
+  P.o_g2b = take(P.gsplit ? f * Nb * P.g2_ld : 0);
   P.fixed = o;
   P.o_w = o;
   P.chunk = 0;
@@ -491,17 +506,28 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
   pp.rinv_a = F(P.o_rinv_a);
   pp.rinv_b = F(P.o_rinv_b);
   pp.pos_cos = F(P.o_pos);
+  pp.stats_done = reinterpret_cast<unsigned*>(ws + P.o_done);
   {
     ProfScope ps(UF_KERNEL_PREP, 1, stream);
     UF_CHECK(launch_prep(pp, stream));
   }
   if (grads) {
+    TransposeParams tp{};
+    tp.d = D;
     if (!oneset) {  // (one set: A^T is B^T)
-      ProfScope ps(UF_KERNEL_TRANSPOSE, 1, stream);
-      UF_CHECK(launch_transpose(A16, At, Na, D, P.lda, stream));
+      tp.X[tp.count] = A16;
+      tp.Xt[tp.count] = At;
+      tp.rows[tp.count] = Na;
+      tp.ld[tp.count] = P.lda;
+      ++tp.count;
     }
+    tp.X[tp.count] = B16;
+    tp.Xt[tp.count] = Bt;
+    tp.rows[tp.count] = Nb;
+    tp.ld[tp.count] = P.ldb;
+    ++tp.count;
     ProfScope ps(UF_KERNEL_TRANSPOSE, 1, stream);
-    UF_CHECK(launch_transpose(B16, Bt, Nb, D, P.ldb, stream));
+    UF_CHECK(launch_transpose(tp, stream));
   }
 
   // SigLIP with a label matrix: the positives' loss terms and counts (the dense passes score
@@ -557,6 +583,8 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
   sp.terms_a = terms_a;
   sp.terms_b = terms_b;
   sp.loss = loss_per_prefix;
+  sp.part = reinterpret_cast<double*>(ws + P.o_spart);
+  sp.done = reinterpret_cast<unsigned*>(ws + P.o_done);
 
   // ---- 2. forward statistics (all kinds without gradients; CLIP/ROWS with them): one pass
   // over the grid gives every row sum and, for CLIP, every column sum (the max-shifted path
@@ -611,7 +639,7 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
       sp.rowacc_b = fp.colacc;
       sp.slots_b = static_cast<int>(P.rb_a);
     }
-    ProfScope ps(UF_KERNEL_STATS, 2, stream);
+    ProfScope ps(UF_KERNEL_STATS, 1, stream);
     UF_CHECK(launch_stats(sp, stream));
   }
   if (!grads) {
@@ -667,6 +695,12 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     gb.X = B16;
     gb.crow = F(P.o_crow_b);
     gb.crow_rows = Nb;
+    if (P.gsplit) {
+      ga.split_rest = gb.split_rest = 1;
+      ga.G2 = F(P.o_g2a);
+      gb.G2 = F(P.o_g2b);
+      ga.g2_ld = gb.g2_ld = P.g2_ld;
+    }
     // The column split of one chunk's weight pass: the whole problem's for SigLIP (its row slots
     // of loss sums are sized by it); for CLIP and ROWS, which keep no per-split state, one sized
     // for the chunk's own row blocks, so a small chunk still fills the GPU.
@@ -741,7 +775,7 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     if (siglip) {
       sp.rowacc_a = F(P.o_acc_a);
       sp.slots_a = 4 * P.wgt.splits;
-      ProfScope ps(UF_KERNEL_STATS, 2, stream);
+      ProfScope ps(UF_KERNEL_STATS, 1, stream);
       UF_CHECK(launch_stats(sp, stream));
     }
   }
@@ -785,6 +819,10 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
       q.crow_slots = P.slices;
       q.csum = (xa && d_logit_scale) ? F(P.o_csum) : nullptr;
       q.G = xa ? dA : dB;
+      if (P.gsplit) {
+        q.G2 = F(xa ? P.o_g2a : P.o_g2b);
+        q.g2_ld = P.g2_ld;
+      }
       q.double_out = oneset ? 1 : 0;
       q.dX = xa ? dA : dB;
     }

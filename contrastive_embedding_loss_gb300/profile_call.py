@@ -3,9 +3,9 @@
   python -m contrastive_embedding_loss_gb300.profile_call --kind clip --n 32768 --warmup 1 --calls 1
 
 Each call is one full uf_contrastive_fwd_bwd (forward, loss, backward).  The kernel
-launch order per CLIP call (tau <= 40, one weight chunk) is: prep, transpose x2, fwd_kernel,
-stats, finalize, wgt_kernel, gemm_kernel (dA, K-major weights), gemm_kernel (dB, MN-major
-weights), norm_bwd x2.
+launch order per CLIP call (tau <= 40, one weight chunk) is: prep, transpose (both sides),
+fwd_kernel, stats, wgt_kernel, gemm_kernel (dA, K-major weights), gemm_kernel (dB, MN-major
+weights) or, below four waves of CTA pairs, gemm_kernel_both (both), norm_bwd (both sides).
 """
 import argparse
 

@@ -238,7 +238,7 @@ UF_API uf_status_t uf_contrastive_oneset_fwd_bwd(const void* X, int64_t N, int D
  * passes inputs and outputs, with the same meaning and rules as uf_contrastive_fwd_bwd.
  *   - A request whose uf_contrastive_workspace_min() exceeds UF_STATIC_WORKSPACE_BYTES
  *     returns UF_WORKSPACE_TOO_SMALL before anything is enqueued (at D = 1024 with the
- *     five-prefix ladder and Na = Nb = N, with gradients: CLIP fits up to N = 14223,
+ *     five-prefix ladder and Na = Nb = N, with gradients: CLIP fits up to N = 14208,
  *     SigLIP up to N = 19456); inside that bound the backward cuts the weights into as many
  *     chunks (rows of A by rows of B) as the array needs.
  *   - The first call on a device looks up the array's device address (with that device
@@ -278,9 +278,9 @@ UF_API uf_status_t uf_contrastive_selftest_wait(int* device_status, int limit_ms
  */
 typedef enum uf_kernel_group {
   UF_KERNEL_PREP = 0,       /* per-prefix inverse norms and positives' cosines (1 launch) */
-  UF_KERNEL_TRANSPOSE = 1,  /* bf16 transposes for the gradient operand (1 launch each) */
+  UF_KERNEL_TRANSPOSE = 1,  /* bf16 transposes for the gradient operand (1 launch) */
   UF_KERNEL_FWD_TILE = 2,   /* fused tcgen05 forward: row sums of every prefix */
-  UF_KERNEL_STATS = 3,      /* loss statistics and per-prefix loss (2 launches) */
+  UF_KERNEL_STATS = 3,      /* loss statistics and per-prefix loss (1 launch; 2 on the max-shifted path) */
   UF_KERNEL_BWD_TILE = 4,   /* tcgen05 backward weight pass: score recompute, bf16 weights to HBM */
   UF_KERNEL_NORM_BWD = 5,   /* projection term and positive-pair correction */
   UF_KERNEL_GEMM = 6,       /* tcgen05 gradient contraction over the bf16 weights */
