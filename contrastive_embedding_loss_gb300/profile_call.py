@@ -21,6 +21,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--calls", type=int, default=1)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--weights-gib", type=float, default=0.0,
+                    help="cap the backward weight array at this many GiB (chunked weights; 0: the default)")
     a = ap.parse_args()
 
     import torch
@@ -38,8 +40,11 @@ def main():
     A = torch.from_numpy(A16.view(np.int16)).view(torch.bfloat16).to(dev)
     B = torch.from_numpy(B16.view(np.int16)).view(torch.bfloat16).to(dev)
     assert binding.uf_contrastive_init(0) == binding.UF_OK
-    ws = torch.empty(binding.uf_contrastive_workspace_size(A.shape[0], B.shape[0], a.d, pre, binding.KINDS[a.kind], 1),
-                     dtype=torch.uint8, device=dev)
+    args = (A.shape[0], B.shape[0], a.d, pre, binding.KINDS[a.kind], 1)
+    nbytes = binding.uf_contrastive_workspace_size(*args)
+    if a.weights_gib > 0:
+        nbytes = min(nbytes, binding.uf_contrastive_workspace_min(*args) + int(a.weights_gib * (1 << 30)))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     out = None
     for _ in range(a.warmup + a.calls):
         out = binding.contrastive_fwd_bwd(A, B, a.kind, pre, scale, bias, workspace=ws)
