@@ -338,9 +338,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_begin = split * p.tiles_per_split;
   const int T = min(p.n_col_tiles, t_begin + p.tiles_per_split) - t_begin;
   const Schedule sched{T, n};
-  int pend[kMaxPrefix];
+  // prefix k's end (selects over the parameter: a runtime index into a local copy would put
+  // the copy in local memory); p_{-1} = 0
+  auto pend = [&](int k) {
+    int e = 0;
 #pragma unroll
-  for (int k = 0; k < kMaxPrefix; ++k) pend[k] = p.prefix_end[k];
+    for (int kk = 0; kk < kMaxPrefix; ++kk)
+      if (kk == k) e = p.prefix_end[kk];
+    return e;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
@@ -376,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < sched.steps() && ok; ++s, si.next()) {
       const int t = si.t(), b = si.b;
       const int j0 = (t_begin + t) * kCols;
-      const int c0 = b == 0 ? 0 : pend[b - 1] / kChunk, c1 = pend[b] / kChunk;
+      const int c0 = pend(b - 1) / kChunk, c1 = pend(b) / kChunk;
       for (int c = c0; c < c1; ++c, ++it) {
         const uint32_t st = it % kNS, ph = (it / kNS) & 1;
         if (!wait_bounded(&s_empty[st], ph ^ 1, abort_flag)) {
@@ -397,20 +403,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- MMA issuer
     const uint32_t idesc = idesc_bf16_f32(kTileRows, kCols);
     uint32_t it = 0;
-    uint32_t uses[2] = {0, 0};
+    uint32_t uses0 = 0, uses1 = 0;  // uses of each accumulator (scalars, as in the epilogue)
     bool ok = true;
     SchedIter si(T, n);
     for (int s = 0; s < sched.steps() && ok; ++s, si.next()) {
       const int t = si.t(), b = si.b;
       const int a = t & 1;
-      if (uses[a] > 0 && !wait_bounded(&acc_empty[a], (uses[a] - 1) & 1, abort_flag)) {
+      const uint32_t ua = a ? uses1 : uses0;
+      if (ua > 0 && !wait_bounded(&acc_empty[a], (ua - 1) & 1, abort_flag)) {
         fail(p, abort_flag);
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d = tmem + a * kCols;
-      const int c0 = b == 0 ? 0 : pend[b - 1] / kChunk, c1 = pend[b] / kChunk;
+      const int c0 = pend(b - 1) / kChunk, c1 = pend(b) / kChunk;
       for (int c = c0; c < c1; ++c, ++it) {
         const uint32_t st = it % kNS, ph = (it / kNS) & 1;
         if (!wait_bounded(&s_full[st], ph, abort_flag)) {
@@ -427,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&s_empty[st]);
       }
       if (ok) umma_commit(&acc_full[a]);
-      ++uses[a];
+      if (a) ++uses1; else ++uses0;
     }
     umma_commit(drain);
     mbar_wait(drain, 0, kWaitLimitNs);

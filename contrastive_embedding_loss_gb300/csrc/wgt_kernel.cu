@@ -286,13 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- MMA issuer (leader)
     const uint32_t idesc = idesc_bf16_f32(2 * kTileRows, kCols);
     uint32_t it = 0;
-    uint32_t uses[2] = {0, 0};
+    uint32_t uses0 = 0, uses1 = 0;  // uses of each accumulator (scalars: a runtime index would put them in local memory)
     bool ok = true;
     for (int s = 0; s < sched.steps() && ok; ++s) {
       int t, b;
       sched.at(s, t, b);
       const int a = t & 1;
-      if (uses[a] > 0 && !wait_bounded(&acc_empty[a], (uses[a] - 1) & 1, abort_flag)) {
+      const uint32_t ua = a ? uses1 : uses0;
+      if (ua > 0 && !wait_bounded(&acc_empty[a], (ua - 1) & 1, abort_flag)) {
         fail(p, abort_flag);
         ok = false;
         break;
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit_pair(&s_empty[st]);  // releases the stage in both CTAs
       }
       if (ok) umma_commit_pair(&acc_full[a]);
-      ++uses[a];
+      if (a) ++uses1; else ++uses0;
     }
     umma_commit_pair(drain);
     mbar_wait(drain, 0, kWaitLimitNs);
