@@ -309,7 +309,6 @@ def main():
         torch.distributed.barrier()
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
-    binding.uf_contrastive_profile(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ev0.record(stream)
@@ -318,6 +317,14 @@ def main():
     ev1.record(stream)
     torch.cuda.synchronize()
     ms_local = ev0.elapsed_time(ev1)
+    # the same K steps again with the library's per-kernel CUDA events on (two event records
+    # around each kernel group, on the call's stream): the kernel split and the dominant
+    # kernel's live launch time; kept out of the timed steps above, whose time they would add to
+    binding.uf_contrastive_profile(True)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        step(A_d.data_ptr(), B_d.data_ptr())
+    torch.cuda.synchronize()
     clk = clocks.stop()
     prof = {binding.KERNEL_GROUPS[g]: binding.uf_contrastive_profile_read(g) for g in range(len(binding.KERNEL_GROUPS))}
     binding.uf_contrastive_profile(False)
@@ -450,6 +457,8 @@ def main():
         "frac_credited_of_bf16_peak": cflops / (ms_step / 1e3) / 1e12 / peak_tf,
         "roofline": roof,
         "kernels_ms_per_step": {g: prof[g][0] / args.steps for g in prof},
+        "kernels_how": "a second pass of the same steps with per-kernel CUDA events on the call's stream "
+                       "(the timed steps run without them)",
         "gpu_launches": int(sum(prof[g][2] for g in prof)),
         "e2e": {"value": e2e_value, "unit": "pairs/s", "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
                 "d2h_bytes_per_step": int(loss_h.numel() * 4), "ms_per_step": ms_e2e / args.steps,

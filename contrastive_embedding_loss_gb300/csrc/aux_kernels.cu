@@ -37,6 +37,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // registers), otherwise the one row.  A lane reads every eighth 16-byte chunk of the row,
 // four chunks in flight, and the eight lanes of an item meet in a 3-stage shuffle reduce.
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
+  griddep_enter();
   const int lane = threadIdx.x & 31;
   const int sub = lane & 7;  // the lane within its item's group of eight
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -125,8 +126,7 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
   const int64_t items = p.na > p.nb ? p.na : p.nb;
   int64_t blocks = (items * 8 + 255) / 256;  // eight lanes per item
   if (blocks > int64_t(16) * current_sm_count()) blocks = int64_t(16) * current_sm_count();
-  prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(prep_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, p);
 }
 
 // ------------------------------------------------------------------------------ transpose
@@ -137,6 +137,7 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
 // 8 columns per 8 threads) and its 16-byte loads hit distinct banks.
 // One launch for up to two matrices: blockIdx.z picks one (blocks past its rows return).
 __global__ void __launch_bounds__(256) transpose_kernel(const TransposeParams p) {
+  griddep_enter();
   __shared__ __align__(16) uint16_t tile[64][64];
   const bool z = blockIdx.z != 0;  // (selects, not indexes: no copy of the parameters to local memory)
   const uint16_t* __restrict__ X = z ? p.X[1] : p.X[0];
@@ -175,8 +176,7 @@ cudaError_t launch_transpose(const TransposeParams& p, cudaStream_t stream) {
   int64_t ld_max = 0;
   for (int z = 0; z < p.count; ++z) ld_max = p.ld[z] > ld_max ? p.ld[z] : ld_max;
   dim3 grid(static_cast<unsigned>((ld_max + 63) / 64), static_cast<unsigned>(p.d / 64), static_cast<unsigned>(p.count));
-  transpose_kernel<<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(transpose_kernel, grid, dim3(256), 0, stream, 1, p);
 }
 
 // ------------------------------------------------------------------------------ stats
@@ -207,6 +207,7 @@ __device__ __forceinline__ float sum_slots(const float* acc, int slots, int64_t 
 // stores the sums in slot blockIdx.x of p.part; the last block to finish adds the slots in
 // block order into L_k.
 __global__ void __launch_bounds__(kStatsThreads) stats_kernel(const StatsParams p) {
+  griddep_enter();
   constexpr float kLn2 = 0.693147180559945309f, kLog2e = 1.442695040888963407f;
   __shared__ double red[kStatsThreads / 32][kMaxPrefix];
   __shared__ bool last_block;
@@ -346,8 +347,7 @@ cudaError_t launch_stats(const StatsParams& p, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(p.n_prefix) * (p.na + p.nb);
   int64_t blocks = (total + kStatsThreads - 1) / kStatsThreads;
   if (blocks > kStatsBlocks) blocks = kStatsBlocks;
-  stats_kernel<<<static_cast<unsigned>(blocks), kStatsThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(stats_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kStatsThreads), 0, stream, 1, p);
 }
 
 // ------------------------------------------------------------------------------ norm_bwd
@@ -486,6 +486,7 @@ template <bool HAS_G2>
 __global__ void __launch_bounds__(256) norm_bwd_kernel(const __grid_constant__ NormBwdParams pa,
                                                        const __grid_constant__ NormBwdParams pb,
                                                        const unsigned split, const int sides) {
+  griddep_enter();
   const bool first = blockIdx.x < split;
   const unsigned blk = first ? blockIdx.x : blockIdx.x - split;
   const unsigned nblk = first ? split : gridDim.x - split;
@@ -498,6 +499,7 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(const __grid_constant__ N
 }
 
 __global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams p) {
+  griddep_enter();
   __shared__ double red[2][32];
   const int n = p.n_prefix;
   const float scale = p.sc.t(), bias = p.sc.b();
@@ -551,6 +553,7 @@ __global__ void __launch_bounds__(1024) scale_grad_kernel(const ScaleGradParams 
 
 // ------------------------------------------------------------------------------ max_reduce
 __global__ void __launch_bounds__(256) max_reduce_kernel(const MaxReduceParams p) {
+  griddep_enter();
   const int n = p.n_prefix;
   const int64_t total_a = static_cast<int64_t>(n) * p.na;
   const int64_t total = total_a + (p.v ? static_cast<int64_t>(n) * p.nb : 0);
@@ -573,8 +576,7 @@ cudaError_t launch_max_reduce(const MaxReduceParams& p, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(p.n_prefix) * (p.na + (p.v ? p.nb : 0));
   int64_t blocks = (total + 255) / 256;
   if (blocks > int64_t(8) * current_sm_count()) blocks = int64_t(8) * current_sm_count();
-  max_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(max_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, p);
 }
 
 // ------------------------------------------------------------------------------ labels
@@ -598,6 +600,7 @@ __device__ __forceinline__ bool has_mirror(const LabelParams& p, int j, int i, i
 }
 
 __global__ void __launch_bounds__(256) labels_kernel(const LabelParams p) {
+  griddep_enter();
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -678,8 +681,7 @@ cudaError_t launch_labels(const LabelParams& p, cudaStream_t stream) {
   int64_t blocks = (rows * 32 + 255) / 256;
   if (blocks > int64_t(16) * current_sm_count()) blocks = int64_t(16) * current_sm_count();
   if (blocks < 1) blocks = 1;
-  labels_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(labels_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, p);
 }
 
 // ------------------------------------------------------------------------------ wait self-test
@@ -706,8 +708,7 @@ cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st
 }
 
 cudaError_t launch_scale_grad(const ScaleGradParams& p, cudaStream_t stream) {
-  scale_grad_kernel<<<1, 1024, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(scale_grad_kernel, dim3(1), dim3(1024), 0, stream, 1, p);
 }
 
 cudaError_t launch_norm_bwd(const NormBwdParams* sides, int n_sides, cudaStream_t stream) {
@@ -722,13 +723,12 @@ cudaError_t launch_norm_bwd(const NormBwdParams* sides, int n_sides, cudaStream_
     if (blocks[s] < 1) blocks[s] = 1;
   }
   const unsigned grid = static_cast<unsigned>(blocks[0] + blocks[1]);
+  const unsigned split = static_cast<unsigned>(blocks[0]);
   if (sides[0].G2)
-    norm_bwd_kernel<true><<<grid, 256, 0, stream>>>(sides[0], sides[n_sides - 1], static_cast<unsigned>(blocks[0]),
-                                                    n_sides);
-  else
-    norm_bwd_kernel<false><<<grid, 256, 0, stream>>>(sides[0], sides[n_sides - 1], static_cast<unsigned>(blocks[0]),
-                                                     n_sides);
-  return cudaGetLastError();
+    return launch_pdl(norm_bwd_kernel<true>, dim3(grid), dim3(256), 0, stream, 1, sides[0], sides[n_sides - 1], split,
+                      n_sides);
+  return launch_pdl(norm_bwd_kernel<false>, dim3(grid), dim3(256), 0, stream, 1, sides[0], sides[n_sides - 1], split,
+                    n_sides);
 }
 
 // Force the module holding these kernels to load now (no lazy loading on the hot path).

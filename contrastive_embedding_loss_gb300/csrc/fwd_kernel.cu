@@ -310,6 +310,7 @@ struct SchedIter {
 template <int KIND, bool COLS, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y, const Params p) {
+  griddep_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sx = smem + off_x;
@@ -667,18 +668,20 @@ cudaError_t launch_fwd(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
   if (kind == KIND_SIGLIP && q.mode != kFwdSum) return cudaErrorInvalidValue;
   if (q.mode == kFwdShifted && (q.shift_x == nullptr || (kind == KIND_CLIP && q.shift_y == nullptr)))
     return cudaErrorInvalidValue;
+  const dim3 blk(T);
   if (kind == KIND_CLIP) {
-    if (q.mode == kFwdMax) fwd_kernel<KIND_CLIP, true, kFwdMax><<<grid, T, S, stream>>>(tm_x, tm_y, p);
-    else if (q.mode == kFwdShifted) fwd_kernel<KIND_CLIP, true, kFwdShifted><<<grid, T, S, stream>>>(tm_x, tm_y, p);
-    else fwd_kernel<KIND_CLIP, true, kFwdSum><<<grid, T, S, stream>>>(tm_x, tm_y, p);
-  } else if (kind == KIND_ROWS) {
-    if (q.mode == kFwdMax) fwd_kernel<KIND_ROWS, false, kFwdMax><<<grid, T, S, stream>>>(tm_x, tm_y, p);
-    else if (q.mode == kFwdShifted) fwd_kernel<KIND_ROWS, false, kFwdShifted><<<grid, T, S, stream>>>(tm_x, tm_y, p);
-    else fwd_kernel<KIND_ROWS, false, kFwdSum><<<grid, T, S, stream>>>(tm_x, tm_y, p);
-  } else {
-    fwd_kernel<KIND_SIGLIP, false, kFwdSum><<<grid, T, S, stream>>>(tm_x, tm_y, p);
+    if (q.mode == kFwdMax) return launch_pdl(fwd_kernel<KIND_CLIP, true, kFwdMax>, grid, blk, S, stream, 1, tm_x, tm_y, p);
+    if (q.mode == kFwdShifted)
+      return launch_pdl(fwd_kernel<KIND_CLIP, true, kFwdShifted>, grid, blk, S, stream, 1, tm_x, tm_y, p);
+    return launch_pdl(fwd_kernel<KIND_CLIP, true, kFwdSum>, grid, blk, S, stream, 1, tm_x, tm_y, p);
   }
-  return cudaGetLastError();
+  if (kind == KIND_ROWS) {
+    if (q.mode == kFwdMax) return launch_pdl(fwd_kernel<KIND_ROWS, false, kFwdMax>, grid, blk, S, stream, 1, tm_x, tm_y, p);
+    if (q.mode == kFwdShifted)
+      return launch_pdl(fwd_kernel<KIND_ROWS, false, kFwdShifted>, grid, blk, S, stream, 1, tm_x, tm_y, p);
+    return launch_pdl(fwd_kernel<KIND_ROWS, false, kFwdSum>, grid, blk, S, stream, 1, tm_x, tm_y, p);
+  }
+  return launch_pdl(fwd_kernel<KIND_SIGLIP, false, kFwdSum>, grid, blk, S, stream, 1, tm_x, tm_y, p);
 }
 
 }  // namespace ufc

@@ -71,6 +71,7 @@ __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u 
 template <bool AMN>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtensorMap& tm_yt,
                                           const CUtensorMap& tm_yt128, const GemmParams& p, uint32_t vblock) {
+  griddep_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem + off_a;
@@ -451,38 +452,16 @@ cudaError_t launch_gemm_both(const CUtensorMap& tk_w, const CUtensorMap& tk_yt, 
                              const GemmParams& pk, const CUtensorMap& tn_w, const CUtensorMap& tn_yt,
                              const CUtensorMap& tn_yt128, const GemmParams& pn, cudaStream_t stream) {
   const unsigned split = gemm::grid_of(pk);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(split + gemm::grid_of(pn));
-  cfg.blockDim = dim3(gemm::kThreads);
-  cfg.dynamicSmemBytes = gemm::smem_bytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel_both, tk_w, tk_yt, tk_yt128, pk, tn_w, tn_yt, tn_yt128, pn,
-                            split);
+  return launch_pdl(gemm::gemm_kernel_both, dim3(split + gemm::grid_of(pn)), dim3(gemm::kThreads), gemm::smem_bytes,
+                    stream, 2, tk_w, tk_yt, tk_yt128, pk, tn_w, tn_yt, tn_yt128, pn, split);
 }
 
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const CUtensorMap& tm_yt128,
                         const GemmParams& p, bool weights_mn, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(gemm::grid_of(p));
-  cfg.blockDim = dim3(gemm::kThreads);
-  cfg.dynamicSmemBytes = gemm::smem_bytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (weights_mn) return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<true>, tm_w, tm_yt, tm_yt128, p);
-  return cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<false>, tm_w, tm_yt, tm_yt128, p);
+  const dim3 grid(gemm::grid_of(p)), block(gemm::kThreads);
+  if (weights_mn)
+    return launch_pdl(gemm::gemm_kernel<true>, grid, block, gemm::smem_bytes, stream, 2, tm_w, tm_yt, tm_yt128, p);
+  return launch_pdl(gemm::gemm_kernel<false>, grid, block, gemm::smem_bytes, stream, 2, tm_w, tm_yt, tm_yt128, p);
 }
 
 }  // namespace ufc

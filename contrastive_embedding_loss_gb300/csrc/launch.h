@@ -11,6 +11,34 @@ namespace ufc {
 // SM count of the current device (grid caps of the grid-stride kernels).
 int current_sm_count();
 
+// Launches kernel k with programmatic stream serialization, so that it may be scheduled while
+// the kernel before it on the stream drains (every kernel here calls griddep_enter() before it
+// touches global memory), and, with cluster > 1, in clusters of that many CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       unsigned cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
+
 // Load every auxiliary kernel now (aux_kernels.cu).
 cudaError_t aux_kernels_setup();
 

@@ -23,6 +23,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
+// Programmatic dependent launch.  Every kernel of the library is launched so that it may be
+// scheduled while the kernel before it on the stream drains; it then waits here, before its
+// first access to global memory, until that grid has completed and its writes are visible
+// (no wait when nothing precedes it programmatically).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream be scheduled once every CTA of this grid has run this (or
+// exited); that kernel still waits for this grid's completion in griddep_wait.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+// Both, at the top of a kernel: nothing of this kernel touches global memory before the wait.
+__device__ __forceinline__ void griddep_enter() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -195,6 +195,7 @@ template <int KIND, bool SHIFTED>
 __global__ void __launch_bounds__(kThreads, 1)
     wgt_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                const __grid_constant__ CUtensorMap tm_w, const WgtParams p) {
+  griddep_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sx = smem + off_x;
@@ -533,24 +534,14 @@ cudaError_t launch_wgt(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
                        const WgtParams& p, dim3 grid, cudaStream_t stream) {
   using wgt::wgt_kernel;
   if (kind == KIND_SIGLIP && p.shifted) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((grid.x + 1) / 2 * 2, grid.y, 1);  // CTA pairs along the row blocks
-  cfg.blockDim = dim3(wgt::kThreads);
-  cfg.dynamicSmemBytes = wgt::smem_bytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  const dim3 g((grid.x + 1) / 2 * 2, grid.y, 1), blk(wgt::kThreads);  // CTA pairs along the row blocks
+  const size_t sm = wgt::smem_bytes;
   if (kind == KIND_CLIP)
-    return p.shifted ? cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_CLIP, true>, tm_x, tm_y, tm_w, p)
-                     : cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_CLIP, false>, tm_x, tm_y, tm_w, p);
-  if (kind == KIND_SIGLIP) return cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_SIGLIP, false>, tm_x, tm_y, tm_w, p);
-  return p.shifted ? cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_ROWS, true>, tm_x, tm_y, tm_w, p)
-                   : cudaLaunchKernelEx(&cfg, wgt_kernel<KIND_ROWS, false>, tm_x, tm_y, tm_w, p);
+    return p.shifted ? launch_pdl(wgt_kernel<KIND_CLIP, true>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p)
+                     : launch_pdl(wgt_kernel<KIND_CLIP, false>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p);
+  if (kind == KIND_SIGLIP) return launch_pdl(wgt_kernel<KIND_SIGLIP, false>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p);
+  return p.shifted ? launch_pdl(wgt_kernel<KIND_ROWS, true>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p)
+                   : launch_pdl(wgt_kernel<KIND_ROWS, false>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p);
 }
 
 }  // namespace ufc

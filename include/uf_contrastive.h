@@ -32,7 +32,12 @@
  * the call path).  All entry points are thread-safe; a call only enqueues work on the
  * caller's stream and returns without synchronising, so it can be captured in a CUDA
  * graph.  Calls on different streams are independent as long as each has its own
- * workspace and outputs.
+ * workspace and outputs.  The kernels of a call are launched with programmatic dependent
+ * launch (each waits for the grid before it on the stream before it touches memory): a
+ * caller's kernel that follows a call on the same stream and is itself launched with the
+ * programmatic stream serialization attribute must wait for its predecessor
+ * (cudaGridDependencySynchronize) before it reads the outputs; an ordinary launch, a copy
+ * or an event needs nothing.
  *
  * Buffers.  No buffer a call writes may overlap another such buffer or any input.  The written
  * buffers are the loss, the terms, the gradients, the scalar gradients, *device_status and the
