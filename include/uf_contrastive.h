@@ -68,7 +68,7 @@ extern "C" {
 typedef enum uf_status {
   UF_OK = 0,
   UF_INVALID_ARGUMENT = 1,    /* null pointer, bad size, misaligned pointer, bad prefix ladder */
-  UF_UNSUPPORTED = 2,         /* valid request this build does not implement (e.g. scale > 256) */
+  UF_UNSUPPORTED = 2,         /* valid request the library does not implement (e.g. scale > 256) */
   UF_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < uf_contrastive_workspace_min(...) */
   UF_CUDA_ERROR = 4,          /* a CUDA runtime call or kernel launch failed */
   UF_DEVICE_TIMEOUT = 5       /* a kernel gave up a bounded wait (read from *device_status) */
