@@ -55,13 +55,13 @@ def credited_flops(kind, Na, Nb, D):
     return (6 if kind == "siglip" else 8) * Na * Nb * D
 
 
-def executed_flops(kind, Na, Nb, D, prefixes=None):
+def executed_flops(kind, Na, Nb, D, prefixes=None, merged=False):
     """Tensor-core flops the library runs per step: the forward score pass (not for SigLIP,
     whose loss comes out of the weight pass), the weight pass, and the two prefix-expanded
-    gradient GEMMs (prefix k contributes p_k dimensions)."""
+    gradient GEMMs (prefix k contributes p_k dimensions; merged: prefix n-1 none below p_{n-2})."""
     pre = list(prefixes) if prefixes else [D]
     score = 2.0 * Na * Nb * pre[-1]
-    gemms = 2 * 2.0 * Na * Nb * sum(pre)
+    gemms = group_flops_executed("gemm", kind, Na, Nb, D, pre, merged)
     return (0.0 if kind == "siglip" else score) + score + gemms
 
 
@@ -79,11 +79,13 @@ def group_flops(group, kind, Na, Nb, D, prefixes):
     return None
 
 
-def group_flops_executed(group, kind, Na, Nb, D, prefixes):
-    """Tensor flops the library's kernels of one group actually issue per step."""
+def group_flops_executed(group, kind, Na, Nb, D, prefixes, merged=False):
+    """Tensor flops the library's kernels of one group actually issue per step.  merged: the two
+    widest prefixes' weights shared one array below p_{n-2}, so prefix n-1 ran only above it."""
     pre = list(prefixes)
     if group == "gemm":
-        return 2 * 2.0 * Na * Nb * sum(pre)  # prefix-expanded: prefix k contributes its p_k dimensions
+        dims = sum(pre) - (pre[-2] if merged and len(pre) >= 2 else 0)
+        return 2 * 2.0 * Na * Nb * dims  # prefix-expanded: prefix k contributes its p_k dimensions
     return group_flops(group, kind, Na, Nb, D, prefixes)
 
 
@@ -428,7 +430,9 @@ def main():
     if alg_step is not None:
         per_launch = args.steps / max(dom_launches, 1)
         alg_launch = alg_step * per_launch
-        exe_launch = group_flops_executed(dom, kind, Na, Nb, D, LADDER) * per_launch
+        # the merged path runs a second kernel in the norm-backward group (its row-scalar sums)
+        merged = prof["norm_bwd"][2] >= 2 * args.steps
+        exe_launch = group_flops_executed(dom, kind, Na, Nb, D, LADDER, merged) * per_launch
         achieved = alg_launch / (per_launch_ms / 1e3) / 1e12
         traffic = ncu_traffic(args.workload)
         alg_bytes = group_bytes(dom, kind, Na, Nb, D, LADDER)
@@ -453,7 +457,8 @@ def main():
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
                    "workspace_bytes": int(ws_bytes)},
         "tflops_credited": cflops / (ms_step / 1e3) / 1e12,
-        "tflops_executed": executed_flops(kind, Na, Nb, D, LADDER) / (ms_step / 1e3) / 1e12,
+        "tflops_executed": executed_flops(kind, Na, Nb, D, LADDER, prof["norm_bwd"][2] >= 2 * args.steps)
+        / (ms_step / 1e3) / 1e12,
         "frac_credited_of_bf16_peak": cflops / (ms_step / 1e3) / 1e12 / peak_tf,
         "roofline": roof,
         "kernels_ms_per_step": {g: prof[g][0] / args.steps for g in prof},

@@ -367,11 +367,23 @@ __device__ __forceinline__ void norm_bwd_body(const NormBwdParams& p, int64_t wa
   for (int64_t i = warp_id; i < p.nx; i += n_warps) {
     const bool diag = i < p.nmin;
     float rk = 0.f, qk = 0.f, Ck = 0.f;
+    float S = 0.f;  // lane k < n: prefix k's slot sum of x . G^k, off the diagonal
+    if (lane < n)
+      for (int s = 0; s < p.crow_slots; ++s) S += p.crow[(static_cast<int64_t>(s) * n + lane) * p.nx + i];
+    if (p.r5) {
+      // merged widest prefixes: prefix n-2's slots hold x . (G^{n-2} + G^{n-1}) below p_{n-2},
+      // prefix n-1's only the part above; r5 is prefix n-1's whole sum (from the weight pass)
+      const float s_top = __shfl_sync(0xffffffffu, S, n - 1);
+      const float r5 = p.r5[i];
+      if (lane == n - 1)
+        S = r5;
+      else if (lane == n - 2)
+        S = S + s_top - r5;
+    }
     if (lane < n) {
       const int k = lane;
       const float rho = p.rinv_x[k * p.nx + i];
-      float C = 0.f;
-      for (int s = 0; s < p.crow_slots; ++s) C += p.crow[(static_cast<int64_t>(s) * n + k) * p.nx + i];
+      float C = S;
       float Wd = 0.f;
       if (diag) {
         const float cosd = p.pos_cos[k * p.nmin + i];
@@ -731,6 +743,36 @@ cudaError_t launch_norm_bwd(const NormBwdParams* sides, int n_sides, cudaStream_
                     n_sides);
 }
 
+// ------------------------------------------------------------------------------ r5
+// Merged widest prefixes: the weight pass's per-slot row sums and per-32-row-block column sums
+// of prefix n-1's C, each added in slot order.
+__global__ void __launch_bounds__(256) r5_kernel(const R5Params p) {
+  griddep_enter();
+  const int64_t total = p.na + p.nb;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool side_a = e < p.na;
+    const int64_t i = side_a ? e : e - p.na;
+    const int64_t rows = side_a ? p.na : p.nb;
+    const float* src = side_a ? p.row : p.col;
+    const int slots = side_a ? p.row_slots : p.col_parts;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight loads in flight
+    int s = 0;
+    for (; s + 8 <= slots; s += 8)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] += src[static_cast<int64_t>(s + u) * rows + i];
+    for (; s < slots; ++s) acc[0] += src[static_cast<int64_t>(s) * rows + i];
+    const float v = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    (side_a ? p.r5_a : p.r5_b)[i] = v;
+  }
+}
+
+cudaError_t launch_r5(const R5Params& p, cudaStream_t stream) {
+  int64_t blocks = (p.na + p.nb + 255) / 256;
+  if (blocks > int64_t(8) * current_sm_count()) blocks = int64_t(8) * current_sm_count();
+  return launch_pdl(r5_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, p);
+}
+
 // Force the module holding these kernels to load now (no lazy loading on the hot path).
 cudaError_t aux_kernels_setup() {
   cudaFuncAttributes fa;
@@ -742,6 +784,7 @@ cudaError_t aux_kernels_setup() {
   if ((e = cudaFuncGetAttributes(&fa, max_reduce_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, labels_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, wait_selftest_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, r5_kernel)) != cudaSuccess) return e;
   if ((e = cudaFuncGetAttributes(&fa, norm_bwd_kernel<true>)) != cudaSuccess) return e;
   return cudaFuncGetAttributes(&fa, norm_bwd_kernel<false>);
 }

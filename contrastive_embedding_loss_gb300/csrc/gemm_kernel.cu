@@ -100,13 +100,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
     if (kk < p.n_prefix) n_slices = (p.prefix_end[kk] + kN - 1) / kN;
   const int n = p.n_prefix;
   // groups 0 .. n_rest_groups - 1 are reached by two or more prefixes (the second widest's end
-  // lies past their first dimension)
-  const int n_rest_groups = (p.split_rest && n >= 2) ? (prefix_end_of(p, n - 2) + 2 * kN - 1) / (2 * kN) : 0;
+  // lies past their first dimension).  With p.merge (and no split) each of those groups runs one
+  // unit from prefix n-2 down: array n-2 holds the merged weights of prefixes n-2 and n-1 below
+  // p_{n-2} (a multiple of 512), and prefix n-1 runs only in the groups above.
+  const bool merge = p.merge && !p.split_rest && n >= 2;
+  const int n_rest_groups =
+      ((p.split_rest || merge) && n >= 2) ? (prefix_end_of(p, n - 2) + 2 * kN - 1) / (2 * kN) : 0;
   const int64_t pairs = (p.m_rows + 2 * kTileRows - 1) / (2 * kTileRows);
   const int64_t cta = vblock >> 1;
   const int type = static_cast<int>(cta / pairs);
-  const bool rest_unit = type < n_rest_groups;
-  const int grp = rest_unit ? type : type - n_rest_groups;
+  // unit types: split: [the rest units of groups 0 .. n_rest_groups - 1][one unit per group];
+  // merge: [one unit per group]; neither: [one unit per group] (n_rest_groups = 0)
+  const bool rest_unit = type < n_rest_groups;  // its prefixes start at n-2
+  const int grp = (merge || rest_unit) ? type : type - n_rest_groups;
   const int64_t pair_i = cta % pairs;
   const int64_t m0 = (pair_i * 2 + rank) * kTileRows;  // first row of G in this launch
   const int d0 = grp * 2 * kN;                          // first dimension of slice s0
@@ -119,8 +125,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
   const int top = rest_unit ? n - 2 : n - 1;
   const bool split_group = grp < n_rest_groups;
   const int n_steps = (!rest_unit && split_group) ? 1 : top + 1 - k_first;
-  float* const gout = rest_unit ? p.G2 : p.G;
-  const int64_t gld = rest_unit ? p.g2_ld : p.d;
+  float* const gout = (rest_unit && !merge) ? p.G2 : p.G;
+  const int64_t gld = (rest_unit && !merge) ? p.g2_ld : p.d;
   // prefix k's width within slice s (0: it does not reach the slice)
   auto width = [&](int k, int sl) {
     const int w = prefix_end_of(p, k) - (d0 + sl * kN);
@@ -286,12 +292,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_w, const CUtenso
     const bool row_ok = gl < p.m_rows;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const int wmax[2] = {width(top, 0), width(top, 1)};  // columns of each slice with data
-    // prefixes that do not reach a slice contribute nothing to its slot
-    if (row_ok && !p.accumulate && !rest_unit)
+    // prefixes that do not reach a slice contribute nothing to its slot (merged: nor does prefix
+    // n-1 below p_{n-2}, whose weights are in the merged array)
+    if (row_ok && !p.accumulate && (merge || !rest_unit))
       for (int sl = 0; sl < 2; ++sl)
         if (2 * grp + sl < n_slices)
           for (int k = 0; k < n; ++k)
-            if (width(k, sl) == 0) p.crow[(static_cast<int64_t>(2 * grp + sl) * n + k) * p.crow_rows + g] = 0.f;
+            if (width(k, sl) == 0 || (merge && rest_unit && k == n - 1))
+              p.crow[(static_cast<int64_t>(2 * grp + sl) * n + k) * p.crow_rows + g] = 0.f;
     float prevd[2][kN / 64], curd[2][kN / 64];
 #pragma unroll
     for (int sl = 0; sl < 2; ++sl)

@@ -101,6 +101,16 @@ struct WgtParams {
   float* rowacc;                  // SigLIP: [split * 4 + quarter][n][nx] loss sums (log2 units), or NULL
   float* rowsig;                  // SigLIP, with rowacc: the same slots, sums of sigmoid(x_ij) over the
                                   // negatives (the bias gradient), or NULL
+  // merge: the two widest prefixes share one array on the dimensions below p_{n-2} (a multiple
+  // of 512).  At prefix n-1 the block that prefix n-2 stored is read back and overwritten with
+  // bf16(W^{n-1} + W^{n-2}) (W = the stored bf16 weights); C = sum_j W^{n-1}_ij d^{n-1}_ij (d the
+  // raw dot) is summed per row into r5_row[split * 4 + quarter][nx] and per 32-row block and
+  // column into r5_col[row block * 4 + quadrant][ny].
+  int merge;
+  float* r5_row;
+  float* r5_col;
+  const uint16_t* w;              // merge: the weight array (tm_w's), for the read-back
+  int64_t ldw;                    // its row stride (elements)
   int* status;
 };
 constexpr int kWgtCols = 256;
@@ -128,6 +138,8 @@ struct GemmParams {
   int prefix_end[kMaxPrefix];
   int accumulate;
   float* G;
+  int merge;                      // 1: slice groups below p_{n-2} contract prefixes n-2 .. (array n-2 holds
+                                  // the merged weights of n-2 and n-1) into G; prefix n-1 runs only above
   int split_rest;                 // 1: the prefixes below the widest run as their own units, into G2
   float* G2;                      // [m_rows][g2_ld] (split_rest): their part of G, dimensions < g2_ld
   int64_t g2_ld;                  // the second-widest prefix's end
@@ -237,12 +249,28 @@ struct NormBwdParams {
   const float* G;          // [nx][d]
   const float* G2;         // NULL, or [nx][g2_ld]: added to G below dimension g2_ld
   int64_t g2_ld;
+  const float* r5;         // NULL, or (merged widest prefixes) [nx]: prefix n-1's C off the diagonal; its
+                           // slots in crow then hold only the dimensions above p_{n-2}, and prefix
+                           // n-2's slots the merged weights' x . G
   float* dX;               // [nx][d]
   float* csum;             // NULL or [nx]: sum over prefixes of the full row scalar C_k (logit-scale gradient)
   int double_out;          // one-set loss: write 2 dX (the row's gradient through both roles of every cell)
 };
 // sides: one or two (A's rows, then B's), run as one grid.
 cudaError_t launch_norm_bwd(const NormBwdParams* sides, int n_sides, cudaStream_t stream);
+
+// Merged widest prefixes: r5_a[i] = sum_s row[s][i] (s < row_slots), r5_b[j] = sum_q col[q][j]
+// (q < col_parts), each in a fixed order.
+struct R5Params {
+  int64_t na, nb;
+  const float* row;
+  int row_slots;
+  const float* col;
+  int col_parts;
+  float* r5_a;
+  float* r5_b;
+};
+cudaError_t launch_r5(const R5Params& p, cudaStream_t stream);
 
 // Gradients of the weighted loss in the logit scale and (SigLIP) the bias, from the row
 // scalars: d_scale = (1 / scale) sum_i csum[i]  (sum_ij W_ij cos_ij = scale dL/dscale), and

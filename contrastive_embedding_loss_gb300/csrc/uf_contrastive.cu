@@ -67,10 +67,12 @@ struct Plan {
   int64_t cchunk = 0;                // rows of B (weight columns) per weight chunk
   bool gsplit = false;               // gradient contractions split below the widest prefix
   int64_t g2_ld = 0;                 // columns of their G2 arrays
+  bool merge = false;                // the two widest prefixes' weights merged (one chunk only)
   size_t fixed = 0;                  // bytes of everything but the weight array
   // offsets
   size_t o_rinv_a, o_rinv_b, o_pos, o_zr, o_zc, o_fa, o_fb, o_acc_a, o_acc_b, o_crow_a, o_crow_b, o_terms_a,
       o_terms_b, o_spart, o_done, o_g2a, o_g2b, o_at, o_bt, o_csum, o_sig, o_sh_a, o_sh_b, o_lab, o_lcount, o_w, total;
+  size_t o_r5row = 0, o_r5col = 0, o_r5a = 0, o_r5b = 0;  // merged widest prefixes
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -164,10 +166,21 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
     const int64_t cols_max = cdiv(Nb, kWgtCols) * kWgtCols;
     const size_t per = sizeof(uint16_t) * static_cast<size_t>(n);  // bytes per (row, column) cell
     const size_t budget = ws_limit ? (ws_limit > o ? ws_limit - o : 0) : kDefaultWeightBytes;
-    if (per * static_cast<size_t>(rows_max) * static_cast<size_t>(P.ldb) <= budget) {
+    const size_t one_chunk = per * static_cast<size_t>(rows_max) * static_cast<size_t>(P.ldb);
+    // The two widest prefixes' weights merged below p_{n-2} (a multiple of 512, so whole slice
+    // groups): the gradient GEMMs then contract prefix n-1 only above it, 7 MMA passes of 9 for
+    // the five-prefix ladder, for one more store of a weight block and the sums of prefix n-1's
+    // row scalars in the weight pass.  Taken when every weight fits in one chunk with those sums
+    // beside it and the contractions are long (not split); CLIP and ROWS only (SigLIP's weight
+    // pass, heavier in its epilogue, loses more than its GEMMs gain: N = 16384 2.91 -> 3.10 ms).
+    const size_t r5_bytes = align256(f * 4 * P.wgt.splits * Na) + align256(f * 4 * P.rb_a * Nb) + align256(f * Na) +
+                            align256(f * Nb);  // (as taken below)
+    const bool merge_ok = kind != KIND_SIGLIP && n >= 2 && prefixes[n - 2] % 512 == 0 && !P.gsplit;
+    if (one_chunk <= budget) {
       P.chunk = rows_max;  // one chunk
       P.cchunk = Nb;
       P.ldw = P.ldb;
+      P.merge = merge_ok && align256(one_chunk) + r5_bytes <= budget;
     } else {
       const double cells = static_cast<double>(budget / per);
       int64_t R = static_cast<int64_t>(std::sqrt(cells)) / kTileRows * kTileRows;
@@ -190,6 +203,12 @@ bool make_plan(int64_t Na, int64_t Nb, int D, const int* prefixes, int n, int ki
       }
     }
     o = align256(o + per * static_cast<size_t>(P.chunk) * static_cast<size_t>(P.ldw));
+    if (P.merge) {
+      P.o_r5row = take(f * 4 * P.wgt.splits * Na);  // per (split, column quarter) row sums
+      P.o_r5col = take(f * 4 * P.rb_a * Nb);        // per (128-row block, 32-row quadrant) column sums
+      P.o_r5a = take(f * Na);
+      P.o_r5b = take(f * Nb);
+    }
   }
   P.total = o;
   return true;
@@ -651,6 +670,9 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
   // one GEMM contracts the chunk's weights with B into dA's rows, another contracts their
   // transpose with the chunk of A into all of dB (added over chunks).  Both write G = dX
   // before its projection in place into dA / dB, and the projection scalars.
+  // the two widest prefixes' weights merged (planned when they fit; not with a label matrix,
+  // whose patch writes each prefix's exact weights, nor for the one-set loss)
+  const bool wmerge = P.merge && !labels && !oneset;
   {
     uint16_t* W = reinterpret_cast<uint16_t*>(ws + P.o_w);
     const int64_t wrows = static_cast<int64_t>(n) * P.chunk;
@@ -678,6 +700,13 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     wp.w_rows_per_prefix = P.chunk;
     wp.rowacc = siglip ? F(P.o_acc_a) : nullptr;  // the SigLIP loss sums
     wp.rowsig = (siglip && d_bias) ? F(P.o_sig) : nullptr;  // and, for the bias gradient, the sigmoid sums
+    if (wmerge) {
+      wp.merge = 1;
+      wp.r5_row = F(P.o_r5row);
+      wp.r5_col = F(P.o_r5col);
+      wp.w = W;
+      wp.ldw = P.ldw;
+    }
     wp.status = device_status;
     GemmParams ga{}, gb{};
     for (GemmParams* g : {&ga, &gb}) {
@@ -695,6 +724,7 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
     gb.X = B16;
     gb.crow = F(P.o_crow_b);
     gb.crow_rows = Nb;
+    ga.merge = gb.merge = wmerge ? 1 : 0;
     if (P.gsplit) {
       ga.split_rest = gb.split_rest = 1;
       ga.G2 = F(P.o_g2a);
@@ -778,6 +808,19 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
       ProfScope ps(UF_KERNEL_STATS, 1, stream);
       UF_CHECK(launch_stats(sp, stream));
     }
+    if (wmerge) {  // prefix n-1's row scalars from the weight pass's partial sums
+      R5Params rp{};
+      rp.na = Na;
+      rp.nb = Nb;
+      rp.row = F(P.o_r5row);
+      rp.row_slots = 4 * P.wgt.splits;
+      rp.col = F(P.o_r5col);
+      rp.col_parts = static_cast<int>(4 * P.rb_a);
+      rp.r5_a = F(P.o_r5a);
+      rp.r5_b = F(P.o_r5b);
+      ProfScope ps(UF_KERNEL_NORM_BWD, 1, stream);
+      UF_CHECK(launch_r5(rp, stream));
+    }
   }
 
   // ---- 4. projection term and diagonal correction
@@ -819,6 +862,7 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
       q.crow_slots = P.slices;
       q.csum = (xa && d_logit_scale) ? F(P.o_csum) : nullptr;
       q.G = xa ? dA : dB;
+      if (wmerge) q.r5 = F(xa ? P.o_r5a : P.o_r5b);
       if (P.gsplit) {
         q.G2 = F(xa ? P.o_g2a : P.o_g2b);
         q.g2_ld = P.g2_ld;

@@ -73,6 +73,49 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// bf16(a + b) of eight bf16 pairs
+__device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b) {
+  return make_uint4(pack_bf16x2(bf16_lo(a.x) + bf16_lo(b.x), bf16_hi(a.x) + bf16_hi(b.x)),
+                    pack_bf16x2(bf16_lo(a.y) + bf16_lo(b.y), bf16_hi(a.y) + bf16_hi(b.y)),
+                    pack_bf16x2(bf16_lo(a.z) + bf16_lo(b.z), bf16_hi(a.z) + bf16_hi(b.z)),
+                    pack_bf16x2(bf16_lo(a.w) + bf16_lo(b.w), bf16_hi(a.w) + bf16_hi(b.w)));
+}
+
+// Wait until at most `pending` of this thread's bulk store groups are incomplete (the immediate
+// of cp.async.bulk.wait_group is a constant; more than 3 waits for all).
+__device__ __forceinline__ void bulk_wait_upto(uint32_t pending) {
+  switch (pending) {
+    case 1: asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.bulk.wait_group 3;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); break;
+  }
+}
+
+// Sums over the warp's 32 rows (one per lane) of 8 columns' values v[0..7]: a reduce-scatter
+// over lane bits 4, 3, 2 (each stage keeps half of the values, the upper half where the lane
+// bit is set, and adds the partner's copy of it), then a butterfly over bits 1, 0.  Every lane
+// ends with the total of column ((lane >> 2) & 7).  A fixed order for every lane.
+__device__ __forceinline__ float colsum8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int st = 0; st < 3; ++st) {
+    const int m = 16 >> st, h = 4 >> st;
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float lo = v[i], hi = v[i + h];
+      const float got = __shfl_xor_sync(0xffffffffu, upper ? lo : hi, m);
+      v[i] = (upper ? hi : lo) + got;
+    }
+  }
+  float t = v[0];
+  t += __shfl_xor_sync(0xffffffffu, t, 2);
+  t += __shfl_xor_sync(0xffffffffu, t, 1);
+  return t;
+}
 
 // 8 cells: their weights as four packed bf16 pairs; (SigLIP, R3 != 0) adds the loss and
 // the sigmoid of the negatives to acc (.x, .y).  c1, c2: shared addresses of the columns'
@@ -191,7 +234,9 @@ struct Schedule {
   }
 };
 
-template <int KIND, bool SHIFTED>
+// MERGE: the two widest prefixes' weights merged (WgtParams::merge); a separate instantiation,
+// so that the kernels without it carry none of its code.
+template <int KIND, bool SHIFTED, bool MERGE>
 __global__ void __launch_bounds__(kThreads, 1)
     wgt_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                const __grid_constant__ CUtensorMap tm_w, const WgtParams p) {
@@ -371,6 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t l2_evict_first = l2_policy_evict_first();
     uint32_t uses = 0;  // uses of each accumulator so far (both advance together)
     bool ok = true;
+    // merge: this row's sum over the tiles of W^{n-1} d^{n-1}; the CTA's 128-row block index
+    float r5acc = 0.f;
+    const int64_t rblk = i0 / kTileRows;
+    // (lane 0) bulk store groups committed so far, and the count just after each tile's prefix
+    // n-2 store (merge: how many later groups may still be pending when that block is read back)
+    uint32_t ncommit = 0, c4_0 = 0, c4_1 = 0;
     // the schedule of Schedule::at as nested loops: tile pairs, bands, the pair's tiles
     for (int tp = 0; tp < T; tp += 2) {
       const int width = tp + 1 < T ? 2 : 1;
@@ -440,35 +491,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           float2 al = make_float2(0.f, 0.f);
           // four 8-column chunks of one half (vh: its 32 values; chb: its first chunk); the mask
           // test is hoisted out of the unrolled loops
+          // merge, at prefix n-1: the stored weights W times the raw dots, into the row sum and
+          // (over the warp's 32 rows) into this 32-row block's column sums
+          const bool mtop = MERGE && k == n - 1;
+          auto r5_cells = [&](const uint4 pk, const float* vd, int ch) {
+            const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
+            float pr[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pr[2 * e] = bf16_lo(w[e]) * vd[2 * e];
+              pr[2 * e + 1] = bf16_hi(w[e]) * vd[2 * e + 1];
+            }
+            r5acc += ((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
+            const float col = colsum8(pr, lane);
+            const int64_t gj = j0 + cq * 64 + ch * 8 + ((lane >> 2) & 7);
+            if ((lane & 3) == 0 && gj < p.ny && il0 < p.rows) p.r5_col[(rblk * 4 + q) * p.ny + gj] = col;
+          };
+          // four 8-column chunks of one half (vh: its 32 values; chb: its first chunk); the mask
+          // test is hoisted out of the unrolled loops
           auto chunks = [&](const float* vh, int chb) {
             const uint32_t dst = stage_row, f1 = c1 + chb * 32, f2 = c2 + chb * 32;
             const int col0 = cq * 64 + chb * 8;
+            auto put = [&](int cc, const uint4 pk) {
+              st_shared_v4(dst + (((chb + cc) ^ swz) << 4), pk);
+              if constexpr (MERGE)
+                if (mtop) r5_cells(pk, vh + cc * 8, chb + cc);
+            };
             if constexpr (SHIFTED) {
               if (check) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                  st_shared_v4(dst + (((chb + cc) ^ swz) << 4),
-                               cells8_shifted<KIND, true>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, wk,
-                                                          col0 + cc * 8, ncols, diag_col, row_ok));
+                  put(cc, cells8_shifted<KIND, true>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, wk,
+                                                     col0 + cc * 8, ncols, diag_col, row_ok));
               } else {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                  st_shared_v4(dst + (((chb + cc) ^ swz) << 4),
-                               cells8_shifted<KIND, false>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, wk, 0,
-                                                           0, 0, true));
+                  put(cc, cells8_shifted<KIND, false>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, wk, 0, 0,
+                                                      0, true));
               }
             } else if (check) {
 #pragma unroll
               for (int cc = 0; cc < 4; ++cc)
-                st_shared_v4(dst + (((chb + cc) ^ swz) << 4),
-                             cells8<KIND, true>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, L, b2,
-                                                col0 + cc * 8, ncols, diag_col, row_ok, al));
+                put(cc, cells8<KIND, true>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, L, b2, col0 + cc * 8,
+                                           ncols, diag_col, row_ok, al));
             } else {
 #pragma unroll
               for (int cc = 0; cc < 4; ++cc)
-                st_shared_v4(dst + (((chb + cc) ^ swz) << 4),
-                             cells8<KIND, false>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, L, b2, 0, 0, 0,
-                                                 true, al));
+                put(cc, cells8<KIND, false>(vh + cc * 8, f1 + cc * 32, f2 + cc * 32, R1, R2, R3, L, b2, 0, 0, 0, true,
+                                            al));
             }
           };
           chunks(v0, 0);
@@ -481,13 +551,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           // a quarter wholly past the last column stores nothing, nor does the second CTA of
           // a pair that lies wholly past the launch's rows (its rows are not in the chunk)
-          if (lane == 0 && il0 < p.rows && j0 + cq * 64 < p.col0 + p.cols) {
+          const bool stores = il0 < p.rows && j0 + cq * 64 < p.col0 + p.cols;  // (uniform over the warp)
+          if (lane == 0 && stores) {
             // the weights are written once here and read back by the GEMMs much later: keep
-            // them from evicting the score operands, which every CTA re-reads
-            tma_store_2d_hint(&tm_w, stage, static_cast<int>(j0 - p.col0 + cq * 64),
-                              static_cast<int>(static_cast<int64_t>(k) * p.w_rows_per_prefix + wrow),
-                              l2_evict_first);
+            // them from evicting the score operands, which every CTA re-reads (merge: prefix
+            // n-2's block is read back and overwritten at prefix n-1, a few microseconds later,
+            // so it stays in L2 as a normal line)
+            const int wc = static_cast<int>(j0 - p.col0 + cq * 64);
+            const int wr = static_cast<int>(static_cast<int64_t>(k) * p.w_rows_per_prefix + wrow);
+            if (MERGE && k == n - 2)
+              tma_store_2d(&tm_w, stage, wc, wr);
+            else
+              tma_store_2d_hint(&tm_w, stage, wc, wr, l2_evict_first);
             bulk_commit();
+            ++ncommit;
+            if (MERGE && k == n - 2) (u ? c4_1 : c4_0) = ncommit;
+          }
+          if (MERGE && mtop && stores) {
+            // prefix n-2's block of this tile (stored a snapshot or two ago) becomes bf16(W^{n-1}
+            // + W^{n-2}): that store has completed (the groups committed after it may still run),
+            // and this prefix's store has read the staging block, which still holds W^{n-1}
+            if (lane == 0) {
+              bulk_wait_upto(ncommit - (u ? c4_1 : c4_0));
+              bulk_wait_read0();
+            }
+            __syncwarp();
+            fence_proxy_async_global();
+            const uint16_t* w2 = p.w + (static_cast<int64_t>(n - 2) * p.w_rows_per_prefix + wrow + lane) * p.ldw +
+                                 (j0 - p.col0 + cq * 64);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint4 lo[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) lo[u] = *reinterpret_cast<const uint4*>(w2 + h * 32 + u * 8);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t addr = stage_row + (((h * 4 + u) ^ swz) << 4);
+                st_shared_v4(addr, add_bf16x8(ld_shared_v4u(addr), lo[u]));
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d_hint(&tm_w, stage, static_cast<int>(j0 - p.col0 + cq * 64),
+                                static_cast<int>(static_cast<int64_t>(n - 2) * p.w_rows_per_prefix + wrow),
+                                l2_evict_first);
+              bulk_commit();
+              ++ncommit;
+            }
           }
           if (KIND == KIND_SIGLIP && p.rowacc && row_ok) {
             float* pl = p.rowacc + slot_off + static_cast<int64_t>(k) * p.nx;
@@ -503,6 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cp_async_wait<0>();
+    if constexpr (MERGE)
+      if (row_ok && T > 0) p.r5_row[static_cast<int64_t>(split * 4 + cq) * p.nx + gi] = r5acc;
     if (lane == 0) bulk_wait0();  // the weights are in global memory before the CTA exits
   }
 
@@ -516,7 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int KIND, bool SHIFTED>
 static cudaError_t setup_one() {
-  return cudaFuncSetAttribute(wgt_kernel<KIND, SHIFTED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaError_t e = cudaFuncSetAttribute(wgt_kernel<KIND, SHIFTED, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(wgt_kernel<KIND, SHIFTED, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes);
 }
 
 }  // namespace wgt
@@ -536,12 +653,13 @@ cudaError_t launch_wgt(int kind, const CUtensorMap& tm_x, const CUtensorMap& tm_
   if (kind == KIND_SIGLIP && p.shifted) return cudaErrorInvalidValue;
   const dim3 g((grid.x + 1) / 2 * 2, grid.y, 1), blk(wgt::kThreads);  // CTA pairs along the row blocks
   const size_t sm = wgt::smem_bytes;
-  if (kind == KIND_CLIP)
-    return p.shifted ? launch_pdl(wgt_kernel<KIND_CLIP, true>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p)
-                     : launch_pdl(wgt_kernel<KIND_CLIP, false>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p);
-  if (kind == KIND_SIGLIP) return launch_pdl(wgt_kernel<KIND_SIGLIP, false>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p);
-  return p.shifted ? launch_pdl(wgt_kernel<KIND_ROWS, true>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p)
-                   : launch_pdl(wgt_kernel<KIND_ROWS, false>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p);
+#define UF_WGT(K, SH)                                                                                      \
+  (p.merge ? launch_pdl(wgt_kernel<K, SH, true>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p)              \
+           : launch_pdl(wgt_kernel<K, SH, false>, g, blk, sm, stream, 2, tm_x, tm_y, tm_w, p))
+  if (kind == KIND_CLIP) return p.shifted ? UF_WGT(KIND_CLIP, true) : UF_WGT(KIND_CLIP, false);
+  if (kind == KIND_SIGLIP) return UF_WGT(KIND_SIGLIP, false);
+  return p.shifted ? UF_WGT(KIND_ROWS, true) : UF_WGT(KIND_ROWS, false);
+#undef UF_WGT
 }
 
 }  // namespace ufc

@@ -194,3 +194,49 @@ def test_rows_q8192_k262144_sampled(ctx):
     check_grad_rows(out["dB"][keys].double().cpu().numpy(), gK, "key gradient rows")
     check_euler(Q16, out["dA"], "dA")
     check_euler(K16, out["dB"], "dB")
+
+
+MERGED = [
+    # kind, Na, Nb, D, prefixes, scale, bias, noise, seed: long contractions (more than one wave
+    # of CTA pairs) with the weights in one chunk, where the two widest prefixes share one weight
+    # array below the second widest's end (a multiple of 512); CLIP and ROWS
+    ("clip", 6144, 6144, 1024, LADDER, 1 / 0.07, 0.0, 1.0, 41),
+    ("rows", 1536, 12288, 1024, LADDER, 1 / 0.05, 0.0, 0.8, 43),
+    ("clip", 5120, 5120, 2048, (64, 128, 256, 512, 1024, 2048), 1 / 0.07, 0.0, 1.0, 44),
+    ("clip", 5376, 5376, 1024, LADDER, 60.0, 0.0, 2.0, 45),  # the max-shifted statistics
+    ("rows", 2048, 10240, 1024, LADDER, 80.0, 0.0, 2.0, 46),  # ROWS on the max-shifted path
+]
+
+
+@pytest.mark.parametrize("kind,Na,Nb,D,pre,scale,bias,noise,seed", MERGED)
+def test_merged_widest_prefixes_sampled(ctx, kind, Na, Nb, D, pre, scale, bias, noise, seed):
+    """The merged path (it reduces prefix n-1's partial row scalars in a second launch of the
+    norm-backward group) against the oracle's gradient rows, and the Euler identity, whose
+    projection scalars the merge recovers as (x . G of both prefixes) - (prefix n-1's)."""
+    A16, B16 = (synth.queries_keys(Na, Nb, D, noise, seed) if kind == "rows" else synth.paired(Na, D, noise, seed))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctx.uf_contrastive_profile(True)
+    out = ctx.contrastive_fwd_bwd(dev(A16), dev(B16), kind, pre, scale, bias, grads=True, terms=True,
+                                  device_status=status)
+    torch.cuda.synchronize()
+    launches = ctx.uf_contrastive_profile_read(ctx.KERNEL_GROUPS.index("norm_bwd"))[2]
+    ctx.uf_contrastive_profile(False)
+    assert int(status.item()) == 0
+    assert launches == 2, "the merged path did not run (its partial sums are reduced in a second launch)"
+    rows = sample(Na, 128, seed)
+    cols = sample(Nb, 128, seed + 100)
+    lse_a = lse_b = None
+    if kind != "siglip":
+        lse_a, _ = oracle.softmax_normalisers(kind, A16, B16, pre, scale)
+        if kind == "clip":
+            lse_b, _ = oracle.softmax_normalisers(kind, B16, A16, pre, scale)
+    if kind == "rows":
+        gA = oracle.grad_rows(kind, True, A16, B16, pre, scale, bias, rows, lse_x=lse_a)
+        gB = oracle.grad_rows(kind, False, B16, A16, pre, scale, bias, cols, lse_y=lse_a)
+    else:
+        gA = oracle.grad_rows(kind, True, A16, B16, pre, scale, bias, rows, lse_x=lse_a, lse_y=lse_b)
+        gB = oracle.grad_rows(kind, False, B16, A16, pre, scale, bias, cols, lse_x=lse_b, lse_y=lse_a)
+    check_grad_rows(out["dA"][rows].double().cpu().numpy(), gA, "dA rows")
+    check_grad_rows(out["dB"][cols].double().cpu().numpy(), gB, "dB rows")
+    check_euler(A16, out["dA"], "dA")
+    check_euler(B16, out["dB"], "dB")
