@@ -101,7 +101,11 @@ UF_API uf_status_t uf_contrastive_init(int device);
  * workspace for the backward as well.  The backward keeps the bf16 weights of every
  * prefix for a chunk of rows of A by rows of B in the workspace (n_prefix x R x C x 2
  * bytes); the recommended size holds every weight in one chunk unless that exceeds 48 GiB,
- * in which case the weights are cut into about square chunks.  Any workspace of at least
+ * in which case the weights are cut into about square chunks.  For CLIP and ROWS with long
+ * contractions (more than about 4864 rows at D = 1024) and a second-widest prefix that is a
+ * multiple of 512, it also holds the sums that let the two widest prefixes share one weight
+ * array (4 (Na/128) Nb + (4 s + 1) Na + Nb floats, s the weight pass's column split; 0.54 GB
+ * at N = 65536), which the backward then uses.  Any workspace of at least
  * uf_contrastive_workspace_min() bytes works: a smaller one only means more chunks (dA then
  * adds over the chunks of B's rows, dB over the chunks of A's rows, in a fixed order).
  */
