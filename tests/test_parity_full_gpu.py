@@ -205,6 +205,8 @@ MERGED = [
     ("clip", 5120, 5120, 2048, (64, 128, 256, 512, 1024, 2048), 1 / 0.07, 0.0, 1.0, 44),
     ("clip", 5376, 5376, 1024, LADDER, 60.0, 0.0, 2.0, 45),  # the max-shifted statistics
     ("rows", 2048, 10240, 1024, LADDER, 80.0, 0.0, 2.0, 46),  # ROWS on the max-shifted path
+    ("clip", 5120, 5120, 1024, (512, 1024), 1 / 0.07, 0.0, 1.0, 47),  # two prefixes: nothing below the merge
+    ("clip", 2560, 2560, 4096, (64, 256, 1024, 4096), 1 / 0.07, 0.0, 1.0, 48),  # six slice groups above it
 ]
 
 
