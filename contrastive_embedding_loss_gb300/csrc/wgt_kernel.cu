@@ -76,12 +76,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
-// bf16(a + b) of eight bf16 pairs
+// bf16(a + b) of eight bf16 values, two per packed add (the exact sum of two bf16 values,
+// rounded once to bf16: the same as rounding their fp32 sum)
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b) {
-  return make_uint4(pack_bf16x2(bf16_lo(a.x) + bf16_lo(b.x), bf16_hi(a.x) + bf16_hi(b.x)),
-                    pack_bf16x2(bf16_lo(a.y) + bf16_lo(b.y), bf16_hi(a.y) + bf16_hi(b.y)),
-                    pack_bf16x2(bf16_lo(a.z) + bf16_lo(b.z), bf16_hi(a.z) + bf16_hi(b.z)),
-                    pack_bf16x2(bf16_lo(a.w) + bf16_lo(b.w), bf16_hi(a.w) + bf16_hi(b.w)));
+  return make_uint4(add_bf16x2(a.x, b.x), add_bf16x2(a.y, b.y), add_bf16x2(a.z, b.z), add_bf16x2(a.w, b.w));
 }
 
 // Wait until at most `pending` of this thread's bulk store groups are incomplete (the immediate
@@ -494,6 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // merge, at prefix n-1: the stored weights W times the raw dots, into the row sum and
           // (over the warp's 32 rows) into this 32-row block's column sums
           const bool mtop = MERGE && k == n - 1;
+          // this lane's column-sum slot of the tile's first 8-column chunk (lanes 4c hold column c)
+          const int64_t gj_lane = j0 + cq * 64 + ((lane >> 2) & 7);
+          float* const r5_lane = MERGE ? p.r5_col + (rblk * 4 + q) * p.ny + gj_lane : nullptr;
+          const bool r5_writes = (lane & 3) == 0 && il0 < p.rows;
           auto r5_cells = [&](const uint4 pk, const float* vd, int ch) {
             const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
             float pr[8];
@@ -504,8 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             r5acc += ((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
             const float col = colsum8(pr, lane);
-            const int64_t gj = j0 + cq * 64 + ch * 8 + ((lane >> 2) & 7);
-            if ((lane & 3) == 0 && gj < p.ny && il0 < p.rows) p.r5_col[(rblk * 4 + q) * p.ny + gj] = col;
+            if (r5_writes && gj_lane + ch * 8 < p.ny) r5_lane[ch * 8] = col;
           };
           // four 8-column chunks of one half (vh: its 32 values; chb: its first chunk); the mask
           // test is hoisted out of the unrolled loops
