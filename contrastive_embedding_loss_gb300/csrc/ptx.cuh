@@ -112,6 +112,16 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const 
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "l"(policy)
                : "memory");
 }
+// Bulk reduce-add of a shared-memory box onto the tensor at (c0, c1), element by element in
+// the tensor map's type (bf16: the exact sum rounded to nearest even, performed in L2), with an
+// L2 cache-policy hint for the written lines.
+__device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* map, const void* src, int c0, int c1,
+                                                       uint64_t policy) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group.L2::cache_hint"
+               " [%0, {%2, %3}], [%1], %4;"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "l"(policy)
+               : "memory");
+}
 // L2 policy: lines are the first to be evicted (a write-once stream that must not push
 // reused data out of L2).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -126,12 +136,6 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Wait until every bulk store group of this thread but the newest has completed.
 __device__ __forceinline__ void bulk_wait1() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
-// Order this thread's later generic-proxy global reads after global writes of the async proxy
-// (a block that a TMA store wrote, read back with ordinary loads).
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -456,12 +460,6 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4u(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
-  return v;
 }
 __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
   float4 v;

@@ -76,17 +76,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
-// bf16(a + b) of eight bf16 values, two per packed add (the exact sum of two bf16 values,
-// rounded once to bf16: the same as rounding their fp32 sum)
-__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b) {
-  return make_uint4(add_bf16x2(a.x, b.x), add_bf16x2(a.y, b.y), add_bf16x2(a.z, b.z), add_bf16x2(a.w, b.w));
-}
-
 // Wait until at most `pending` of this thread's bulk store groups are incomplete (the immediate
 // of cp.async.bulk.wait_group is a constant; more than 3 waits for all).
 __device__ __forceinline__ void bulk_wait_upto(uint32_t pending) {
@@ -561,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && stores) {
             // the weights are written once here and read back by the GEMMs much later: keep
             // them from evicting the score operands, which every CTA re-reads (merge: prefix
-            // n-2's block is read back and overwritten at prefix n-1, a few microseconds later,
-            // so it stays in L2 as a normal line)
+            // n-2's block is added to at prefix n-1, a few microseconds later, so it stays in L2
+            // as a normal line)
             const int wc = static_cast<int>(j0 - p.col0 + cq * 64);
             const int wr = static_cast<int>(static_cast<int64_t>(k) * p.w_rows_per_prefix + wrow);
             if (MERGE && k == n - 2)
@@ -572,36 +561,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit();
             ++ncommit;
             if (MERGE && k == n - 2) (u ? c4_1 : c4_0) = ncommit;
-          }
-          if (MERGE && mtop && stores) {
-            // prefix n-2's block of this tile (stored a snapshot or two ago) becomes bf16(W^{n-1}
-            // + W^{n-2}): that store has completed (the groups committed after it may still run),
-            // and this prefix's store has read the staging block, which still holds W^{n-1}
-            if (lane == 0) {
+            if (MERGE && mtop) {
+              // prefix n-2's block of this tile (stored a snapshot or two ago) becomes
+              // bf16(W^{n-1} + W^{n-2}): once that store has completed (the groups committed
+              // after it may still run), the staging block, which holds W^{n-1}, is
+              // reduce-added onto it in L2
               bulk_wait_upto(ncommit - (u ? c4_1 : c4_0));
-              bulk_wait_read0();
-            }
-            __syncwarp();
-            fence_proxy_async_global();
-            const uint16_t* w2 = p.w + (static_cast<int64_t>(n - 2) * p.w_rows_per_prefix + wrow + lane) * p.ldw +
-                                 (j0 - p.col0 + cq * 64);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint4 lo[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) lo[u] = *reinterpret_cast<const uint4*>(w2 + h * 32 + u * 8);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const uint32_t addr = stage_row + (((h * 4 + u) ^ swz) << 4);
-                st_shared_v4(addr, add_bf16x8(ld_shared_v4u(addr), lo[u]));
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d_hint(&tm_w, stage, static_cast<int>(j0 - p.col0 + cq * 64),
-                                static_cast<int>(static_cast<int64_t>(n - 2) * p.w_rows_per_prefix + wrow),
-                                l2_evict_first);
+              tma_reduce_add_2d_hint(&tm_w, stage, wc, wr - static_cast<int>(p.w_rows_per_prefix), l2_evict_first);
               bulk_commit();
               ++ncommit;
             }
