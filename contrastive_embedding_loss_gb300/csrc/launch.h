@@ -102,15 +102,13 @@ struct WgtParams {
   float* rowsig;                  // SigLIP, with rowacc: the same slots, sums of sigmoid(x_ij) over the
                                   // negatives (the bias gradient), or NULL
   // merge: the two widest prefixes share one array on the dimensions below p_{n-2} (a multiple
-  // of 512).  At prefix n-1 the block that prefix n-2 stored is read back and overwritten with
-  // bf16(W^{n-1} + W^{n-2}) (W = the stored bf16 weights); C = sum_j W^{n-1}_ij d^{n-1}_ij (d the
-  // raw dot) is summed per row into r5_row[split * 4 + quarter][nx] and per 32-row block and
-  // column into r5_col[row block * 4 + quadrant][ny].
+  // of 512).  At prefix n-1 the block that prefix n-2 stored becomes bf16(W^{n-1} + W^{n-2})
+  // (W = the stored bf16 weights) by a bulk reduce-add through tm_w; C = sum_j W^{n-1}_ij
+  // d^{n-1}_ij (d the raw dot) is summed per row into r5_row[split * 4 + quarter][nx] and per
+  // 32-row block and column into r5_col[row block * 4 + quadrant][ny].
   int merge;
   float* r5_row;
   float* r5_col;
-  const uint16_t* w;              // merge: the weight array (tm_w's), for the read-back
-  int64_t ldw;                    // its row stride (elements)
   int* status;
 };
 constexpr int kWgtCols = 256;

@@ -704,8 +704,6 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
       wp.merge = 1;
       wp.r5_row = F(P.o_r5row);
       wp.r5_col = F(P.o_r5col);
-      wp.w = W;
-      wp.ldw = P.ldw;
     }
     wp.status = device_status;
     GemmParams ga{}, gb{};

@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float r5acc = 0.f;
     const int64_t rblk = i0 / kTileRows;
     // (lane 0) bulk store groups committed so far, and the count just after each tile's prefix
-    // n-2 store (merge: how many later groups may still be pending when that block is read back)
+    // n-2 store (merge: how many later groups may still be pending when that block is added to)
     uint32_t ncommit = 0, c4_0 = 0, c4_1 = 0;
     // the schedule of Schedule::at as nested loops: tile pairs, bands, the pair's tiles
     for (int tp = 0; tp < T; tp += 2) {
