@@ -9,6 +9,7 @@ import os
 import socket
 import subprocess
 import sys
+import time
 
 import pytest
 
@@ -65,7 +66,9 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
            "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus",
            "2", "--workload", "clip_n256", "--steps", "1", "--warmup", "0"]
     env = dict(os.environ, OMP_NUM_THREADS="2")
+    t0 = time.perf_counter()
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    wall_ms = 1000 * (time.perf_counter() - t0)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1, r.stdout
@@ -79,6 +82,17 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["config"]["workload"] == "clip_n256"
+    # the same workload description as the native arm's line (both come from run_config)
+    sys.path.insert(0, ROOT)
+    import bench
+    from contrastive_embedding_loss_gb300 import synth
+
+    kind, A16, B16, scale, bias = synth.workload("clip_n256")
+    args = type("Args", (), {"workload": "clip_n256"})()
+    assert d["config"] == json.loads(json.dumps(bench.run_config(args, kind, A16, B16, scale, bias, 2)))
+    # its step time is the time of the step as run (a sub-batch), which fits inside the run
+    assert 0 < d["ms_per_step"] * (d["steps"] + d["warmup"]) <= wall_ms
+    assert d["ms_per_step_full_batch"] >= d["ms_per_step"]
 
 
 @pytest.mark.parametrize("impl", ["native"])
