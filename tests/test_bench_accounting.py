@@ -55,3 +55,18 @@ def test_credited_flops_and_algorithmic_bytes():
 def test_merged_count_for_other_ladders(pre, dims):
     # merged: every prefix but the second widest contributes its dimensions (one prefix: no merge)
     assert bench.group_flops_executed("gemm", "clip", 3, 5, pre[-1], pre, merged=True) == 2 * 2 * 3 * 5 * dims
+
+
+def test_l2_statement_follows_the_input_size():
+    import numpy as np
+
+    def rows(n, d=1024):
+        return np.zeros((n, d), dtype=np.uint16)
+
+    # the benchmark workload: A and B are 2 x 134 MB, larger than L2
+    assert bench.l2_policy(rows(65536), rows(65536)) == "inputs larger than L2 (no flush)"
+    # ROWS: 8192 queries and 262144 keys
+    assert bench.l2_policy(rows(8192), rows(262144)) == "inputs larger than L2 (no flush)"
+    # the small configurations fit in L2, and the line says so
+    assert bench.l2_policy(rows(4096), rows(4096)).startswith("inputs (17 MB) fit in L2")
+    assert bench.l2_policy(rows(16384), rows(16384)).startswith("inputs (67 MB) fit in L2")
