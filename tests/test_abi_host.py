@@ -87,6 +87,26 @@ def test_workspace_size(lib):
     assert 2 * 1024 * 65536 * 2 + per_weight_chunk <= extra < 2 * 1024 * 65536 * 2 + per_weight_chunk + (32 << 20)
 
 
+def test_workspace_holds_the_merged_prefixes_sums(lib):
+    """The recommended workspace adds, for CLIP and ROWS with long contractions and a second
+    widest prefix that is a multiple of 512, the partial sums that let the two widest prefixes
+    share one weight array: 4 (Na/128) Nb + (4 s + 1) Na + Nb floats (s: the weight pass's column
+    split, 2 at N = 65536), as the header states."""
+    ws = binding.uf_contrastive_workspace_size
+    N = 65536
+    plain = (64, 128, 256, 384, 1024)  # second widest not a multiple of 512: nothing merged
+    sums = 4 * (4 * (N // 128) * N + (4 * 2 + 1) * N + N)
+    assert sums == 539492352  # 0.54 GB
+    assert ws(N, N, 1024, LADDER, 0, 1) - ws(N, N, 1024, plain, 0, 1) == sums
+    # ROWS (8192 queries, 262144 keys) holds them too; its column sums dominate
+    q, k = 8192, 262144
+    extra = ws(q, k, 1024, LADDER, 2, 1) - ws(q, k, 1024, plain, 2, 1)
+    assert 4 * 4 * (q // 128) * k + 4 * (q + k) <= extra < 4 * 4 * (q // 128) * k + 4 * (q + k) + 4 * 4 * 64 * q
+    # SigLIP never merges, nor does a forward-only call (no weights)
+    assert ws(N, N, 1024, LADDER, 1, 1) == ws(N, N, 1024, plain, 1, 1)
+    assert ws(N, N, 1024, LADDER, 0, 0) == ws(N, N, 1024, plain, 0, 0)
+
+
 # Fake device addresses for calls that return before any CUDA call: 256-byte aligned, one
 # 4 GiB slot per argument so that no two buffers overlap (the library refuses overlapping
 # written buffers); the workspace sits above every slot, so its 1 TiB reaches none of them.
