@@ -153,7 +153,7 @@ cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_yt, const
 // CTA pairs of one contraction's grid, and the dA grid size (in waves of CTA pairs) below which
 // both contractions go in one grid.
 double gemm_grid_pairs(const GemmParams& p);
-constexpr double kGemmMergeWaves = 4.0;
+constexpr double kGemmOneGridWaves = 4.0;
 // Both contractions of one weight chunk (dA with K-major weights, dB with MN-major ones) as one
 // grid, so the dB CTAs fill the dA contraction's last wave.
 cudaError_t launch_gemm_both(const CUtensorMap& tk_w, const CUtensorMap& tk_yt, const CUtensorMap& tk_yt128,

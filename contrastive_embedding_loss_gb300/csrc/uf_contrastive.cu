@@ -780,9 +780,9 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
         // A dA contraction of few waves (few rows: ROWS's queries, small batches) leaves SMs idle
         // in its last wave, which one grid with the dB contraction fills (ROWS 8192 x 262144:
         // GEMMs 14.0 -> 12.2 ms).  A long one runs alone: the two read the weights in different
-        // orders, and mixed they share L2 worse (CLIP N = 65536: 23.7 -> 24.6 ms merged).
-        const bool merge = !oneset && gemm_grid_pairs(ga) / (0.5 * g_sm_count[dev]) < kGemmMergeWaves;
-        ProfScope ps(UF_KERNEL_GEMM, oneset || merge ? 1 : 2, stream);
+        // orders, and mixed they share L2 worse (CLIP N = 65536: 23.7 -> 24.6 ms in one grid).
+        const bool one_grid = !oneset && gemm_grid_pairs(ga) / (0.5 * g_sm_count[dev]) < kGemmOneGridWaves;
+        ProfScope ps(UF_KERNEL_GEMM, oneset || one_grid ? 1 : 2, stream);
         if (oneset) {  // (the B side of the one-set loss is the A side's mirror)
           UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
         } else {
@@ -791,7 +791,7 @@ uf_status_t run_loss(const void* A, const void* B, int64_t Na, int64_t Nb, int D
           gb.kdim = rows;
           gb.b_col0 = r0;
           gb.accumulate = r0 > 0;
-          if (merge) {
+          if (one_grid) {
             UF_CHECK(launch_gemm_both(tmWk, tmBt, tmBt128, ga, tmWm, tmAt, tmAt128, gb, stream));
           } else {
             UF_CHECK(launch_gemm(tmWk, tmBt, tmBt128, ga, false, stream));
